@@ -1,0 +1,466 @@
+/*
+ * fadkv_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously-correct CPU statement of the FAD-KV per-token KV
+ * encoding path, used to check the CUDA library.  Only the test suite, the
+ * smoke check and the benchmark's CPU-baseline leg may load it.  It shares no
+ * code, header, table or helper with the CUDA library.
+ *
+ * Source: "FAD-KV: Adaptive Dictionary KV Caching for Efficient Reasoning
+ * Decoding" (thelatestinai.com/papers/2610.37921):
+ *   - abstract: screening-based sparse coding -- a one-shot Top-n selection
+ *     gives a small candidate pool, followed by lightweight coefficient
+ *     refinement; a fixed-size dictionary adaptation that reuses inactive
+ *     atoms instead of appending new ones;
+ *   - Fig. 1 caption: a small Top-n screened pool recalls most full-OMP atoms;
+ *     many atoms stay inactive;
+ *   - Fig. 2 caption: each incoming KV vector is encoded by screening-based
+ *     sparse coding; if the reconstruction error is high, an inactive atom is
+ *     replaced by a context-relevant one and the dictionary size stays fixed;
+ *   - Table 5: ridge parameter lambda = 1e-4 + 0.20 diag(G); threshold delta
+ *     0.50 (key) / 0.70 (value); n, s, N defaults.
+ * Conventions the pages leave open and this library fixes:
+ *   - the s atoms are chosen greedily inside the pool (orthogonal matching
+ *     pursuit restricted to the pool, with the ridge refit at every step);
+ *   - every tie (Top-n cut, greedy argmax) goes to the lower atom index;
+ *   - flagged vectors take inactive atoms in a fixed order: the m-th flagged
+ *     vector (ascending vector index) takes the m-th inactive atom (ascending
+ *     atom index).
+ *
+ * Arithmetic is IEEE double throughout.  Stored values (atoms, inputs) are
+ * binary16 or binary32 and are widened exactly; binary16 is decoded and
+ * encoded here from the format's definition (no library conversion).
+ *
+ * Build: cc -std=c11 -O2 -ffp-contract=off -fPIC -shared -o liboracle.so
+ * fadkv_oracle.c -lm.  (-ffp-contract=off keeps the rounding of every
+ * product and sum the same on every host.)
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_F16 0
+#define ORACLE_F32 1
+
+typedef struct {
+    int32_t N;          /* atoms in the dictionary */
+    int32_t d;          /* head dimension */
+    int32_t n;          /* Top-n pool size */
+    int32_t s;          /* sparsity (atoms per vector) */
+    double lambda_abs;  /* ridge: absolute part, 1e-4 */
+    double lambda_rel;  /* ridge: relative part, 0.20 * G_ii */
+    int32_t dtype;      /* ORACLE_F16 or ORACLE_F32 storage */
+} oracle_params;
+
+/* ---------------------------------------------------------------------- */
+/* binary16 <-> double, from the IEEE-754 definition                       */
+/* (1 sign bit, 5 exponent bits with bias 15, 10 fraction bits).          */
+/* ---------------------------------------------------------------------- */
+
+double oracle_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);               /* zero or subnormal: f * 2^-24 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);   /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* Round to nearest, ties to even (the default floating-point environment
+   makes nearbyint() round half to even). */
+uint16_t oracle_double_to_half(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isnan(x))
+        return 0x7e00;
+    /* 65504 is the largest finite value; anything at or above the midpoint
+       65520 to the next power of two rounds to infinity. */
+    if (a >= 65520.0)
+        return sign | 0x7c00;
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: multiples of 2^-24; a result of 1024 is the
+           smallest normal number and encodes correctly as 0x0400. */
+        double q = nearbyint(ldexp(a, 24));
+        return sign | (uint16_t)q;
+    }
+    int ex;
+    frexp(a, &ex);              /* a = m * 2^ex, m in [0.5, 1) */
+    int E = ex - 1;             /* a = (1 + f/1024) * 2^E */
+    double q = nearbyint(ldexp(a, 10 - E));   /* in [1024, 2048] */
+    if (q == 2048.0) {
+        q = 1024.0;
+        E += 1;
+    }
+    if (E > 15)
+        return sign | 0x7c00;
+    return sign | (uint16_t)((E + 15) << 10) | (uint16_t)((int)q - 1024);
+}
+
+static double load_elem(const void* base, int32_t dtype, int64_t i)
+{
+    if (dtype == ORACLE_F16)
+        return oracle_half_to_double(((const uint16_t*)base)[i]);
+    return (double)((const float*)base)[i];
+}
+
+static void store_elem(void* base, int32_t dtype, int64_t i, double v)
+{
+    if (dtype == ORACLE_F16)
+        ((uint16_t*)base)[i] = oracle_double_to_half(v);
+    else
+        ((float*)base)[i] = (float)v;   /* C conversion rounds to nearest */
+}
+
+static double dot(const double* a, const double* b, int d)
+{
+    double acc = 0.0;
+    for (int t = 0; t < d; ++t)
+        acc += a[t] * b[t];
+    return acc;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Top-n ordering: key (-|r_j|, j).                                        */
+/* ---------------------------------------------------------------------- */
+
+typedef struct {
+    double mag;
+    int32_t id;
+} ranked;
+
+static int ranked_cmp(const void* pa, const void* pb)
+{
+    const ranked* a = (const ranked*)pa;
+    const ranked* b = (const ranked*)pb;
+    if (a->mag > b->mag) return -1;
+    if (a->mag < b->mag) return 1;
+    return (a->id < b->id) ? -1 : (a->id > b->id);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Ridge refit on a support S (k atoms):                                   */
+/*   A = G + diag(lambda_abs + lambda_rel * G_ii),  G = D_S D_S^T,         */
+/*   A c = D_S x,  solved by a Cholesky factorisation A = L L^T.           */
+/* (Table 5, ridge parameter.)  Returns 0 on success, -1 if A is not       */
+/* numerically positive definite.                                          */
+/* ---------------------------------------------------------------------- */
+
+static int ridge_refit(const double* D, int d, const int32_t* S, int k,
+                       const double* x, double lambda_abs, double lambda_rel,
+                       double* c, double* Lwork, double* bwork, int64_t* macs)
+{
+    /* A (stored in Lwork, row-major k x k) */
+    for (int i = 0; i < k; ++i) {
+        for (int l = 0; l <= i; ++l) {
+            double g = dot(D + (int64_t)S[i] * d, D + (int64_t)S[l] * d, d);
+            Lwork[i * k + l] = g;
+            Lwork[l * k + i] = g;
+        }
+        bwork[i] = dot(D + (int64_t)S[i] * d, x, d);
+    }
+    if (macs) *macs += (int64_t)d * (k * (k + 1) / 2 + k);
+    for (int i = 0; i < k; ++i)
+        Lwork[i * k + i] += lambda_abs + lambda_rel * Lwork[i * k + i];
+
+    /* Cholesky, in place in the lower triangle */
+    for (int j = 0; j < k; ++j) {
+        double diag = Lwork[j * k + j];
+        for (int m = 0; m < j; ++m)
+            diag -= Lwork[j * k + m] * Lwork[j * k + m];
+        if (!(diag > 0.0))
+            return -1;
+        double ljj = sqrt(diag);
+        Lwork[j * k + j] = ljj;
+        for (int i = j + 1; i < k; ++i) {
+            double v = Lwork[i * k + j];
+            for (int m = 0; m < j; ++m)
+                v -= Lwork[i * k + m] * Lwork[j * k + m];
+            Lwork[i * k + j] = v / ljj;
+        }
+    }
+    /* forward: L y = b  (y kept in c) */
+    for (int i = 0; i < k; ++i) {
+        double v = bwork[i];
+        for (int m = 0; m < i; ++m)
+            v -= Lwork[i * k + m] * c[m];
+        c[i] = v / Lwork[i * k + i];
+    }
+    /* backward: L^T c = y */
+    for (int i = k - 1; i >= 0; --i) {
+        double v = c[i];
+        for (int m = i + 1; m < k; ++m)
+            v -= Lwork[m * k + i] * c[m];
+        c[i] = v / Lwork[i * k + i];
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Encode (abstract: screening-based sparse coding; Fig. 2 caption).       */
+/*                                                                          */
+/* For each vector x:                                                       */
+/*  1. screening: r_j = <d_j, x> for every atom j;                          */
+/*  2. pool P = the first n atoms in the order (-|r_j|, j);                 */
+/*  3. greedy: e_0 = x; for k = 0..s-1: pick j* = argmax over P \ S of      */
+/*     |<d_j, e_k>| (ties to the lower j), append it to S, refit c on S by  */
+/*     the ridge solve, e_{k+1} = x - D_S c;                                */
+/*  4. relres = ||e_s|| / ||x|| (0 when x = 0).                            */
+/* With full_omp != 0 the pool is the whole dictionary and step 1 is       */
+/* skipped: that is plain OMP with the same refit (the prior-art coder the  */
+/* pages compare against), used only to count operations.                   */
+/*                                                                          */
+/* Outputs: idx [V][s] in pick order, coef [V][s], relres [V].  A vector    */
+/* holding a NaN or infinity gets idx = -1, coef = 0, relres = NaN.         */
+/* Optional diagnostics (NULL to skip):                                     */
+/*   pool    [V][n]  the pool in (-|r|, j) order;                           */
+/*   cut_gap [V]     (|r|_(n) - |r|_(n+1)) / |r|_(n)  (+inf if n == N,      */
+/*                   0 if |r|_(n) == 0);                                    */
+/*   pick_gap [V][s] (a_best - a_second) / a_best at each greedy step       */
+/*                   (+inf when only one candidate is left, 0 if a_best=0); */
+/*   macs    total multiply-accumulates spent (for the cost count).         */
+/* Returns 0, or -1 on bad arguments / allocation failure, -2 if a refit   */
+/* matrix was not positive definite (never expected with lambda_abs > 0).  */
+/* ---------------------------------------------------------------------- */
+
+int oracle_encode(const oracle_params* p, const void* atoms, const void* xin,
+                  int32_t V, int32_t* idx, double* coef, double* relres,
+                  int32_t* pool, double* cut_gap, double* pick_gap,
+                  int64_t* macs, int32_t full_omp)
+{
+    const int N = p->N, d = p->d, s = p->s;
+    const int n = full_omp ? p->N : p->n;
+    if (N <= 0 || d <= 0 || n <= 0 || s <= 0 || n > N || s > n || V < 0)
+        return -1;
+
+    double* D = (double*)malloc(sizeof(double) * (size_t)N * d);
+    double* x = (double*)malloc(sizeof(double) * d);
+    double* e = (double*)malloc(sizeof(double) * d);
+    ranked* rk = (ranked*)malloc(sizeof(ranked) * (size_t)N);
+    int32_t* P = (int32_t*)malloc(sizeof(int32_t) * (size_t)n);
+    char* inS = (char*)malloc((size_t)n);
+    int32_t* S = (int32_t*)malloc(sizeof(int32_t) * s);
+    double* c = (double*)malloc(sizeof(double) * s);
+    double* Lw = (double*)malloc(sizeof(double) * s * s);
+    double* bw = (double*)malloc(sizeof(double) * s);
+    int rc = 0;
+    if (!D || !x || !e || !rk || !P || !inS || !S || !c || !Lw || !bw) {
+        rc = -1;
+        goto done;
+    }
+    for (int64_t i = 0; i < (int64_t)N * d; ++i)
+        D[i] = load_elem(atoms, p->dtype, i);
+
+    for (int32_t v = 0; v < V; ++v) {
+        int finite = 1;
+        for (int t = 0; t < d; ++t) {
+            x[t] = load_elem(xin, p->dtype, (int64_t)v * d + t);
+            if (!isfinite(x[t])) finite = 0;
+        }
+        if (!finite) {
+            for (int k = 0; k < s; ++k) {
+                idx[(int64_t)v * s + k] = -1;
+                coef[(int64_t)v * s + k] = 0.0;
+                if (pick_gap) pick_gap[(int64_t)v * s + k] = INFINITY;
+            }
+            relres[v] = NAN;
+            if (pool)
+                for (int i = 0; i < n; ++i) pool[(int64_t)v * n + i] = -1;
+            if (cut_gap) cut_gap[v] = INFINITY;
+            continue;
+        }
+
+        /* 1-2. screening and the Top-n pool */
+        if (full_omp) {
+            for (int j = 0; j < N; ++j) P[j] = j;
+            if (cut_gap) cut_gap[v] = INFINITY;
+        } else {
+            for (int j = 0; j < N; ++j) {
+                rk[j].mag = fabs(dot(D + (int64_t)j * d, x, d));
+                rk[j].id = j;
+            }
+            if (macs) *macs += (int64_t)N * d;
+            qsort(rk, (size_t)N, sizeof(ranked), ranked_cmp);
+            for (int i = 0; i < n; ++i) P[i] = rk[i].id;
+            if (cut_gap) {
+                if (n == N)
+                    cut_gap[v] = INFINITY;
+                else if (rk[n - 1].mag == 0.0)
+                    cut_gap[v] = 0.0;
+                else
+                    cut_gap[v] = (rk[n - 1].mag - rk[n].mag) / rk[n - 1].mag;
+            }
+        }
+        if (pool)
+            for (int i = 0; i < n; ++i) pool[(int64_t)v * n + i] = P[i];
+
+        /* 3. greedy selection inside the pool with a ridge refit per step */
+        memset(inS, 0, (size_t)n);
+        memcpy(e, x, sizeof(double) * d);
+        for (int k = 0; k < s; ++k) {
+            int best = -1;
+            double abest = -1.0, asecond = -1.0;
+            for (int i = 0; i < n; ++i) {
+                if (inS[i]) continue;
+                double a = fabs(dot(D + (int64_t)P[i] * d, e, d));
+                /* strict order by (a desc, atom id asc) */
+                if (best < 0 || a > abest || (a == abest && P[i] < P[best])) {
+                    asecond = abest;
+                    abest = a;
+                    best = i;
+                } else if (a > asecond) {
+                    asecond = a;
+                }
+            }
+            if (macs) *macs += (int64_t)(n - k) * d;
+            if (pick_gap) {
+                double g;
+                if (asecond < 0.0) g = INFINITY;
+                else if (abest == 0.0) g = 0.0;
+                else g = (abest - asecond) / abest;
+                pick_gap[(int64_t)v * s + k] = g;
+            }
+            inS[best] = 1;
+            S[k] = P[best];
+            if (ridge_refit(D, d, S, k + 1, x, p->lambda_abs, p->lambda_rel,
+                            c, Lw, bw, macs) != 0) {
+                rc = -2;
+                goto done;
+            }
+            for (int t = 0; t < d; ++t) {
+                double acc = x[t];
+                for (int i = 0; i <= k; ++i)
+                    acc -= c[i] * D[(int64_t)S[i] * d + t];
+                e[t] = acc;
+            }
+            if (macs) *macs += (int64_t)(k + 1) * d;
+        }
+
+        /* 4. outputs */
+        double xn = sqrt(dot(x, x, d));
+        double en = sqrt(dot(e, e, d));
+        for (int k = 0; k < s; ++k) {
+            idx[(int64_t)v * s + k] = S[k];
+            coef[(int64_t)v * s + k] = c[k];
+        }
+        relres[v] = (xn == 0.0) ? 0.0 : en / xn;
+    }
+
+done:
+    free(D); free(x); free(e); free(rk); free(P); free(inS);
+    free(S); free(c); free(Lw); free(bw);
+    return rc;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Adapt: fixed-size dictionary adaptation (abstract; Fig. 2 caption).     */
+/*                                                                          */
+/* One batch of V vectors, all encoded against the same dictionary state:  */
+/*  1. usage[idx[v][k]] += 1 for every selected atom (idx >= 0);            */
+/*  2. L = atoms with usage == 0, ascending id (the inactive atoms);        */
+/*  3. F = vectors with relres > delta (strict), ascending v;               */
+/*  4. for m < min(|F|, |L|): v = F[m], j = L[m]:                           */
+/*        e = x_v - sum_k coef[v][k] d_{idx[v][k]};                         */
+/*        atom j <- e / ||e|| (rounded to the storage type);                */
+/*        usage[j] = 1; repl_id[v] = j; repl_coef[v] = ||e||;               */
+/*  5. every other vector: repl_id = -1, repl_coef = 0.                     */
+/* The dictionary keeps exactly N rows.  Flagged vectors beyond |L| are    */
+/* counted in *overflow; *replaced counts the overwritten atoms.           */
+/* Returns 0, or -1 on bad arguments / allocation failure.                  */
+/* ---------------------------------------------------------------------- */
+
+int oracle_adapt(const oracle_params* p, void* atoms, int32_t* usage,
+                 const void* xin, int32_t V, const int32_t* idx,
+                 const double* coef, const double* relres, double delta,
+                 int32_t* repl_id, double* repl_coef,
+                 int64_t* replaced, int64_t* overflow)
+{
+    const int N = p->N, d = p->d, s = p->s;
+    if (N <= 0 || d <= 0 || s <= 0 || V < 0)
+        return -1;
+    int32_t* L = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+    double* e = (double*)malloc(sizeof(double) * d);
+    if (!L || !e) {
+        free(L); free(e);
+        return -1;
+    }
+
+    for (int32_t v = 0; v < V; ++v)
+        for (int k = 0; k < s; ++k) {
+            int32_t j = idx[(int64_t)v * s + k];
+            if (j >= 0 && j < N) usage[j] += 1;
+        }
+
+    int nL = 0;
+    for (int j = 0; j < N; ++j)
+        if (usage[j] == 0) L[nL++] = j;
+
+    int m = 0;
+    int64_t flagged = 0;
+    for (int32_t v = 0; v < V; ++v) {
+        repl_id[v] = -1;
+        repl_coef[v] = 0.0;
+        if (!(relres[v] > delta)) continue;
+        ++flagged;
+        if (m >= nL) continue;
+        int32_t j = L[m++];
+        for (int t = 0; t < d; ++t) {
+            double acc = load_elem(xin, p->dtype, (int64_t)v * d + t);
+            for (int k = 0; k < s; ++k) {
+                int32_t a = idx[(int64_t)v * s + k];
+                if (a >= 0)
+                    acc -= coef[(int64_t)v * s + k] * load_elem(atoms, p->dtype, (int64_t)a * d + t);
+            }
+            e[t] = acc;
+        }
+        double en = sqrt(dot(e, e, d));
+        for (int t = 0; t < d; ++t)
+            store_elem(atoms, p->dtype, (int64_t)j * d + t, e[t] / en);
+        usage[j] = 1;
+        repl_id[v] = j;
+        repl_coef[v] = en;
+    }
+    if (replaced) *replaced += m;
+    if (overflow) *overflow += flagged - m;
+    free(L);
+    free(e);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Reconstruct (abstract: each token's KV state is a sparse combination of */
+/* atoms):  xhat_v = sum_k coef[v][k] d_{idx[v][k]}                         */
+/*                   + repl_coef[v] d_{repl_id[v]}   (if repl_id >= 0).     */
+/* repl_id may be NULL (no replacement terms).                              */
+/* ---------------------------------------------------------------------- */
+
+int oracle_reconstruct(const oracle_params* p, const void* atoms, int32_t V,
+                       const int32_t* idx, const double* coef,
+                       const int32_t* repl_id, const double* repl_coef,
+                       double* xhat)
+{
+    const int N = p->N, d = p->d, s = p->s;
+    if (N <= 0 || d <= 0 || s <= 0 || V < 0)
+        return -1;
+    for (int32_t v = 0; v < V; ++v) {
+        for (int t = 0; t < d; ++t) {
+            double acc = 0.0;
+            for (int k = 0; k < s; ++k) {
+                int32_t a = idx[(int64_t)v * s + k];
+                if (a >= 0 && a < N)
+                    acc += coef[(int64_t)v * s + k] * load_elem(atoms, p->dtype, (int64_t)a * d + t);
+            }
+            if (repl_id && repl_id[v] >= 0 && repl_id[v] < N)
+                acc += repl_coef[v] * load_elem(atoms, p->dtype, (int64_t)repl_id[v] * d + t);
+            xhat[(int64_t)v * d + t] = acc;
+        }
+    }
+    return 0;
+}

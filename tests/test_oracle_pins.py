@@ -1,0 +1,422 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+Each test pins one part of the oracle to something other than the oracle's
+own formulas: the pages' printed values (Table 4 cost, Table 5 defaults), a
+closed form, a theorem's special case, an exhaustive search on tiny inputs,
+or a library routine applied to a case that reduces to it.  A plausible slip
+in the oracle (a dropped ridge term, a wrong sign in the residual, a wrong
+index in the tie rule, a transposed Gram matrix) fails at least one of them.
+
+Source: "FAD-KV: Adaptive Dictionary KV Caching for Efficient Reasoning
+Decoding" (abstract; Fig. 1 and Fig. 2 captions; Table 4; Table 5).
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from dictionary_sparse_kv_gb300 import synthetic as S
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+LA, LR = 1e-4, 0.20
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _ridge_closed_form(D, S_ids, x, la=LA, lr=LR):
+    """Normal equations of the ridge refit, solved by numpy (LAPACK)."""
+    DS = D[S_ids].astype(np.float64)
+    G = DS @ DS.T
+    A = G + np.diag(la + lr * np.diag(G))
+    return np.linalg.solve(A, DS @ x.astype(np.float64))
+
+
+# --------------------------------------------------------------------------
+# binary16 codec: against numpy's float16 conversion (exhaustive decode)
+# --------------------------------------------------------------------------
+
+def test_half_decode_exhaustive(oracle_lib):
+    O = oracle_lib
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([O.half_to_double(int(b)) for b in bits])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+def test_half_encode_rounding(oracle_lib):
+    O = oracle_lib
+    g = np.random.default_rng(7)
+    b = np.arange(0, 0x7bff, 3, dtype=np.uint16)
+    mid = (b.view(np.float16).astype(np.float64) + (b + 1).view(np.float16).astype(np.float64)) / 2
+    vals = np.concatenate([
+        g.standard_normal(20000) * 10.0 ** g.integers(-9, 6, 20000),
+        # exact midpoints between neighbouring finite halves (ties to even), both signs
+        mid, -mid,
+        [0.0, -0.0, 65504.0, 65519.99, 65520.0, -65520.0, 1e9, 2.0**-24, 2.0**-25,
+         3 * 2.0**-26, 2.0**-14, 2.0**-14 - 2.0**-25, np.inf, -np.inf],
+    ])
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([O.double_to_half(float(v)) for v in vals], dtype=np.uint16)
+    assert (got == ref).all()
+
+
+# --------------------------------------------------------------------------
+# Table 5 defaults and Table 4 cost
+# --------------------------------------------------------------------------
+
+def test_table4_cost_reproduced_by_operation_count(oracle_lib):
+    """Table 4 prints Cost 0.19 for GM relative to OMP over the whole
+    dictionary (1.00).  Counting the oracle's multiply-accumulates at the 3B
+    shape (N=4096, d=128, n=256, s=8) must reproduce that to two decimals."""
+    O = oracle_lib
+    g = _golden("table4_cost.json")
+    sh = g["shape"]
+    p = O.Params(sh["N"], sh["d"], sh["n"], sh["s"])
+    D = S.make_dictionary(sh["N"], sh["d"], np.float16, 11)
+    x = S.make_sparse_inputs(D, 3, sh["s"], 12)
+    gm = O.encode(p, D, x)
+    omp = O.encode(p, D, x, full_omp=True)
+    cost = gm.macs / omp.macs
+    assert round(cost, 2) == g["GM"]
+    # the count has a closed form: screening N d; at step k, correlations over
+    # the n - k unpicked pool atoms, the (k+1)(k+2)/2 Gram entries and k+1
+    # right-hand-side products of the refit, and the k+1 residual terms
+    N, d, n, s = sh["N"], sh["d"], sh["n"], sh["s"]
+    per_vec = N * d + sum(((n - k) + (k + 1) * (k + 2) // 2 + 2 * (k + 1)) * d for k in range(s))
+    assert gm.macs == 3 * per_vec
+    assert omp.macs == 3 * sum(((N - k) + (k + 1) * (k + 2) // 2 + 2 * (k + 1)) * d for k in range(s))
+
+
+def test_table5_defaults_file():
+    g = _golden("table5_defaults.json")
+    assert g["ridge_lambda_abs"] == LA and g["ridge_lambda_rel"] == LR
+    assert (g["delta_key"], g["delta_value"]) == (0.5, 0.7)
+
+
+# --------------------------------------------------------------------------
+# screening + Top-n against a full stable sort
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,d,n,dt", [(512, 64, 32, np.float32), (4096, 128, 256, np.float16)])
+def test_topn_matches_full_sort(oracle_lib, N, d, n, dt):
+    O = oracle_lib
+    p = O.Params(N, d, n, 4, dtype=O.F32 if dt == np.float32 else O.F16)
+    D = S.make_dictionary(N, d, dt, 21, N)
+    x = S.make_sparse_inputs(D, 40, 4, 22, N, dtype=dt)
+    r = O.encode(p, D, x)
+    R = x.astype(np.float64) @ D.astype(np.float64).T
+    for v in range(x.shape[0]):
+        mag = np.abs(R[v])
+        order = np.lexsort((np.arange(N), -mag))      # key (-|r|, j), stable
+        if r.cut_gap[v] < 1e-9:
+            continue
+        assert list(r.pool[v]) == list(order[:n])
+
+
+def test_topn_tie_rule_on_exact_zeros(oracle_lib):
+    """Signed permutation dictionary (N = d): a 4-sparse x leaves N-4 scores
+    exactly zero, so the pool is the 4 support atoms by |coefficient|, then
+    the lowest remaining ids in ascending order."""
+    O = oracle_lib
+    d = N = 64
+    g = np.random.default_rng(3)
+    perm = g.permutation(N)
+    D = np.zeros((N, d), np.float32)
+    D[np.arange(N), perm] = g.choice([-1.0, 1.0], N)
+    supp = np.array([40, 7, 55, 13])
+    b = np.array([-3.0, 2.5, 2.0, -1.0])
+    x = (b @ D[supp]).astype(np.float32)[None]
+    p = O.Params(N, d, 10, 3, dtype=O.F32)
+    r = O.encode(p, D, x)
+    rest = [j for j in range(N) if j not in supp][:6]
+    assert list(r.pool[0]) == list(supp) + rest
+    assert r.cut_gap[0] == 0.0
+
+
+# --------------------------------------------------------------------------
+# ridge refit
+# --------------------------------------------------------------------------
+
+def test_ridge_matches_normal_equations(oracle_lib):
+    O = oracle_lib
+    p = O.Params(512, 64, 32, 4, dtype=O.F32)
+    D = S.make_dictionary(512, 64, np.float32, 0)
+    x = S.make_tiny_inputs(D, 64, 4, 1)
+    r = O.encode(p, D, x)
+    for v in range(64):
+        c = _ridge_closed_form(D, r.idx[v], x[v])
+        assert np.allclose(r.coef[v], c, rtol=1e-10, atol=1e-12)
+
+
+def test_orthogonal_closed_form(oracle_lib):
+    """Orthogonal atoms of norms w_j: G is diagonal, so
+    c_i = b_i w_i^2 / (w_i^2 (1 + lambda_rel) + lambda_abs), picks go by
+    |b_i| w_i^2 (ties to the lower id), and the residual is known exactly."""
+    O = oracle_lib
+    d = N = 32
+    w = np.array([0.5, 1.0, 2.0, 1.5] * 8)
+    D = (np.diag(w)).astype(np.float32)            # atom j = w_j e_j
+    supp = np.array([2, 5, 9, 20, 30])
+    b = np.array([0.75, -2.0, 1.0, -0.5, 0.25])    # |b| w^2 = 3, 2, 0.25, 4, 0.5625... see below
+    x = np.zeros(d)
+    x[supp] = b * w[supp]
+    x32 = x.astype(np.float32)[None]
+    s = 5
+    p = O.Params(N, d, 8, s, dtype=O.F32)
+    r = O.encode(p, D, x32)
+    score = np.abs(b) * w[supp] ** 2
+    order = supp[np.lexsort((supp, -score))]
+    assert list(r.idx[0]) == list(order)
+    w2 = w ** 2
+    c_expect = {j: b[i] * w2[j] / (w2[j] * (1 + LR) + LA) for i, j in enumerate(supp)}
+    for k, j in enumerate(r.idx[0]):
+        assert r.coef[0, k] == pytest.approx(c_expect[j], rel=1e-13)
+    e = x.copy()
+    for k, j in enumerate(r.idx[0]):
+        e[j] -= r.coef[0, k] * w[j]
+    assert r.relres[0] == pytest.approx(np.linalg.norm(e) / np.linalg.norm(x), rel=1e-13)
+
+
+def test_unit_orthonormal_relres_constant(oracle_lib):
+    """Unit-norm orthonormal atoms and a noise-free s-sparse x: c = b/1.2001
+    and relres = 0.2001/1.2001 whatever b is."""
+    O = oracle_lib
+    d = N = 64
+    D = np.eye(N, dtype=np.float32)[::-1].copy()
+    g = np.random.default_rng(5)
+    for trial in range(5):
+        supp = g.choice(N, 6, replace=False)
+        b = g.choice([-1, 1], 6) * (1 + g.integers(0, 64, 6) / 16.0)
+        x = (b @ D[supp]).astype(np.float32)[None]
+        r = O.encode(O.Params(N, d, 12, 6, dtype=O.F32), D, x)
+        assert sorted(r.idx[0]) == sorted(supp)
+        for k, j in enumerate(r.idx[0]):
+            assert r.coef[0, k] == pytest.approx(b[list(supp).index(j)] / 1.2001, rel=1e-14)
+        assert r.relres[0] == pytest.approx(0.2001 / 1.2001, rel=1e-13)
+
+
+# --------------------------------------------------------------------------
+# greedy selection: exact recovery (Tropp's condition) and brute force
+# --------------------------------------------------------------------------
+
+def _sylvester(m):
+    H = np.array([[1.0]])
+    while H.shape[0] < m:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+@pytest.mark.parametrize("ridge", [False, True])
+def test_exact_recovery_incoherent(oracle_lib, ridge):
+    """D = [I | H/sqrt(d)] at d = 64 has coherence 1/8; s = 4 < (1 + 8)/2,
+    so OMP recovers every noise-free 4-sparse x exactly (Tropp 2004).  Here
+    the pool is the whole dictionary.  The same recovery is checked with the
+    ridge refit of Table 5."""
+    O = oracle_lib
+    d = 64
+    D = np.vstack([np.eye(d), _sylvester(d) / 8.0]).astype(np.float32)
+    N = D.shape[0]
+    g = np.random.default_rng(9)
+    p = O.Params(N, d, N, 4, lambda_abs=LA if ridge else 0.0,
+                 lambda_rel=LR if ridge else 0.0, dtype=O.F32)
+    fails = 0
+    for trial in range(200):
+        supp = g.choice(N, 4, replace=False)
+        b = g.choice([-1, 1], 4) * (1 + g.integers(0, 9, 4) / 8.0)   # |b| in [1, 2]
+        x = (b @ D[supp].astype(np.float64)).astype(np.float32)[None]
+        r = O.encode(p, D, x)
+        fails += sorted(r.idx[0]) != sorted(supp)
+        if not ridge:
+            assert np.allclose(sorted(zip(r.idx[0], r.coef[0])), sorted(zip(supp, b)), atol=1e-6)
+    assert fails == 0
+
+
+def test_greedy_steps_brute_force(oracle_lib):
+    """Tiny inputs (d=16, N=32, n=8): at every step k the pick must be the
+    argmax over P \\ S_k of |<d_j, e_k>| (ties to the lower id), where e_k is
+    rebuilt by numpy from the oracle's own k-atom encode, and the final
+    support's objective must equal the best over its own coefficients."""
+    O = oracle_lib
+    d, N, n = 16, 32, 8
+    D = S.make_dictionary(N, d, np.float32, 31)
+    x = S.make_tiny_inputs(D, 30, 3, 32, sigma=0.05)
+    D64 = D.astype(np.float64)
+    for s in (2, 3):
+        full = O.encode(O.Params(N, d, n, s, dtype=O.F32), D, x)
+        for v in range(x.shape[0]):
+            P = list(full.pool[v])
+            for k in range(s):
+                if k == 0:
+                    e = x[v].astype(np.float64)
+                else:
+                    part = O.encode(O.Params(N, d, n, k, dtype=O.F32), D, x[v:v + 1])
+                    assert list(part.idx[0]) == list(full.idx[v][:k])
+                    e = x[v] - part.coef[0] @ D64[part.idx[0]]
+                cand = [j for j in P if j not in full.idx[v][:k]]
+                a = np.abs(D64[cand] @ e)
+                best = min(cand[i] for i in range(len(cand)) if a[i] == a.max())
+                if full.pick_gap[v, k] > 1e-9:
+                    assert full.idx[v][k] == best
+
+
+def test_brute_force_subset_objective(oracle_lib):
+    """Exhaustive search over every s-subset of the pool of the ridge
+    objective ||x - D_T c||^2 + sum_i (lambda_abs + lambda_rel G_ii) c_i^2.
+    The greedy support's objective, evaluated at the oracle's c, equals the
+    closed-form minimum for that support and is >= the global minimum; on
+    noise-free inputs over orthogonal atoms greedy attains the minimum."""
+    O = oracle_lib
+
+    def objective(D, T, c, x):
+        DT = D[list(T)].astype(np.float64)
+        G = DT @ DT.T
+        lam = LA + LR * np.diag(G)
+        e = x - c @ DT
+        return e @ e + lam @ (c * c)
+
+    d, N, n = 16, 32, 8
+    D = S.make_dictionary(N, d, np.float32, 41)
+    x = S.make_tiny_inputs(D, 20, 3, 42, sigma=0.1).astype(np.float64)
+    for s in (2, 3):
+        r = O.encode(O.Params(N, d, n, s, dtype=O.F32), D, x.astype(np.float32))
+        for v in range(x.shape[0]):
+            xv = x[v].astype(np.float32).astype(np.float64)
+            f_g = objective(D, r.idx[v], r.coef[v], xv)
+            f_cf = objective(D, r.idx[v], _ridge_closed_form(D, r.idx[v], xv), xv)
+            assert f_g == pytest.approx(f_cf, rel=1e-12)
+            best = min(objective(D, T, _ridge_closed_form(D, list(T), xv), xv)
+                       for T in itertools.combinations(r.pool[v], s))
+            assert f_g >= best * (1 - 1e-12)
+    # orthogonal atoms, noise-free: greedy == exhaustive argmin
+    Q = np.eye(d, dtype=np.float32)
+    Dq = np.vstack([Q, Q[::-1] * 0.5]).astype(np.float32)   # N = 32, pairs of parallel atoms
+    g = np.random.default_rng(4)
+    for trial in range(20):
+        supp = g.choice(d, 3, replace=False)
+        b = g.choice([-1, 1], 3) * (1 + g.integers(0, 16, 3) / 8.0)
+        xv = (b @ Dq[supp]).astype(np.float32)
+        r = O.encode(O.Params(32, d, 8, 3, dtype=O.F32), Dq, xv[None])
+        vals = {T: objective(Dq, T, _ridge_closed_form(Dq, list(T), xv.astype(np.float64)),
+                             xv.astype(np.float64))
+                for T in itertools.combinations(sorted(r.pool[0]), 3)}
+        assert objective(Dq, r.idx[0], r.coef[0], xv.astype(np.float64)) == pytest.approx(
+            min(vals.values()), rel=1e-12)
+
+
+# --------------------------------------------------------------------------
+# special inputs
+# --------------------------------------------------------------------------
+
+def test_zero_and_nonfinite_inputs(oracle_lib):
+    O = oracle_lib
+    p = O.Params(512, 64, 32, 4, dtype=O.F32)
+    D = S.make_dictionary(512, 64, np.float32, 0)
+    x = np.zeros((3, 64), np.float32)
+    x[1, 5] = np.nan
+    x[2, 9] = np.inf
+    r = O.encode(p, D, x)
+    assert list(r.idx[0]) == [0, 1, 2, 3] and (r.coef[0] == 0).all() and r.relres[0] == 0
+    assert list(r.pool[0]) == list(range(32))
+    for v in (1, 2):
+        assert (r.idx[v] == -1).all() and math.isnan(r.relres[v])
+
+
+# --------------------------------------------------------------------------
+# adapt: hand-derived cases and invariants
+# --------------------------------------------------------------------------
+
+def test_adapt_golden_cases(oracle_lib):
+    O = oracle_lib
+    g = _golden("adapt_cases.json")
+    for case in g["cases"]:
+        atoms = np.array(g["atoms"], np.float32)
+        before = atoms.copy()
+        usage = np.array(case["usage"], np.int32)
+        x = np.array(case["x"], np.float32)
+        idx = np.array(case["idx"], np.int32)
+        coef = np.array(case["coef"], np.float64)
+        rel = np.array([float(v) for v in case["relres"]], np.float64)
+        p = O.Params(atoms.shape[0], atoms.shape[1], 2, idx.shape[1], dtype=O.F32)
+        res = O.adapt(p, atoms, usage, x, idx, coef, rel, case["delta"])
+        assert list(usage) == case["expect_usage"], case["name"]
+        assert list(res.repl_id) == case["expect_repl_id"], case["name"]
+        assert np.allclose(res.repl_coef, case["expect_repl_coef"], rtol=0, atol=1e-12)
+        assert (res.replaced, res.overflow) == (case["expect_replaced"], case["expect_overflow"])
+        changed = {int(k): v for k, v in case["expect_atoms_changed"].items()}
+        for j in range(atoms.shape[0]):
+            want = changed.get(j, before[j])
+            assert np.array_equal(atoms[j], np.array(want, np.float32)), (case["name"], j)
+
+
+def test_adapt_invariants_random(oracle_lib):
+    """Row count fixed at N; usage never decreases and is conserved
+    (sum after = sum before + s * #encoded + #replaced); only atoms inactive
+    after the increments are overwritten, in ascending order, by unit-norm
+    rows (within d * 2^-11 for binary16)."""
+    O = oracle_lib
+    N, d, n, s = 4096, 128, 256, 8
+    p = O.Params(N, d, n, s)
+    D = S.make_dictionary(N, d, np.float16, 51)
+    usage = S.make_usage(N, int(0.3 * N), 52)
+    src = D[usage > 0]
+    x = S.make_sparse_inputs(src, 96, s, 53, off_frac=0.9)   # large residuals: many flags
+    r = O.encode(p, D, x)
+    before_D, before_u = D.copy(), usage.copy()
+    res = O.adapt(p, D, usage, x, r.idx, r.coef, r.relres, 0.5)
+    assert D.shape == (N, d)
+    inc = np.zeros(N, np.int64)
+    np.add.at(inc, r.idx.ravel(), 1)
+    after_inc = before_u + inc
+    L = np.nonzero(after_inc == 0)[0]
+    F = np.nonzero(r.relres > 0.5)[0]
+    m = min(len(L), len(F))
+    assert res.replaced == m and res.overflow == len(F) - m
+    assert m > 0
+    assert list(res.repl_id[F[:m]]) == list(L[:m])
+    assert (res.repl_id[np.setdiff1d(np.arange(len(x)), F[:m])] == -1).all()
+    assert usage.sum() == before_u.sum() + s * len(x) + m
+    assert (usage >= before_u).all()
+    changed = np.nonzero((D != before_D).any(axis=1))[0]
+    assert set(changed) <= set(L[:m])
+    norms = np.linalg.norm(D[L[:m]].astype(np.float64), axis=1)
+    assert np.all(np.abs(norms - 1) <= d * 2.0 ** -11)
+    # each new atom is the normalised ridge residual of its vector
+    for v, j in zip(F[:m], L[:m]):
+        e = x[v].astype(np.float64) - r.coef[v] @ before_D[r.idx[v]].astype(np.float64)
+        assert res.repl_coef[v] == pytest.approx(np.linalg.norm(e), rel=1e-12)
+        assert np.array_equal(D[j], (e / np.linalg.norm(e)).astype(np.float16))
+
+
+# --------------------------------------------------------------------------
+# reconstruct
+# --------------------------------------------------------------------------
+
+def test_reconstruct_consistency(oracle_lib):
+    """reconstruct(encode(x)) = x - e_s, so ||x - xhat|| / ||x|| = relres;
+    after a replacement, xhat = x up to the binary16 rounding of the new atom."""
+    O = oracle_lib
+    N, d, n, s = 4096, 128, 256, 8
+    p = O.Params(N, d, n, s)
+    D = S.make_dictionary(N, d, np.float16, 61)
+    usage = S.make_usage(N, 400, 62)
+    x = S.make_sparse_inputs(D[usage > 0], 32, s, 63, off_frac=0.9)
+    r = O.encode(p, D, x)
+    xh = O.reconstruct(p, D, r.idx, r.coef)
+    x64 = x.astype(np.float64)
+    rel = np.linalg.norm(x64 - xh, axis=1) / np.linalg.norm(x64, axis=1)
+    assert np.allclose(rel, r.relres, rtol=1e-10)
+    res = O.adapt(p, D, usage, x, r.idx, r.coef, r.relres, 0.5)
+    xh2 = O.reconstruct(p, D, r.idx, r.coef, res.repl_id, res.repl_coef)
+    rep = res.repl_id >= 0
+    assert rep.any()
+    err = np.linalg.norm(xh2[rep] - x64[rep], axis=1)
+    bound = res.repl_coef[rep] * np.sqrt(d) * 2.0 ** -11
+    assert (err <= bound).all()
