@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Throughput of the FAD-KV per-token KV encoding path on GB300.
+
+A step is one decode step of every dictionary of Llama-3.2-3B (28 layers x
+{K, V} = 56 dictionaries, N=4096 binary16 atoms, d=128, n=256, s=8; 8 KV
+heads x 16 sequences = 128 vectors per dictionary): encode (screening, Top-n
+pool, greedy + ridge), fixed-size adaptation and sparse reconstruction,
+through the C ABI.  Inputs are synthetic (seeded sparse mixtures, see
+dictionary_sparse_kv_gb300/synthetic.py).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its
+own 56 dictionaries (weak scaling, no collective on the data path); the time
+is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from dataclasses import replace
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV vectors encoded/s at N=4096,d=128,n=256,s=8; % HBM / tensor-pipe roofline"
+UNIT = "vectors/s"
+WORKLOAD = "decode_3b"
+L2_FLUSH_BYTES = 256 << 20           # twice the 129 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def workload_config(w, vectors_per_step):
+    return {
+        "workload": f"{w.name}: {w.G} dictionaries (layers x K,V), N={w.N}, d={w.d}, n={w.n}, s={w.s}, "
+                    f"{w.V} vectors per dictionary per step (8 KV heads x {w.V // 8} sequences)",
+        "vectors_per_step": vectors_per_step,
+        "step": "encode + adapt + reconstruct",
+        "storage": "binary16 atoms and inputs",
+        "l2": "flushed between timed steps (256 MiB write outside the step's events)",
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# algorithmic work per kernel launch (the roofline numerators)
+# --------------------------------------------------------------------------
+
+def kernel_work(w, kernel: str, vectors: int):
+    """(bound, algorithmic units per launch, unit) for one launch that covers
+    `vectors` vectors of every dictionary (G * vectors vectors in total)."""
+    G, N, d, n, s = w.G, w.N, w.d, w.n, w.s
+    esz = 2 if w.dtype.__name__ == "float16" else 4
+    nv = G * vectors
+    if kernel == "screen":
+        # one pass over every dictionary plus the inputs; 2 N d flops per vector
+        return "alu", 2.0 * N * d * nv, "TFLOP/s"
+    if kernel == "topn":
+        return "hbm", 4.0 * N * nv + 8.0 * n * nv, "GB/s"
+    if kernel == "greedy":
+        # correlations of the s-1 later picks over the pool, plus per step k
+        # the Gram row (k+1 dots), right-hand side (1 dot) and residual (k+1)
+        per = 2.0 * (s - 1) * n * d + sum(2.0 * d * (2 * (k + 1) + 1) for k in range(s))
+        return "alu", per * nv, "TFLOP/s"
+    if kernel == "adapt":
+        return "hbm", 4.0 * (s + 3) * nv + 4.0 * G * N, "GB/s"
+    if kernel == "reconstruct":
+        return "hbm", (esz * (s + 1) * d + 4 * (s + 1) + 4 * d) * nv, "GB/s"
+    raise KeyError(kernel)
+
+
+def kernel_sources():
+    import glob
+    out = {}
+    for p in glob.glob(os.path.join(ROOT, "dictionary_sparse_kv_gb300", "csrc", "*")):
+        with open(p, "rb") as f:
+            out[os.path.basename(p)] = hashlib.sha256(f.read()).hexdigest()[:16]
+    return out
+
+
+KERNEL_FILES = {"screen": "k_screen_ffma.cu", "topn": "k_topn.cu", "greedy": "k_greedy.cu",
+                "adapt": "k_adapt_reconstruct.cu", "reconstruct": "k_adapt_reconstruct.cu"}
+
+
+def traffic_for(kernel: str, w):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel (profiles/traffic.json)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        tab = json.load(f)
+    ent = tab.get(w.name, {}).get(kernel)
+    if not ent:
+        return None
+    src = kernel_sources().get(KERNEL_FILES.get(kernel, ""), None)
+    if ent.get("source_sha256_16") != src:
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def roofline(w, prof, vectors_per_launch, peaks, peak_kind, sm_count, sm_mhz_max):
+    """Roofline object for the kernel with the largest share of device time."""
+    kern = max(prof, key=lambda k: prof[k][1]) if prof else None
+    if kern is None:
+        return None, {}
+    shares = {}
+    tot = sum(v[1] for v in prof.values()) or 1.0
+    for k, (n_l, ms) in prof.items():
+        shares[k] = {"launches": n_l, "ms_total": round(ms, 4), "share": round(ms / tot, 4)}
+    n_launch, ms = prof[kern]
+    bound, work, unit = kernel_work(w, kern, vectors_per_launch)
+    sec = ms / 1e3 / n_launch
+    if unit == "GB/s":
+        achieved = work / sec / 1e9
+        peak = peaks["hbm_gbs"]
+        pk = f"hbm_gbs ({peak_kind})"
+    else:
+        achieved = work / sec / 1e12
+        if bound == "alu":
+            # FP32 pipe: 128 FMA lanes per SM, 2 flops per FMA, max SM clock
+            peak = sm_count * 128 * 2 * sm_mhz_max * 1e6 / 1e12
+            pk = f"fp32 fma: {sm_count} SMs x 128 lanes x 2 x {sm_mhz_max:.0f} MHz"
+        else:
+            peak = peaks["bf16_tflops"]
+            pk = f"bf16_tflops ({peak_kind})"
+    obj = {"kernel": kern, "bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": unit,
+           "frac": round(achieved / peak, 4), "traffic": traffic_for(kern, w), "peak_source": pk,
+           "launch_ms": round(ms / n_launch, 5)}
+    return obj, shares
+
+
+# --------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_steps(w, data, steps, threads):
+    """Run the oracle over `steps` decode steps of every dictionary of `data`
+    (encode on `threads` host threads, then the sequential adapt and
+    reconstruct).  Returns
+    (vectors, seconds)."""
+    import numpy as np
+    from oracle import oracle as O
+    p = O.Params(w.N, w.d, w.n, w.s, 1e-4, 0.20, O.F16 if w.dtype.__name__ == "float16" else O.F32)
+    atoms = data.atoms.copy()
+    usage = data.usage.copy()
+    xs = [data.inputs(t) for t in range(steps)]
+    t0 = time.perf_counter()
+    nvec = 0
+    for t in range(steps):
+        x = xs[t]
+        for g in range(len(data.dicts)):
+            r = O.encode_threaded(p, atoms[g], x[g], threads)
+            a = O.adapt(p, atoms[g], usage[g], x[g], r.idx, r.coef, r.relres, data.deltas()[g])
+            O.reconstruct(p, atoms[g], r.idx, r.coef, a.repl_id, a.repl_coef)
+            nvec += x.shape[1]
+    return nvec, time.perf_counter() - t0
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from dictionary_sparse_kv_gb300 import synthetic as S
+    w = S.WORKLOADS[args.workload]
+    data = S.WorkloadData(w)
+    threads = os.cpu_count() or 1
+    # warm-up steps, then K timed steps; each step is one full decode step
+    oracle_steps(w, data, max(0, min(args.warmup, 1)), threads)
+    nvec, sec = oracle_steps(w, data, args.steps, threads)
+    value = nvec / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, w.G * w.V),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} full decode steps ({w.G} x {w.V} vectors each), "
+                                   f"plain C double-precision oracle, encode split over {threads} host "
+                                   f"threads, adapt sequential; CPU: {cpu_model()}"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    from dictionary_sparse_kv_gb300 import build as B
+    from dictionary_sparse_kv_gb300 import fadkv as F
+    from dictionary_sparse_kv_gb300 import synthetic as S
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        B.build()
+    if world > 1:
+        dist.barrier()
+    F.lib()
+
+    w0 = S.WORKLOADS[args.workload]
+    w = replace(w0, seed=w0.seed + 1000 * rank)       # each rank its own dictionaries
+    data = S.WorkloadData(w)
+    K, W = args.steps, max(3, args.warmup)
+    G, V, d = w.G, w.V, w.d
+    xs_host = [torch.from_numpy(data.inputs(t)).pin_memory() for t in range(W + K)]
+    xs_dev = [x.to(dev) for x in xs_host]
+    D = F.Dictionary(torch.from_numpy(data.atoms).to(dev), torch.from_numpy(data.usage).to(dev),
+                     data.deltas(), w.n, w.s, V)
+    codes = D.new_codes(V)
+    xhat = torch.empty((G, V, d), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for t in range(W):
+        D.step(xs_dev[t], codes, xhat)
+    torch.cuda.synchronize(dev)
+    F.profile_read(D.h, reset=True)
+
+    # ---- device-resident timed region ----
+    F.profile_enable(D.h, True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    if rank == 0:
+        clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for t in range(K):
+        flush.fill_(float(t))
+        ev[t][0].record(stream)
+        D.step(xs_dev[W + t], codes, xhat)
+        ev[t][1].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop() if rank == 0 else None
+    F.profile_enable(D.h, False)
+    prof = F.profile_read(D.h, reset=True)
+    dev_ms = sum(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        tt = torch.tensor([dev_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        dev_ms = float(tt.item())
+    launches = sum(n for n, _ in prof.values())
+
+    # ---- end to end: pinned host inputs in, codes out, every step ----
+    xin = torch.empty_like(xs_dev[0])
+    outs = [torch.empty(c.shape, dtype=c.dtype).pin_memory() for c in
+            (codes.idx, codes.coef, codes.relres, codes.repl_id, codes.repl_coef)]
+    h2d = xs_host[0].numel() * xs_host[0].element_size()
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    for t in range(K):
+        flush.fill_(float(t))
+        ev2[t][0].record(stream)
+        xin.copy_(xs_host[W + t], non_blocking=True)
+        D.step(xin, codes, xhat)
+        for o, c in zip(outs, (codes.idx, codes.coef, codes.relres, codes.repl_id, codes.repl_coef)):
+            o.copy_(c, non_blocking=True)
+        ev2[t][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    stats = D.stats()
+
+    if rank != 0:
+        dist.barrier() if world > 1 else None
+        return 0
+
+    vectors_per_step = G * V
+    value = world * K * vectors_per_step / (dev_ms / 1e3)
+    e2e = world * K * vectors_per_step / (e2e_ms / 1e3)
+    peaks, peak_kind = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sm_max = float(peaks.get("sm_max_mhz") or clk.get("sm_max_mhz") or 2070.0)
+    roof, shares = roofline(w, prof, V, peaks, peak_kind, props.multi_processor_count, sm_max)
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        sub = S.WorkloadData(w)
+        nvec, sec = oracle_steps(w, sub, 2, threads)
+        cpu = {"value": round(nvec / sec, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"first 2 decode steps of all {w.G} dictionaries ({nvec} vectors), oracle encode "
+                         f"over {threads} host threads + sequential adapt; CPU: {cpu_model()}"}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(dev_ms / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": workload_config(w, vectors_per_step),
+        "e2e": {"value": round(e2e, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches, "roofline": roof, "kernels": shares, "clocks": clk, "cpu_baseline": cpu,
+        "wall_s_timed": round(wall, 4),
+        "adapt": {"replaced": sum(s["replaced"] for s in stats), "overflow": sum(s["overflow"] for s in stats)},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+    return 0
+
+
+def main(argv=None):
+    args = parse(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

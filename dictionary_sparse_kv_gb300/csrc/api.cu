@@ -1,0 +1,430 @@
+// Host side of the C ABI declared in include/fadkv.h: argument checks, the
+// encode/adapt sequence contract, workspace carving and kernel launches.
+// The library never allocates device memory: the caller passes the
+// dictionary, the usage counts and one zero-filled workspace.
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "fadkv_internal.cuh"
+
+using namespace fadkv;
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+void set_error(const char* where, cudaError_t e)
+{
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+}
+
+// Host-side fault injection for tests: FADKV_FAULT=cuda makes every call
+// that would launch work fail with FADKV_ERR_CUDA before launching anything.
+bool fault_injected()
+{
+    const char* f = getenv("FADKV_FAULT");
+    return f && strcmp(f, "cuda") == 0;
+}
+
+constexpr size_t kAlign = 256;
+constexpr size_t kScoreBudget = size_t(1) << 30;   // bytes of materialised scores per chunk
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {
+    int chunk;   // vectors per dictionary per encode pass
+    size_t counters, scores, pool_id, pool_r, inactive, flagged, total;
+};
+
+Layout make_layout(const fadkv_params& p)
+{
+    Layout L;
+    const size_t per_vec = (size_t)p.num_dicts * (size_t)p.N * sizeof(float);
+    size_t chunk = kScoreBudget / per_vec;
+    if (chunk < 1) chunk = 1;
+    if (chunk > (size_t)p.max_batch) chunk = (size_t)p.max_batch;
+    if (chunk < 1) chunk = 1;
+    L.chunk = (int)chunk;
+    const size_t G = (size_t)p.num_dicts;
+    size_t o = 0;
+    L.counters = o; o = align_up(o + G * kCntFields * sizeof(long long), kAlign);
+    L.scores = o;   o = align_up(o + G * chunk * (size_t)p.N * sizeof(float), kAlign);
+    L.pool_id = o;  o = align_up(o + G * chunk * (size_t)p.n * sizeof(int32_t), kAlign);
+    L.pool_r = o;   o = align_up(o + G * chunk * (size_t)p.n * sizeof(float), kAlign);
+    L.inactive = o; o = align_up(o + G * (size_t)p.N * sizeof(int32_t), kAlign);
+    L.flagged = o;  o = align_up(o + G * (size_t)(p.max_batch > 0 ? p.max_batch : 1) * sizeof(int32_t), kAlign);
+    L.total = o;
+    return L;
+}
+
+fadkv_status check_params(const fadkv_params* p)
+{
+    if (!p) return FADKV_ERR_INVALID_ARG;
+    if (p->num_dicts < 1 || p->N < 1 || p->d < 1 || p->n < 1 || p->s < 1 || p->max_batch < 0)
+        return FADKV_ERR_INVALID_ARG;
+    if (p->s > p->n || p->n > p->N) return FADKV_ERR_INVALID_ARG;
+    if (!(p->lambda_abs >= 0.f) || !(p->lambda_rel >= 0.f)) return FADKV_ERR_INVALID_ARG;
+    if (p->dtype != FADKV_F16 && p->dtype != FADKV_F32) return FADKV_ERR_INVALID_ARG;
+    if (p->num_dicts > FADKV_MAX_DICTS || p->s > FADKV_MAX_S || p->n > FADKV_MAX_POOL)
+        return FADKV_ERR_UNSUPPORTED;
+    if (p->d != 64 && p->d != 128) return FADKV_ERR_UNSUPPORTED;
+    if (p->N % 64 != 0) return FADKV_ERR_UNSUPPORTED;
+    if ((size_t)p->N * sizeof(uint32_t) > 200 * 1024) return FADKV_ERR_UNSUPPORTED;   // Top-n keys in smem
+    if (p->lambda_abs == 0.f && p->lambda_rel == 0.f) {
+        // plain least squares is allowed; positive definiteness then rests on
+        // the selected atoms being linearly independent (status bit if not)
+    }
+    Shape sh{p->num_dicts, p->N, p->d, p->n, p->s, p->dtype, p->lambda_abs, p->lambda_rel};
+    if (greedy_smem_bytes(sh) > 227 * 1024) return FADKV_ERR_UNSUPPORTED;
+    return FADKV_OK;
+}
+
+bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+}  // namespace
+
+struct ProfRec {
+    int cls;
+    cudaEvent_t start, stop;
+};
+
+struct fadkv_dict_s {
+    fadkv_params p;
+    Shape sh;
+    Layout L;
+    void* atoms;
+    int32_t* usage;
+    unsigned char* ws;
+    size_t ws_bytes;
+    DeltaTable delta;
+    bool pending;      // an encode batch waits for its adapt
+    int32_t pending_V;
+    // tracing
+    bool prof_on;
+    int64_t launches[FADKV_PROFILE_KERNELS];
+    double ms[FADKV_PROFILE_KERNELS];
+    std::vector<ProfRec> prof_pending;
+    std::vector<cudaEvent_t> prof_free;
+};
+
+namespace {
+
+long long* counters(fadkv_dict h) { return (long long*)(h->ws + h->L.counters); }
+
+cudaEvent_t prof_event(fadkv_dict h)
+{
+    if (!h->prof_free.empty()) {
+        cudaEvent_t e = h->prof_free.back();
+        h->prof_free.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Brackets one kernel launch for tracing; `launch` returns its cudaError_t.
+template <typename F>
+cudaError_t traced(fadkv_dict h, int cls, cudaStream_t st, F&& launch)
+{
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (h->prof_on) {
+        a = prof_event(h);
+        b = prof_event(h);
+        if (a && b) cudaEventRecord(a, st);
+    }
+    const cudaError_t e = launch();
+    if (e == cudaSuccess) h->launches[cls] += 1;
+    if (a && b) {
+        cudaEventRecord(b, st);
+        h->prof_pending.push_back(ProfRec{cls, a, b});
+    } else {
+        if (a) h->prof_free.push_back(a);
+        if (b) h->prof_free.push_back(b);
+    }
+    return e;
+}
+
+// Screening + Top-n for vectors [v0, v0+Vc) of every dictionary.
+cudaError_t run_pool(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, cudaStream_t st)
+{
+    float* scores = (float*)(h->ws + h->L.scores);
+    int32_t* pid = (int32_t*)(h->ws + h->L.pool_id);
+    float* pr = (float*)(h->ws + h->L.pool_r);
+    cudaError_t e = traced(h, FADKV_K_SCREEN, st, [&] {
+        return launch_screen_ffma(h->sh, h->atoms, x, (int64_t)V * h->p.d, v0, Vc, scores, st);
+    });
+    if (e != cudaSuccess) return e;
+    return traced(h, FADKV_K_TOPN, st, [&] { return launch_topn_radix(h->sh, scores, Vc, pid, pr, st); });
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t fadkv_abi_version(void) { return FADKV_ABI_VERSION; }
+
+const char* fadkv_status_string(fadkv_status s)
+{
+    switch (s) {
+    case FADKV_OK: return "ok";
+    case FADKV_ERR_INVALID_ARG: return "invalid argument";
+    case FADKV_ERR_UNSUPPORTED: return "unsupported shape";
+    case FADKV_ERR_SEQUENCE: return "encode/adapt called out of order";
+    case FADKV_ERR_CUDA: return "CUDA error";
+    case FADKV_ERR_WORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+const char* fadkv_last_error(void) { return g_last_error; }
+
+fadkv_status fadkv_workspace_bytes(const fadkv_params* p, size_t* bytes)
+{
+    if (!bytes) return FADKV_ERR_INVALID_ARG;
+    const fadkv_status st = check_params(p);
+    if (st != FADKV_OK) return st;
+    *bytes = make_layout(*p).total;
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_dict_create(const fadkv_params* p, void* atoms, int32_t* usage, const float* delta,
+                               void* workspace, size_t workspace_bytes, fadkv_dict* out)
+{
+    if (!out) return FADKV_ERR_INVALID_ARG;
+    *out = nullptr;
+    const fadkv_status st = check_params(p);
+    if (st != FADKV_OK) return st;
+    if (!atoms || !usage || !delta || !workspace) return FADKV_ERR_INVALID_ARG;
+    if (!aligned(atoms, 16) || !aligned(usage, 4) || !aligned(workspace, kAlign)) return FADKV_ERR_INVALID_ARG;
+    for (int g = 0; g < p->num_dicts; ++g)
+        if (!(delta[g] >= 0.f)) return FADKV_ERR_INVALID_ARG;
+    const Layout L = make_layout(*p);
+    if (workspace_bytes < L.total) return FADKV_ERR_WORKSPACE;
+    fadkv_dict h = new (std::nothrow) fadkv_dict_s();
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    h->p = *p;
+    h->sh = Shape{p->num_dicts, p->N, p->d, p->n, p->s, p->dtype, p->lambda_abs, p->lambda_rel};
+    h->L = L;
+    h->atoms = atoms;
+    h->usage = usage;
+    h->ws = (unsigned char*)workspace;
+    h->ws_bytes = workspace_bytes;
+    memset(&h->delta, 0, sizeof(h->delta));
+    for (int g = 0; g < p->num_dicts; ++g) h->delta.v[g] = delta[g];
+    h->pending = false;
+    h->pending_V = 0;
+    h->prof_on = false;
+    for (int i = 0; i < FADKV_PROFILE_KERNELS; ++i) {
+        h->launches[i] = 0;
+        h->ms[i] = 0.0;
+    }
+    *out = h;
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_dict_destroy(fadkv_dict h)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    for (auto& r : h->prof_pending) {
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    for (auto e : h->prof_free) cudaEventDestroy(e);
+    delete h;
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_profile_enable(fadkv_dict h, int32_t enable)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    h->prof_on = enable != 0;
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_profile_read(fadkv_dict h, int64_t* launches, double* ms, int32_t reset)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    cudaError_t err = cudaSuccess;
+    for (auto& r : h->prof_pending) {
+        float t = 0.f;
+        cudaError_t e = cudaEventSynchronize(r.stop);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.start, r.stop);
+        if (e == cudaSuccess) h->ms[r.cls] += (double)t;
+        else if (err == cudaSuccess) err = e;
+        h->prof_free.push_back(r.start);
+        h->prof_free.push_back(r.stop);
+    }
+    h->prof_pending.clear();
+    for (int i = 0; i < FADKV_PROFILE_KERNELS; ++i) {
+        if (launches) launches[i] = h->launches[i];
+        if (ms) ms[i] = h->ms[i];
+        if (reset) {
+            h->launches[i] = 0;
+            h->ms[i] = 0.0;
+        }
+    }
+    if (err != cudaSuccess) {
+        set_error("fadkv_profile_read", err);
+        return FADKV_ERR_CUDA;
+    }
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_encode(fadkv_dict h, const void* x, int32_t V, int32_t* idx, float* coef, float* relres,
+                          void* stream)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    if (V < 0 || V > h->p.max_batch) return FADKV_ERR_INVALID_ARG;
+    if (V > 0 && (!x || !idx || !coef || !relres)) return FADKV_ERR_INVALID_ARG;
+    if (V > 0 && (!aligned(x, 16) || !aligned(idx, 4) || !aligned(coef, 4) || !aligned(relres, 4)))
+        return FADKV_ERR_INVALID_ARG;
+    if (h->pending) return FADKV_ERR_SEQUENCE;
+    if (fault_injected()) {
+        set_error("fadkv_encode", cudaErrorLaunchFailure);
+        return FADKV_ERR_CUDA;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    const int chunk = h->L.chunk;
+    for (int v0 = 0; v0 < V; v0 += chunk) {
+        const int Vc = (V - v0 < chunk) ? V - v0 : chunk;
+        cudaError_t e = run_pool(h, x, V, v0, Vc, st);
+        if (e == cudaSuccess) {
+            GreedyArgs a;
+            a.atoms = h->atoms;
+            a.x = x;
+            a.pool_id = (const int32_t*)(h->ws + h->L.pool_id);
+            a.pool_r = (const float*)(h->ws + h->L.pool_r);
+            a.idx = idx;
+            a.coef = coef;
+            a.relres = relres;
+            a.counters = counters(h);
+            a.V = V;
+            a.v0 = v0;
+            a.Vc = Vc;
+            e = traced(h, FADKV_K_GREEDY, st, [&] { return launch_greedy(h->sh, a, st); });
+        }
+        if (e != cudaSuccess) {
+            set_error("fadkv_encode", e);
+            return FADKV_ERR_CUDA;
+        }
+    }
+    h->pending = true;
+    h->pending_V = V;
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_adapt(fadkv_dict h, const void* x, int32_t V, const int32_t* idx, const float* coef,
+                         const float* relres, int32_t* repl_id, float* repl_coef, void* stream)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    if (V < 0 || V > h->p.max_batch) return FADKV_ERR_INVALID_ARG;
+    if (V > 0 && (!x || !idx || !coef || !relres || !repl_id || !repl_coef)) return FADKV_ERR_INVALID_ARG;
+    if (V > 0 && (!aligned(x, 16) || !aligned(repl_id, 4) || !aligned(repl_coef, 4)))
+        return FADKV_ERR_INVALID_ARG;
+    if (!h->pending || h->pending_V != V) return FADKV_ERR_SEQUENCE;
+    if (fault_injected()) {
+        set_error("fadkv_adapt", cudaErrorLaunchFailure);
+        return FADKV_ERR_CUDA;
+    }
+    AdaptArgs a;
+    a.atoms = h->atoms;
+    a.usage = h->usage;
+    a.x = x;
+    a.idx = idx;
+    a.coef = coef;
+    a.relres = relres;
+    a.repl_id = repl_id;
+    a.repl_coef = repl_coef;
+    a.inactive = (int32_t*)(h->ws + h->L.inactive);
+    a.flagged = (int32_t*)(h->ws + h->L.flagged);
+    a.counters = counters(h);
+    a.V = V;
+    cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e = traced(h, FADKV_K_ADAPT, st, [&] { return launch_adapt(h->sh, a, h->delta, st); });
+    if (e != cudaSuccess) {
+        set_error("fadkv_adapt", e);
+        return FADKV_ERR_CUDA;
+    }
+    h->pending = false;
+    h->pending_V = 0;
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_reconstruct(fadkv_dict h, int32_t V, const int32_t* idx, const float* coef,
+                               const int32_t* repl_id, const float* repl_coef, float* xhat, void* stream)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    if (V < 0 || V > h->p.max_batch) return FADKV_ERR_INVALID_ARG;
+    if (V > 0 && (!idx || !coef || !xhat)) return FADKV_ERR_INVALID_ARG;
+    if ((repl_id == nullptr) != (repl_coef == nullptr)) return FADKV_ERR_INVALID_ARG;
+    if (fault_injected()) {
+        set_error("fadkv_reconstruct", cudaErrorLaunchFailure);
+        return FADKV_ERR_CUDA;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e = traced(h, FADKV_K_RECONSTRUCT, st, [&] {
+        return launch_reconstruct(h->sh, h->atoms, V, idx, coef, repl_id, repl_coef, xhat, st);
+    });
+    if (e != cudaSuccess) {
+        set_error("fadkv_reconstruct", e);
+        return FADKV_ERR_CUDA;
+    }
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_dict_stats(fadkv_dict h, int64_t* host_out, void* stream)
+{
+    if (!h || !host_out) return FADKV_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(host_out, counters(h),
+                                    sizeof(long long) * kCntFields * (size_t)h->p.num_dicts,
+                                    cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        set_error("fadkv_dict_stats", e);
+        return FADKV_ERR_CUDA;
+    }
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_debug_pool(fadkv_dict h, const void* x, int32_t V, int32_t* pool, float* pool_r,
+                              void* stream)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    if (V < 0 || V > h->p.max_batch) return FADKV_ERR_INVALID_ARG;
+    if (V > 0 && (!x || !pool || !aligned(x, 16))) return FADKV_ERR_INVALID_ARG;
+    if (fault_injected()) {
+        set_error("fadkv_debug_pool", cudaErrorLaunchFailure);
+        return FADKV_ERR_CUDA;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    const int chunk = h->L.chunk;
+    const size_t G = (size_t)h->p.num_dicts, n = (size_t)h->p.n;
+    for (int v0 = 0; v0 < V; v0 += chunk) {
+        const int Vc = (V - v0 < chunk) ? V - v0 : chunk;
+        cudaError_t e = run_pool(h, x, V, v0, Vc, st);
+        // copy [G][Vc][n] chunk rows into [G][V][n]
+        for (size_t g = 0; g < G && e == cudaSuccess; ++g) {
+            const int32_t* src = (const int32_t*)(h->ws + h->L.pool_id) + g * Vc * n;
+            e = cudaMemcpyAsync(pool + (g * V + v0) * n, src, sizeof(int32_t) * Vc * n,
+                                cudaMemcpyDeviceToDevice, st);
+            if (e == cudaSuccess && pool_r) {
+                const float* srcr = (const float*)(h->ws + h->L.pool_r) + g * Vc * n;
+                e = cudaMemcpyAsync(pool_r + (g * V + v0) * n, srcr, sizeof(float) * Vc * n,
+                                    cudaMemcpyDeviceToDevice, st);
+            }
+        }
+        if (e != cudaSuccess) {
+            set_error("fadkv_debug_pool", e);
+            return FADKV_ERR_CUDA;
+        }
+    }
+    return FADKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,209 @@
+// Fixed-size dictionary adaptation and sparse reconstruction.
+//
+// "FAD-KV: Adaptive Dictionary KV Caching for Efficient Reasoning
+// Decoding": abstract (a fixed-size dictionary adaptation mechanism reuses
+// inactive atoms instead of expanding the dictionary; each token's KV state
+// is a sparse combination of atoms), Fig. 2 caption (if the reconstruction
+// error is high, an inactive atom is replaced by a context-relevant atom and
+// the dictionary size stays fixed) and Table 5 (delta = 0.50 key / 0.70
+// value).  The replacement order is a convention of this library: the m-th
+// flagged vector (ascending index) takes the m-th inactive atom (ascending
+// index), which block-wide ordered compactions produce deterministically --
+// never the order in which atomics happen to land.
+#include "fadkv_internal.cuh"
+
+namespace fadkv {
+namespace {
+
+constexpr int kAdaptThreads = 1024;
+constexpr int kAdaptWarps = kAdaptThreads / 32;
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Ordered compaction over [0, count): out[pos] = i for every i with pred(i),
+// in ascending i.  Returns the number kept.  Whole block must call it.
+template <typename Pred>
+__device__ int block_compact(int count, Pred pred, int32_t* out, int* ws)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int base = 0;
+    for (int i0 = 0; i0 < count; i0 += kAdaptThreads) {
+        const int i = i0 + tid;
+        const int f = (i < count && pred(i)) ? 1 : 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, f);
+        if (lane == 0) ws[warp] = __popc(bal);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int w = 0; w < kAdaptWarps; ++w) {
+            const int c = ws[w];
+            before += (w < warp) ? c : 0;
+            total += c;
+        }
+        if (f) out[base + before + __popc(bal & ((1u << lane) - 1u))] = i;
+        base += total;
+        __syncthreads();
+    }
+    return base;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kAdaptThreads)
+adapt_kernel(Shape sh, AdaptArgs a, DeltaTable delta, int max_batch)
+{
+    __shared__ int ws[kAdaptWarps];
+    const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int N = sh.N, s = sh.s, V = a.V;
+    T* atoms = (T*)a.atoms + (size_t)g * N * D;
+    int32_t* usage = a.usage + (size_t)g * N;
+    const int32_t* idx = a.idx + (size_t)g * V * s;
+    const float* coef = a.coef + (size_t)g * V * s;
+    const float* relres = a.relres + (size_t)g * V;
+    const T* X = (const T*)a.x + (size_t)g * V * D;
+    int32_t* repl_id = a.repl_id + (size_t)g * V;
+    float* repl_coef = a.repl_coef + (size_t)g * V;
+    int32_t* inactive = a.inactive + (size_t)g * N;
+    int32_t* flagged = a.flagged + (size_t)g * max_batch;
+    long long* cnt = a.counters + (size_t)g * kCntFields;
+    const float dg = delta.v[g];
+
+    // 1. usage += 1 for every selected atom; default "no replacement"
+    for (int i = tid; i < V * s; i += kAdaptThreads) {
+        const int j = idx[i];
+        if (j >= 0 && j < N) atomicAdd(&usage[j], 1);
+    }
+    for (int v = tid; v < V; v += kAdaptThreads) {
+        repl_id[v] = -1;
+        repl_coef[v] = 0.f;
+    }
+    __syncthreads();
+
+    // 2. inactive atoms in ascending id; 3. flagged vectors in ascending v
+    const int nL = block_compact(N, [&](int j) { return usage[j] == 0; }, inactive, ws);
+    const int nF = block_compact(V, [&](int v) { return relres[v] > dg; }, flagged, ws);
+    const int m = min(nL, nF);
+
+    // 4. the r-th flagged vector takes the r-th inactive atom (one warp each).
+    //    The residual reads only atoms selected in this batch (usage >= 1),
+    //    never an atom being overwritten (usage == 0 after step 1).
+    constexpr int PL = D / 32;
+    for (int r = warp; r < m; r += kAdaptWarps) {
+        const int v = flagged[r], j = inactive[r];
+        float e[PL];
+#pragma unroll
+        for (int q = 0; q < PL; ++q) e[q] = to_f32(X[(size_t)v * D + lane + 32 * q]);
+        for (int k = 0; k < s; ++k) {
+            const int sj = idx[(size_t)v * s + k];
+            if (sj < 0 || sj >= N) continue;
+            const float c = coef[(size_t)v * s + k];
+#pragma unroll
+            for (int q = 0; q < PL; ++q)
+                e[q] = fmaf(-c, to_f32(atoms[(size_t)sj * D + lane + 32 * q]), e[q]);
+        }
+        float sq = 0.f;
+#pragma unroll
+        for (int q = 0; q < PL; ++q) sq = fmaf(e[q], e[q], sq);
+        const float nrm = sqrtf(warp_sum(sq));
+#pragma unroll
+        for (int q = 0; q < PL; ++q)
+            atoms[(size_t)j * D + lane + 32 * q] = from_f32<T>(nrm > 0.f ? e[q] / nrm : 0.f);
+        if (lane == 0) {
+            usage[j] = 1;
+            repl_id[v] = j;
+            repl_coef[v] = nrm;
+        }
+    }
+    if (tid == 0) {
+        cnt[kCntEncoded] += V;
+        cnt[kCntReplaced] += m;
+        cnt[kCntFlagged] += nF;
+        cnt[kCntOverflow] += nF - m;
+    }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+reconstruct_kernel(const T* __restrict__ atoms, int G, int N, int s, int V, const int32_t* __restrict__ idx,
+                   const float* __restrict__ coef, const int32_t* __restrict__ repl_id,
+                   const float* __restrict__ repl_coef, float* __restrict__ xhat)
+{
+    constexpr int PL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long gv = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gv >= (long long)G * V) return;
+    const int g = (int)(gv / V);
+    const T* A = atoms + (size_t)g * N * D;
+    float acc[PL];
+#pragma unroll
+    for (int q = 0; q < PL; ++q) acc[q] = 0.f;
+    for (int k = 0; k < s; ++k) {
+        const int j = idx[gv * s + k];
+        if (j < 0 || j >= N) continue;
+        const float c = coef[gv * s + k];
+#pragma unroll
+        for (int q = 0; q < PL; ++q) acc[q] = fmaf(c, to_f32(A[(size_t)j * D + lane + 32 * q]), acc[q]);
+    }
+    if (repl_id) {
+        const int j = repl_id[gv];
+        if (j >= 0 && j < N) {
+            const float c = repl_coef[gv];
+#pragma unroll
+            for (int q = 0; q < PL; ++q) acc[q] = fmaf(c, to_f32(A[(size_t)j * D + lane + 32 * q]), acc[q]);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < PL; ++q) xhat[gv * D + lane + 32 * q] = acc[q];
+}
+
+template <typename T, int D>
+cudaError_t adapt_t(const Shape& sh, const AdaptArgs& a, const DeltaTable& delta, int max_batch,
+                    cudaStream_t st)
+{
+    adapt_kernel<T, D><<<sh.G, kAdaptThreads, 0, st>>>(sh, a, delta, max_batch);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t reconstruct_t(const Shape& sh, const void* atoms, int V, const int32_t* idx, const float* coef,
+                          const int32_t* repl_id, const float* repl_coef, float* xhat, cudaStream_t st)
+{
+    const long long warps = (long long)sh.G * V;
+    const unsigned blocks = (unsigned)((warps + 7) / 8);
+    reconstruct_kernel<T, D><<<blocks, 256, 0, st>>>((const T*)atoms, sh.G, sh.N, sh.s, V, idx, coef,
+                                                     repl_id, repl_coef, xhat);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_adapt(const Shape& sh, const AdaptArgs& a, const DeltaTable& delta, cudaStream_t st)
+{
+    // flagged scratch holds max_batch entries per dictionary; V <= max_batch
+    // is checked on the host, so the stride V is a valid lower bound here.
+    const int stride = a.V > 0 ? a.V : 1;
+    if (sh.dtype == FADKV_F16) {
+        if (sh.d == 128) return adapt_t<__half, 128>(sh, a, delta, stride, st);
+        return adapt_t<__half, 64>(sh, a, delta, stride, st);
+    }
+    if (sh.d == 128) return adapt_t<float, 128>(sh, a, delta, stride, st);
+    return adapt_t<float, 64>(sh, a, delta, stride, st);
+}
+
+cudaError_t launch_reconstruct(const Shape& sh, const void* atoms, int V, const int32_t* idx,
+                               const float* coef, const int32_t* repl_id, const float* repl_coef,
+                               float* xhat, cudaStream_t st)
+{
+    if (V <= 0) return cudaSuccess;
+    if (sh.dtype == FADKV_F16) {
+        if (sh.d == 128) return reconstruct_t<__half, 128>(sh, atoms, V, idx, coef, repl_id, repl_coef, xhat, st);
+        return reconstruct_t<__half, 64>(sh, atoms, V, idx, coef, repl_id, repl_coef, xhat, st);
+    }
+    if (sh.d == 128) return reconstruct_t<float, 128>(sh, atoms, V, idx, coef, repl_id, repl_coef, xhat, st);
+    return reconstruct_t<float, 64>(sh, atoms, V, idx, coef, repl_id, repl_coef, xhat, st);
+}
+
+}  // namespace fadkv

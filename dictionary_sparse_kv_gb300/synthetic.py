@@ -141,3 +141,95 @@ class DriftingSources:
             fresh /= np.linalg.norm(fresh, axis=1, keepdims=True)
             self._src[rows] = fresh
         return self._src
+
+
+# ---------------------------------------------------------------------------
+# Named workloads: shapes and input recipes of the FAD-KV decode / prefill
+# settings (Table 5 shapes; Llama-3.2-3B: 28 layers, Llama-3.1-8B: 32 layers,
+# 8 KV heads, head dimension 128).  Dictionary g = 2*layer + {0: key, 1: value}.
+# ---------------------------------------------------------------------------
+
+from dataclasses import dataclass, field
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    G: int                 # dictionaries (layers x {K, V})
+    N: int
+    d: int
+    n: int
+    s: int
+    V: int                 # vectors per dictionary per step
+    steps: int
+    dtype: type = np.float16
+    inactive: float = 0.30           # initial inactive fraction (or count if >= 1)
+    kind: str = "mixture"            # "mixture" (Student-t + off-dictionary part) or "tiny"
+    off_frac: float = 0.05
+    sigma: float = 0.01
+    drift_period: int = 0            # >0: sources drift every drift_period steps
+    drift_frac: float = 0.10
+    seed: int = 0
+    deltas: tuple = field(default=())
+
+    def delta(self, g: int) -> float:
+        if self.deltas:
+            return self.deltas[g]
+        return 0.50 if g % 2 == 0 else 0.70   # Table 5: key 0.50, value 0.70
+
+    @property
+    def n_inactive(self) -> int:
+        return int(self.inactive) if self.inactive >= 1 else int(round(self.inactive * self.N))
+
+
+WORKLOADS = {
+    # d=64, N=512 fp32, n=32, s=4, 256 vectors, 16 inactive atoms, delta 0.5
+    "tiny": Workload("tiny", 1, 512, 64, 32, 4, 256, 1, np.float32, inactive=16, kind="tiny",
+                     deltas=(0.5,)),
+    # Llama-3.2-3B decode step: 28 layers x {K,V}, 8 KV heads x 16 sequences
+    "decode_3b": Workload("decode_3b", 56, 4096, 128, 256, 8, 128, 1024, seed=2),
+    # Llama-3.2-3B prefill at 16K context: 16384 tokens x 8 heads per dictionary
+    "prefill_3b_16k": Workload("prefill_3b_16k", 2, 4096, 128, 256, 8, 131072, 1, seed=3),
+    # Llama-3.1-8B decode step: 32 layers x {K,V}, 8 KV heads x 64 sequences
+    "decode_8b": Workload("decode_8b", 64, 8192, 128, 512, 16, 512, 1024, seed=4),
+    # adaptation stress: one K and one V dictionary, 8 heads x 32 sequences,
+    # generating subspace drifts every 128 steps (10% of sources replaced)
+    "adapt_stress": Workload("adapt_stress", 2, 4096, 128, 256, 8, 256, 2048, seed=5,
+                             drift_period=128, drift_frac=0.10),
+}
+
+
+class WorkloadData:
+    """Initial dictionaries, usage counts and per-step inputs of a workload,
+    restricted to a subset of its dictionaries if asked."""
+
+    def __init__(self, w: Workload, dicts=None):
+        self.w = w
+        self.dicts = list(range(w.G)) if dicts is None else list(dicts)
+        self.atoms = np.stack([make_dictionary(w.N, w.d, w.dtype, w.seed, 1, g) for g in self.dicts])
+        self.usage = np.stack([make_usage(w.N, w.n_inactive, w.seed, 2, g) for g in self.dicts])
+        if w.kind == "tiny":
+            self._sources = [self.atoms[i] for i in range(len(self.dicts))]
+        else:
+            self._sources = [self.atoms[i][self.usage[i] > 0] for i in range(len(self.dicts))]
+        self._drift = None
+        if w.drift_period > 0:
+            self._drift = [DriftingSources(self._sources[i], w.drift_period, w.drift_frac, w.seed, 3, g)
+                           for i, g in enumerate(self.dicts)]
+
+    def deltas(self):
+        return [self.w.delta(g) for g in self.dicts]
+
+    def inputs(self, step: int, V: int | None = None) -> np.ndarray:
+        """[len(dicts)][V][d] inputs of decode step ``step``."""
+        w = self.w
+        V = w.V if V is None else V
+        out = []
+        for i, g in enumerate(self.dicts):
+            src = self._drift[i].sources_at(step) if self._drift else self._sources[i]
+            if w.kind == "tiny":
+                out.append(make_tiny_inputs(src, V, w.s, w.seed, 4, g, step, sigma=w.sigma, dtype=w.dtype))
+            else:
+                out.append(make_sparse_inputs(src, V, w.s, w.seed, 4, g, step, off_frac=w.off_frac,
+                                              dtype=w.dtype))
+        return np.ascontiguousarray(np.stack(out))

@@ -1,0 +1,215 @@
+/*
+ * fadkv.h -- C ABI of the FAD-KV per-token KV encoding library (sm_103a).
+ *
+ * What it computes comes from "FAD-KV: Adaptive Dictionary KV Caching for
+ * Efficient Reasoning Decoding" (thelatestinai.com/papers/2610.37921):
+ *   - abstract: each token's key or value head-vector is represented as a
+ *     sparse combination of dictionary atoms; a screening-based sparse coder
+ *     makes a one-shot Top-n selection of a small candidate pool and then
+ *     refines coefficients; a fixed-size adaptation reuses inactive atoms
+ *     instead of growing the dictionary;
+ *   - Fig. 2 caption: if the reconstruction error of an incoming vector is
+ *     high, an inactive atom is replaced by a context-relevant atom, keeping
+ *     the dictionary size fixed throughout decoding;
+ *   - Table 5: ridge parameter 1e-4 + 0.20 diag(G), thresholds 0.50 (key) /
+ *     0.70 (value), N = 4096 / 8192, s = 8 / 16, n = 256 / 512.
+ * Conventions the pages leave open, fixed by this library:
+ *   - the s atoms are chosen greedily inside the pool: at step k the atom of
+ *     the pool (not yet chosen) with the largest |<d_j, e_k>| is added, the
+ *     coefficients are refit by the ridge solve, e_{k+1} = x - D_S c;
+ *   - every tie (Top-n cut, greedy choice) goes to the lower atom index;
+ *   - replacement order: the m-th flagged vector of a call (ascending vector
+ *     index, relres > delta strictly) takes the m-th inactive atom (ascending
+ *     atom index, usage == 0 after the call's usage increments);
+ *   - the replacement atom is the normalised ridge residual e/||e||; the
+ *     vector gets it as an extra term with coefficient ||e||.
+ *
+ * Memory and threading model
+ *   - Every array argument is a DEVICE pointer unless stated otherwise.  The
+ *     caller owns all device memory (dictionary, usage counts, workspace,
+ *     inputs, outputs); the library never allocates or frees device memory.
+ *   - A handle covers G = num_dicts independent dictionaries of the same
+ *     shape, stored back to back, so one call encodes a whole decode step
+ *     (all layers, keys and values) in one launch per kernel.
+ *     Layouts (row-major, dictionary-major):
+ *       atoms     [G][N][d]   binary16 or binary32 (params.dtype)
+ *       usage     [G][N]      int32
+ *       x         [G][V][d]   same type as atoms
+ *       idx       [G][V][s]   int32, pick order; -1 for a non-finite input
+ *       coef      [G][V][s]   float32
+ *       relres    [G][V]      float32, ||x - D_S c|| / ||x||  (0 if x = 0)
+ *       repl_id   [G][V]      int32, replacement atom or -1
+ *       repl_coef [G][V]      float32
+ *       xhat      [G][V][d]   float32
+ *   - All calls are asynchronous on the given CUDA stream (a cudaStream_t
+ *     passed as void*; NULL = legacy default stream).  A handle is not
+ *     thread-safe: issue its calls from one thread, in stream order.
+ *   - Every encode batch must be passed to fadkv_adapt before the next
+ *     encode or adapt on the same handle (otherwise the usage counts would
+ *     miss that batch and an atom in use could be overwritten).  The host
+ *     enforces this and returns FADKV_ERR_SEQUENCE.
+ *
+ * Errors
+ *   - Functions return a fadkv_status; nothing is thrown across the ABI.
+ *   - Argument errors are detected on the host before any launch, and leave
+ *     the handle's state unchanged.
+ *   - Conditions found on the device (non-finite input, a refit matrix that
+ *     is not positive definite) set bits in the per-dictionary device status
+ *     word, read back by fadkv_dict_stats after a stream sync.
+ */
+#ifndef FADKV_H
+#define FADKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FADKV_ABI_VERSION 1
+#define FADKV_MAX_DICTS 256   /* dictionaries per handle */
+#define FADKV_MAX_S 32        /* largest sparsity s */
+#define FADKV_MAX_POOL 1024   /* largest pool size n */
+
+typedef enum {
+    FADKV_OK = 0,
+    FADKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+    FADKV_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels implement */
+    FADKV_ERR_SEQUENCE = 3,      /* encode/adapt called out of order */
+    FADKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    FADKV_ERR_WORKSPACE = 5      /* workspace too small */
+} fadkv_status;
+
+typedef enum { FADKV_F16 = 0, FADKV_F32 = 1 } fadkv_dtype;
+
+/* Device status word bits (per dictionary, see fadkv_dict_stats). */
+#define FADKV_DEV_NONFINITE_INPUT 0x1   /* an input held a NaN or infinity */
+#define FADKV_DEV_NOT_SPD 0x2           /* a refit matrix lost positive definiteness */
+
+typedef struct {
+    int32_t num_dicts;   /* G, 1 .. FADKV_MAX_DICTS */
+    int32_t N;           /* atoms per dictionary, multiple of 64 */
+    int32_t d;           /* head dimension: 64 or 128 */
+    int32_t n;           /* Top-n pool size, s <= n <= min(N, FADKV_MAX_POOL) */
+    int32_t s;           /* atoms per vector, 1 .. FADKV_MAX_S */
+    float lambda_abs;    /* ridge, absolute part (Table 5: 1e-4) */
+    float lambda_rel;    /* ridge, part relative to diag(G) (Table 5: 0.20) */
+    int32_t dtype;       /* fadkv_dtype of atoms and inputs */
+    int32_t max_batch;   /* largest V (vectors per dictionary) of one call */
+} fadkv_params;
+
+typedef struct fadkv_dict_s* fadkv_dict;
+
+/* Version of this ABI (FADKV_ABI_VERSION of the built library). */
+int32_t fadkv_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* fadkv_status_string(fadkv_status status);
+
+/* Message of the last CUDA error seen by a call on this host thread
+   (static thread-local buffer; "" if none). */
+const char* fadkv_last_error(void);
+
+/* Bytes of device workspace a handle with these parameters needs.
+   Host-only; writes *bytes.  Errors: INVALID_ARG, UNSUPPORTED. */
+fadkv_status fadkv_workspace_bytes(const fadkv_params* params, size_t* bytes);
+
+/* Create a handle over caller-owned device memory.
+     atoms      [G][N][d] dictionary (mutated by fadkv_adapt), 16-byte aligned
+     usage      [G][N] usage counts (mutated by fadkv_adapt); an atom is
+                inactive while its count is 0
+     delta      HOST array [G] of adaptation thresholds (Table 5: 0.50 for a
+                key dictionary, 0.70 for a value dictionary); copied
+     workspace  device buffer of at least fadkv_workspace_bytes bytes,
+                256-byte aligned, ZERO-FILLED before this call (it holds the
+                per-dictionary counters); owned by the caller, used by the
+                handle until fadkv_dict_destroy
+   Host-only: makes no CUDA call.  Errors: INVALID_ARG, UNSUPPORTED,
+   WORKSPACE. */
+fadkv_status fadkv_dict_create(const fadkv_params* params, void* atoms, int32_t* usage,
+                               const float* delta, void* workspace, size_t workspace_bytes,
+                               fadkv_dict* out);
+
+/* Free the host-side handle.  Device memory stays with the caller.
+   The caller must make sure no work of this handle is still running. */
+fadkv_status fadkv_dict_destroy(fadkv_dict dict);
+
+/* Encode V vectors per dictionary (abstract; Fig. 2 caption: screening-based
+   sparse coding).  For every x: scores r = D x; pool P = the n atoms with the
+   largest |r_j| (ties to the lower j); s greedy picks inside P with the ridge
+   refit (G + diag(lambda_abs + lambda_rel G_ii)) c = D_S x after each pick;
+   relres = ||x - D_S c|| / ||x||.
+     x [G][V][d]; outputs idx [G][V][s], coef [G][V][s], relres [G][V].
+   0 <= V <= max_batch.  Every vector is encoded against the dictionary as it
+   stands at the start of the call.  A vector holding a NaN or infinity gets
+   idx = -1, coef = 0, relres = NaN and sets FADKV_DEV_NONFINITE_INPUT.
+   Errors: INVALID_ARG, SEQUENCE (previous encode not adapted yet), CUDA. */
+fadkv_status fadkv_encode(fadkv_dict dict, const void* x, int32_t V, int32_t* idx, float* coef,
+                          float* relres, void* stream);
+
+/* Fixed-size adaptation of the batch just encoded (abstract; Fig. 2 caption).
+   usage[idx] += 1 for every selected atom; then the m-th vector with
+   relres > delta[g] (ascending v) takes the m-th atom with usage == 0
+   (ascending id): that atom becomes e/||e|| with e = x - D_S c (rounded to
+   the dictionary type), its usage becomes 1, repl_id[v] = its id and
+   repl_coef[v] = ||e||.  Other vectors get repl_id = -1, repl_coef = 0.
+   Flagged vectors left without an inactive atom keep their s-term code and
+   are counted as overflow.  The dictionary keeps N atoms.
+   Arguments are the same x, V, idx, coef, relres as the encode call.
+   Errors: INVALID_ARG, SEQUENCE (no encode pending, or a different V), CUDA. */
+fadkv_status fadkv_adapt(fadkv_dict dict, const void* x, int32_t V, const int32_t* idx,
+                         const float* coef, const float* relres, int32_t* repl_id,
+                         float* repl_coef, void* stream);
+
+/* Sparse reconstruction (abstract: a sparse combination of atoms):
+   xhat_v = sum_k coef[v][k] d_{idx[v][k]} + repl_coef[v] d_{repl_id[v]}.
+   repl_id / repl_coef may both be NULL (no replacement terms); entries with
+   idx or repl_id = -1 are skipped.  Valid for any code produced earlier by
+   encode + adapt: atoms in use are never overwritten.
+   Errors: INVALID_ARG, CUDA. */
+fadkv_status fadkv_reconstruct(fadkv_dict dict, int32_t V, const int32_t* idx, const float* coef,
+                               const int32_t* repl_id, const float* repl_coef, float* xhat,
+                               void* stream);
+
+/* Per-dictionary counters, copied to HOST memory host_out[G][FADKV_STATS_FIELDS];
+   synchronises the stream.  Fields, in order: vectors encoded (adapted),
+   atoms replaced, flagged vectors, overflow (flagged without an inactive
+   atom), non-finite inputs, Top-n slow-path uses, device status word, 0.
+   Errors: INVALID_ARG, CUDA. */
+#define FADKV_STATS_FIELDS 8
+fadkv_status fadkv_dict_stats(fadkv_dict dict, int64_t* host_out, void* stream);
+
+/* Test hook: the Top-n pool of each x without changing any state.
+   pool [G][V][n] int32 in ascending atom order (-1 for a non-finite input);
+   pool_r (may be NULL) [G][V][n] float32 screening scores of those atoms.
+   Errors: INVALID_ARG, CUDA. */
+fadkv_status fadkv_debug_pool(fadkv_dict dict, const void* x, int32_t V, int32_t* pool,
+                              float* pool_r, void* stream);
+
+/* Kernel classes reported by fadkv_profile_read. */
+#define FADKV_PROFILE_KERNELS 8
+#define FADKV_K_SCREEN 0       /* screening scores */
+#define FADKV_K_TOPN 1         /* Top-n pool selection */
+#define FADKV_K_GREEDY 2       /* in-pool greedy selection + ridge refit */
+#define FADKV_K_ADAPT 3        /* fixed-size adaptation */
+#define FADKV_K_RECONSTRUCT 4  /* sparse reconstruction */
+
+/* Tracing.  The library always counts its kernel launches per class.  With
+   profiling enabled it also brackets every launch with a pair of CUDA events
+   recorded on the launch stream and accumulates the device time between
+   them.  Not for use inside CUDA-graph capture.  Errors: INVALID_ARG. */
+fadkv_status fadkv_profile_enable(fadkv_dict dict, int32_t enable);
+
+/* Launch counts and device milliseconds per kernel class since the last
+   reset, written to HOST arrays launches[FADKV_PROFILE_KERNELS] and
+   ms[FADKV_PROFILE_KERNELS] (either may be NULL).  Waits for the recorded
+   events.  reset != 0 clears the accumulators afterwards.
+   Errors: INVALID_ARG, CUDA. */
+fadkv_status fadkv_profile_read(fadkv_dict dict, int64_t* launches, double* ms, int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FADKV_H */

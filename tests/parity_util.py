@@ -1,0 +1,96 @@
+"""Comparison of the CUDA library with the CPU oracle on the same inputs.
+
+Tolerances (the spec of this library):
+  * pool ids, selected ids and replacement ids are compared exactly, except
+    for vectors the oracle itself shows to sit on a near tie: the relative
+    gap at the Top-n cut, (|r|_(n) - |r|_(n+1)) / |r|_(n), below 1e-5, or a
+    greedy step whose best and runner-up correlations differ by less than
+    1e-5 relative.  fp32 accumulation cannot order such pairs reliably;
+  * coefficients: ||c_gpu - c_oracle|| <= 1e-3 ||c_oracle|| per vector;
+  * relres: |rho_gpu - rho_oracle| <= 1e-3 rho_oracle;
+  * replaced atoms: every element within one binary16 (or binary32) ulp of
+    the oracle's rounding (the GPU rounds an fp32 value, the oracle a double);
+  * reconstruction: ||xhat_gpu - xhat_oracle|| <= 1e-5 ||xhat_oracle|| + 1e-6.
+"""
+from __future__ import annotations
+
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+from oracle import oracle as O
+
+CUT_GAP = 1e-5
+PICK_GAP = 1e-5
+COEF_TOL = 1e-3
+RELRES_TOL = 1e-3
+XHAT_TOL = 1e-5
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+def oparams(w, dtype=None):
+    dt = w.dtype if dtype is None else dtype
+    return O.Params(w.N, w.d, w.n, w.s, 1e-4, 0.20, O.F16 if dt == np.float16 else O.F32)
+
+
+@dataclass
+class EncodeReport:
+    checked: int
+    exempt: int
+    mismatched_idx: list
+    worst_coef: float
+    worst_relres: float
+
+
+def exempt_mask(res: O.EncodeResult) -> np.ndarray:
+    return (res.cut_gap < CUT_GAP) | (res.pick_gap.min(axis=1) < PICK_GAP)
+
+
+def compare_encode(res: O.EncodeResult, idx, coef, relres) -> EncodeReport:
+    """res: oracle result for V vectors; idx/coef/relres: GPU arrays [V]..."""
+    ex = exempt_mask(res)
+    bad = []
+    worst_c = 0.0
+    worst_r = 0.0
+    for v in range(len(ex)):
+        if ex[v]:
+            continue
+        if not np.array_equal(idx[v], res.idx[v]):
+            bad.append(v)
+            continue
+        if res.idx[v][0] < 0:           # non-finite input
+            assert np.isnan(relres[v])
+            continue
+        co = res.coef[v]
+        cn = np.linalg.norm(co)
+        dc = np.linalg.norm(coef[v].astype(np.float64) - co)
+        worst_c = max(worst_c, dc / cn if cn > 0 else dc)
+        ro = res.relres[v]
+        dr = abs(float(relres[v]) - ro)
+        worst_r = max(worst_r, dr / ro if ro > 0 else dr)
+    return EncodeReport(len(ex) - int(ex.sum()), int(ex.sum()), bad, worst_c, worst_r)
+
+
+def assert_encode_ok(rep: EncodeReport, max_exempt_frac=0.05):
+    assert not rep.mismatched_idx, f"selected ids differ on vectors {rep.mismatched_idx[:10]}"
+    assert rep.worst_coef <= COEF_TOL, rep.worst_coef
+    assert rep.worst_relres <= RELRES_TOL, rep.worst_relres
+    total = rep.checked + rep.exempt
+    assert rep.exempt <= max(2, max_exempt_frac * total), f"{rep.exempt} of {total} vectors exempt"
+
+
+def ulp(a: np.ndarray) -> np.ndarray:
+    """Spacing of the storage type at |a| (binary16 or binary32)."""
+    return np.spacing(np.abs(a).astype(a.dtype)).astype(np.float64)
+
+
+def compare_atoms(gpu: np.ndarray, orc: np.ndarray, rows) -> float:
+    """Max deviation in ulps over the given rows."""
+    worst = 0.0
+    for j in rows:
+        g = gpu[j].astype(np.float64)
+        o = orc[j].astype(np.float64)
+        u = np.maximum(ulp(orc[j]), ulp(gpu[j]))
+        worst = max(worst, float(np.max(np.abs(g - o) / u)))
+    return worst

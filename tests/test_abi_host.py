@@ -1,0 +1,127 @@
+"""C-ABI library: loads without a GPU, exports every declared symbol, and its
+host-side logic (argument checks, sequence contract, workspace sizing, fault
+injection) behaves as include/fadkv.h documents.  No call here launches work."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from dictionary_sparse_kv_gb300 import build as B
+from dictionary_sparse_kv_gb300 import fadkv as F
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fadkv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return F.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fadkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 11
+    for name in names:
+        assert hasattr(L, name), name
+    raw = C.CDLL(F.LIB_PATH)
+    for name in names:
+        C.cast(getattr(raw, name), C.c_void_p)
+
+
+def test_version_and_strings(L):
+    assert F.abi_version() == 1
+    assert F.status_string(0) == "ok"
+    assert F.status_string(3) == "encode/adapt called out of order"
+
+
+def test_param_validation(L):
+    ok = F.params(56, 4096, 128, 256, 8, F.F16, 128)
+    assert F.workspace_bytes(ok) > 0
+    bad = [
+        F.params(0, 4096, 128, 256, 8),            # no dictionaries
+        F.params(1, 4096, 128, 4, 8),              # s > n
+        F.params(1, 128, 128, 256, 8),             # n > N
+        F.params(1, 4096, 128, 256, 8, dtype=7),
+        F.params(1, 4096, 128, 256, 8, lambda_abs=-1.0),
+    ]
+    for p in bad:
+        with pytest.raises(F.FadkvError) as e:
+            F.workspace_bytes(p)
+        assert e.value.status == 1
+    unsupported = [
+        F.params(1, 4096, 96, 256, 8),             # d not 64/128
+        F.params(1, 4096, 128, 256, 33),           # s above the maximum
+        F.params(1, 4096, 128, 2048, 8),           # n above the maximum
+        F.params(1, 4000, 128, 256, 8),            # N not a multiple of 64
+        F.params(300, 4096, 128, 256, 8),          # too many dictionaries
+    ]
+    for p in unsupported:
+        with pytest.raises(F.FadkvError) as e:
+            F.workspace_bytes(p)
+        assert e.value.status == 2
+
+
+def test_workspace_grows_with_batch(L):
+    a = F.workspace_bytes(F.params(2, 4096, 128, 256, 8, F.F16, 128))
+    b = F.workspace_bytes(F.params(2, 4096, 128, 256, 8, F.F16, 4096))
+    assert b > a
+
+
+def test_create_checks_without_gpu(L):
+    p = F.params(2, 512, 64, 32, 4, F.F32, 16)
+    ws = F.workspace_bytes(p)
+    fake = 0x10000   # never dereferenced: create makes no CUDA call
+    h = F.dict_create(p, fake, fake, [0.5, 0.7], fake, ws)
+    try:
+        # workspace too small
+        with pytest.raises(F.FadkvError) as e:
+            F.dict_create(p, fake, fake, [0.5, 0.7], fake, ws - 1)
+        assert e.value.status == 5
+        # misaligned dictionary / workspace
+        with pytest.raises(F.FadkvError):
+            F.dict_create(p, fake + 4, fake, [0.5, 0.7], fake, ws)
+        with pytest.raises(F.FadkvError):
+            F.dict_create(p, fake, fake, [0.5, 0.7], fake + 16, ws)
+        # negative threshold
+        with pytest.raises(F.FadkvError):
+            F.dict_create(p, fake, fake, [0.5, -0.1], fake, ws)
+        # sequence: adapt before any encode
+        with pytest.raises(F.FadkvError) as e:
+            F.adapt(h, fake, 4, fake, fake, fake, fake, fake, stream=0)
+        assert e.value.status == 3
+        # batch above max_batch
+        with pytest.raises(F.FadkvError) as e:
+            F.encode(h, fake, 17, fake, fake, fake, stream=0)
+        assert e.value.status == 1
+        # repl_id without repl_coef
+        with pytest.raises(F.FadkvError) as e:
+            F.reconstruct(h, 4, fake, fake, fake, None, fake, stream=0)
+        assert e.value.status == 1
+    finally:
+        F.dict_destroy(h)
+
+
+def test_fault_injection_leaves_state(L, monkeypatch):
+    p = F.params(1, 512, 64, 32, 4, F.F32, 16)
+    ws = F.workspace_bytes(p)
+    fake = 0x10000
+    h = F.dict_create(p, fake, fake, [0.5], fake, ws)
+    try:
+        monkeypatch.setenv("FADKV_FAULT", "cuda")
+        with pytest.raises(F.FadkvError) as e:
+            F.encode(h, fake, 4, fake, fake, fake, stream=0)
+        assert e.value.status == 4
+        assert "fadkv_encode" in F.last_error()
+        # the failed encode did not advance the sequence: adapt still refused
+        with pytest.raises(F.FadkvError) as e:
+            F.adapt(h, fake, 4, fake, fake, fake, fake, fake, stream=0)
+        assert e.value.status == 3
+    finally:
+        F.dict_destroy(h)
