@@ -230,10 +230,38 @@ static int ridge_refit(const double* D, int d, const int32_t* S, int k,
 /* matrix was not positive definite (never expected with lambda_abs > 0).  */
 /* ---------------------------------------------------------------------- */
 
+static int encode_impl(const oracle_params* p, const void* atoms, const void* xin,
+                       int32_t V, int32_t* idx, double* coef, double* relres,
+                       int32_t* pool, double* cut_gap, double* pick_gap,
+                       int64_t* macs, int32_t full_omp, const int32_t* pool_in);
+
 int oracle_encode(const oracle_params* p, const void* atoms, const void* xin,
                   int32_t V, int32_t* idx, double* coef, double* relres,
                   int32_t* pool, double* cut_gap, double* pick_gap,
                   int64_t* macs, int32_t full_omp)
+{
+    return encode_impl(p, atoms, xin, V, idx, coef, relres, pool, cut_gap, pick_gap,
+                       macs, full_omp, NULL);
+}
+
+/* Steps 3-4 only, on a pool given per vector (pool_in [V][n], any order):
+   the greedy selection and refit of a vector whose pool is already known.
+   Used to check a candidate pool that differs from the oracle's own only
+   inside a near tie at the Top-n cut. */
+int oracle_greedy_on_pool(const oracle_params* p, const void* atoms, const void* xin,
+                          int32_t V, const int32_t* pool_in, int32_t* idx, double* coef,
+                          double* relres, double* pick_gap)
+{
+    if (!pool_in)
+        return -1;
+    return encode_impl(p, atoms, xin, V, idx, coef, relres, NULL, NULL, pick_gap,
+                       NULL, 0, pool_in);
+}
+
+static int encode_impl(const oracle_params* p, const void* atoms, const void* xin,
+                       int32_t V, int32_t* idx, double* coef, double* relres,
+                       int32_t* pool, double* cut_gap, double* pick_gap,
+                       int64_t* macs, int32_t full_omp, const int32_t* pool_in)
 {
     const int N = p->N, d = p->d, s = p->s;
     const int n = full_omp ? p->N : p->n;
@@ -278,7 +306,15 @@ int oracle_encode(const oracle_params* p, const void* atoms, const void* xin,
         }
 
         /* 1-2. screening and the Top-n pool */
-        if (full_omp) {
+        if (pool_in) {
+            for (int i = 0; i < n; ++i) {
+                P[i] = pool_in[(int64_t)v * n + i];
+                if (P[i] < 0 || P[i] >= N) {
+                    rc = -1;
+                    goto done;
+                }
+            }
+        } else if (full_omp) {
             for (int j = 0; j < N; ++j) P[j] = j;
             if (cut_gap) cut_gap[v] = INFINITY;
         } else {

@@ -94,6 +94,9 @@ def load(path: str):
     L.oracle_reconstruct.argtypes = [P(_Params), C.c_void_p, C.c_int32, C.c_void_p,
                                      C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
     L.oracle_reconstruct.restype = C.c_int
+    L.oracle_greedy_on_pool.argtypes = [P(_Params), C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p,
+                                        C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+    L.oracle_greedy_on_pool.restype = C.c_int
     L.oracle_half_to_double.argtypes = [C.c_uint16]
     L.oracle_half_to_double.restype = C.c_double
     L.oracle_double_to_half.argtypes = [C.c_double]
@@ -120,7 +123,7 @@ class Variant:
         import types
         mod = globals()
         for name in ("encode", "adapt", "reconstruct", "half_to_double", "double_to_half",
-                     "encode_threaded"):
+                     "encode_threaded", "greedy_on_pool"):
             fn = mod[name]
             setattr(self, name, types.FunctionType(fn.__code__, dict(mod, lib=lambda: self._L),
                                                    fn.__name__, fn.__defaults__, fn.__closure__))
@@ -167,6 +170,27 @@ def encode(p: Params, atoms: np.ndarray, x: np.ndarray, full_omp: bool = False) 
     if rc != 0:
         raise RuntimeError(f"oracle_encode failed: {rc}")
     return EncodeResult(idx, coef, rel, pool, cut, gap, int(macs.value))
+
+
+def greedy_on_pool(p: Params, atoms: np.ndarray, x: np.ndarray, pool: np.ndarray) -> EncodeResult:
+    """Greedy selection + refit of each row of ``x`` over the given pool
+    ([V][n] atom ids).  pool/cut_gap of the result are the inputs / NaN."""
+    _check_store(atoms, p, "atoms")
+    _check_store(x, p, "x")
+    V = x.shape[0]
+    pool = np.ascontiguousarray(pool, np.int32)
+    if pool.shape != (V, p.n):
+        raise ValueError("pool must be [V][n]")
+    idx = np.empty((V, p.s), np.int32)
+    coef = np.empty((V, p.s), np.float64)
+    rel = np.empty(V, np.float64)
+    gap = np.empty((V, p.s), np.float64)
+    pc = p.c()
+    rc = lib().oracle_greedy_on_pool(C.byref(pc), _ptr(atoms), _ptr(x), V, _ptr(pool), _ptr(idx),
+                                     _ptr(coef), _ptr(rel), _ptr(gap))
+    if rc != 0:
+        raise RuntimeError(f"oracle_greedy_on_pool failed: {rc}")
+    return EncodeResult(idx, coef, rel, pool, np.full(V, np.nan), gap, 0)
 
 
 def encode_threaded(p: Params, atoms: np.ndarray, x: np.ndarray, threads: int) -> EncodeResult:

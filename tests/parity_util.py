@@ -47,14 +47,46 @@ def exempt_mask(res: O.EncodeResult) -> np.ndarray:
     return (res.cut_gap < CUT_GAP) | (res.pick_gap.min(axis=1) < PICK_GAP)
 
 
-def compare_encode(res: O.EncodeResult, idx, coef, relres) -> EncodeReport:
-    """res: oracle result for V vectors; idx/coef/relres: GPU arrays [V]..."""
+def check_cut_tie(p, atoms, x, res, gpu_pool, v):
+    """A vector on a near tie at the Top-n cut: the GPU pool may differ from
+    the oracle's only by atoms inside the tie band (|r| within CUT_GAP of
+    the cut value), and the oracle's greedy run on the GPU's pool is then the
+    unique answer.  Returns the oracle result on the GPU pool (or None if
+    that run itself sits on a greedy near tie)."""
+    r = np.abs(atoms.astype(np.float64) @ x[v].astype(np.float64))
+    cut = r[res.pool[v][-1]]
+    diff = set(gpu_pool[v].tolist()) ^ set(res.pool[v].tolist())
+    for j in diff:
+        assert abs(r[j] - cut) <= 2 * CUT_GAP * cut, f"pool atom {j} outside the tie band"
+    alt = O.greedy_on_pool(p, atoms, np.ascontiguousarray(x[v:v + 1]), gpu_pool[v:v + 1])
+    if alt.pick_gap.min() < PICK_GAP:
+        return None
+    return alt
+
+
+def compare_encode(res: O.EncodeResult, idx, coef, relres, gpu_pool=None, p=None, atoms=None,
+                   x=None) -> EncodeReport:
+    """res: oracle result for V vectors; idx/coef/relres: GPU arrays [V]...
+    With gpu_pool/p/atoms/x given, vectors on a near tie at the Top-n cut are
+    checked against the oracle's greedy run on the GPU's pool instead of
+    being skipped."""
     ex = exempt_mask(res)
     bad = []
     worst_c = 0.0
     worst_r = 0.0
     for v in range(len(ex)):
         if ex[v]:
+            if gpu_pool is None or res.pick_gap[v].min() < PICK_GAP or res.idx[v][0] < 0:
+                continue
+            alt = check_cut_tie(p, atoms, x, res, gpu_pool, v)
+            if alt is None:
+                continue
+            one = O.EncodeResult(alt.idx, alt.coef, alt.relres, alt.pool, np.full(1, np.inf), alt.pick_gap, 0)
+            sub = compare_encode(one, idx[v:v + 1], coef[v:v + 1], relres[v:v + 1])
+            bad += [v] if sub.mismatched_idx else []
+            worst_c = max(worst_c, sub.worst_coef)
+            worst_r = max(worst_r, sub.worst_relres)
+            ex[v] = False
             continue
         if not np.array_equal(idx[v], res.idx[v]):
             bad.append(v)
@@ -72,7 +104,7 @@ def compare_encode(res: O.EncodeResult, idx, coef, relres) -> EncodeReport:
     return EncodeReport(len(ex) - int(ex.sum()), int(ex.sum()), bad, worst_c, worst_r)
 
 
-def assert_encode_ok(rep: EncodeReport, max_exempt_frac=0.05):
+def assert_encode_ok(rep: EncodeReport, max_exempt_frac=0.10):
     assert not rep.mismatched_idx, f"selected ids differ on vectors {rep.mismatched_idx[:10]}"
     assert rep.worst_coef <= COEF_TOL, rep.worst_coef
     assert rep.worst_relres <= RELRES_TOL, rep.worst_relres

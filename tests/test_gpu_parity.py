@@ -69,15 +69,17 @@ def test_pool_matches_oracle(name, over, V):
     pool, _ = D.pool(_t(x))
     pool = pool.cpu().numpy()
     p = PU.oparams(w)
-    exempt = 0
+    ties = 0
     for g in range(w.G):
         res = O.encode_threaded(p, data.atoms[g], x[g], PU.THREADS)
         for v in range(V):
             if res.cut_gap[v] < PU.CUT_GAP:
-                exempt += 1
+                # near tie at the cut: the pools may differ only inside the band
+                ties += 1
+                PU.check_cut_tie(p, data.atoms[g], x[g], res, pool[g], v)
                 continue
             assert np.array_equal(pool[g, v], np.sort(res.pool[v])), (g, v)
-    assert exempt <= max(2, 0.05 * w.G * V)
+    assert ties <= max(3, 0.10 * w.G * V)
 
 
 def test_pool_tie_rule_exact_zeros():
@@ -107,12 +109,14 @@ def test_encode_matches_oracle(name, over, V):
     V = w.V if V is None else V
     x = data.inputs(0, V)
     D = make_dict(w, data, V)
+    gpool = D.pool(_t(x))[0].cpu().numpy()
     c = gpu_encode(D, x)
     idx, coef, rel = (t.cpu().numpy() for t in (c.idx, c.coef, c.relres))
     p = PU.oparams(w)
     for g in range(w.G):
         res = O.encode_threaded(p, data.atoms[g], x[g], PU.THREADS)
-        PU.assert_encode_ok(PU.compare_encode(res, idx[g], coef[g], rel[g]))
+        rep = PU.compare_encode(res, idx[g], coef[g], rel[g], gpool[g], p, data.atoms[g], x[g])
+        PU.assert_encode_ok(rep, max_exempt_frac=0.02)
 
 
 def test_encode_special_inputs():
