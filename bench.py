@@ -249,12 +249,20 @@ def oracle_steps(w, data, steps, threads):
     return nvec, time.perf_counter() - t0
 
 
+ARM_PARTS = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "Arm Neoverse-N1",
+             "0xd49": "Arm Neoverse-N2", "0xd8e": "Arm Neoverse-N3", "0xd84": "Arm Neoverse-V3"}
+
+
 def cpu_model():
     try:
         with open("/proc/cpuinfo") as f:
             for ln in f:
-                if ln.lower().startswith(("model name", "cpu part")):
+                key = ln.split(":", 1)[0].strip().lower()
+                if key == "model name":
                     return ln.split(":", 1)[1].strip()
+                if key == "cpu part":
+                    part = ln.split(":", 1)[1].strip().lower()
+                    return ARM_PARTS.get(part, f"Arm part {part}")
     except OSError:
         pass
     return "unknown"

@@ -2,6 +2,7 @@
 // encode/adapt sequence contract, workspace carving and kernel launches.
 // The library never allocates device memory: the caller passes the
 // dictionary, the usage counts and one zero-filled workspace.
+#include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -31,34 +32,65 @@ bool fault_injected()
 }
 
 constexpr size_t kAlign = 256;
-constexpr size_t kScoreBudget = size_t(1) << 30;   // bytes of materialised scores per chunk
+constexpr size_t kScoreBudget = size_t(1) << 30;   // FP32 path: materialised scores per chunk
+constexpr size_t kCandBudget = size_t(512) << 20;  // candidate lists per chunk
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Screening path: tensor cores for binary16 dictionaries (FADKV_SCREEN=ffma
+// forces the FP32 path, used to cross-check the two).
+bool use_tc(const fadkv_params& p)
+{
+    const char* f = getenv("FADKV_SCREEN");
+    if (f && strcmp(f, "ffma") == 0) return false;
+    Shape sh{p.num_dicts, p.N, p.d, p.n, p.s, p.dtype, p.lambda_abs, p.lambda_rel};
+    return screen_tc_supported(sh);
+}
+
 struct Layout {
+    bool tc;     // screening on tensor cores with candidate filtering
     int chunk;   // vectors per dictionary per encode pass
-    size_t counters, scores, pool_id, pool_r, inactive, flagged, total;
+    int cap;     // candidate capacity per vector
+    size_t counters, scores, cand, cand_count, inactive, flagged, total;
 };
 
 Layout make_layout(const fadkv_params& p)
 {
     Layout L;
-    const size_t per_vec = (size_t)p.num_dicts * (size_t)p.N * sizeof(float);
-    size_t chunk = kScoreBudget / per_vec;
-    if (chunk < 1) chunk = 1;
-    if (chunk > (size_t)p.max_batch) chunk = (size_t)p.max_batch;
+    L.tc = use_tc(p);
+    L.cap = cand_cap(p.n);
+    const size_t G = (size_t)p.num_dicts;
+    const size_t mb = (size_t)(p.max_batch > 0 ? p.max_batch : 1);
+    size_t chunk = L.tc ? kCandBudget / (G * (size_t)L.cap * 8) : kScoreBudget / (G * (size_t)p.N * sizeof(float));
+    if (chunk > mb) chunk = mb;
+    if (chunk >= 256) chunk = chunk / 128 * 128;   // whole MMA tiles
     if (chunk < 1) chunk = 1;
     L.chunk = (int)chunk;
-    const size_t G = (size_t)p.num_dicts;
     size_t o = 0;
-    L.counters = o; o = align_up(o + G * kCntFields * sizeof(long long), kAlign);
-    L.scores = o;   o = align_up(o + G * chunk * (size_t)p.N * sizeof(float), kAlign);
-    L.pool_id = o;  o = align_up(o + G * chunk * (size_t)p.n * sizeof(int32_t), kAlign);
-    L.pool_r = o;   o = align_up(o + G * chunk * (size_t)p.n * sizeof(float), kAlign);
-    L.inactive = o; o = align_up(o + G * (size_t)p.N * sizeof(int32_t), kAlign);
-    L.flagged = o;  o = align_up(o + G * (size_t)(p.max_batch > 0 ? p.max_batch : 1) * sizeof(int32_t), kAlign);
+    L.counters = o;   o = align_up(o + G * kCntFields * sizeof(long long), kAlign);
+    L.scores = o;     o = align_up(o + (L.tc ? 0 : G * chunk * (size_t)p.N * sizeof(float)), kAlign);
+    L.cand = o;       o = align_up(o + G * chunk * (size_t)L.cap * 8, kAlign);
+    L.cand_count = o; o = align_up(o + G * chunk * sizeof(int), kAlign);
+    L.inactive = o;   o = align_up(o + G * (size_t)p.N * sizeof(int32_t), kAlign);
+    L.flagged = o;    o = align_up(o + G * mb * sizeof(int32_t), kAlign);
     L.total = o;
     return L;
+}
+
+// alpha with P(|Z| >= alpha) = min(1, 2n/N) for a standard normal Z, by
+// bisection on erfc: an atom uncorrelated with x has |<d, x>| ~ ||x||/sqrt(d)
+// |Z|, so tau = alpha ||x|| / sqrt(d) keeps about 2n candidates per vector.
+float screen_alpha(int n, int N)
+{
+    double f = 2.0 * n / (double)N;
+    if (f >= 1.0) return 0.f;
+    double lo = 0.0, hi = 40.0;
+    for (int i = 0; i < 200; ++i) {
+        const double mid = 0.5 * (lo + hi);
+        if (erfc(mid / sqrt(2.0)) > f) lo = mid;
+        else hi = mid;
+    }
+    return (float)lo;
 }
 
 fadkv_status check_params(const fadkv_params* p)
@@ -103,6 +135,8 @@ struct fadkv_dict_s {
     DeltaTable delta;
     bool pending;      // an encode batch waits for its adapt
     int32_t pending_V;
+    int sms;           // multiprocessors of the device (queried at first use)
+    float alpha;       // screening threshold factor
     // tracing
     bool prof_on;
     int64_t launches[FADKV_PROFILE_KERNELS];
@@ -149,17 +183,69 @@ cudaError_t traced(fadkv_dict h, int cls, cudaStream_t st, F&& launch)
     return e;
 }
 
-// Screening + Top-n for vectors [v0, v0+Vc) of every dictionary.
-cudaError_t run_pool(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, cudaStream_t st)
+cudaError_t ensure_device_info(fadkv_dict h)
 {
-    float* scores = (float*)(h->ws + h->L.scores);
-    int32_t* pid = (int32_t*)(h->ws + h->L.pool_id);
-    float* pr = (float*)(h->ws + h->L.pool_r);
-    cudaError_t e = traced(h, FADKV_K_SCREEN, st, [&] {
+    if (h->sms > 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) h->sms = sms > 0 ? sms : 1;
+    return e;
+}
+
+unsigned long long* cand_buf(fadkv_dict h) { return (unsigned long long*)(h->ws + h->L.cand); }
+int* cand_count_buf(fadkv_dict h) { return (int*)(h->ws + h->L.cand_count); }
+
+// Screening of vectors [v0, v0+Vc) of every dictionary: candidate lists
+// (tensor-core path) or the exact Top-n keys (FP32 path).  With `dump` set,
+// writes all scores [G][Vc][N] instead (test hook).
+cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, float* dump, cudaStream_t st)
+{
+    cudaError_t e = ensure_device_info(h);
+    if (e != cudaSuccess) return e;
+    if (h->L.tc) {
+        ScreenTCArgs a;
+        a.N = h->p.N;
+        a.V = V;
+        a.v0 = v0;
+        a.Vc = Vc;
+        a.slices = screen_tc_slices(h->sh, Vc, h->sms);
+        a.alpha = h->alpha;
+        a.cap = h->L.cap;
+        a.cand = cand_buf(h);
+        a.cand_count = cand_count_buf(h);
+        a.dump = dump;
+        a.counters = counters(h);
+        return traced(h, FADKV_K_SCREEN, st, [&] { return launch_screen_tc(h->sh, h->atoms, x, V, a, h->sms, st); });
+    }
+    float* scores = dump ? dump : (float*)(h->ws + h->L.scores);
+    e = traced(h, FADKV_K_SCREEN, st, [&] {
         return launch_screen_ffma(h->sh, h->atoms, x, (int64_t)V * h->p.d, v0, Vc, scores, st);
     });
-    if (e != cudaSuccess) return e;
-    return traced(h, FADKV_K_TOPN, st, [&] { return launch_topn_radix(h->sh, scores, Vc, pid, pr, st); });
+    if (e != cudaSuccess || dump) return e;
+    return traced(h, FADKV_K_TOPN, st, [&] {
+        return launch_topn_radix(h->sh, scores, Vc, cand_buf(h), cand_count_buf(h), h->L.cap, st);
+    });
+}
+
+GreedyArgs greedy_args(fadkv_dict h, const void* x, int32_t V, int v0, int Vc)
+{
+    GreedyArgs a;
+    a.atoms = h->atoms;
+    a.x = x;
+    a.cand = cand_buf(h);
+    a.cand_count = cand_count_buf(h);
+    a.cap = h->L.cap;
+    a.idx = nullptr;
+    a.coef = nullptr;
+    a.relres = nullptr;
+    a.pool_out = nullptr;
+    a.pool_r_out = nullptr;
+    a.counters = counters(h);
+    a.V = V;
+    a.v0 = v0;
+    a.Vc = Vc;
+    return a;
 }
 
 }  // namespace
@@ -218,6 +304,8 @@ fadkv_status fadkv_dict_create(const fadkv_params* p, void* atoms, int32_t* usag
     for (int g = 0; g < p->num_dicts; ++g) h->delta.v[g] = delta[g];
     h->pending = false;
     h->pending_V = 0;
+    h->sms = 0;
+    h->alpha = screen_alpha(p->n, p->N);
     h->prof_on = false;
     for (int i = 0; i < FADKV_PROFILE_KERNELS; ++i) {
         h->launches[i] = 0;
@@ -292,20 +380,12 @@ fadkv_status fadkv_encode(fadkv_dict h, const void* x, int32_t V, int32_t* idx, 
     const int chunk = h->L.chunk;
     for (int v0 = 0; v0 < V; v0 += chunk) {
         const int Vc = (V - v0 < chunk) ? V - v0 : chunk;
-        cudaError_t e = run_pool(h, x, V, v0, Vc, st);
+        cudaError_t e = run_screen(h, x, V, v0, Vc, nullptr, st);
         if (e == cudaSuccess) {
-            GreedyArgs a;
-            a.atoms = h->atoms;
-            a.x = x;
-            a.pool_id = (const int32_t*)(h->ws + h->L.pool_id);
-            a.pool_r = (const float*)(h->ws + h->L.pool_r);
+            GreedyArgs a = greedy_args(h, x, V, v0, Vc);
             a.idx = idx;
             a.coef = coef;
             a.relres = relres;
-            a.counters = counters(h);
-            a.V = V;
-            a.v0 = v0;
-            a.Vc = Vc;
             e = traced(h, FADKV_K_GREEDY, st, [&] { return launch_greedy(h->sh, a, st); });
         }
         if (e != cudaSuccess) {
@@ -404,25 +484,38 @@ fadkv_status fadkv_debug_pool(fadkv_dict h, const void* x, int32_t V, int32_t* p
     }
     cudaStream_t st = (cudaStream_t)stream;
     const int chunk = h->L.chunk;
-    const size_t G = (size_t)h->p.num_dicts, n = (size_t)h->p.n;
     for (int v0 = 0; v0 < V; v0 += chunk) {
         const int Vc = (V - v0 < chunk) ? V - v0 : chunk;
-        cudaError_t e = run_pool(h, x, V, v0, Vc, st);
-        // copy [G][Vc][n] chunk rows into [G][V][n]
-        for (size_t g = 0; g < G && e == cudaSuccess; ++g) {
-            const int32_t* src = (const int32_t*)(h->ws + h->L.pool_id) + g * Vc * n;
-            e = cudaMemcpyAsync(pool + (g * V + v0) * n, src, sizeof(int32_t) * Vc * n,
-                                cudaMemcpyDeviceToDevice, st);
-            if (e == cudaSuccess && pool_r) {
-                const float* srcr = (const float*)(h->ws + h->L.pool_r) + g * Vc * n;
-                e = cudaMemcpyAsync(pool_r + (g * V + v0) * n, srcr, sizeof(float) * Vc * n,
-                                    cudaMemcpyDeviceToDevice, st);
-            }
+        cudaError_t e = run_screen(h, x, V, v0, Vc, nullptr, st);
+        if (e == cudaSuccess) {
+            GreedyArgs a = greedy_args(h, x, V, v0, Vc);
+            a.pool_out = pool;
+            a.pool_r_out = pool_r;
+            e = launch_greedy(h->sh, a, st);
         }
         if (e != cudaSuccess) {
             set_error("fadkv_debug_pool", e);
             return FADKV_ERR_CUDA;
         }
+    }
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_debug_scores(fadkv_dict h, const void* x, int32_t V, float* scores, void* stream)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    if (V < 0 || V > h->p.max_batch) return FADKV_ERR_INVALID_ARG;
+    if (V > 0 && (!x || !scores || !aligned(x, 16))) return FADKV_ERR_INVALID_ARG;
+    if (V > h->L.chunk) return FADKV_ERR_INVALID_ARG;   // one pass: [G][V][N] output
+    if (fault_injected()) {
+        set_error("fadkv_debug_scores", cudaErrorLaunchFailure);
+        return FADKV_ERR_CUDA;
+    }
+    if (V == 0) return FADKV_OK;
+    const cudaError_t e = run_screen(h, x, V, 0, V, scores, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        set_error("fadkv_debug_scores", e);
+        return FADKV_ERR_CUDA;
     }
     return FADKV_OK;
 }

@@ -47,28 +47,55 @@ template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return
 // Launchers (one translation unit each).  All return the launch error.
 // ---------------------------------------------------------------------------
 
+// Candidate capacity per vector: three times the pool size (the screening
+// threshold aims at about 2n candidates).
+__host__ __device__ inline int cand_cap(int n) { return 3 * n; }
+
+// Candidate keys: (bits(|r_j|) << 32) | (0xffffffff - j).  The larger key is
+// the larger |r|, then the lower atom index: the Top-n pool is the n largest
+// keys of a vector.
+
 // Screening scores r[g][v][j] = <x_gv, d_gj> for vectors [v0, v0+Vc) of
-// every dictionary; scores is [G][Vc][N] fp32.
+// every dictionary on the FP32 pipe; scores is [G][Vc][N] fp32.
 cudaError_t launch_screen_ffma(const Shape& sh, const void* atoms, const void* x, int64_t x_gstride,
                                int v0, int Vc, float* scores, cudaStream_t st);
 
-// Exact Top-n of |scores| per vector (ties to the lower atom index), pools
-// written in ascending atom order: pool_id/pool_r [G][Vc][n].  A vector whose
-// scores hold a NaN or infinity gets pool ids -1.
-cudaError_t launch_topn_radix(const Shape& sh, const float* scores, int Vc, int32_t* pool_id,
-                              float* pool_r, cudaStream_t st);
+// Exact Top-n of materialised scores: writes the n pool keys of every vector
+// to cand[g][v][0..n) and cand_count = n (count = -1 for non-finite scores).
+cudaError_t launch_topn_radix(const Shape& sh, const float* scores, int Vc, unsigned long long* cand,
+                              int* cand_count, int cap, cudaStream_t st);
 
-// Greedy selection inside the pool plus ridge refit; writes idx/coef/relres
-// for vectors [v0, v0+Vc) (output arrays are [G][V][...] with per-dictionary
-// stride V).
+// Tensor-core screening with the fused |r| >= tau filter (binary16 only).
+struct ScreenTCArgs {
+    int N, V, v0, Vc;         // V: vectors per dictionary of the whole call
+    int slices;               // atom slices per dictionary (grid = tiles*slices x G)
+    float alpha;              // tau = alpha * ||x|| / sqrt(d)
+    int cap;                  // candidate capacity per vector
+    unsigned long long* cand; // [G][Vc][cap]
+    int* cand_count;          // [G][Vc], zero on entry
+    float* dump;              // test hook: if set, write all scores [G][Vc][N] instead
+    long long* counters;      // [G][kCntFields] (status word)
+};
+bool screen_tc_supported(const Shape& sh);
+int screen_tc_slices(const Shape& sh, int Vc, int sms);
+cudaError_t launch_screen_tc(const Shape& sh, const void* atoms, const void* x, int V, const ScreenTCArgs& a,
+                             int sms, cudaStream_t st);
+
+// Exact Top-n from the candidate lists (slow exact path for lists shorter
+// than n or longer than cap), then greedy selection inside the pool plus
+// ridge refit; writes idx/coef/relres for vectors [v0, v0+Vc) (outputs are
+// [G][V][...]).  With pool_out set it only writes the pool ids (debug hook).
 struct GreedyArgs {
     const void* atoms;
     const void* x;
-    const int32_t* pool_id;   // [G][Vc][n], ascending atom order
-    const float* pool_r;      // [G][Vc][n]
+    unsigned long long* cand; // [G][Vc][cap]
+    int* cand_count;          // [G][Vc]; reset to 0 once consumed
+    int cap;
     int32_t* idx;
     float* coef;
     float* relres;
+    int32_t* pool_out;        // optional [G][V][n]
+    float* pool_r_out;        // optional [G][V][n] (with pool_out)
     long long* counters;      // [G][kCntFields]
     int V;                    // vectors per dictionary in the whole call
     int v0, Vc;

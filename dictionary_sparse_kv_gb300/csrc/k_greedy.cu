@@ -1,4 +1,5 @@
-// In-pool greedy selection with a ridge refit after every pick.
+// Exact Top-n pool, then in-pool greedy selection with a ridge refit after
+// every pick.
 //
 // "FAD-KV: Adaptive Dictionary KV Caching for Efficient Reasoning Decoding":
 // abstract (screening-based sparse coding: a one-shot Top-n pool followed by
@@ -6,22 +7,27 @@
 // lambda = 1e-4 + 0.20 diag(G)).  Greedy selection inside the pool and the
 // lower-index tie rule are conventions of this library.
 //
-// Per vector x with pool P (ascending atom order):
+// Per vector x:
+//   pool P = the n largest candidate keys (bits(|r_j|) << 32 | ~j), i.e. the
+//            n largest |r_j|, ties to the lower j.  The candidates are the
+//            atoms that passed the screening filter; if there are fewer than
+//            n of them (or the list overflowed) every score is recomputed
+//            here on the FP32 pipe and all N atoms are candidates;
 //   e_0 = x;  for k = 0..s-1:
 //     j* = argmax_{j in P \ S} |<d_j, e_k>|   (ties: lower atom index)
 //     S <- S + j*
 //     A = G_SS + diag(lambda_abs + lambda_rel G_ii),  A c = D_S x
 //     e_{k+1} = x - D_S c
 //   relres = ||e_s|| / ||x||
-// At k = 0 the correlations are the screening scores of the pool.  The
-// Cholesky factor of A grows by one row per pick (the factor of a leading
-// block is the leading block of the factor), so each refit costs O(k^2).
+// At k = 0 the correlations are the screening magnitudes |r_j| of the pool.
+// The Cholesky factor of A grows by one row per pick (the factor of a
+// leading block is the leading block of the factor), so a refit costs O(k^2).
 //
-// v1 layout: one CTA (256 threads) per vector; the pool's atoms are gathered
-// once into shared memory (rows padded by 16 bytes so that eight threads
-// reading eight consecutive rows hit distinct banks); each thread owns pool
-// slots tid, tid+256, ...; correlations run on the FP32 pipe against the
-// residual held in shared memory.
+// Layout: one CTA (256 threads) per vector.  The n-th largest key is found
+// by an MSD radix select over the 64-bit keys (stopping once the boundary
+// bin is taken whole); the pool's atoms are then gathered once into shared
+// memory (rows padded by 16 bytes: eight threads reading eight consecutive
+// rows hit distinct banks); thread t owns pool slots t, t+256, ...
 #include "fadkv_internal.cuh"
 
 namespace fadkv {
@@ -32,16 +38,18 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxPerThread = kMaxPool / kThreads;   // 4
 
 struct GreedyLayout {
-    size_t pool, xs, es, sa, lm, z, c, gram, fred, kred, pid, sslot, total;
+    size_t uni, xs, es, sa, lm, z, c, gram, fred, a0, kred, pid, sslot, hist, scan, misc, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline GreedyLayout greedy_layout(int n, int d, int elem)
+__host__ __device__ inline GreedyLayout greedy_layout(int n, int d, int elem, int N, int cap)
 {
     GreedyLayout L;
     size_t o = 0;
-    L.pool = o;  o += align_up((size_t)n * (d * elem + 16), 16);
+    const size_t pool = (size_t)n * (d * elem + 16);
+    const size_t keys = (size_t)(N > cap ? N : cap) * 8;
+    L.uni = o;   o += align_up(pool > keys ? pool : keys, 16);
     L.xs = o;    o += sizeof(float) * d;
     L.es = o;    o += sizeof(float) * d;
     L.sa = o;    o += sizeof(float) * kMaxS * d;
@@ -50,10 +58,14 @@ __host__ __device__ inline GreedyLayout greedy_layout(int n, int d, int elem)
     L.c = o;     o += sizeof(float) * kMaxS;
     L.gram = o;  o += sizeof(float) * (kMaxS + 4);
     L.fred = o;  o += sizeof(float) * kWarps * 2;
+    L.a0 = o;    o += sizeof(float) * n;
     o = align_up(o, 8);
-    L.kred = o;  o += sizeof(unsigned long long) * (kWarps + 1);
+    L.kred = o;  o += sizeof(unsigned long long) * (kWarps + 2);
     L.pid = o;   o += sizeof(int) * n;
     L.sslot = o; o += sizeof(int) * kMaxS;
+    L.hist = o;  o += sizeof(uint32_t) * 256;
+    L.scan = o;  o += sizeof(uint32_t) * kWarps;
+    L.misc = o;  o += sizeof(uint32_t) * 8;
     L.total = align_up(o, 16);
     return L;
 }
@@ -87,6 +99,7 @@ __device__ __forceinline__ float chunk_dot(const uint4& q, const float* e, const
     return acc;
 }
 
+// <row, e> over D elements; `row` is 16-byte aligned (shared or global).
 template <typename T, int D>
 __device__ __forceinline__ float row_dot(const T* row, const float* e)
 {
@@ -118,12 +131,20 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     return v;
 }
 
-// Selection key: larger |a| first, then the lower pool slot (pools are in
-// ascending atom order, so the lower slot is the lower atom index).
-__device__ __forceinline__ unsigned long long pick_key(float a, int slot)
+// Screening key: larger |r| first, then the lower atom index.
+__device__ __forceinline__ unsigned long long screen_key(float r, int atom)
 {
-    return ((unsigned long long)(__float_as_uint(a) & 0x7fffffffu) << 32) |
-           (unsigned long long)(0xffffffffu - (unsigned)slot);
+    return ((unsigned long long)(__float_as_uint(r) & 0x7fffffffu) << 32) |
+           (unsigned long long)(0xffffffffu - (unsigned)atom);
+}
+
+// Greedy key: larger |a| first, then the lower atom index (atom < 2^23);
+// the low 10 bits carry the pool slot, which never decides the order since
+// (|a|, atom) is unique.
+__device__ __forceinline__ unsigned long long pick_key(float a, int atom, int slot)
+{
+    return ((unsigned long long)(__float_as_uint(a) & 0x7fffffffu) << 33) |
+           ((unsigned long long)(0x7fffffu - (unsigned)atom) << 10) | (unsigned long long)slot;
 }
 
 template <typename T, int D>
@@ -134,11 +155,12 @@ greedy_kernel(Shape sh, GreedyArgs a)
     const int v = a.v0 + vc;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = sh.n, s = sh.s, N = sh.N;
-    constexpr int RSB = D * (int)sizeof(T) + 16;   // padded row, bytes
+    constexpr int RSB = D * (int)sizeof(T) + 16;   // padded pool row, bytes
 
-    const GreedyLayout L = greedy_layout(n, D, sizeof(T));
+    const GreedyLayout L = greedy_layout(n, D, sizeof(T), N, a.cap);
     extern __shared__ __align__(16) unsigned char smem[];
-    unsigned char* P = smem + L.pool;
+    unsigned char* P = smem + L.uni;
+    unsigned long long* keys = (unsigned long long*)(smem + L.uni);
     float* xs = (float*)(smem + L.xs);
     float* es = (float*)(smem + L.es);
     float* SA = (float*)(smem + L.sa);
@@ -147,19 +169,20 @@ greedy_kernel(Shape sh, GreedyArgs a)
     float* cc = (float*)(smem + L.c);
     float* gram = (float*)(smem + L.gram);
     float* fred = (float*)(smem + L.fred);
+    float* a0 = (float*)(smem + L.a0);
     unsigned long long* kred = (unsigned long long*)(smem + L.kred);
     int* pid = (int*)(smem + L.pid);
     int* sslot = (int*)(smem + L.sslot);
+    uint32_t* hist = (uint32_t*)(smem + L.hist);
+    uint32_t* scan_ws = (uint32_t*)(smem + L.scan);
+    uint32_t* misc = (uint32_t*)(smem + L.misc);
 
+    const size_t gv = (size_t)g * a.Vc + vc;
     const T* X = (const T*)a.x + ((size_t)g * a.V + v) * D;
     const T* A = (const T*)a.atoms + (size_t)g * N * D;
-    const int32_t* pool_id = a.pool_id + ((size_t)g * a.Vc + vc) * n;
-    const float* pool_r = a.pool_r + ((size_t)g * a.Vc + vc) * n;
-    int32_t* out_idx = a.idx + ((size_t)g * a.V + v) * s;
-    float* out_coef = a.coef + ((size_t)g * a.V + v) * s;
     long long* cnt = a.counters + (size_t)g * kCntFields;
 
-    // x, its norm and finiteness
+    // ---- x, its norm and finiteness; the candidate count ----
     float xsq = 0.f;
     int bad = 0;
     for (int t = tid; t < D; t += kThreads) {
@@ -169,33 +192,20 @@ greedy_kernel(Shape sh, GreedyArgs a)
         bad |= !isfinite(xv);
         xsq = fmaf(xv, xv, xsq);
     }
-    if (__syncthreads_or(bad)) {
-        for (int k = tid; k < s; k += kThreads) {
-            out_idx[k] = -1;
-            out_coef[k] = 0.f;
-        }
-        if (tid == 0) {
-            a.relres[(size_t)g * a.V + v] = __int_as_float(0x7fc00000);
-            atomicAdd((unsigned long long*)&cnt[kCntNonfinite], 1ull);
-            atomicOr((unsigned long long*)&cnt[kCntStatus], (unsigned long long)FADKV_DEV_NONFINITE_INPUT);
-        }
-        return;
-    }
     xsq = warp_sum(xsq);
     if (lane == 0) fred[warp] = xsq;
-
-    // pool ids (a pool id outside [0, N) means the scores were not finite),
-    // then the pool's atoms into shared memory
-    int badpool = 0;
-    for (int i = tid; i < n; i += kThreads) {
-        const int j = pool_id[i];
-        badpool |= (j < 0 || j >= N);
-        pid[i] = j;
-    }
-    if (__syncthreads_or(badpool)) {
+    if (tid == 0) misc[0] = (uint32_t)a.cand_count[gv];
+    bad = __syncthreads_or(bad);
+    const int count = (int)misc[0];
+    if (tid == 0) a.cand_count[gv] = 0;          // consumed: ready for the next call
+    if (bad) {
+        if (a.pool_out) {
+            for (int i = tid; i < n; i += kThreads) a.pool_out[((size_t)g * a.V + v) * n + i] = -1;
+            return;
+        }
         for (int k = tid; k < s; k += kThreads) {
-            out_idx[k] = -1;
-            out_coef[k] = 0.f;
+            a.idx[((size_t)g * a.V + v) * s + k] = -1;
+            a.coef[((size_t)g * a.V + v) * s + k] = 0.f;
         }
         if (tid == 0) {
             a.relres[(size_t)g * a.V + v] = __int_as_float(0x7fc00000);
@@ -206,6 +216,108 @@ greedy_kernel(Shape sh, GreedyArgs a)
     }
     float xnorm2 = 0.f;
     for (int w = 0; w < kWarps; ++w) xnorm2 += fred[w];
+
+    // ---- candidate keys into shared memory ----
+    int K;
+    if (count >= n && count <= a.cap) {
+        K = count;
+        const unsigned long long* src = a.cand + gv * a.cap;
+        for (int i = tid; i < K; i += kThreads) keys[i] = src[i];
+    } else {
+        // exact slow path: every atom's score on the FP32 pipe
+        K = N;
+        for (int j = tid; j < N; j += kThreads) {
+            const float r = row_dot<T, D>(A + (size_t)j * D, xs);
+            keys[j] = screen_key(r, j);
+        }
+        if (tid == 0) atomicAdd((unsigned long long*)&cnt[kCntFallback], 1ull);
+    }
+    __syncthreads();
+
+    // ---- the n largest keys: MSD radix select over 64-bit keys ----
+    unsigned long long prefix = 0ull, mask = 0ull;
+    uint32_t remaining = (uint32_t)n;
+    int shift = 56;
+    for (;; shift -= 8) {
+        for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < K; i += kThreads) {
+            const unsigned long long k = keys[i];
+            if ((k & mask) == prefix) atomicAdd(&hist[(uint32_t)(k >> shift) & 0xffu], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const int hi = 255 - 8 * lane;
+            uint32_t local = 0;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) local += hist[hi - b];
+            uint32_t incl = local;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const uint32_t above = incl - local;
+            if (above < remaining && remaining <= incl) {
+                uint32_t acc = above;
+                for (int b = 0; b < 8; ++b) {
+                    const uint32_t c = hist[hi - b];
+                    if (acc + c >= remaining) {
+                        kred[kWarps] = prefix | ((unsigned long long)(hi - b) << shift);
+                        misc[1] = remaining - acc;
+                        misc[2] = (c == remaining - acc) ? 1u : 0u;   // boundary bin taken whole
+                        break;
+                    }
+                    acc += c;
+                }
+            }
+        }
+        __syncthreads();
+        prefix = kred[kWarps];
+        remaining = misc[1];
+        mask |= 0xffull << shift;
+        if (misc[2] || shift == 0) break;
+    }
+    // selected: keys whose bits above `shift` are >= prefix's
+
+    // ---- compaction of the pool (candidate order) ----
+    {
+        uint32_t base = 0;
+        const unsigned long long lim = prefix >> shift;
+        for (int i0 = 0; i0 < K; i0 += kThreads) {
+            const int i = i0 + tid;
+            const unsigned long long k = (i < K) ? keys[i] : 0ull;
+            const uint32_t f = (i < K && (k >> shift) >= lim) ? 1u : 0u;
+            const unsigned bal = __ballot_sync(0xffffffffu, f);
+            if (lane == 0) scan_ws[warp] = __popc(bal);
+            __syncthreads();
+            uint32_t before = 0, total = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                const uint32_t c = scan_ws[w];
+                before += (w < warp) ? c : 0u;
+                total += c;
+            }
+            if (f) {
+                const uint32_t pos = base + before + __popc(bal & ((1u << lane) - 1u));
+                if (pos < (uint32_t)n) {
+                    pid[pos] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+                    a0[pos] = __uint_as_float((uint32_t)(k >> 32));
+                }
+            }
+            base += total;
+            __syncthreads();
+        }
+    }
+
+    if (a.pool_out) {
+        for (int i = tid; i < n; i += kThreads) {
+            a.pool_out[((size_t)g * a.V + v) * n + i] = pid[i];
+            if (a.pool_r_out) a.pool_r_out[((size_t)g * a.V + v) * n + i] = a0[i];
+        }
+        return;
+    }
+
+    // ---- the pool's atoms into shared memory (over the keys) ----
     {
         constexpr int CPR = D * (int)sizeof(T) / 16;
         for (int c = tid; c < n * CPR; c += kThreads) {
@@ -214,42 +326,39 @@ greedy_kernel(Shape sh, GreedyArgs a)
             *reinterpret_cast<uint4*>(P + (size_t)i * RSB + part * 16) = q;
         }
     }
-
-    // step-0 correlations: the screening scores of the pool
     float av[kMaxPerThread];
+    int aid[kMaxPerThread];
     unsigned picked = 0;
 #pragma unroll
     for (int m = 0; m < kMaxPerThread; ++m) {
         const int i = tid + m * kThreads;
-        av[m] = (i < n) ? pool_r[i] : 0.f;
+        av[m] = (i < n) ? a0[i] : 0.f;
+        aid[m] = (i < n) ? pid[i] : 0;
     }
     __syncthreads();
 
     const float la = sh.lambda_abs, lr = sh.lambda_rel;
     for (int k = 0; k < s; ++k) {
-        // ---- argmax over the unpicked pool slots ----
+        // ---- argmax over the unpicked pool atoms ----
         unsigned long long best = 0ull;
 #pragma unroll
         for (int m = 0; m < kMaxPerThread; ++m) {
             const int i = tid + m * kThreads;
             if (i < n && !((picked >> m) & 1u)) {
-                const unsigned long long key = pick_key(av[m], i);
+                const unsigned long long key = pick_key(av[m], aid[m], i);
                 best = key > best ? key : best;
             }
         }
         best = warp_max_u64(best);
         if (lane == 0) kred[warp] = best;
         __syncthreads();
-        if (warp == 0) {
-            unsigned long long b = (lane < kWarps) ? kred[lane] : 0ull;
-            b = warp_max_u64(b);
-            if (lane == 0) kred[kWarps] = b;
-        }
-        __syncthreads();
-        const int slot = (int)(0xffffffffu - (unsigned)(kred[kWarps] & 0xffffffffull));
+        unsigned long long win = 0ull;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) win = kred[w] > win ? kred[w] : win;
+        const int slot = (int)(win & 0x3ffull);
         if ((slot % kThreads) == tid) picked |= 1u << (slot / kThreads);
         if (tid == 0) sslot[k] = slot;
-        // picked atom -> SA[k] (fp32)
+        // the picked atom -> SA[k] (fp32)
         {
             const T* row = (const T*)(P + (size_t)slot * RSB);
             for (int t = tid; t < D; t += kThreads) SA[k * D + t] = to_f32(row[t]);
@@ -326,15 +435,15 @@ greedy_kernel(Shape sh, GreedyArgs a)
         a.relres[(size_t)g * a.V + v] = (xnorm2 > 0.f) ? sqrtf(e2) / sqrtf(xnorm2) : 0.f;
     }
     for (int k = tid; k < s; k += kThreads) {
-        out_idx[k] = pid[sslot[k]];
-        out_coef[k] = cc[k];
+        a.idx[((size_t)g * a.V + v) * s + k] = pid[sslot[k]];
+        a.coef[((size_t)g * a.V + v) * s + k] = cc[k];
     }
 }
 
 template <typename T, int D>
 cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 {
-    const size_t smem = greedy_layout(sh.n, D, sizeof(T)).total;
+    const size_t smem = greedy_layout(sh.n, D, sizeof(T), sh.N, a.cap).total;
     auto k = greedy_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -347,7 +456,7 @@ cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 
 size_t greedy_smem_bytes(const Shape& sh)
 {
-    return greedy_layout(sh.n, sh.d, sh.dtype == FADKV_F16 ? 2 : 4).total;
+    return greedy_layout(sh.n, sh.d, sh.dtype == FADKV_F16 ? 2 : 4, sh.N, cand_cap(sh.n)).total;
 }
 
 cudaError_t launch_greedy(const Shape& sh, const GreedyArgs& a, cudaStream_t st)

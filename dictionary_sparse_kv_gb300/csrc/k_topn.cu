@@ -10,7 +10,9 @@
 // so an MSD radix select over 4 x 8 bits finds the n-th largest key T
 // exactly.  The pool is then every atom with key > T plus the lowest-index
 // atoms with key == T, written in ascending atom order by an ordered block
-// compaction.  The result is unique, so it is deterministic.
+// compaction.  The result is unique, so it is deterministic.  The pool is
+// handed on as candidate keys (bits(|r_j|) << 32 | (0xffffffff - j)) with a
+// count of exactly n, the form the greedy kernel consumes.
 #include "fadkv_internal.cuh"
 
 namespace fadkv {
@@ -45,8 +47,8 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 }
 
 __global__ void __launch_bounds__(kThreads)
-topn_radix_kernel(const float* __restrict__ scores, int N, int n, int Vc, int32_t* __restrict__ pool_id,
-                  float* __restrict__ pool_r)
+topn_radix_kernel(const float* __restrict__ scores, int N, int n, int Vc, unsigned long long* __restrict__ cand,
+                  int* __restrict__ cand_count, int cap)
 {
     extern __shared__ uint32_t keys[];   // [N]
     __shared__ uint32_t hist[256];
@@ -55,8 +57,7 @@ topn_radix_kernel(const float* __restrict__ scores, int N, int n, int Vc, int32_
 
     const int v = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
     const float* r = scores + ((size_t)g * Vc + v) * N;
-    int32_t* out_id = pool_id + ((size_t)g * Vc + v) * n;
-    float* out_r = pool_r + ((size_t)g * Vc + v) * n;
+    unsigned long long* out = cand + ((size_t)g * Vc + v) * cap;
 
     int bad = 0;
     for (int j = tid; j < N; j += kThreads) {
@@ -65,10 +66,9 @@ topn_radix_kernel(const float* __restrict__ scores, int N, int n, int Vc, int32_
         keys[j] = k;
     }
     if (__syncthreads_or(bad)) {
-        for (int i = tid; i < n; i += kThreads) {
-            out_id[i] = -1;
-            out_r[i] = __int_as_float(0x7fc00000);
-        }
+        // non-finite scores come only from a non-finite input, which the
+        // consumer detects on its own; an empty list sends it there
+        if (tid == 0) cand_count[(size_t)g * Vc + v] = 0;
         return;
     }
 
@@ -130,19 +130,19 @@ topn_radix_kernel(const float* __restrict__ scores, int N, int n, int Vc, int32_
         const bool take = gt || (eq && rank_eq < eq_left);
         if (take) {
             const uint32_t pos = base_out + rank_gt + min(rank_eq, eq_left);
-            out_id[pos] = j;
-            out_r[pos] = r[j];
+            out[pos] = ((unsigned long long)k << 32) | (unsigned long long)(0xffffffffu - (uint32_t)j);
         }
         const uint32_t tot_eq = tot & 0xffffu, tot_gt = tot >> 16;
         base_out += tot_gt + min(tot_eq, eq_left);
         base_eq += tot_eq;
     }
+    if (tid == 0) cand_count[(size_t)g * Vc + v] = n;
 }
 
 }  // namespace
 
-cudaError_t launch_topn_radix(const Shape& sh, const float* scores, int Vc, int32_t* pool_id,
-                              float* pool_r, cudaStream_t st)
+cudaError_t launch_topn_radix(const Shape& sh, const float* scores, int Vc, unsigned long long* cand,
+                              int* cand_count, int cap, cudaStream_t st)
 {
     if (Vc <= 0) return cudaSuccess;
     const size_t smem = sizeof(uint32_t) * (size_t)sh.N;
@@ -150,7 +150,7 @@ cudaError_t launch_topn_radix(const Shape& sh, const float* scores, int Vc, int3
                                          (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(Vc, sh.G);
-    topn_radix_kernel<<<grid, kThreads, smem, st>>>(scores, sh.N, sh.n, Vc, pool_id, pool_r);
+    topn_radix_kernel<<<grid, kThreads, smem, st>>>(scores, sh.N, sh.n, Vc, cand, cand_count, cap);
     return cudaGetLastError();
 }
 

@@ -79,6 +79,7 @@ _SIGS = {
                            C.c_void_p], C.c_int),
     "fadkv_dict_stats": ([C.c_void_p, C.POINTER(C.c_int64), C.c_void_p], C.c_int),
     "fadkv_debug_pool": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "fadkv_debug_scores": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p], C.c_int),
     "fadkv_profile_enable": ([C.c_void_p, C.c_int32], C.c_int),
     "fadkv_profile_read": ([C.c_void_p, C.POINTER(C.c_int64), C.POINTER(C.c_double), C.c_int32], C.c_int),
 }
@@ -187,6 +188,11 @@ def debug_pool(h: int, x, V: int, pool, pool_r=None, stream=None) -> None:
     _check("fadkv_debug_pool", lib().fadkv_debug_pool(h, _addr(x), V, _addr(pool), _addr(pool_r), st))
 
 
+def debug_scores(h: int, x, V: int, scores, stream=None) -> None:
+    st = _stream(stream, x, scores)
+    _check("fadkv_debug_scores", lib().fadkv_debug_scores(h, _addr(x), V, _addr(scores), st))
+
+
 def profile_enable(h: int, enable: bool = True) -> None:
     _check("fadkv_profile_enable", lib().fadkv_profile_enable(h, 1 if enable else 0))
 
@@ -276,6 +282,13 @@ class Dictionary:
 
     def stats(self, stream=None):
         return dict_stats(self.h, self.G, stream)
+
+    def scores(self, x, stream=None):
+        import torch
+        V = x.shape[1]
+        out = torch.empty((self.G, V, self.N), dtype=torch.float32, device=x.device)
+        debug_scores(self.h, x, V, out, stream)
+        return out
 
     def pool(self, x, stream=None):
         import torch

@@ -86,6 +86,7 @@ typedef enum { FADKV_F16 = 0, FADKV_F32 = 1 } fadkv_dtype;
 /* Device status word bits (per dictionary, see fadkv_dict_stats). */
 #define FADKV_DEV_NONFINITE_INPUT 0x1   /* an input held a NaN or infinity */
 #define FADKV_DEV_NOT_SPD 0x2           /* a refit matrix lost positive definiteness */
+#define FADKV_DEV_TIMEOUT 0x4           /* a kernel gave up waiting on its own pipeline */
 
 typedef struct {
     int32_t num_dicts;   /* G, 1 .. FADKV_MAX_DICTS */
@@ -181,16 +182,22 @@ fadkv_status fadkv_reconstruct(fadkv_dict dict, int32_t V, const int32_t* idx, c
 fadkv_status fadkv_dict_stats(fadkv_dict dict, int64_t* host_out, void* stream);
 
 /* Test hook: the Top-n pool of each x without changing any state.
-   pool [G][V][n] int32 in ascending atom order (-1 for a non-finite input);
-   pool_r (may be NULL) [G][V][n] float32 screening scores of those atoms.
-   Errors: INVALID_ARG, CUDA. */
+   pool [G][V][n] int32, the pool's atom ids in no particular order (-1 for
+   a non-finite input); pool_r (may be NULL) [G][V][n] float32 |r| of those
+   atoms, in the same order.  Errors: INVALID_ARG, CUDA. */
 fadkv_status fadkv_debug_pool(fadkv_dict dict, const void* x, int32_t V, int32_t* pool,
                               float* pool_r, void* stream);
 
+/* Test hook: screening scores [G][V][N] float32 of each x, from the same
+   screening kernel encode uses (tensor cores for binary16 dictionaries).
+   No state changes.  V must not exceed the handle's internal pass size
+   (at least min(max_batch, 128)).  Errors: INVALID_ARG, CUDA. */
+fadkv_status fadkv_debug_scores(fadkv_dict dict, const void* x, int32_t V, float* scores, void* stream);
+
 /* Kernel classes reported by fadkv_profile_read. */
 #define FADKV_PROFILE_KERNELS 8
-#define FADKV_K_SCREEN 0       /* screening scores */
-#define FADKV_K_TOPN 1         /* Top-n pool selection */
+#define FADKV_K_SCREEN 0       /* screening (tensor cores + candidate filter, or FP32 scores) */
+#define FADKV_K_TOPN 1         /* Top-n over materialised FP32 scores (binary32 dictionaries) */
 #define FADKV_K_GREEDY 2       /* in-pool greedy selection + ridge refit */
 #define FADKV_K_ADAPT 3        /* fixed-size adaptation */
 #define FADKV_K_RECONSTRUCT 4  /* sparse reconstruction */

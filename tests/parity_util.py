@@ -117,12 +117,35 @@ def ulp(a: np.ndarray) -> np.ndarray:
     return np.spacing(np.abs(a).astype(a.dtype)).astype(np.float64)
 
 
-def compare_atoms(gpu: np.ndarray, orc: np.ndarray, rows) -> float:
-    """Max deviation in ulps over the given rows."""
+def compare_atoms(gpu: np.ndarray, orc: np.ndarray, rows, bound=None) -> float:
+    """Max deviation over the given rows, in units of the allowed error:
+    one ulp of the storage type plus, if given, bound[j] (an [d] array of the
+    fp32 arithmetic's error bound for that row).  <= 1 passes."""
     worst = 0.0
     for j in rows:
         g = gpu[j].astype(np.float64)
         o = orc[j].astype(np.float64)
         u = np.maximum(ulp(orc[j]), ulp(gpu[j]))
+        if bound is not None:
+            u = u + bound[j]
         worst = max(worst, float(np.max(np.abs(g - o) / u)))
     return worst
+
+
+def replacement_bounds(atoms_before, x, idx, coef, repl_id, s):
+    """Per replaced atom j = repl_id[v]: an elementwise bound on the fp32
+    error of e/||e|| with e = x - sum_k c_k d_k formed by s fused
+    multiply-adds (unit roundoff 2^-24 each, plus the division):
+    (s + 3) * 2^-24 * (|x_t| + sum_k |c_k d_kt|) / ||e||."""
+    u = 2.0 ** -24
+    out = {}
+    for v, j in enumerate(repl_id):
+        if j < 0:
+            continue
+        A = atoms_before[idx[v]].astype(np.float64)
+        c = coef[v].astype(np.float64)
+        xv = x[v].astype(np.float64)
+        e = xv - c @ A
+        mag = np.abs(xv) + np.abs(c) @ np.abs(A)
+        out[int(j)] = (s + 3) * u * mag / np.linalg.norm(e) + 2 * u * np.abs(e) / np.linalg.norm(e)
+    return out

@@ -1,0 +1,116 @@
+"""Screening kernels on the GPU: tensor-core scores and the candidate filter.
+
+* Raw scores of the tensor-core kernel (binary16 dictionaries) and of the
+  FP32 kernel against the exact products in float64, within the fp32
+  accumulation bound d * 2^-24 * sum_t |x_t d_jt| per score.
+* Encodes through the two screening paths agree with each other and with
+  the oracle.
+* The exact slow path: a candidate list shorter than n (x is a basis vector
+  of a dictionary made of repeated signed bases, so only a few scores pass
+  the threshold) and a list that overflows (x = 0: every score passes).
+"""
+import numpy as np
+import pytest
+
+from dictionary_sparse_kv_gb300 import synthetic as S
+from oracle import oracle as O
+from tests import parity_util as PU
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dictionary_sparse_kv_gb300 import build as B
+    B.build()
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _dict(atoms, usage, deltas, n, s, max_batch):
+    from dictionary_sparse_kv_gb300 import fadkv as F
+    return F.Dictionary(_t(atoms), _t(usage), deltas, n, s, max_batch)
+
+
+@pytest.mark.parametrize("path", ["tc", "ffma"])
+@pytest.mark.parametrize("N,d,G,V", [(4096, 128, 3, 200), (8192, 128, 2, 128), (1024, 64, 2, 300)])
+def test_scores_against_float64(monkeypatch, path, N, d, G, V):
+    if path == "ffma":
+        monkeypatch.setenv("FADKV_SCREEN", "ffma")
+    atoms = np.stack([S.make_dictionary(N, d, np.float16, 7, g) for g in range(G)])
+    x = np.stack([S.make_sparse_inputs(atoms[g], V, 8, 8, g) for g in range(G)])
+    D = _dict(atoms, np.ones((G, N), np.int32), [0.5] * G, 64, 8, V)
+    sc = D.scores(_t(x)).cpu().numpy().astype(np.float64)
+    for g in range(G):
+        A = atoms[g].astype(np.float64)
+        X = x[g].astype(np.float64)
+        exact = X @ A.T
+        bound = d * 2.0 ** -24 * (np.abs(X) @ np.abs(A).T) + 1e-30
+        err = np.abs(sc[g] - exact)
+        assert np.all(err <= bound), float(np.max(err / bound))
+
+
+def test_two_screening_paths_agree(monkeypatch):
+    from dataclasses import replace
+    w = replace(S.WORKLOADS["decode_3b"], G=3)
+    data = S.WorkloadData(w)
+    x = data.inputs(0, 160)
+    outs = {}
+    for path in ("tc", "ffma"):
+        if path == "ffma":
+            monkeypatch.setenv("FADKV_SCREEN", "ffma")
+        D = _dict(data.atoms, data.usage, data.deltas(), w.n, w.s, 160)
+        c = D.new_codes(160)
+        D.encode(_t(x), c)
+        torch.cuda.synchronize()
+        pool = D.pool(_t(x))[0].cpu().numpy()
+        outs[path] = (c.idx.cpu().numpy(), c.coef.cpu().numpy(), np.sort(pool, axis=2))
+    p = PU.oparams(w)
+    for g in range(w.G):
+        res = O.encode_threaded(p, data.atoms[g], x[g], PU.THREADS)
+        ok = ~PU.exempt_mask(res)
+        for path in ("tc", "ffma"):
+            idx, coef, pool = outs[path]
+            assert np.array_equal(idx[g][ok], res.idx[ok])
+            assert np.array_equal(pool[g][ok], np.sort(res.pool[ok], axis=1))
+        assert np.array_equal(outs["tc"][0][g][ok], outs["ffma"][0][g][ok])
+
+
+def test_slow_path_short_and_overflowing_lists():
+    d, N, n, s = 128, 4096, 256, 8
+    g = np.random.default_rng(11)
+    # 32 signed copies of the standard basis: x = e_t has exactly 32 nonzero
+    # scores (|r| = 1), far fewer than n, all others exactly 0
+    A = np.zeros((N, d), np.float16)
+    A[np.arange(N), np.arange(N) % d] = g.choice([-1.0, 1.0], N)
+    x = np.zeros((1, 4, d), np.float16)
+    x[0, 0, 5] = 1.0                     # short list
+    x[0, 1] = 0.0                        # x = 0: every score passes, list overflows
+    x[0, 2, 17] = -2.0
+    x[0, 2, 99] = 0.5
+    x[0, 3] = S.make_sparse_inputs(A, 1, 8, 3)[0]
+    D = _dict(A[None], np.ones((1, N), np.int32), [0.5], n, s, 4)
+    pool = D.pool(_t(x))[0].cpu().numpy()[0]
+    c = D.new_codes(4)
+    D.encode(_t(x), c)
+    torch.cuda.synchronize()
+    st = D.stats()[0]
+    assert st["topn_slow_path"] >= 3 * 2          # pool() and encode() both took it
+    p = O.Params(N, d, n, s)
+    res = O.encode(p, A, x[0])
+    for v in range(4):
+        assert np.array_equal(np.sort(pool[v]), np.sort(res.pool[v])), v
+    # every tie here is exact (equal |r| or |a| in both precisions), so the
+    # index rule decides it identically on both sides: no exemption
+    idx, coef, rel = (t.cpu().numpy()[0] for t in (c.idx, c.coef, c.relres))
+    assert np.array_equal(idx, res.idx)
+    for v in range(4):
+        cn = np.linalg.norm(res.coef[v])
+        assert np.linalg.norm(coef[v] - res.coef[v]) <= PU.COEF_TOL * cn + 1e-7
+        assert abs(rel[v] - res.relres[v]) <= PU.RELRES_TOL * res.relres[v] + 1e-7
