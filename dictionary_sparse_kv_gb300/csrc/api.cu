@@ -62,15 +62,15 @@ Layout make_layout(const fadkv_params& p)
     const size_t G = (size_t)p.num_dicts;
     const size_t mb = (size_t)(p.max_batch > 0 ? p.max_batch : 1);
     size_t chunk = L.tc ? kCandBudget / (G * (size_t)L.cap * 8) : kScoreBudget / (G * (size_t)p.N * sizeof(float));
-    if (chunk > mb) chunk = mb;
-    if (chunk >= 256) chunk = chunk / 128 * 128;   // whole MMA tiles
+    if (chunk >= mb) chunk = mb;
+    else if (chunk >= 256) chunk = chunk / 128 * 128;   // whole MMA tiles
     if (chunk < 1) chunk = 1;
     L.chunk = (int)chunk;
     size_t o = 0;
     L.counters = o;   o = align_up(o + G * kCntFields * sizeof(long long), kAlign);
     L.scores = o;     o = align_up(o + (L.tc ? 0 : G * chunk * (size_t)p.N * sizeof(float)), kAlign);
     L.cand = o;       o = align_up(o + G * chunk * (size_t)L.cap * 8, kAlign);
-    L.cand_count = o; o = align_up(o + G * chunk * sizeof(int), kAlign);
+    L.cand_count = o; o = align_up(o + G * chunk * kCountSlots * sizeof(int), kAlign);
     L.inactive = o;   o = align_up(o + G * (size_t)p.N * sizeof(int32_t), kAlign);
     L.flagged = o;    o = align_up(o + G * mb * sizeof(int32_t), kAlign);
     L.total = o;
@@ -199,6 +199,8 @@ int* cand_count_buf(fadkv_dict h) { return (int*)(h->ws + h->L.cand_count); }
 // Screening of vectors [v0, v0+Vc) of every dictionary: candidate lists
 // (tensor-core path) or the exact Top-n keys (FP32 path).  With `dump` set,
 // writes all scores [G][Vc][N] instead (test hook).
+int slices_for(fadkv_dict h, int Vc) { return h->L.tc ? screen_tc_slices(h->sh, Vc, h->sms) : 1; }
+
 cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, float* dump, cudaStream_t st)
 {
     cudaError_t e = ensure_device_info(h);
@@ -209,7 +211,7 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
         a.V = V;
         a.v0 = v0;
         a.Vc = Vc;
-        a.slices = screen_tc_slices(h->sh, Vc, h->sms);
+        a.slices = slices_for(h, Vc);
         a.alpha = h->alpha;
         a.cap = h->L.cap;
         a.cand = cand_buf(h);
@@ -236,6 +238,7 @@ GreedyArgs greedy_args(fadkv_dict h, const void* x, int32_t V, int v0, int Vc)
     a.cand = cand_buf(h);
     a.cand_count = cand_count_buf(h);
     a.cap = h->L.cap;
+    a.slices = slices_for(h, Vc);
     a.idx = nullptr;
     a.coef = nullptr;
     a.relres = nullptr;

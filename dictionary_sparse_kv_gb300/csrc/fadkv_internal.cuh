@@ -47,9 +47,13 @@ template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return
 // Launchers (one translation unit each).  All return the launch error.
 // ---------------------------------------------------------------------------
 
-// Candidate capacity per vector: three times the pool size (the screening
-// threshold aims at about 2n candidates).
-__host__ __device__ inline int cand_cap(int n) { return 3 * n; }
+// Candidate capacity per vector: four times the pool size (the screening
+// threshold aims at about 2n candidates).  The list is split into
+// 2 * slices regions (one per atom slice and accumulator buffer of the
+// screening kernel), each with its own count in cand_count[.][kCountSlots].
+__host__ __device__ inline int cand_cap(int n) { return 4 * n; }
+constexpr int kMaxSlices = 16;
+constexpr int kCountSlots = 2 * kMaxSlices;
 
 // Candidate keys: (bits(|r_j|) << 32) | (0xffffffff - j).  The larger key is
 // the larger |r|, then the lower atom index: the Top-n pool is the n largest
@@ -61,7 +65,8 @@ cudaError_t launch_screen_ffma(const Shape& sh, const void* atoms, const void* x
                                int v0, int Vc, float* scores, cudaStream_t st);
 
 // Exact Top-n of materialised scores: writes the n pool keys of every vector
-// to cand[g][v][0..n) and cand_count = n (count = -1 for non-finite scores).
+// to region 0 of its candidate list (one slice: regions of cap/2 entries)
+// with count n (0 for non-finite scores).
 cudaError_t launch_topn_radix(const Shape& sh, const float* scores, int Vc, unsigned long long* cand,
                               int* cand_count, int cap, cudaStream_t st);
 
@@ -71,8 +76,8 @@ struct ScreenTCArgs {
     int slices;               // atom slices per dictionary (grid = tiles*slices x G)
     float alpha;              // tau = alpha * ||x|| / sqrt(d)
     int cap;                  // candidate capacity per vector
-    unsigned long long* cand; // [G][Vc][cap]
-    int* cand_count;          // [G][Vc], zero on entry
+    unsigned long long* cand; // [G][Vc][cap], region r at [r * cap/(2*slices), ...)
+    int* cand_count;          // [G][Vc][kCountSlots], region counts
     float* dump;              // test hook: if set, write all scores [G][Vc][N] instead
     long long* counters;      // [G][kCntFields] (status word)
 };
@@ -89,8 +94,9 @@ struct GreedyArgs {
     const void* atoms;
     const void* x;
     unsigned long long* cand; // [G][Vc][cap]
-    int* cand_count;          // [G][Vc]; reset to 0 once consumed
+    int* cand_count;          // [G][Vc][kCountSlots]; reset to 0 once consumed
     int cap;
+    int slices;               // regions used: 2 * slices
     int32_t* idx;
     float* coef;
     float* relres;
@@ -102,6 +108,9 @@ struct GreedyArgs {
 };
 cudaError_t launch_greedy(const Shape& sh, const GreedyArgs& a, cudaStream_t st);
 size_t greedy_smem_bytes(const Shape& sh);
+// the tensor-core variant for binary16 dictionaries (used by launch_greedy)
+cudaError_t launch_greedy_mma(const Shape& sh, const GreedyArgs& a, cudaStream_t st);
+size_t greedy_mma_smem_bytes(const Shape& sh);
 
 // Fixed-size adaptation, one CTA per dictionary.
 struct AdaptArgs {

@@ -23,12 +23,16 @@
 // The Cholesky factor of A grows by one row per pick (the factor of a
 // leading block is the leading block of the factor), so a refit costs O(k^2).
 //
-// Layout: one CTA (256 threads) per vector.  The n-th largest key is found
-// by an MSD radix select over the 64-bit keys (stopping once the boundary
-// bin is taken whole); the pool's atoms are then gathered once into shared
-// memory (rows padded by 16 bytes: eight threads reading eight consecutive
-// rows hit distinct banks); thread t owns pool slots t, t+256, ...
-#include "fadkv_internal.cuh"
+// This is the FP32-pipe kernel, used for binary32 dictionaries (and on
+// request for binary16, to cross-check the tensor-core kernel): one CTA
+// (256 threads) per vector; the pool (exact Top-n from select.cuh) is
+// gathered once into shared memory (rows padded by 16 bytes: eight threads
+// reading eight consecutive rows hit distinct banks); thread t owns pool
+// slots t, t+256, ...
+#include <stdlib.h>
+#include <string.h>
+
+#include "select.cuh"
 
 namespace fadkv {
 namespace {
@@ -65,7 +69,7 @@ __host__ __device__ inline GreedyLayout greedy_layout(int n, int d, int elem, in
     L.sslot = o; o += sizeof(int) * kMaxS;
     L.hist = o;  o += sizeof(uint32_t) * 256;
     L.scan = o;  o += sizeof(uint32_t) * kWarps;
-    L.misc = o;  o += sizeof(uint32_t) * 8;
+    L.misc = o;  o += sizeof(uint32_t) * (4 + kCountSlots);
     L.total = align_up(o, 16);
     return L;
 }
@@ -101,7 +105,7 @@ __device__ __forceinline__ float chunk_dot(const uint4& q, const float* e, const
 
 // <row, e> over D elements; `row` is 16-byte aligned (shared or global).
 template <typename T, int D>
-__device__ __forceinline__ float row_dot(const T* row, const float* e)
+__device__ __forceinline__ float row_dot(const T* row, const float* e)  // pool rows in shared memory
 {
     constexpr int EPC = 16 / sizeof(T);   // elements per 16-byte chunk
     constexpr int CPR = D / EPC;          // chunks per row
@@ -129,13 +133,6 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
         v = t > v ? t : v;
     }
     return v;
-}
-
-// Screening key: larger |r| first, then the lower atom index.
-__device__ __forceinline__ unsigned long long screen_key(float r, int atom)
-{
-    return ((unsigned long long)(__float_as_uint(r) & 0x7fffffffu) << 32) |
-           (unsigned long long)(0xffffffffu - (unsigned)atom);
 }
 
 // Greedy key: larger |a| first, then the lower atom index (atom < 2^23);
@@ -194,10 +191,9 @@ greedy_kernel(Shape sh, GreedyArgs a)
     }
     xsq = warp_sum(xsq);
     if (lane == 0) fred[warp] = xsq;
-    if (tid == 0) misc[0] = (uint32_t)a.cand_count[gv];
+    sel::Scratch sc{hist, scan_ws, misc, kred + kWarps};
+    const int count = sel::intake_counts(a, gv, sc);
     bad = __syncthreads_or(bad);
-    const int count = (int)misc[0];
-    if (tid == 0) a.cand_count[gv] = 0;          // consumed: ready for the next call
     if (bad) {
         if (a.pool_out) {
             for (int i = tid; i < n; i += kThreads) a.pool_out[((size_t)g * a.V + v) * n + i] = -1;
@@ -217,97 +213,9 @@ greedy_kernel(Shape sh, GreedyArgs a)
     float xnorm2 = 0.f;
     for (int w = 0; w < kWarps; ++w) xnorm2 += fred[w];
 
-    // ---- candidate keys into shared memory ----
-    int K;
-    if (count >= n && count <= a.cap) {
-        K = count;
-        const unsigned long long* src = a.cand + gv * a.cap;
-        for (int i = tid; i < K; i += kThreads) keys[i] = src[i];
-    } else {
-        // exact slow path: every atom's score on the FP32 pipe
-        K = N;
-        for (int j = tid; j < N; j += kThreads) {
-            const float r = row_dot<T, D>(A + (size_t)j * D, xs);
-            keys[j] = screen_key(r, j);
-        }
-        if (tid == 0) atomicAdd((unsigned long long*)&cnt[kCntFallback], 1ull);
-    }
-    __syncthreads();
-
-    // ---- the n largest keys: MSD radix select over 64-bit keys ----
-    unsigned long long prefix = 0ull, mask = 0ull;
-    uint32_t remaining = (uint32_t)n;
-    int shift = 56;
-    for (;; shift -= 8) {
-        for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
-        __syncthreads();
-        for (int i = tid; i < K; i += kThreads) {
-            const unsigned long long k = keys[i];
-            if ((k & mask) == prefix) atomicAdd(&hist[(uint32_t)(k >> shift) & 0xffu], 1u);
-        }
-        __syncthreads();
-        if (warp == 0) {
-            const int hi = 255 - 8 * lane;
-            uint32_t local = 0;
-#pragma unroll
-            for (int b = 0; b < 8; ++b) local += hist[hi - b];
-            uint32_t incl = local;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            const uint32_t above = incl - local;
-            if (above < remaining && remaining <= incl) {
-                uint32_t acc = above;
-                for (int b = 0; b < 8; ++b) {
-                    const uint32_t c = hist[hi - b];
-                    if (acc + c >= remaining) {
-                        kred[kWarps] = prefix | ((unsigned long long)(hi - b) << shift);
-                        misc[1] = remaining - acc;
-                        misc[2] = (c == remaining - acc) ? 1u : 0u;   // boundary bin taken whole
-                        break;
-                    }
-                    acc += c;
-                }
-            }
-        }
-        __syncthreads();
-        prefix = kred[kWarps];
-        remaining = misc[1];
-        mask |= 0xffull << shift;
-        if (misc[2] || shift == 0) break;
-    }
-    // selected: keys whose bits above `shift` are >= prefix's
-
-    // ---- compaction of the pool (candidate order) ----
-    {
-        uint32_t base = 0;
-        const unsigned long long lim = prefix >> shift;
-        for (int i0 = 0; i0 < K; i0 += kThreads) {
-            const int i = i0 + tid;
-            const unsigned long long k = (i < K) ? keys[i] : 0ull;
-            const uint32_t f = (i < K && (k >> shift) >= lim) ? 1u : 0u;
-            const unsigned bal = __ballot_sync(0xffffffffu, f);
-            if (lane == 0) scan_ws[warp] = __popc(bal);
-            __syncthreads();
-            uint32_t before = 0, total = 0;
-            for (int w = 0; w < kWarps; ++w) {
-                const uint32_t c = scan_ws[w];
-                before += (w < warp) ? c : 0u;
-                total += c;
-            }
-            if (f) {
-                const uint32_t pos = base + before + __popc(bal & ((1u << lane) - 1u));
-                if (pos < (uint32_t)n) {
-                    pid[pos] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
-                    a0[pos] = __uint_as_float((uint32_t)(k >> 32));
-                }
-            }
-            base += total;
-            __syncthreads();
-        }
-    }
+    // ---- the pool ----
+    const int K = sel::intake_keys<T, D>(a, gv, count, n, N, A, xs, keys, sc, cnt);
+    sel::top_n(keys, K, n, pid, a0, sc);
 
     if (a.pool_out) {
         for (int i = tid; i < n; i += kThreads) {
@@ -454,14 +362,23 @@ cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 
 }  // namespace
 
+static bool use_mma(const Shape& sh)
+{
+    if (sh.dtype != FADKV_F16) return false;
+    const char* f = getenv("FADKV_GREEDY");
+    return !(f && strcmp(f, "ffma") == 0);
+}
+
 size_t greedy_smem_bytes(const Shape& sh)
 {
+    if (use_mma(sh)) return greedy_mma_smem_bytes(sh);
     return greedy_layout(sh.n, sh.d, sh.dtype == FADKV_F16 ? 2 : 4, sh.N, cand_cap(sh.n)).total;
 }
 
 cudaError_t launch_greedy(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 {
     if (a.Vc <= 0) return cudaSuccess;
+    if (use_mma(sh)) return launch_greedy_mma(sh, a, st);
     if (sh.dtype == FADKV_F16) {
         if (sh.d == 128) return launch_t<__half, 128>(sh, a, st);
         return launch_t<__half, 64>(sh, a, st);

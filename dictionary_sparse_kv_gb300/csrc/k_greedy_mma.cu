@@ -1,0 +1,411 @@
+// In-pool greedy selection with a ridge refit after every pick -- binary16
+// dictionaries, pool correlations on the tensor cores.
+//
+// "FAD-KV: Adaptive Dictionary KV Caching for Efficient Reasoning Decoding":
+// abstract (screening-based sparse coding: a one-shot Top-n pool followed by
+// lightweight coefficient refinement) and Table 5 (ridge parameter
+// lambda = 1e-4 + 0.20 diag(G)).  Greedy selection inside the pool and the
+// lower-index tie rule are conventions of this library.
+//
+// Per vector x with pool P (exact Top-n from select.cuh):
+//   e_0 = x;  for k = 0..s-1:
+//     j* = argmax_{j in P \ S} |<d_j, e_k>|   (ties: lower atom index)
+//     S <- S + j*
+//     A = G_SS + diag(lambda_abs + lambda_rel G_ii),  A c = D_S x
+//     e_{k+1} = x - D_S c
+//   relres = ||e_s|| / ||x||
+//
+// One CTA of NW warps per vector; warp w owns pool slots 64w .. 64w+63.  The
+// pool's binary16 atoms stay in registers for the whole greedy loop, as the
+// A fragments of mma.sync.m16n8k16 (rows = atoms).  Each correlation pass
+// multiplies them by a B operand whose column 0 and 1 hold the residual
+// split in two binary16 terms, e*2^p = hi + lo (p from ||x||, so no term
+// overflows; the split leaves a relative error near 2^-22), and columns 2..7
+// zero: <d_j, e> = (acc_0 + acc_1) 2^-p, fp32 accumulation.  Inside each
+// 32-element block of the head dimension, thread t of a fragment row holds
+// the 8 consecutive elements 8t..8t+7 (one 16-byte load) -- a permutation of
+// the contraction index, applied identically to A and B, so the products are
+// unchanged.  The Cholesky factor of A grows by one row per pick.
+#include "select.cuh"
+
+namespace fadkv {
+namespace {
+
+template <int D>
+struct MmaLayout {
+    size_t keys, xs, es, sa, bsm, lm, z, c, gram, fred, kred, pid, mag, sslot, hist, scan, misc, pref, total;
+};
+
+__host__ __device__ inline size_t al(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+template <int D>
+__host__ __device__ inline MmaLayout<D> mma_layout(int n_pad, int N, int cap, int nw)
+{
+    MmaLayout<D> L;
+    size_t o = 0;
+    L.keys = o;  o += al((size_t)(N > cap ? N : cap) * 8, 16);
+    L.xs = o;    o += 4 * D;
+    L.es = o;    o += 4 * D;
+    L.sa = o;    o += 4 * (size_t)kMaxS * D;
+    L.bsm = o;   o += 2 * 8 * D;                 // B operand: 8 columns x D binary16
+    L.lm = o;    o += 4 * kMaxS * kMaxS;
+    L.z = o;     o += 4 * kMaxS;
+    L.c = o;     o += 4 * kMaxS;
+    L.gram = o;  o += 4 * (kMaxS + 4);
+    L.fred = o;  o += 4 * 2 * nw;
+    o = al(o, 8);
+    L.kred = o;  o += 8 * (nw + 1);
+    L.pref = o;  o += 8;
+    L.pid = o;   o += 4 * (size_t)n_pad;
+    L.mag = o;   o += 4 * (size_t)n_pad;
+    L.sslot = o; o += 4 * kMaxS;
+    L.hist = o;  o += 4 * 256;
+    L.scan = o;  o += 4 * nw;
+    L.misc = o;  o += 4 * (4 + kCountSlots);
+    L.total = al(o, 16);
+    return L;
+}
+
+__device__ __forceinline__ void hmma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long t = __shfl_xor_sync(0xffffffffu, v, o);
+        v = t > v ? t : v;
+    }
+    return v;
+}
+
+// Larger |a| first, then the lower atom index (atom < 2^23); the low 10
+// bits carry the pool slot, which never decides the order.
+__device__ __forceinline__ unsigned long long pick_key(float a, int atom, int slot)
+{
+    return ((unsigned long long)(__float_as_uint(a) & 0x7fffffffu) << 33) |
+           ((unsigned long long)(0x7fffffu - (unsigned)atom) << 10) | (unsigned long long)slot;
+}
+
+__device__ __forceinline__ void put8(float* dst, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3)
+{
+    const uint32_t w[4] = {w0, w1, w2, w3};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        dst[2 * i] = f.x;
+        dst[2 * i + 1] = f.y;
+    }
+}
+
+template <int D, int NW>
+__global__ void __launch_bounds__(NW * 32, (NW <= 4 ? 3 : 1))
+greedy_mma_kernel(Shape sh, GreedyArgs a)
+{
+    constexpr int KT = D / 16, KP = D / 32, NT = NW * 32;
+    const int vc = blockIdx.x, g = blockIdx.y;
+    const int v = a.v0 + vc;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int n = sh.n, s = sh.s, N = sh.N;
+    const int n_pad = NW * 64;
+
+    const MmaLayout<D> L = mma_layout<D>(n_pad, N, a.cap, NW);
+    extern __shared__ __align__(16) unsigned char smem[];
+    unsigned long long* keys = (unsigned long long*)(smem + L.keys);
+    float* xs = (float*)(smem + L.xs);
+    float* es = (float*)(smem + L.es);
+    float* SA = (float*)(smem + L.sa);
+    __half* Bsm = (__half*)(smem + L.bsm);
+    float* Lm = (float*)(smem + L.lm);
+    float* zz = (float*)(smem + L.z);
+    float* cc = (float*)(smem + L.c);
+    float* gram = (float*)(smem + L.gram);
+    float* fred = (float*)(smem + L.fred);
+    unsigned long long* kred = (unsigned long long*)(smem + L.kred);
+    int* pid = (int*)(smem + L.pid);
+    float* mag = (float*)(smem + L.mag);
+    int* sslot = (int*)(smem + L.sslot);
+    sel::Scratch sc{(uint32_t*)(smem + L.hist), (uint32_t*)(smem + L.scan), (uint32_t*)(smem + L.misc),
+                    (unsigned long long*)(smem + L.pref)};
+
+    const size_t gv = (size_t)g * a.Vc + vc;
+    const __half* X = (const __half*)a.x + ((size_t)g * a.V + v) * D;
+    const __half* Aglob = (const __half*)a.atoms + (size_t)g * N * D;
+    long long* cnt = a.counters + (size_t)g * kCntFields;
+
+    // ---- x, its norm and finiteness ----
+    float xsq = 0.f;
+    int bad = 0;
+    for (int t = tid; t < D; t += NT) {
+        const float xv = __half2float(X[t]);
+        xs[t] = xv;
+        bad |= !isfinite(xv);
+        xsq = fmaf(xv, xv, xsq);
+    }
+    xsq = warp_sum(xsq);
+    if (lane == 0) fred[warp] = xsq;
+    const int count = sel::intake_counts(a, gv, sc);
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        if (a.pool_out) {
+            for (int i = tid; i < n; i += NT) a.pool_out[((size_t)g * a.V + v) * n + i] = -1;
+            return;
+        }
+        for (int k = tid; k < s; k += NT) {
+            a.idx[((size_t)g * a.V + v) * s + k] = -1;
+            a.coef[((size_t)g * a.V + v) * s + k] = 0.f;
+        }
+        if (tid == 0) {
+            a.relres[(size_t)g * a.V + v] = __int_as_float(0x7fc00000);
+            atomicAdd((unsigned long long*)&cnt[kCntNonfinite], 1ull);
+            atomicOr((unsigned long long*)&cnt[kCntStatus], (unsigned long long)FADKV_DEV_NONFINITE_INPUT);
+        }
+        return;
+    }
+    float xnorm2 = 0.f;
+    for (int w = 0; w < NW; ++w) xnorm2 += fred[w];
+
+    // ---- the pool ----
+    const int K = sel::intake_keys<__half, D>(a, gv, count, n, N, Aglob, xs, keys, sc, cnt);
+    sel::top_n(keys, K, n, pid, mag, sc);
+    if (a.pool_out) {
+        for (int i = tid; i < n; i += NT) {
+            a.pool_out[((size_t)g * a.V + v) * n + i] = pid[i];
+            if (a.pool_r_out) a.pool_r_out[((size_t)g * a.V + v) * n + i] = mag[i];
+        }
+        return;
+    }
+
+    // ---- pool atoms -> A fragments (registers), B operand columns 2..7 = 0 ----
+    uint32_t Af[4][KT][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+        const int s0 = warp * 64 + mt * 16 + g8;
+        const int r0 = (s0 < n) ? pid[s0] : -1;
+        const int r1 = (s0 + 8 < n) ? pid[s0 + 8] : -1;
+#pragma unroll
+        for (int kp = 0; kp < KP; ++kp) {
+            uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+            if (r0 >= 0) q0 = *reinterpret_cast<const uint4*>(Aglob + (size_t)r0 * D + 32 * kp + 8 * t4);
+            if (r1 >= 0) q1 = *reinterpret_cast<const uint4*>(Aglob + (size_t)r1 * D + 32 * kp + 8 * t4);
+            Af[mt][2 * kp][0] = q0.x;
+            Af[mt][2 * kp][2] = q0.y;
+            Af[mt][2 * kp + 1][0] = q0.z;
+            Af[mt][2 * kp + 1][2] = q0.w;
+            Af[mt][2 * kp][1] = q1.x;
+            Af[mt][2 * kp][3] = q1.y;
+            Af[mt][2 * kp + 1][1] = q1.z;
+            Af[mt][2 * kp + 1][3] = q1.w;
+        }
+    }
+    for (int i = tid; i < 8 * D; i += NT) Bsm[i] = __float2half_rn(0.f);
+
+    // scale 2^p with ||e|| <= ||x|| < 2^ex: |e_t| 2^p < 2^14 (no binary16 overflow)
+    int ex = 0;
+    frexpf(sqrtf(xnorm2), &ex);
+    const float scale = (xnorm2 > 0.f) ? ldexpf(1.f, 14 - ex) : 1.f;
+    const float inv_scale = (xnorm2 > 0.f) ? ldexpf(1.f, ex - 14) : 1.f;
+
+    // per-lane correlations: lanes with t4 == 0 own slots
+    //   m = 2*mt + h  ->  slot 64*warp + 16*mt + 8*h + g8
+    float av[8];
+    unsigned live = 0;   // bit m: slot m is in the pool and not picked
+    if (t4 == 0) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int sl = warp * 64 + (m >> 1) * 16 + (m & 1) * 8 + g8;
+            av[m] = (sl < n) ? mag[sl] : 0.f;
+            if (sl < n) live |= 1u << m;
+        }
+    } else {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) av[m] = 0.f;
+    }
+    __syncthreads();
+
+    const float la = sh.lambda_abs, lr = sh.lambda_rel;
+    for (int k = 0; k < s; ++k) {
+        // ---- argmax over the live pool slots ----
+        unsigned long long best = 0ull;
+        if (t4 == 0) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                if ((live >> m) & 1u) {
+                    const int sl = warp * 64 + (m >> 1) * 16 + (m & 1) * 8 + g8;
+                    const unsigned long long key = pick_key(av[m], pid[sl], sl);
+                    best = key > best ? key : best;
+                }
+            }
+        }
+        best = warp_max_u64(best);
+        if (lane == 0) kred[warp] = best;
+        __syncthreads();
+        unsigned long long win = 0ull;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) win = kred[w] > win ? kred[w] : win;
+        const int slot = (int)(win & 0x3ffull);
+        const int w_o = slot >> 6, mt_o = (slot >> 4) & 3, h_o = (slot >> 3) & 1, g_o = slot & 7;
+        if (tid == 0) sslot[k] = slot;
+        if (warp == w_o && g8 == g_o) {
+            if (t4 == 0) live &= ~(1u << (2 * mt_o + h_o));
+            // the picked atom -> SA[k] (fp32) from this row's fragments
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                if (mt == mt_o) {
+#pragma unroll
+                    for (int kp = 0; kp < KP; ++kp) {
+                        const uint32_t w0 = h_o ? Af[mt][2 * kp][1] : Af[mt][2 * kp][0];
+                        const uint32_t w1 = h_o ? Af[mt][2 * kp][3] : Af[mt][2 * kp][2];
+                        const uint32_t w2 = h_o ? Af[mt][2 * kp + 1][1] : Af[mt][2 * kp + 1][0];
+                        const uint32_t w3 = h_o ? Af[mt][2 * kp + 1][3] : Af[mt][2 * kp + 1][2];
+                        put8(SA + k * D + 32 * kp + 8 * t4, w0, w1, w2, w3);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- Gram row of the new atom and its right-hand side ----
+        for (int i = warp; i <= k + 1; i += NW) {
+            const float* u = (i <= k) ? SA + i * D : xs;
+            const float* w = SA + k * D;
+            float acc = 0.f;
+            for (int t = lane; t < D; t += 32) acc = fmaf(u[t], w[t], acc);
+            acc = warp_sum(acc);
+            if (lane == 0) gram[i] = acc;
+        }
+        __syncthreads();
+
+        // ---- Cholesky row k, forward and back substitution (one thread) ----
+        if (tid == 0) {
+            float* Lk = Lm + k * kMaxS;
+            for (int i = 0; i < k; ++i) {
+                float val = gram[i];
+                const float* Li = Lm + i * kMaxS;
+                for (int m = 0; m < i; ++m) val = fmaf(-Li[m], Lk[m], val);
+                Lk[i] = val / Li[i];
+            }
+            float dk = fmaf(gram[k], lr, gram[k]) + la;
+            for (int m = 0; m < k; ++m) dk = fmaf(-Lk[m], Lk[m], dk);
+            if (!(dk > 0.f)) {
+                atomicOr((unsigned long long*)&cnt[kCntStatus], (unsigned long long)FADKV_DEV_NOT_SPD);
+                dk = 1e-30f;
+            }
+            const float lkk = sqrtf(dk);
+            Lk[k] = lkk;
+            float zk = gram[k + 1];
+            for (int m = 0; m < k; ++m) zk = fmaf(-Lk[m], zz[m], zk);
+            zz[k] = zk / lkk;
+            for (int i = k; i >= 0; --i) {
+                float val = zz[i];
+                for (int m = i + 1; m <= k; ++m) val = fmaf(-Lm[m * kMaxS + i], cc[m], val);
+                cc[i] = val / Lm[i * kMaxS + i];
+            }
+        }
+        __syncthreads();
+
+        // ---- residual e = x - D_S c, split into the B operand ----
+        for (int t = tid; t < D; t += NT) {
+            float val = xs[t];
+            for (int i = 0; i <= k; ++i) val = fmaf(-cc[i], SA[i * D + t], val);
+            es[t] = val;
+            const float sv = val * scale;
+            const __half hi = __float2half_rn(sv);
+            Bsm[t] = hi;
+            Bsm[D + t] = __float2half_rn(sv - __half2float(hi));
+        }
+        if (k + 1 == s) break;
+        __syncthreads();
+
+        // ---- correlations with the new residual on the tensor cores ----
+        float acc[4][4];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
+#pragma unroll
+        for (int kp = 0; kp < KP; ++kp) {
+            const uint4 qb = *reinterpret_cast<const uint4*>(Bsm + g8 * D + 32 * kp + 8 * t4);
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                hmma(acc[mt], Af[mt][2 * kp], qb.x, qb.y);
+                hmma(acc[mt], Af[mt][2 * kp + 1], qb.z, qb.w);
+            }
+        }
+        if (t4 == 0) {
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                av[2 * mt] = (acc[mt][0] + acc[mt][1]) * inv_scale;
+                av[2 * mt + 1] = (acc[mt][2] + acc[mt][3]) * inv_scale;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- outputs ----
+    float esq = 0.f;
+    for (int t = tid; t < D; t += NT) esq = fmaf(es[t], es[t], esq);
+    esq = warp_sum(esq);
+    if (lane == 0) fred[NW + warp] = esq;
+    __syncthreads();
+    if (tid == 0) {
+        float e2 = 0.f;
+        for (int w = 0; w < NW; ++w) e2 += fred[NW + w];
+        a.relres[(size_t)g * a.V + v] = (xnorm2 > 0.f) ? sqrtf(e2) / sqrtf(xnorm2) : 0.f;
+    }
+    for (int k = tid; k < s; k += NT) {
+        a.idx[((size_t)g * a.V + v) * s + k] = pid[sslot[k]];
+        a.coef[((size_t)g * a.V + v) * s + k] = cc[k];
+    }
+}
+
+template <int D, int NW>
+cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+{
+    const size_t smem = mma_layout<D>(NW * 64, sh.N, a.cap, NW).total;
+    auto k = greedy_mma_kernel<D, NW>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.Vc, sh.G);
+    k<<<grid, NW * 32, smem, st>>>(sh, a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+{
+    if (sh.n <= 256) return launch_t<D, 4>(sh, a, st);
+    if (sh.n <= 512) return launch_t<D, 8>(sh, a, st);
+    return launch_t<D, 16>(sh, a, st);
+}
+
+}  // namespace
+
+size_t greedy_mma_smem_bytes(const Shape& sh)
+{
+    const int nw = sh.n <= 256 ? 4 : (sh.n <= 512 ? 8 : 16);
+    return sh.d == 128 ? mma_layout<128>(nw * 64, sh.N, cand_cap(sh.n), nw).total
+                       : mma_layout<64>(nw * 64, sh.N, cand_cap(sh.n), nw).total;
+}
+
+cudaError_t launch_greedy_mma(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+{
+    if (a.Vc <= 0) return cudaSuccess;
+    return sh.d == 128 ? launch_d<128>(sh, a, st) : launch_d<64>(sh, a, st);
+}
+
+}  // namespace fadkv

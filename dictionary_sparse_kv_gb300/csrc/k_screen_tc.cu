@@ -12,16 +12,20 @@
 // two accumulator buffers so the epilogue of chunk c overlaps the MMAs of
 // chunk c+1.  Scores never reach HBM: the epilogue thread of vector v keeps
 // atom j only if |S[v][j]| >= tau_v and appends the 64-bit key
-// (bits(|S|) << 32) | (0xffffffff - j) to the vector's candidate list; the
-// exact Top-n (ties to the lower index) is then taken from that list.
-// tau_v = alpha * ||x_v|| / sqrt(d), with alpha set on the host so that an
-// atom uncorrelated with x_v passes with probability ~2n/N; lists that end
-// shorter than n or longer than their capacity are redone exactly by the
+// (bits(|S|) << 32) | (0xffffffff - j) to its own region of the vector's
+// candidate list -- one region per (atom slice, accumulator buffer), so
+// appends are plain stores, with no atomics and nothing to wait for; the
+// exact Top-n (ties to the lower index) is taken from the regions by the
+// consumer.  tau_v = alpha * ||x_v|| / sqrt(d), with alpha set on the host so
+// that an atom uncorrelated with x_v passes with probability ~2n/N; lists
+// that end shorter than n or overflow a region are redone exactly by the
 // consumer.
 //
-// Warp roles (256 threads): warp 0 issues TMA loads, warp 1 issues MMAs
-// (one thread), warp 2 owns the TMEM allocation, warps 4..7 are the epilogue
-// (warp 4+q reads TMEM lanes 32q..32q+31).  Every wait is bounded by a
+// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 issues MMAs
+// (one thread), warp 2 owns the TMEM allocation, warps 4..11 are the
+// epilogue (warp 4+e reads TMEM lanes 32(e%4).. and handles the chunks
+// whose accumulator buffer is e/4).  About 97 KB of shared memory and 256
+// TMEM columns per CTA: two CTAs share an SM.  Every wait is bounded by a
 // wall-clock limit; on expiry the CTA sets FADKV_DEV_TIMEOUT in the status
 // word, drains its own copies and MMAs (bounded), frees TMEM and returns.
 #include <cuda.h>
@@ -32,12 +36,11 @@
 namespace fadkv {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kTileV = 128;        // vectors per CTA (MMA M)
 constexpr int kChunk = 128;        // atoms per MMA chunk (MMA N)
-constexpr int kStages = 4;         // B (atom chunk) pipeline depth
+constexpr int kStages = 2;         // B (atom chunk) pipeline depth
 constexpr int kTmemCols = 2 * kChunk;
-constexpr int kStageEntries = 8;   // candidate staging per epilogue thread
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;   // 200 ms
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
@@ -160,23 +163,12 @@ struct SmemLayout {
     static constexpr int bar_off = b_off + kStages * kTileBytes;
     static constexpr int n_bars = 2 * kStages + 4 + 1;
     static constexpr int taddr_off = bar_off + n_bars * 8;
-    static constexpr int stage_off = (taddr_off + 4 + 15) / 16 * 16;
-    static constexpr int total = stage_off + 128 * kStageEntries * 8;
+    static constexpr int total = taddr_off + 16;
     static constexpr int alloc = total + 1024;                 // slack for 1024-byte alignment
 };
 
-// Append `cnt` staged keys to the vector's candidate list.
-__device__ __forceinline__ void flush_keys(const unsigned long long* stage, int cnt, int* count,
-                                           unsigned long long* list, int cap)
-{
-    if (cnt <= 0) return;
-    const int pos = atomicAdd(count, cnt);
-    for (int i = 0; i < cnt; ++i)
-        if (pos + i < cap) list[pos + i] = stage[i];
-}
-
 template <int D, bool kDump>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 screen_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_d,
                  ScreenTCArgs a)
 {
@@ -282,18 +274,22 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
         }
     } else if (warp >= 4) {
         // ---------------- epilogue ----------------
-        const int q = warp - 4;
-        const int r = q * 32 + lane;                       // TMEM lane = row of the vector tile
+        const int e = warp - 4;
+        const int q = e & 3;                                // TMEM lane group
+        const int hb = e >> 2;                              // accumulator buffer handled
+        const int r = q * 32 + lane;                        // TMEM lane = row of the vector tile
         const int vloc = tile * kTileV + r;                 // vector index inside the chunk
         const bool valid = vloc < a.Vc;
-        unsigned long long* stage = (unsigned long long*)(smem + L::stage_off) + (size_t)(q * 32 + lane) * kStageEntries;
-        int scnt = 0;
-        int* count = a.cand_count + (size_t)g * a.Vc + (valid ? vloc : 0);
-        unsigned long long* list = a.cand + ((size_t)g * a.Vc + (valid ? vloc : 0)) * a.cap;
-        float tau = 0.f;
+        const int region = slice * 2 + hb;
+        const int cs = a.cap / (2 * a.slices);              // entries per region
+        unsigned long long* list =
+            a.cand + ((size_t)g * a.Vc + (valid ? vloc : 0)) * a.cap + (size_t)region * cs;
+        uint32_t tau_bits = 0u;
+        int cnt = 0;
         bool ok = mbar_wait(afull_bar, 0, status);
         if (ok && !kDump) {
-            // ||x||^2 from this row of the swizzled A tile
+            // ||x||^2 from this row of the swizzled A tile (all 16-byte chunks
+            // of the row, whatever their swizzled order)
             float sq = 0.f;
 #pragma unroll
             for (int h = 0; h < L::KH; ++h) {
@@ -310,43 +306,45 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
                     }
                 }
             }
-            tau = a.alpha * sqrtf(sq * (1.0f / (float)D));
+            // rows past the batch never pass (|S| bits are below 0xffffffff)
+            tau_bits = valid ? __float_as_uint(a.alpha * sqrtf(sq * (1.0f / (float)D))) : 0xffffffffu;
         }
-        for (int c = 0; c < nch && ok; ++c) {
-            const int buf = c & 1;
+        for (int c = hb; c < nch && ok; c += 2) {
             const uint32_t bph = (uint32_t)(c >> 1) & 1u;
-            ok = mbar_wait(tfull_bar(buf), bph, status);
+            ok = mbar_wait(tfull_bar(hb), bph, status);
             if (!ok) break;
             tc_fence_after();
             const int atom0 = (c0 + c) * kChunk;
 #pragma unroll
             for (int qq = 0; qq < kChunk / 32; ++qq) {
                 uint32_t v[32];
-                tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kChunk + qq * 32), v);
-                if (!valid) continue;
+                tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(hb * kChunk + qq * 32), v);
                 if (kDump) {
-                    float* out = a.dump + ((size_t)g * a.Vc + vloc) * a.N + atom0 + qq * 32;
+                    if (valid) {
+                        float* out = a.dump + ((size_t)g * a.Vc + vloc) * a.N + atom0 + qq * 32;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(v[i]);
+                        for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(v[i]);
+                    }
                 } else {
+                    const uint32_t lo0 = 0xffffffffu - (uint32_t)(atom0 + qq * 32);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const uint32_t mag = v[i] & 0x7fffffffu;
-                        if (__uint_as_float(mag) >= tau) {
-                            const uint32_t j = (uint32_t)(atom0 + qq * 32 + i);
-                            stage[scnt++] = ((unsigned long long)mag << 32) | (unsigned long long)(0xffffffffu - j);
-                            if (scnt == kStageEntries) {
-                                flush_keys(stage, scnt, count, list, a.cap);
-                                scnt = 0;
-                            }
+                        if (mag >= tau_bits) {
+                            // past the region's end the last slot is reused:
+                            // the count then exceeds the region and the
+                            // consumer redoes the vector exactly
+                            list[min(cnt, cs - 1)] = ((unsigned long long)mag << 32) | (lo0 - (uint32_t)i);
+                            ++cnt;
                         }
                     }
                 }
             }
             tc_fence_before();
-            mbar_arrive(tempty_bar(buf));
+            mbar_arrive(tempty_bar(hb));
         }
-        if (valid && !kDump) flush_keys(stage, scnt, count, list, a.cap);
+        if (valid && !kDump)
+            a.cand_count[((size_t)g * a.Vc + vloc) * kCountSlots + region] = cnt;
     }
 
     tc_fence_before();
@@ -410,11 +408,15 @@ cudaError_t launch_t(const Shape& sh, const void* atoms, const void* x, int V, c
 
 int screen_tc_slices(const Shape& sh, int Vc, int sms)
 {
+    // two CTAs per SM; at least 64 entries per candidate region
     const int tiles = (Vc + kTileV - 1) / kTileV;
     const int nchunks = sh.N / kChunk;
-    int s = sms / (sh.G * tiles);
-    if (s < 1) s = 1;
+    int s = 2 * sms / (sh.G * tiles);
+    const int by_cap = cand_cap(sh.n) / 128;
+    if (s > by_cap) s = by_cap;
+    if (s > kMaxSlices) s = kMaxSlices;
     if (s > nchunks) s = nchunks;
+    if (s < 1) s = 1;
     return s;
 }
 

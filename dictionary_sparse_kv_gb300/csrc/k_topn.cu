@@ -68,7 +68,7 @@ topn_radix_kernel(const float* __restrict__ scores, int N, int n, int Vc, unsign
     if (__syncthreads_or(bad)) {
         // non-finite scores come only from a non-finite input, which the
         // consumer detects on its own; an empty list sends it there
-        if (tid == 0) cand_count[(size_t)g * Vc + v] = 0;
+        if (tid == 0) cand_count[((size_t)g * Vc + v) * kCountSlots] = 0;
         return;
     }
 
@@ -136,7 +136,7 @@ topn_radix_kernel(const float* __restrict__ scores, int N, int n, int Vc, unsign
         base_out += tot_gt + min(tot_eq, eq_left);
         base_eq += tot_eq;
     }
-    if (tid == 0) cand_count[(size_t)g * Vc + v] = n;
+    if (tid == 0) cand_count[((size_t)g * Vc + v) * kCountSlots] = n;
 }
 
 }  // namespace

@@ -114,3 +114,30 @@ def test_slow_path_short_and_overflowing_lists():
         cn = np.linalg.norm(res.coef[v])
         assert np.linalg.norm(coef[v] - res.coef[v]) <= PU.COEF_TOL * cn + 1e-7
         assert abs(rel[v] - res.relres[v]) <= PU.RELRES_TOL * res.relres[v] + 1e-7
+
+
+@pytest.mark.parametrize("name,G,V", [("decode_3b", 3, 200), ("decode_8b", 2, 64)])
+def test_greedy_kernels_agree(monkeypatch, name, G, V):
+    """The tensor-core greedy kernel (binary16 pools as mma.sync operands,
+    residual split in two binary16 terms) and the FP32-pipe kernel give the
+    same picks and coefficients within the parity tolerance, and both match
+    the oracle."""
+    from dataclasses import replace
+    w = replace(S.WORKLOADS[name], G=G)
+    data = S.WorkloadData(w)
+    x = data.inputs(0, V)
+    outs = {}
+    for path in ("mma", "ffma"):
+        if path == "ffma":
+            monkeypatch.setenv("FADKV_GREEDY", "ffma")
+        D = _dict(data.atoms, data.usage, data.deltas(), w.n, w.s, V)
+        c = D.new_codes(V)
+        D.encode(_t(x), c)
+        torch.cuda.synchronize()
+        outs[path] = tuple(t.cpu().numpy() for t in (c.idx, c.coef, c.relres))
+    p = PU.oparams(w)
+    for g in range(w.G):
+        res = O.encode_threaded(p, data.atoms[g], x[g], PU.THREADS)
+        for path in ("mma", "ffma"):
+            idx, coef, rel = outs[path]
+            PU.assert_encode_ok(PU.compare_encode(res, idx[g], coef[g], rel[g]))
