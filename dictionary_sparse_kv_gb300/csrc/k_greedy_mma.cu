@@ -17,15 +17,23 @@
 //
 // One CTA of NW warps per vector; warp w owns pool slots 64w .. 64w+63.  The
 // pool's binary16 atoms stay in registers for the whole greedy loop, as the
-// A fragments of mma.sync.m16n8k16 (rows = atoms).  Each correlation pass
-// multiplies them by a B operand whose column 0 and 1 hold the residual
-// split in two binary16 terms, e*2^p = hi + lo (p from ||x||, so no term
-// overflows; the split leaves a relative error near 2^-22), and columns 2..7
-// zero: <d_j, e> = (acc_0 + acc_1) 2^-p, fp32 accumulation.  Inside each
+// A fragments of mma.sync.m16n8k16 (rows = atoms).  Every pass multiplies
+// them by an 8-column B operand (fp32 accumulation):
+//   columns 0, 1: the residual split in two binary16 terms, e 2^p = hi + lo
+//                 (p from ||x||, so no term overflows; the split leaves a
+//                 relative error near 2^-22): <d_j, e> = (acc_0 + acc_1) 2^-p;
+//   column 2:     the atom picked last (exact in binary16): its Gram column
+//                 <d_j, d_pick> over the pool, kept in shared memory, so the
+//                 next refit reads its Gram row instead of computing it.
+// The first pass takes x instead of e: the signed scores r_j of the pool
+// (step-0 correlations and the refit's right-hand sides).  Inside each
 // 32-element block of the head dimension, thread t of a fragment row holds
 // the 8 consecutive elements 8t..8t+7 (one 16-byte load) -- a permutation of
 // the contraction index, applied identically to A and B, so the products are
-// unchanged.  The Cholesky factor of A grows by one row per pick.
+// unchanged.  The refit grows the Cholesky factor of A by one row per pick
+// (forward and back substitution by one thread, partial sums in registers,
+// reciprocal diagonal), overlapped with the copy of the picked atom.
+// Three barriers per step.
 #include "select.cuh"
 
 namespace fadkv {
@@ -33,7 +41,8 @@ namespace {
 
 template <int D>
 struct MmaLayout {
-    size_t keys, xs, es, sa, bsm, lm, z, c, gram, fred, kred, pid, mag, sslot, hist, scan, misc, pref, total;
+    size_t keys, xs, es, sa, bsm, lm, z, c, gram, gcol, rsl, nrm, fred, kred, pid, mag, sslot, hist, scan, misc, pref,
+        total;
 };
 
 __host__ __device__ inline size_t al(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -51,7 +60,10 @@ __host__ __device__ inline MmaLayout<D> mma_layout(int n_pad, int N, int cap, in
     L.lm = o;    o += 4 * kMaxS * kMaxS;
     L.z = o;     o += 4 * kMaxS;
     L.c = o;     o += 4 * kMaxS;
-    L.gram = o;  o += 4 * (kMaxS + 4);
+    L.gram = o;  o += 4 * kMaxS;                 // reciprocal diagonal of the factor
+    L.gcol = o;  o += 4 * (size_t)n_pad * kMaxS; // Gram columns of the picks: [slot][i]
+    L.rsl = o;   o += 4 * (size_t)n_pad;         // signed scores of the pool
+    L.nrm = o;   o += 4 * (size_t)n_pad;         // squared norms of the pool atoms
     L.fred = o;  o += 4 * 2 * nw;
     o = al(o, 8);
     L.kred = o;  o += 8 * (nw + 1);
@@ -111,7 +123,57 @@ __device__ __forceinline__ void put8(float* dst, uint32_t w0, uint32_t w1, uint3
     }
 }
 
-template <int D, int NW>
+// One pick of the ridge refit: grows the Cholesky factor L of
+// A = G_SS + diag(lambda_abs + lambda_rel G_ii) by row k and solves
+// A c = D_S x.  grow[0..k) = <d_i, d_new>, gkk = ||d_new||^2, bk = <d_new, x>.
+// L (row-major, stride kMaxS), its reciprocal diagonal invd, z = L^-1 b and
+// c live in shared memory; partial sums stay in registers so each step of
+// the forward and back substitution is one dependent fused multiply-add.
+template <int SMAX>
+__device__ __forceinline__ void refit_step(int k, const float* grow, float gkk, float bk, float la, float lr,
+                                           float* Lm, float* invd, float* zz, float* cc,
+                                           unsigned long long* status)
+{
+    float p[SMAX];
+#pragma unroll
+    for (int i = 0; i < SMAX; ++i) p[i] = (i < k) ? grow[i] : 0.f;
+    float ll = 0.f, lz = 0.f;
+#pragma unroll
+    for (int m = 0; m < SMAX; ++m) {
+        if (m < k) {
+            const float lm = p[m] * invd[m];
+            Lm[k * kMaxS + m] = lm;
+            ll = fmaf(lm, lm, ll);
+            lz = fmaf(lm, zz[m], lz);
+#pragma unroll
+            for (int i = m + 1; i < SMAX; ++i)
+                if (i < k) p[i] = fmaf(-Lm[i * kMaxS + m], lm, p[i]);
+        }
+    }
+    float dk = fmaf(gkk, lr, gkk) + la - ll;
+    if (!(dk > 0.f)) {
+        atomicOr(status, (unsigned long long)FADKV_DEV_NOT_SPD);
+        dk = 1e-30f;
+    }
+    const float lkk = sqrtf(dk);
+    const float inv = __frcp_rn(lkk);
+    Lm[k * kMaxS + k] = lkk;
+    invd[k] = inv;
+    zz[k] = (bk - lz) * inv;
+#pragma unroll
+    for (int i = 0; i < SMAX; ++i) p[i] = (i <= k) ? zz[i] : 0.f;
+#pragma unroll
+    for (int m = SMAX - 1; m >= 0; --m) {
+        if (m <= k) {
+            const float cm = p[m] * invd[m];
+            cc[m] = cm;
+#pragma unroll
+            for (int i = 0; i < m; ++i) p[i] = fmaf(-Lm[m * kMaxS + i], cm, p[i]);
+        }
+    }
+}
+
+template <int D, int NW, int SMAX>
 __global__ void __launch_bounds__(NW * 32, (NW <= 4 ? 3 : 1))
 greedy_mma_kernel(Shape sh, GreedyArgs a)
 {
@@ -190,13 +252,17 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
         return;
     }
 
-    // ---- pool atoms -> A fragments (registers), B operand columns 2..7 = 0 ----
+    // ---- pool atoms -> A fragments (registers), squared norms ----
+    float* gcol = (float*)(smem + L.gcol);
+    float* rsl = (float*)(smem + L.rsl);
+    float* nrm = (float*)(smem + L.nrm);
     uint32_t Af[4][KT][4];
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) {
         const int s0 = warp * 64 + mt * 16 + g8;
         const int r0 = (s0 < n) ? pid[s0] : -1;
         const int r1 = (s0 + 8 < n) ? pid[s0 + 8] : -1;
+        float n0 = 0.f, n1 = 0.f;
 #pragma unroll
         for (int kp = 0; kp < KP; ++kp) {
             uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
@@ -210,9 +276,24 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
             Af[mt][2 * kp][3] = q1.y;
             Af[mt][2 * kp + 1][1] = q1.z;
             Af[mt][2 * kp + 1][3] = q1.w;
+            const __half2* h0 = reinterpret_cast<const __half2*>(&q0);
+            const __half2* h1 = reinterpret_cast<const __half2*>(&q1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f0 = __half22float2(h0[i]), f1 = __half22float2(h1[i]);
+                n0 = fmaf(f0.x, f0.x, fmaf(f0.y, f0.y, n0));
+                n1 = fmaf(f1.x, f1.x, fmaf(f1.y, f1.y, n1));
+            }
+        }
+        n0 += __shfl_xor_sync(0xffffffffu, n0, 1);
+        n0 += __shfl_xor_sync(0xffffffffu, n0, 2);
+        n1 += __shfl_xor_sync(0xffffffffu, n1, 1);
+        n1 += __shfl_xor_sync(0xffffffffu, n1, 2);
+        if (t4 == 0) {
+            nrm[s0] = n0;
+            nrm[s0 + 8] = n1;
         }
     }
-    for (int i = tid; i < 8 * D; i += NT) Bsm[i] = __float2half_rn(0.f);
 
     // scale 2^p with ||e|| <= ||x|| < 2^ex: |e_t| 2^p < 2^14 (no binary16 overflow)
     int ex = 0;
@@ -220,119 +301,20 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
     const float scale = (xnorm2 > 0.f) ? ldexpf(1.f, 14 - ex) : 1.f;
     const float inv_scale = (xnorm2 > 0.f) ? ldexpf(1.f, ex - 14) : 1.f;
 
-    // per-lane correlations: lanes with t4 == 0 own slots
-    //   m = 2*mt + h  ->  slot 64*warp + 16*mt + 8*h + g8
-    float av[8];
-    unsigned live = 0;   // bit m: slot m is in the pool and not picked
-    if (t4 == 0) {
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int sl = warp * 64 + (m >> 1) * 16 + (m & 1) * 8 + g8;
-            av[m] = (sl < n) ? mag[sl] : 0.f;
-            if (sl < n) live |= 1u << m;
+    // B operand of the first pass: x split into columns 0, 1; the rest 0
+    for (int i = tid; i < 8 * D; i += NT) {
+        __half val = __float2half_rn(0.f);
+        if (i < 2 * D) {
+            const float sv = xs[i % D] * scale;
+            const __half hi = __float2half_rn(sv);
+            val = (i < D) ? hi : __float2half_rn(sv - __half2float(hi));
         }
-    } else {
-#pragma unroll
-        for (int m = 0; m < 8; ++m) av[m] = 0.f;
+        Bsm[i] = val;
     }
     __syncthreads();
 
-    const float la = sh.lambda_abs, lr = sh.lambda_rel;
-    for (int k = 0; k < s; ++k) {
-        // ---- argmax over the live pool slots ----
-        unsigned long long best = 0ull;
-        if (t4 == 0) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                if ((live >> m) & 1u) {
-                    const int sl = warp * 64 + (m >> 1) * 16 + (m & 1) * 8 + g8;
-                    const unsigned long long key = pick_key(av[m], pid[sl], sl);
-                    best = key > best ? key : best;
-                }
-            }
-        }
-        best = warp_max_u64(best);
-        if (lane == 0) kred[warp] = best;
-        __syncthreads();
-        unsigned long long win = 0ull;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) win = kred[w] > win ? kred[w] : win;
-        const int slot = (int)(win & 0x3ffull);
-        const int w_o = slot >> 6, mt_o = (slot >> 4) & 3, h_o = (slot >> 3) & 1, g_o = slot & 7;
-        if (tid == 0) sslot[k] = slot;
-        if (warp == w_o && g8 == g_o) {
-            if (t4 == 0) live &= ~(1u << (2 * mt_o + h_o));
-            // the picked atom -> SA[k] (fp32) from this row's fragments
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                if (mt == mt_o) {
-#pragma unroll
-                    for (int kp = 0; kp < KP; ++kp) {
-                        const uint32_t w0 = h_o ? Af[mt][2 * kp][1] : Af[mt][2 * kp][0];
-                        const uint32_t w1 = h_o ? Af[mt][2 * kp][3] : Af[mt][2 * kp][2];
-                        const uint32_t w2 = h_o ? Af[mt][2 * kp + 1][1] : Af[mt][2 * kp + 1][0];
-                        const uint32_t w3 = h_o ? Af[mt][2 * kp + 1][3] : Af[mt][2 * kp + 1][2];
-                        put8(SA + k * D + 32 * kp + 8 * t4, w0, w1, w2, w3);
-                    }
-                }
-            }
-        }
-        __syncthreads();
-
-        // ---- Gram row of the new atom and its right-hand side ----
-        for (int i = warp; i <= k + 1; i += NW) {
-            const float* u = (i <= k) ? SA + i * D : xs;
-            const float* w = SA + k * D;
-            float acc = 0.f;
-            for (int t = lane; t < D; t += 32) acc = fmaf(u[t], w[t], acc);
-            acc = warp_sum(acc);
-            if (lane == 0) gram[i] = acc;
-        }
-        __syncthreads();
-
-        // ---- Cholesky row k, forward and back substitution (one thread) ----
-        if (tid == 0) {
-            float* Lk = Lm + k * kMaxS;
-            for (int i = 0; i < k; ++i) {
-                float val = gram[i];
-                const float* Li = Lm + i * kMaxS;
-                for (int m = 0; m < i; ++m) val = fmaf(-Li[m], Lk[m], val);
-                Lk[i] = val / Li[i];
-            }
-            float dk = fmaf(gram[k], lr, gram[k]) + la;
-            for (int m = 0; m < k; ++m) dk = fmaf(-Lk[m], Lk[m], dk);
-            if (!(dk > 0.f)) {
-                atomicOr((unsigned long long*)&cnt[kCntStatus], (unsigned long long)FADKV_DEV_NOT_SPD);
-                dk = 1e-30f;
-            }
-            const float lkk = sqrtf(dk);
-            Lk[k] = lkk;
-            float zk = gram[k + 1];
-            for (int m = 0; m < k; ++m) zk = fmaf(-Lk[m], zz[m], zk);
-            zz[k] = zk / lkk;
-            for (int i = k; i >= 0; --i) {
-                float val = zz[i];
-                for (int m = i + 1; m <= k; ++m) val = fmaf(-Lm[m * kMaxS + i], cc[m], val);
-                cc[i] = val / Lm[i * kMaxS + i];
-            }
-        }
-        __syncthreads();
-
-        // ---- residual e = x - D_S c, split into the B operand ----
-        for (int t = tid; t < D; t += NT) {
-            float val = xs[t];
-            for (int i = 0; i <= k; ++i) val = fmaf(-cc[i], SA[i * D + t], val);
-            es[t] = val;
-            const float sv = val * scale;
-            const __half hi = __float2half_rn(sv);
-            Bsm[t] = hi;
-            Bsm[D + t] = __float2half_rn(sv - __half2float(hi));
-        }
-        if (k + 1 == s) break;
-        __syncthreads();
-
-        // ---- correlations with the new residual on the tensor cores ----
-        float acc[4][4];
+    float acc[4][4];
+    auto mma_pass = [&]() {
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
@@ -346,11 +328,110 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
                 hmma(acc[mt], Af[mt][2 * kp + 1], qb.z, qb.w);
             }
         }
+    };
+
+    // ---- first pass: signed scores of the pool, step-0 correlations ----
+    // lanes with t4 == 0 own slots m = 2*mt + h -> 64*warp + 16*mt + 8*h + g8
+    mma_pass();
+    float av[8];
+    unsigned live = 0;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+        const float r0 = (acc[mt][0] + acc[mt][1]) * inv_scale;
+        const float r1 = (acc[mt][2] + acc[mt][3]) * inv_scale;
+        av[2 * mt] = r0;
+        av[2 * mt + 1] = r1;
+        const int s0 = warp * 64 + mt * 16 + g8;
+        if (t4 == 0) {
+            rsl[s0] = r0;
+            rsl[s0 + 8] = r1;
+            if (s0 < n) live |= 1u << (2 * mt);
+            if (s0 + 8 < n) live |= 1u << (2 * mt + 1);
+        }
+    }
+    __syncthreads();
+
+    const float la = sh.lambda_abs, lr = sh.lambda_rel;
+    unsigned long long* status = (unsigned long long*)&cnt[kCntStatus];
+    for (int k = 0; k < s; ++k) {
+        // ---- argmax over the live pool slots (lanes t4 == 0 hold them) ----
+        unsigned long long best = 0ull;
+        if (t4 == 0) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                if ((live >> m) & 1u) {
+                    const int sl = warp * 64 + (m >> 1) * 16 + (m & 1) * 8 + g8;
+                    const unsigned long long key = pick_key(av[m], pid[sl], sl);
+                    best = key > best ? key : best;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            const unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
+            best = t > best ? t : best;
+        }
+        if (lane == 0) kred[warp] = best;
+        __syncthreads();
+        unsigned long long win = 0ull;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) win = kred[w] > win ? kred[w] : win;
+        const int slot = (int)(win & 0x3ffull);
+        const int w_o = slot >> 6, mt_o = (slot >> 4) & 3, h_o = (slot >> 3) & 1, g_o = slot & 7;
+
+        // ---- the picked atom: fp32 copy SA[k] and B column 2 (owner lanes) ----
+        if (warp == w_o && g8 == g_o) {
+            if (t4 == 0) live &= ~(1u << (2 * mt_o + h_o));
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                if (mt == mt_o) {
+#pragma unroll
+                    for (int kp = 0; kp < KP; ++kp) {
+                        const uint32_t w0 = h_o ? Af[mt][2 * kp][1] : Af[mt][2 * kp][0];
+                        const uint32_t w1 = h_o ? Af[mt][2 * kp][3] : Af[mt][2 * kp][2];
+                        const uint32_t w2 = h_o ? Af[mt][2 * kp + 1][1] : Af[mt][2 * kp + 1][0];
+                        const uint32_t w3 = h_o ? Af[mt][2 * kp + 1][3] : Af[mt][2 * kp + 1][2];
+                        put8(SA + k * D + 32 * kp + 8 * t4, w0, w1, w2, w3);
+                        *reinterpret_cast<uint4*>(Bsm + 2 * D + 32 * kp + 8 * t4) = make_uint4(w0, w1, w2, w3);
+                    }
+                }
+            }
+        }
+        // ---- ridge refit, one thread outside the owner warp ----
+        if (tid == ((w_o + 1) % NW) * 32) {
+            sslot[k] = slot;
+            refit_step<SMAX>(k, gcol + (size_t)slot * kMaxS, nrm[slot], rsl[slot], la, lr, Lm, gram, zz, cc,
+                             status);
+        }
+        __syncthreads();
+
+        // ---- residual e = x - D_S c, split into B columns 0, 1 ----
+        for (int t = tid; t < D; t += NT) {
+            float val = xs[t];
+            for (int i = 0; i <= k; ++i) val = fmaf(-cc[i], SA[i * D + t], val);
+            es[t] = val;
+            const float sv = val * scale;
+            const __half hi = __float2half_rn(sv);
+            Bsm[t] = hi;
+            Bsm[D + t] = __float2half_rn(sv - __half2float(hi));
+        }
+        if (k + 1 == s) break;
+        __syncthreads();
+
+        // ---- correlations with the new residual; Gram column of the pick ----
+        mma_pass();
         if (t4 == 0) {
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt) {
                 av[2 * mt] = (acc[mt][0] + acc[mt][1]) * inv_scale;
                 av[2 * mt + 1] = (acc[mt][2] + acc[mt][3]) * inv_scale;
+            }
+        } else if (t4 == 1) {
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                const int s0 = warp * 64 + mt * 16 + g8;
+                gcol[(size_t)s0 * kMaxS + k] = acc[mt][0];
+                gcol[(size_t)(s0 + 8) * kMaxS + k] = acc[mt][2];
             }
         }
     }
@@ -373,11 +454,11 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
     }
 }
 
-template <int D, int NW>
+template <int D, int NW, int SMAX>
 cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 {
     const size_t smem = mma_layout<D>(NW * 64, sh.N, a.cap, NW).total;
-    auto k = greedy_mma_kernel<D, NW>;
+    auto k = greedy_mma_kernel<D, NW, SMAX>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Vc, sh.G);
@@ -385,12 +466,20 @@ cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
     return cudaGetLastError();
 }
 
+template <int D, int NW>
+cudaError_t launch_s(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+{
+    if (sh.s <= 8) return launch_t<D, NW, 8>(sh, a, st);
+    if (sh.s <= 16) return launch_t<D, NW, 16>(sh, a, st);
+    return launch_t<D, NW, 32>(sh, a, st);
+}
+
 template <int D>
 cudaError_t launch_d(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 {
-    if (sh.n <= 256) return launch_t<D, 4>(sh, a, st);
-    if (sh.n <= 512) return launch_t<D, 8>(sh, a, st);
-    return launch_t<D, 16>(sh, a, st);
+    if (sh.n <= 256) return launch_s<D, 4>(sh, a, st);
+    if (sh.n <= 512) return launch_s<D, 8>(sh, a, st);
+    return launch_s<D, 16>(sh, a, st);
 }
 
 }  // namespace
