@@ -30,10 +30,9 @@
 // 32-element block of the head dimension, thread t of a fragment row holds
 // the 8 consecutive elements 8t..8t+7 (one 16-byte load) -- a permutation of
 // the contraction index, applied identically to A and B, so the products are
-// unchanged.  The refit grows the Cholesky factor of A by one row per pick
-// (forward and back substitution by one thread, partial sums in registers,
-// reciprocal diagonal), overlapped with the copy of the picked atom.
-// Three barriers per step.
+// unchanged.  The refit updates the inverse Cholesky factor of A by one row
+// per pick on one warp (see refit_warp), overlapped with the copy of the
+// picked atom.  Three barriers per step.
 #include "select.cuh"
 
 namespace fadkv {
@@ -57,10 +56,10 @@ __host__ __device__ inline MmaLayout<D> mma_layout(int n_pad, int N, int cap, in
     L.es = o;    o += 4 * D;
     L.sa = o;    o += 4 * (size_t)kMaxS * D;
     L.bsm = o;   o += 2 * 8 * D;                 // B operand: 8 columns x D binary16
-    L.lm = o;    o += 4 * kMaxS * kMaxS;
+    L.lm = o;    o += 4 * kMaxS * (kMaxS + 1);    // inverse Cholesky factor, padded rows
     L.z = o;     o += 4 * kMaxS;
     L.c = o;     o += 4 * kMaxS;
-    L.gram = o;  o += 4 * kMaxS;                 // reciprocal diagonal of the factor
+    L.gram = o;  o += 4 * kMaxS;                 // l of the current refit
     L.gcol = o;  o += 4 * (size_t)n_pad * kMaxS; // Gram columns of the picks: [slot][i]
     L.rsl = o;   o += 4 * (size_t)n_pad;         // signed scores of the pool
     L.nrm = o;   o += 4 * (size_t)n_pad;         // squared norms of the pool atoms
@@ -123,54 +122,53 @@ __device__ __forceinline__ void put8(float* dst, uint32_t w0, uint32_t w1, uint3
     }
 }
 
-// One pick of the ridge refit: grows the Cholesky factor L of
-// A = G_SS + diag(lambda_abs + lambda_rel G_ii) by row k and solves
-// A c = D_S x.  grow[0..k) = <d_i, d_new>, gkk = ||d_new||^2, bk = <d_new, x>.
-// L (row-major, stride kMaxS), its reciprocal diagonal invd, z = L^-1 b and
-// c live in shared memory; partial sums stay in registers so each step of
-// the forward and back substitution is one dependent fused multiply-add.
-template <int SMAX>
-__device__ __forceinline__ void refit_step(int k, const float* grow, float gkk, float bk, float la, float lr,
-                                           float* Lm, float* invd, float* zz, float* cc,
+// One pick of the ridge refit, by one warp.  With A = G_SS + diag(lambda_abs
+// + lambda_rel G_ii) = L L^T, the warp keeps M = L^-1 (lower triangular,
+// rows padded to kMaxS + 1 floats), z = M b and c = M^T z = A^-1 b.  Adding
+// pick k with Gram row g = <d_i, d_new> (i < k), gkk = ||d_new||^2 and
+// bk = <d_new, x>:
+//   l = M g,  L_kk = sqrt(gkk (1 + lambda_rel) + lambda_abs - l.l),
+//   z_k = (bk - l.z) / L_kk,  w = -(l^T M) / L_kk  (the new row of M),
+//   c <- c + z_k w,  c_k = z_k / L_kk.
+// Lane i owns row i (for l) and column i (for w and c): O(k) work per lane.
+constexpr int kMS = kMaxS + 1;   // padded row stride of M (conflict-free rows and columns)
+
+__device__ __forceinline__ void refit_warp(int k, int lane, const float* grow, float gkk, float bk, float la, float lr,
+                                           float* M, float* lbuf, float* zz, float* cc,
                                            unsigned long long* status)
 {
-    float p[SMAX];
+    float li = 0.f;
+    if (lane < k) {
+        for (int m = 0; m <= lane; ++m) li = fmaf(M[lane * kMS + m], grow[m], li);
+        lbuf[lane] = li;
+    }
+    float ll = li * li;
+    float lz = (lane < k) ? li * zz[lane] : 0.f;
 #pragma unroll
-    for (int i = 0; i < SMAX; ++i) p[i] = (i < k) ? grow[i] : 0.f;
-    float ll = 0.f, lz = 0.f;
-#pragma unroll
-    for (int m = 0; m < SMAX; ++m) {
-        if (m < k) {
-            const float lm = p[m] * invd[m];
-            Lm[k * kMaxS + m] = lm;
-            ll = fmaf(lm, lm, ll);
-            lz = fmaf(lm, zz[m], lz);
-#pragma unroll
-            for (int i = m + 1; i < SMAX; ++i)
-                if (i < k) p[i] = fmaf(-Lm[i * kMaxS + m], lm, p[i]);
-        }
+    for (int o = 16; o > 0; o >>= 1) {
+        ll += __shfl_xor_sync(0xffffffffu, ll, o);
+        lz += __shfl_xor_sync(0xffffffffu, lz, o);
     }
     float dk = fmaf(gkk, lr, gkk) + la - ll;
     if (!(dk > 0.f)) {
-        atomicOr(status, (unsigned long long)FADKV_DEV_NOT_SPD);
+        if (lane == 0) atomicOr(status, (unsigned long long)FADKV_DEV_NOT_SPD);
         dk = 1e-30f;
     }
-    const float lkk = sqrtf(dk);
-    const float inv = __frcp_rn(lkk);
-    Lm[k * kMaxS + k] = lkk;
-    invd[k] = inv;
-    zz[k] = (bk - lz) * inv;
-#pragma unroll
-    for (int i = 0; i < SMAX; ++i) p[i] = (i <= k) ? zz[i] : 0.f;
-#pragma unroll
-    for (int m = SMAX - 1; m >= 0; --m) {
-        if (m <= k) {
-            const float cm = p[m] * invd[m];
-            cc[m] = cm;
-#pragma unroll
-            for (int i = 0; i < m; ++i) p[i] = fmaf(-Lm[m * kMaxS + i], cm, p[i]);
-        }
+    const float inv = __frcp_rn(sqrtf(dk));
+    const float zk = (bk - lz) * inv;
+    __syncwarp();
+    if (lane < k) {
+        float acc = 0.f;
+        for (int i = lane; i < k; ++i) acc = fmaf(lbuf[i], M[i * kMS + lane], acc);
+        const float w = -acc * inv;
+        M[k * kMS + lane] = w;
+        cc[lane] = fmaf(zk, w, cc[lane]);
+    } else if (lane == k) {
+        M[k * kMS + k] = inv;
+        zz[k] = zk;
+        cc[k] = zk * inv;
     }
+    __syncwarp();
 }
 
 template <int D, int NW, int SMAX>
@@ -397,18 +395,20 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
                 }
             }
         }
-        // ---- ridge refit, one thread outside the owner warp ----
-        if (tid == ((w_o + 1) % NW) * 32) {
-            sslot[k] = slot;
-            refit_step<SMAX>(k, gcol + (size_t)slot * kMaxS, nrm[slot], rsl[slot], la, lr, Lm, gram, zz, cc,
-                             status);
+        // ---- ridge refit, by the warp after the owner warp ----
+        if (warp == (w_o + 1) % NW) {
+            if (lane == 0) sslot[k] = slot;
+            refit_warp(k, lane, gcol + (size_t)slot * kMaxS, nrm[slot], rsl[slot], la, lr, Lm, gram, zz, cc,
+                       status);
         }
         __syncthreads();
 
         // ---- residual e = x - D_S c, split into B columns 0, 1 ----
         for (int t = tid; t < D; t += NT) {
             float val = xs[t];
-            for (int i = 0; i <= k; ++i) val = fmaf(-cc[i], SA[i * D + t], val);
+#pragma unroll
+            for (int i = 0; i < SMAX; ++i)
+                if (i <= k) val = fmaf(-cc[i], SA[i * D + t], val);
             es[t] = val;
             const float sv = val * scale;
             const __half hi = __float2half_rn(sv);

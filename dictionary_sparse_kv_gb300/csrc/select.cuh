@@ -167,9 +167,15 @@ __device__ __forceinline__ void top_n(const unsigned long long* keys, int K, int
     for (;; shift -= 8) {
         for (int i = tid; i < 256; i += nt) sc.hist[i] = 0;
         __syncthreads();
-        for (int i = tid; i < K; i += nt) {
-            const unsigned long long k = keys[i];
-            if ((k & mask) == prefix) atomicAdd(&sc.hist[(uint32_t)(k >> shift) & 0xffu], 1u);
+        for (int i0 = 0; i0 < K; i0 += nt) {
+            // one shared-memory atomic per distinct bin per warp: keys crowd
+            // into few bins in the first passes
+            const int i = i0 + tid;
+            const unsigned long long k = (i < K) ? keys[i] : 0ull;
+            const bool in = (i < K) && (k & mask) == prefix;
+            const uint32_t bin = in ? ((uint32_t)(k >> shift) & 0xffu) : 0x100u;
+            const unsigned peers = __match_any_sync(0xffffffffu, bin);
+            if (in && (__ffs(peers) - 1) == lane) atomicAdd(&sc.hist[bin], (uint32_t)__popc(peers));
         }
         __syncthreads();
         if (warp == 0) {
