@@ -51,7 +51,7 @@ struct Layout {
     bool tc;     // screening on tensor cores with candidate filtering
     int chunk;   // vectors per dictionary per encode pass
     int cap;     // candidate capacity per vector
-    size_t counters, scores, cand, cand_count, inactive, flagged, total;
+    size_t counters, scores, cand, cand_count, pool, inactive, flagged, total;
 };
 
 Layout make_layout(const fadkv_params& p)
@@ -71,6 +71,7 @@ Layout make_layout(const fadkv_params& p)
     L.scores = o;     o = align_up(o + (L.tc ? 0 : G * chunk * (size_t)p.N * sizeof(float)), kAlign);
     L.cand = o;       o = align_up(o + G * chunk * (size_t)L.cap * 8, kAlign);
     L.cand_count = o; o = align_up(o + G * chunk * kCountSlots * sizeof(int), kAlign);
+    L.pool = o;       o = align_up(o + (L.tc ? G * chunk * (size_t)p.n * sizeof(int32_t) : 0), kAlign);
     L.inactive = o;   o = align_up(o + G * (size_t)p.N * sizeof(int32_t), kAlign);
     L.flagged = o;    o = align_up(o + G * mb * sizeof(int32_t), kAlign);
     L.total = o;
@@ -218,7 +219,18 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
         a.cand_count = cand_count_buf(h);
         a.dump = dump;
         a.counters = counters(h);
-        return traced(h, FADKV_K_SCREEN, st, [&] { return launch_screen_tc(h->sh, h->atoms, x, V, a, h->sms, st); });
+        e = traced(h, FADKV_K_SCREEN, st, [&] { return launch_screen_tc(h->sh, h->atoms, x, V, a, h->sms, st); });
+        if (e != cudaSuccess || dump) return e;
+        SelectArgs sa;
+        sa.G = h->p.num_dicts;
+        sa.Vc = Vc;
+        sa.n = h->p.n;
+        sa.cap = h->L.cap;
+        sa.slices = a.slices;
+        sa.cand = cand_buf(h);
+        sa.cand_count = cand_count_buf(h);
+        sa.pool = (int32_t*)(h->ws + h->L.pool);
+        return traced(h, FADKV_K_TOPN, st, [&] { return launch_select(sa, st); });
     }
     float* scores = dump ? dump : (float*)(h->ws + h->L.scores);
     e = traced(h, FADKV_K_SCREEN, st, [&] {
@@ -239,6 +251,7 @@ GreedyArgs greedy_args(fadkv_dict h, const void* x, int32_t V, int v0, int Vc)
     a.cand_count = cand_count_buf(h);
     a.cap = h->L.cap;
     a.slices = slices_for(h, Vc);
+    a.pool_in = h->L.tc ? (const int32_t*)(h->ws + h->L.pool) : nullptr;
     a.idx = nullptr;
     a.coef = nullptr;
     a.relres = nullptr;

@@ -86,6 +86,18 @@ int screen_tc_slices(const Shape& sh, int Vc, int sms);
 cudaError_t launch_screen_tc(const Shape& sh, const void* atoms, const void* x, int V, const ScreenTCArgs& a,
                              int sms, cudaStream_t st);
 
+// Exact Top-n pool from the candidate lists, one warp per vector; pool
+// [G][Vc][n] atom ids, pool[0] = -2 where the greedy kernel must take the
+// exact slow path (list overflowed or shorter than n).
+struct SelectArgs {
+    int G, Vc, n, cap, slices;
+    unsigned long long* cand; // [G][Vc][cap]
+    int* cand_count;          // [G][Vc][kCountSlots]; reset to 0 once consumed
+    int32_t* pool;            // [G][Vc][n]
+};
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
+size_t select_smem_bytes(int cap);
+
 // Exact Top-n from the candidate lists (slow exact path for lists shorter
 // than n or longer than cap), then greedy selection inside the pool plus
 // ridge refit; writes idx/coef/relres for vectors [v0, v0+Vc) (outputs are
@@ -100,6 +112,7 @@ struct GreedyArgs {
     int32_t* idx;
     float* coef;
     float* relres;
+    const int32_t* pool_in;   // optional [G][Vc][n] pool from launch_select (then cand* unused)
     int32_t* pool_out;        // optional [G][V][n]
     float* pool_r_out;        // optional [G][V][n] (with pool_out)
     long long* counters;      // [G][kCntFields]

@@ -19,7 +19,7 @@
 //     A = G_SS + diag(lambda_abs + lambda_rel G_ii),  A c = D_S x
 //     e_{k+1} = x - D_S c
 //   relres = ||e_s|| / ||x||
-// At k = 0 the correlations are the screening magnitudes |r_j| of the pool.
+// At k = 0 the correlations are <d_j, x> recomputed over the gathered pool.
 // The Cholesky factor of A grows by one row per pick (the factor of a
 // leading block is the leading block of the factor), so a refit costs O(k^2).
 //
@@ -192,8 +192,14 @@ greedy_kernel(Shape sh, GreedyArgs a)
     xsq = warp_sum(xsq);
     if (lane == 0) fred[warp] = xsq;
     sel::Scratch sc{hist, scan_ws, misc, kred + kWarps};
-    const int count = sel::intake_counts(a, gv, sc);
+    int count = -1;                               // < n: exact slow path
+    if (a.pool_in) {
+        if (tid == 0) misc[0] = (uint32_t)a.pool_in[gv * n];
+    } else {
+        count = sel::intake_counts(a, gv, sc);
+    }
     bad = __syncthreads_or(bad);
+    const bool have_pool = a.pool_in && (int)misc[0] != -2;
     if (bad) {
         if (a.pool_out) {
             for (int i = tid; i < n; i += kThreads) a.pool_out[((size_t)g * a.V + v) * n + i] = -1;
@@ -214,16 +220,13 @@ greedy_kernel(Shape sh, GreedyArgs a)
     for (int w = 0; w < kWarps; ++w) xnorm2 += fred[w];
 
     // ---- the pool ----
-    const int K = sel::intake_keys<T, D>(a, gv, count, n, N, A, xs, keys, sc, cnt);
-    sel::top_n(keys, K, n, pid, a0, sc);
-
-    if (a.pool_out) {
-        for (int i = tid; i < n; i += kThreads) {
-            a.pool_out[((size_t)g * a.V + v) * n + i] = pid[i];
-            if (a.pool_r_out) a.pool_r_out[((size_t)g * a.V + v) * n + i] = a0[i];
-        }
-        return;
+    if (have_pool) {
+        for (int i = tid; i < n; i += kThreads) pid[i] = a.pool_in[gv * n + i];
+    } else {
+        const int K = sel::intake_keys<T, D>(a, gv, count, n, N, A, xs, keys, sc, cnt);
+        sel::top_n(keys, K, n, pid, a0, sc);
     }
+    __syncthreads();
 
     // ---- the pool's atoms into shared memory (over the keys) ----
     {
@@ -234,16 +237,26 @@ greedy_kernel(Shape sh, GreedyArgs a)
             *reinterpret_cast<uint4*>(P + (size_t)i * RSB + part * 16) = q;
         }
     }
+    __syncthreads();
+    // step-0 correlations <d_j, x> of the pool on the FP32 pipe
     float av[kMaxPerThread];
     int aid[kMaxPerThread];
     unsigned picked = 0;
 #pragma unroll
     for (int m = 0; m < kMaxPerThread; ++m) {
         const int i = tid + m * kThreads;
-        av[m] = (i < n) ? a0[i] : 0.f;
+        av[m] = (i < n) ? row_dot<T, D>((const T*)(P + (size_t)i * RSB), xs) : 0.f;
         aid[m] = (i < n) ? pid[i] : 0;
+        if (i < n) a0[i] = fabsf(av[m]);
     }
-    __syncthreads();
+    if (a.pool_out) {
+        __syncthreads();
+        for (int i = tid; i < n; i += kThreads) {
+            a.pool_out[((size_t)g * a.V + v) * n + i] = pid[i];
+            if (a.pool_r_out) a.pool_r_out[((size_t)g * a.V + v) * n + i] = a0[i];
+        }
+        return;
+    }
 
     const float la = sh.lambda_abs, lr = sh.lambda_rel;
     for (int k = 0; k < s; ++k) {

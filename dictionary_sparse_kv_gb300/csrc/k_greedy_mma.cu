@@ -133,15 +133,16 @@ __device__ __forceinline__ void put8(float* dst, uint32_t w0, uint32_t w1, uint3
 // Lane i owns row i (for l) and column i (for w and c): O(k) work per lane.
 constexpr int kMS = kMaxS + 1;   // padded row stride of M (conflict-free rows and columns)
 
+template <int SMAX>
 __device__ __forceinline__ void refit_warp(int k, int lane, const float* grow, float gkk, float bk, float la, float lr,
                                            float* M, float* lbuf, float* zz, float* cc,
                                            unsigned long long* status)
 {
     float li = 0.f;
-    if (lane < k) {
-        for (int m = 0; m <= lane; ++m) li = fmaf(M[lane * kMS + m], grow[m], li);
-        lbuf[lane] = li;
-    }
+#pragma unroll
+    for (int m = 0; m < SMAX; ++m)
+        if (m <= lane && lane < k) li = fmaf(M[lane * kMS + m], grow[m], li);
+    if (lane < k) lbuf[lane] = li;
     float ll = li * li;
     float lz = (lane < k) ? li * zz[lane] : 0.f;
 #pragma unroll
@@ -159,7 +160,9 @@ __device__ __forceinline__ void refit_warp(int k, int lane, const float* grow, f
     __syncwarp();
     if (lane < k) {
         float acc = 0.f;
-        for (int i = lane; i < k; ++i) acc = fmaf(lbuf[i], M[i * kMS + lane], acc);
+#pragma unroll
+        for (int i = 0; i < SMAX; ++i)
+            if (i >= lane && i < k) acc = fmaf(lbuf[i], M[i * kMS + lane], acc);
         const float w = -acc * inv;
         M[k * kMS + lane] = w;
         cc[lane] = fmaf(zk, w, cc[lane]);
@@ -218,8 +221,14 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
     }
     xsq = warp_sum(xsq);
     if (lane == 0) fred[warp] = xsq;
-    const int count = sel::intake_counts(a, gv, sc);
+    int count = -1;                               // < n: exact slow path
+    if (a.pool_in) {
+        if (tid == 0) sc.misc[0] = (uint32_t)a.pool_in[gv * n];
+    } else {
+        count = sel::intake_counts(a, gv, sc);
+    }
     bad = __syncthreads_or(bad);
+    const bool have_pool = a.pool_in && (int)sc.misc[0] != -2;
     if (bad) {
         if (a.pool_out) {
             for (int i = tid; i < n; i += NT) a.pool_out[((size_t)g * a.V + v) * n + i] = -1;
@@ -240,14 +249,17 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
     for (int w = 0; w < NW; ++w) xnorm2 += fred[w];
 
     // ---- the pool ----
-    const int K = sel::intake_keys<__half, D>(a, gv, count, n, N, Aglob, xs, keys, sc, cnt);
-    sel::top_n(keys, K, n, pid, mag, sc);
+    if (have_pool) {
+        for (int i = tid; i < n; i += NT) pid[i] = a.pool_in[gv * n + i];
+        __syncthreads();
+    } else {
+        const int K = sel::intake_keys<__half, D>(a, gv, count, n, N, Aglob, xs, keys, sc, cnt);
+        sel::top_n(keys, K, n, pid, mag, sc);
+    }
     if (a.pool_out) {
-        for (int i = tid; i < n; i += NT) {
-            a.pool_out[((size_t)g * a.V + v) * n + i] = pid[i];
-            if (a.pool_r_out) a.pool_r_out[((size_t)g * a.V + v) * n + i] = mag[i];
-        }
-        return;
+        // |r| of the pool members comes from the first MMA pass below
+        for (int i = tid; i < n; i += NT) a.pool_out[((size_t)g * a.V + v) * n + i] = pid[i];
+        if (!a.pool_r_out) return;
     }
 
     // ---- pool atoms -> A fragments (registers), squared norms ----
@@ -347,12 +359,13 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
             if (s0 + 8 < n) live |= 1u << (2 * mt + 1);
         }
     }
-    __syncthreads();
-
-    const float la = sh.lambda_abs, lr = sh.lambda_rel;
-    unsigned long long* status = (unsigned long long*)&cnt[kCntStatus];
-    for (int k = 0; k < s; ++k) {
-        // ---- argmax over the live pool slots (lanes t4 == 0 hold them) ----
+    if (a.pool_out) {
+        __syncthreads();
+        for (int i = tid; i < n; i += NT) a.pool_r_out[((size_t)g * a.V + v) * n + i] = fabsf(rsl[i]);
+        return;
+    }
+    // the first argmax: best live slot of this warp -> kred[warp]
+    auto warp_best = [&]() {
         unsigned long long best = 0ull;
         if (t4 == 0) {
 #pragma unroll
@@ -370,7 +383,14 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
             best = t > best ? t : best;
         }
         if (lane == 0) kred[warp] = best;
-        __syncthreads();
+    };
+    warp_best();
+    __syncthreads();
+
+    const float la = sh.lambda_abs, lr = sh.lambda_rel;
+    unsigned long long* status = (unsigned long long*)&cnt[kCntStatus];
+    for (int k = 0; k < s; ++k) {
+        // ---- the pick: best of the warps' bests ----
         unsigned long long win = 0ull;
 #pragma unroll
         for (int w = 0; w < NW; ++w) win = kred[w] > win ? kred[w] : win;
@@ -398,8 +418,8 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
         // ---- ridge refit, by the warp after the owner warp ----
         if (warp == (w_o + 1) % NW) {
             if (lane == 0) sslot[k] = slot;
-            refit_warp(k, lane, gcol + (size_t)slot * kMaxS, nrm[slot], rsl[slot], la, lr, Lm, gram, zz, cc,
-                       status);
+            refit_warp<SMAX>(k, lane, gcol + (size_t)slot * kMaxS, nrm[slot], rsl[slot], la, lr, Lm, gram, zz, cc,
+                             status);
         }
         __syncthreads();
 
@@ -434,6 +454,8 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
                 gcol[(size_t)(s0 + 8) * kMaxS + k] = acc[mt][2];
             }
         }
+        warp_best();
+        __syncthreads();
     }
     __syncthreads();
 
