@@ -15,7 +15,8 @@
 //     e_{k+1} = x - D_S c
 //   relres = ||e_s|| / ||x||
 //
-// One CTA of NW warps per vector; warp w owns pool slots 64w .. 64w+63.  The
+// One CTA of NW warps per vector; warp w owns pool slots SPW*w .. SPW*w+SPW-1
+// (SPW = 16 * m16-tiles per warp).  The
 // pool's binary16 atoms stay in registers for the whole greedy loop, as the
 // A fragments of mma.sync.m16n8k16 (rows = atoms).  Every pass multiplies
 // them by an 8-column B operand (fp32 accumulation):
@@ -33,6 +34,9 @@
 // unchanged.  The refit updates the inverse Cholesky factor of A by one row
 // per pick on one warp (see refit_warp), overlapped with the copy of the
 // picked atom.  Three barriers per step.
+#include <stdlib.h>
+#include <string.h>
+
 #include "select.cuh"
 
 namespace fadkv {
@@ -174,17 +178,27 @@ __device__ __forceinline__ void refit_warp(int k, int lane, const float* grow, f
     __syncwarp();
 }
 
-template <int D, int NW, int SMAX>
-__global__ void __launch_bounds__(NW * 32, (NW <= 4 ? 3 : 1))
+// NW warps per vector, MT m16 tiles (16 pool slots each) per warp; with
+// MT <= 2 the head dimension is split across two accumulator sets (KS = 2)
+// so each warp runs 2*MT independent chains of KP/KS*2 dependent MMAs.
+template <int NW, int MT>
+struct MinBlocks {
+    static constexpr int value = (NW * 32 <= 128) ? 3 : ((NW * 32 <= 256 && MT <= 2) ? 2 : 1);
+};
+
+template <int D, int NW, int MT, int SMAX>
+__global__ void __launch_bounds__(NW * 32, MinBlocks<NW, MT>::value)
 greedy_mma_kernel(Shape sh, GreedyArgs a)
 {
     constexpr int KT = D / 16, KP = D / 32, NT = NW * 32;
+    constexpr int SPW = MT * 16;                 // pool slots per warp
+    constexpr int KS = (MT <= 2) ? 2 : 1;        // accumulator sets along the head dimension
     const int vc = blockIdx.x, g = blockIdx.y;
     const int v = a.v0 + vc;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, t4 = lane & 3;
     const int n = sh.n, s = sh.s, N = sh.N;
-    const int n_pad = NW * 64;
+    const int n_pad = NW * SPW;
 
     const MmaLayout<D> L = mma_layout<D>(n_pad, N, a.cap, NW);
     extern __shared__ __align__(16) unsigned char smem[];
@@ -266,10 +280,10 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
     float* gcol = (float*)(smem + L.gcol);
     float* rsl = (float*)(smem + L.rsl);
     float* nrm = (float*)(smem + L.nrm);
-    uint32_t Af[4][KT][4];
+    uint32_t Af[MT][KT][4];
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-        const int s0 = warp * 64 + mt * 16 + g8;
+    for (int mt = 0; mt < MT; ++mt) {
+        const int s0 = warp * SPW + mt * 16 + g8;
         const int r0 = (s0 < n) ? pid[s0] : -1;
         const int r1 = (s0 + 8 < n) ? pid[s0 + 8] : -1;
         float n0 = 0.f, n1 = 0.f;
@@ -323,35 +337,47 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
     }
     __syncthreads();
 
-    float acc[4][4];
+    float acc[MT][4];
     auto mma_pass = [&]() {
+        float part[MT][KS][4];
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) part[mt][ks][r] = 0.f;
 #pragma unroll
         for (int kp = 0; kp < KP; ++kp) {
             const uint4 qb = *reinterpret_cast<const uint4*>(Bsm + g8 * D + 32 * kp + 8 * t4);
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                hmma(acc[mt], Af[mt][2 * kp], qb.x, qb.y);
-                hmma(acc[mt], Af[mt][2 * kp + 1], qb.z, qb.w);
+            for (int mt = 0; mt < MT; ++mt) {
+                hmma(part[mt][kp % KS], Af[mt][2 * kp], qb.x, qb.y);
+                hmma(part[mt][kp % KS], Af[mt][2 * kp + 1], qb.z, qb.w);
             }
         }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float t = part[mt][0][r];
+#pragma unroll
+                for (int ks = 1; ks < KS; ++ks) t += part[mt][ks][r];
+                acc[mt][r] = t;
+            }
     };
 
     // ---- first pass: signed scores of the pool, step-0 correlations ----
-    // lanes with t4 == 0 own slots m = 2*mt + h -> 64*warp + 16*mt + 8*h + g8
+    // lanes with t4 == 0 own slots m = 2*mt + h -> SPW*warp + 16*mt + 8*h + g8
     mma_pass();
-    float av[8];
+    float av[2 * MT];
     unsigned live = 0;
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
+    for (int mt = 0; mt < MT; ++mt) {
         const float r0 = (acc[mt][0] + acc[mt][1]) * inv_scale;
         const float r1 = (acc[mt][2] + acc[mt][3]) * inv_scale;
         av[2 * mt] = r0;
         av[2 * mt + 1] = r1;
-        const int s0 = warp * 64 + mt * 16 + g8;
+        const int s0 = warp * SPW + mt * 16 + g8;
         if (t4 == 0) {
             rsl[s0] = r0;
             rsl[s0 + 8] = r1;
@@ -369,9 +395,9 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
         unsigned long long best = 0ull;
         if (t4 == 0) {
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
+            for (int m = 0; m < 2 * MT; ++m) {
                 if ((live >> m) & 1u) {
-                    const int sl = warp * 64 + (m >> 1) * 16 + (m & 1) * 8 + g8;
+                    const int sl = warp * SPW + (m >> 1) * 16 + (m & 1) * 8 + g8;
                     const unsigned long long key = pick_key(av[m], pid[sl], sl);
                     best = key > best ? key : best;
                 }
@@ -395,13 +421,13 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
 #pragma unroll
         for (int w = 0; w < NW; ++w) win = kred[w] > win ? kred[w] : win;
         const int slot = (int)(win & 0x3ffull);
-        const int w_o = slot >> 6, mt_o = (slot >> 4) & 3, h_o = (slot >> 3) & 1, g_o = slot & 7;
+        const int w_o = slot / SPW, mt_o = (slot % SPW) >> 4, h_o = (slot >> 3) & 1, g_o = slot & 7;
 
         // ---- the picked atom: fp32 copy SA[k] and B column 2 (owner lanes) ----
         if (warp == w_o && g8 == g_o) {
             if (t4 == 0) live &= ~(1u << (2 * mt_o + h_o));
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
+            for (int mt = 0; mt < MT; ++mt) {
                 if (mt == mt_o) {
 #pragma unroll
                     for (int kp = 0; kp < KP; ++kp) {
@@ -442,14 +468,14 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
         mma_pass();
         if (t4 == 0) {
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
+            for (int mt = 0; mt < MT; ++mt) {
                 av[2 * mt] = (acc[mt][0] + acc[mt][1]) * inv_scale;
                 av[2 * mt + 1] = (acc[mt][2] + acc[mt][3]) * inv_scale;
             }
         } else if (t4 == 1) {
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                const int s0 = warp * 64 + mt * 16 + g8;
+            for (int mt = 0; mt < MT; ++mt) {
+                const int s0 = warp * SPW + mt * 16 + g8;
                 gcol[(size_t)s0 * kMaxS + k] = acc[mt][0];
                 gcol[(size_t)(s0 + 8) * kMaxS + k] = acc[mt][2];
             }
@@ -476,11 +502,11 @@ greedy_mma_kernel(Shape sh, GreedyArgs a)
     }
 }
 
-template <int D, int NW, int SMAX>
+template <int D, int NW, int MT, int SMAX>
 cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 {
-    const size_t smem = mma_layout<D>(NW * 64, sh.N, a.cap, NW).total;
-    auto k = greedy_mma_kernel<D, NW, SMAX>;
+    const size_t smem = mma_layout<D>(NW * MT * 16, sh.N, a.cap, NW).total;
+    auto k = greedy_mma_kernel<D, NW, MT, SMAX>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Vc, sh.G);
@@ -488,29 +514,44 @@ cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
     return cudaGetLastError();
 }
 
-template <int D, int NW>
+template <int D, int NW, int MT>
 cudaError_t launch_s(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 {
-    if (sh.s <= 8) return launch_t<D, NW, 8>(sh, a, st);
-    if (sh.s <= 16) return launch_t<D, NW, 16>(sh, a, st);
-    return launch_t<D, NW, 32>(sh, a, st);
+    if (sh.s <= 8) return launch_t<D, NW, MT, 8>(sh, a, st);
+    if (sh.s <= 16) return launch_t<D, NW, MT, 16>(sh, a, st);
+    return launch_t<D, NW, MT, 32>(sh, a, st);
+}
+
+// Warps per vector: 2 m16 tiles (32 pool slots) per warp by default;
+// FADKV_GREEDY_TILES=4 selects 4 tiles per warp (fewer, register-heavier warps).
+int tiles_per_warp()
+{
+    const char* f = getenv("FADKV_GREEDY_TILES");
+    return (f && strcmp(f, "4") == 0) ? 4 : 2;
 }
 
 template <int D>
 cudaError_t launch_d(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 {
-    if (sh.n <= 256) return launch_s<D, 4>(sh, a, st);
-    if (sh.n <= 512) return launch_s<D, 8>(sh, a, st);
-    return launch_s<D, 16>(sh, a, st);
+    if (tiles_per_warp() == 4) {
+        if (sh.n <= 256) return launch_s<D, 4, 4>(sh, a, st);
+        if (sh.n <= 512) return launch_s<D, 8, 4>(sh, a, st);
+        return launch_s<D, 16, 4>(sh, a, st);
+    }
+    if (sh.n <= 256) return launch_s<D, 8, 2>(sh, a, st);
+    if (sh.n <= 512) return launch_s<D, 16, 2>(sh, a, st);
+    return launch_s<D, 16, 4>(sh, a, st);
 }
 
 }  // namespace
 
 size_t greedy_mma_smem_bytes(const Shape& sh)
 {
-    const int nw = sh.n <= 256 ? 4 : (sh.n <= 512 ? 8 : 16);
-    return sh.d == 128 ? mma_layout<128>(nw * 64, sh.N, cand_cap(sh.n), nw).total
-                       : mma_layout<64>(nw * 64, sh.N, cand_cap(sh.n), nw).total;
+    // the largest of the layouts the launcher may pick
+    const int npad = sh.n <= 256 ? 256 : (sh.n <= 512 ? 512 : 1024);
+    const int nw = 16;
+    return sh.d == 128 ? mma_layout<128>(npad, sh.N, cand_cap(sh.n), nw).total
+                       : mma_layout<64>(npad, sh.N, cand_cap(sh.n), nw).total;
 }
 
 cudaError_t launch_greedy_mma(const Shape& sh, const GreedyArgs& a, cudaStream_t st)

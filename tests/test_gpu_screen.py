@@ -119,16 +119,19 @@ def test_slow_path_short_and_overflowing_lists():
 @pytest.mark.parametrize("name,G,V", [("decode_3b", 3, 200), ("decode_8b", 2, 64)])
 def test_greedy_kernels_agree(monkeypatch, name, G, V):
     """The tensor-core greedy kernel (binary16 pools as mma.sync operands,
-    residual split in two binary16 terms) and the FP32-pipe kernel give the
-    same picks and coefficients within the parity tolerance, and both match
-    the oracle."""
+    residual split in two binary16 terms; 2 or 4 m16 tiles per warp) and the
+    FP32-pipe kernel give the same picks and coefficients within the parity
+    tolerance, and all match the oracle."""
     from dataclasses import replace
     w = replace(S.WORKLOADS[name], G=G)
     data = S.WorkloadData(w)
     x = data.inputs(0, V)
     outs = {}
-    for path in ("mma", "ffma"):
+    for path in ("mma", "mma4", "ffma"):
+        if path == "mma4":
+            monkeypatch.setenv("FADKV_GREEDY_TILES", "4")
         if path == "ffma":
+            monkeypatch.delenv("FADKV_GREEDY_TILES")
             monkeypatch.setenv("FADKV_GREEDY", "ffma")
         D = _dict(data.atoms, data.usage, data.deltas(), w.n, w.s, V)
         c = D.new_codes(V)
@@ -138,6 +141,6 @@ def test_greedy_kernels_agree(monkeypatch, name, G, V):
     p = PU.oparams(w)
     for g in range(w.G):
         res = O.encode_threaded(p, data.atoms[g], x[g], PU.THREADS)
-        for path in ("mma", "ffma"):
+        for path in ("mma", "mma4", "ffma"):
             idx, coef, rel = outs[path]
             PU.assert_encode_ok(PU.compare_encode(res, idx[g], coef[g], rel[g]))
