@@ -6,14 +6,19 @@
 //
 // The candidates of a vector arrive as 64-bit keys (bits(|r_j|) << 32) |
 // (0xffffffff - j) split into regions with one count each.  A warp gathers
-// them into its own slice of shared memory, finds the n-th largest by an MSD
-// radix select over bytes -- a 256-bin histogram per warp, one shared atomic
-// per distinct bin per 32 keys -- and writes the pool's atom ids (in no
-// particular order) with ballots.  Only warp-level synchronisation: many
-// warps share an SM and hide each other's latency, and the register-heavy
-// greedy kernel starts from the finished pool.  A vector whose list
-// overflowed or holds fewer than n keys gets pool[0] = -2 and is left to the
-// exact slow path of the greedy kernel.
+// them into its slice of shared memory (asynchronous copies, all in flight
+// at once), then:
+//   1. buckets the keys by |r| on a linear grid of 256 buckets over
+//      [min |r|, max |r|] of the list (monotone in |r|, so every key of a
+//      higher bucket beats every key of a lower one);
+//   2. finds the bucket B holding the n-th largest key from the histogram;
+//   3. takes all keys above B, and the best `rem` keys of B by full 64-bit
+//      key (|r|, then the lower index) -- by rank within the warp when B holds
+//      at most 32 keys, else by an MSD radix select restricted to B.
+// Only warp-level synchronisation, so many warps share an SM and hide each
+// other's latency.  A vector whose list overflowed or holds fewer than n
+// keys gets pool[0] = -2 and is left to the exact slow path of the greedy
+// kernel.
 #include "fadkv_internal.cuh"
 
 namespace fadkv {
@@ -59,82 +64,177 @@ select_kernel(SelectArgs a)
     }
     __syncwarp();
 
-    // gather the regions back to back
+    // gather the regions back to back (8-byte asynchronous copies)
     const unsigned long long* src = a.cand + gw * a.cap;
     for (int r = 0; r < nreg; ++r) {
         const int o0 = offs[r];
         const int len = (r + 1 < nreg ? offs[r + 1] : K) - o0;
-        for (int i = lane; i < len; i += 32) keys[o0 + i] = src[(size_t)r * cs + i];
+        for (int i = lane; i < len; i += 32) {
+            const uint32_t dst = (uint32_t)__cvta_generic_to_shared(keys + o0 + i);
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src + (size_t)r * cs + i)
+                         : "memory");
+        }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
 
-    // MSD radix select of the n-th largest key
+    // 1. range of |r| and the bucket grid
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int i = lane; i < K; i += 32) {
+        const uint32_t m = (uint32_t)(keys[i] >> 32);
+        lo = min(lo, m);
+        hi = max(hi, m);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    const float flo = __uint_as_float(lo), fhi = __uint_as_float(hi);
+    const float scale = (fhi > flo) ? 255.99f / (fhi - flo) : 0.f;
+    auto bucket = [&](unsigned long long k) -> uint32_t {
+        const float m = __uint_as_float((uint32_t)(k >> 32));
+        return min(255u, (uint32_t)((m - flo) * scale));
+    };
+
+    // 2. histogram and the boundary bucket (lane l scans buckets 255-8l .. 248-8l)
+#pragma unroll
+    for (int b = 0; b < 8; ++b) hist[lane * 8 + b] = 0;
+    __syncwarp();
+    for (int i = lane; i < K; i += 32) atomicAdd(&hist[bucket(keys[i])], 1u);
+    __syncwarp();
+    const int top = 255 - 8 * lane;
+    uint32_t local = 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) local += hist[top - b];
+    uint32_t inc = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    const uint32_t above0 = inc - local;
+    const bool mine = above0 < (uint32_t)n && (uint32_t)n <= inc;
+    uint32_t bsel = 0, rem = 0, nb = 0;
+    if (mine) {
+        uint32_t acc = above0;
+        for (int b = 0; b < 8; ++b) {
+            const uint32_t h = hist[top - b];
+            if (acc + h >= (uint32_t)n) {
+                bsel = (uint32_t)(top - b);
+                rem = (uint32_t)n - acc;
+                nb = h;
+                break;
+            }
+            acc += h;
+        }
+    }
+    const int sl = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    bsel = __shfl_sync(0xffffffffu, bsel, sl);
+    rem = __shfl_sync(0xffffffffu, rem, sl);
+    nb = __shfl_sync(0xffffffffu, nb, sl);
+
+    // 3a. keys above the boundary bucket
+    int base = 0;
+    for (int i0 = 0; i0 < K; i0 += 32) {
+        const int i = i0 + lane;
+        const unsigned long long k = (i < K) ? keys[i] : 0ull;
+        const bool f = (i < K) && bucket(k) > bsel;
+        const unsigned bal = __ballot_sync(0xffffffffu, f);
+        if (f) pool[base + __popc(bal & ((1u << lane) - 1u))] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+        base += __popc(bal);
+    }
+    if (rem == nb) {
+        // the whole boundary bucket
+        for (int i0 = 0; i0 < K; i0 += 32) {
+            const int i = i0 + lane;
+            const unsigned long long k = (i < K) ? keys[i] : 0ull;
+            const bool f = (i < K) && bucket(k) == bsel;
+            const unsigned bal = __ballot_sync(0xffffffffu, f);
+            if (f) pool[base + __popc(bal & ((1u << lane) - 1u))] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+            base += __popc(bal);
+        }
+        return;
+    }
+    // 3b. the boundary bucket's keys, compacted in place to the front of the
+    //     buffer (a write never passes the read position); one per lane when
+    //     the bucket holds at most 32
+    unsigned long long* bkeys = keys;
+    int mb = 0;
+    for (int i0 = 0; i0 < K; i0 += 32) {
+        const int i = i0 + lane;
+        const unsigned long long k = (i < K) ? keys[i] : 0ull;
+        const bool f = (i < K) && bucket(k) == bsel;
+        const unsigned bal = __ballot_sync(0xffffffffu, f);
+        if (f) bkeys[mb + __popc(bal & ((1u << lane) - 1u))] = k;
+        mb += __popc(bal);
+        __syncwarp();
+    }
+    __syncwarp();
+    if (mb <= 32) {
+        const unsigned long long mk = (lane < mb) ? bkeys[lane] : 0ull;
+        uint32_t rank = 0;   // keys of the bucket larger than mine (keys are unique)
+        for (int j = 0; j < mb; ++j) rank += (__shfl_sync(0xffffffffu, mk, j) > mk) ? 1u : 0u;
+        const bool f = lane < mb && rank < rem;
+        const unsigned bal = __ballot_sync(0xffffffffu, f);
+        if (f) pool[base + __popc(bal & ((1u << lane) - 1u))] = (int)(0xffffffffu - (uint32_t)(mk & 0xffffffffull));
+        return;
+    }
+    // rare: a crowded bucket -- MSD radix select over the bucket's keys
     unsigned long long prefix = 0ull, mask = 0ull;
-    uint32_t remaining = (uint32_t)n;
+    uint32_t remaining = rem;
     int shift = 56;
     for (;; shift -= 8) {
 #pragma unroll
         for (int b = 0; b < 8; ++b) hist[lane * 8 + b] = 0;
         __syncwarp();
-        for (int i0 = 0; i0 < K; i0 += 32) {
-            const int i = i0 + lane;
-            const unsigned long long k = (i < K) ? keys[i] : 0ull;
-            const bool in = (i < K) && (k & mask) == prefix;
-            const uint32_t bin = in ? ((uint32_t)(k >> shift) & 0xffu) : 0x100u;
-            const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (in && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+        for (int i = lane; i < mb; i += 32) {
+            const unsigned long long k = bkeys[i];
+            if ((k & mask) == prefix) atomicAdd(&hist[(uint32_t)(k >> shift) & 0xffu], 1u);
         }
         __syncwarp();
-        // lane l covers bins 255-8l .. 248-8l (lane 0 holds the top)
-        const int hi = 255 - 8 * lane;
-        uint32_t local = 0;
+        uint32_t loc = 0;
 #pragma unroll
-        for (int b = 0; b < 8; ++b) local += hist[hi - b];
-        uint32_t inc = local;
+        for (int b = 0; b < 8; ++b) loc += hist[top - b];
+        uint32_t in2 = loc;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += t;
+            const uint32_t t = __shfl_up_sync(0xffffffffu, in2, o);
+            if (lane >= o) in2 += t;
         }
-        const uint32_t above = inc - local;
-        const bool mine = above < remaining && remaining <= inc;
-        uint32_t bin_sel = 0, rem_new = 0, whole = 0;
-        if (mine) {
-            uint32_t acc = above;
+        const uint32_t ab = in2 - loc;
+        const bool mn = ab < remaining && remaining <= in2;
+        uint32_t bs = 0, rn = 0, whole = 0;
+        if (mn) {
+            uint32_t acc = ab;
             for (int b = 0; b < 8; ++b) {
-                const uint32_t h = hist[hi - b];
+                const uint32_t h = hist[top - b];
                 if (acc + h >= remaining) {
-                    bin_sel = (uint32_t)(hi - b);
-                    rem_new = remaining - acc;
-                    whole = (h == rem_new) ? 1u : 0u;
+                    bs = (uint32_t)(top - b);
+                    rn = remaining - acc;
+                    whole = (h == rn) ? 1u : 0u;
                     break;
                 }
                 acc += h;
             }
         }
-        const int src_lane = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
-        bin_sel = __shfl_sync(0xffffffffu, bin_sel, src_lane);
-        rem_new = __shfl_sync(0xffffffffu, rem_new, src_lane);
-        whole = __shfl_sync(0xffffffffu, whole, src_lane);
-        prefix |= (unsigned long long)bin_sel << shift;
-        remaining = rem_new;
+        const int s2 = __ffs(__ballot_sync(0xffffffffu, mn)) - 1;
+        bs = __shfl_sync(0xffffffffu, bs, s2);
+        rn = __shfl_sync(0xffffffffu, rn, s2);
+        whole = __shfl_sync(0xffffffffu, whole, s2);
+        prefix |= (unsigned long long)bs << shift;
+        remaining = rn;
         mask |= 0xffull << shift;
         __syncwarp();
         if (whole || shift == 0) break;
     }
-
-    // selected: keys whose bits from `shift` up are >= prefix's
     const unsigned long long lim = prefix >> shift;
-    int base = 0;
-    for (int i0 = 0; i0 < K; i0 += 32) {
+    for (int i0 = 0; i0 < mb; i0 += 32) {
         const int i = i0 + lane;
-        const unsigned long long k = (i < K) ? keys[i] : 0ull;
-        const bool f = (i < K) && (k >> shift) >= lim;
+        const unsigned long long k = (i < mb) ? bkeys[i] : 0ull;
+        const bool f = (i < mb) && (k >> shift) >= lim;
         const unsigned bal = __ballot_sync(0xffffffffu, f);
-        if (f) {
-            const int pos = base + __popc(bal & ((1u << lane) - 1u));
-            if (pos < n) pool[pos] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
-        }
+        if (f) pool[base + __popc(bal & ((1u << lane) - 1u))] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
         base += __popc(bal);
     }
 }

@@ -144,3 +144,35 @@ def test_greedy_kernels_agree(monkeypatch, name, G, V):
         for path in ("mma", "mma4", "ffma"):
             idx, coef, rel = outs[path]
             PU.assert_encode_ok(PU.compare_encode(res, idx[g], coef[g], rel[g]))
+
+
+@pytest.mark.parametrize("case", ["crowded_tie", "rank_tie", "whole_bucket"])
+def test_select_exact_ties(case):
+    """Top-n selection with exact ties at the cut (32 signed copies of each
+    basis vector, x a combination of basis vectors): the pool must be the
+    oracle's -- all atoms above the cut plus the lowest-index tied ones --
+    whichever branch of the selection kernel decides the boundary."""
+    d, N, s = 128, 4096, 8
+    g = np.random.default_rng(12)
+    A = np.zeros((N, d), np.float16)
+    A[np.arange(N), np.arange(N) % d] = g.choice([-1.0, 1.0], N)
+    x = np.zeros((1, 1, d), np.float32)
+    if case == "crowded_tie":      # 512 atoms tie at |r| = 1; n = 256 of them
+        n = 256
+        x[0, 0, :16] = 1.0
+    elif case == "rank_tie":       # 224 above the cut, 32 tied at the cut, 16 taken
+        n = 240
+        x[0, 0, :7] = 2.0
+        x[0, 0, 7] = 1.0
+        x[0, 0, 8] = 0.9
+    else:                          # the boundary bucket is taken whole
+        n = 256
+        x[0, 0, :7] = 2.0
+        x[0, 0, 7] = 1.0
+        x[0, 0, 8] = 0.9
+    x = x.astype(np.float16)
+    D = _dict(A[None], np.ones((1, N), np.int32), [0.5], n, s, 1)
+    pool = D.pool(_t(x))[0].cpu().numpy()[0, 0]
+    assert D.stats()[0]["topn_slow_path"] == 0      # decided by the selection kernel
+    res = O.encode(O.Params(N, d, n, s), A, x[0])
+    assert sorted(pool) == sorted(res.pool[0])
