@@ -329,14 +329,19 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
                     const uint32_t lo0 = 0xffffffffu - (uint32_t)(atom0 + qq * 32);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
+                        // branch-free: a predicated store, then the count.  Past
+                        // the region's end the last slot is reused: the count
+                        // then exceeds the region and the consumer redoes the
+                        // vector exactly.
                         const uint32_t mag = v[i] & 0x7fffffffu;
-                        if (mag >= tau_bits) {
-                            // past the region's end the last slot is reused:
-                            // the count then exceeds the region and the
-                            // consumer redoes the vector exactly
-                            list[min(cnt, cs - 1)] = ((unsigned long long)mag << 32) | (lo0 - (uint32_t)i);
-                            ++cnt;
-                        }
+                        unsigned long long* slot = list + min(cnt, cs - 1);
+                        asm volatile(
+                            "{\n\t.reg .pred p;\n\t"
+                            "setp.ge.u32 p, %0, %1;\n\t"
+                            "@p st.global.v2.u32 [%2], {%3, %0};\n\t}"
+                            ::"r"(mag), "r"(tau_bits), "l"(slot), "r"(lo0 - (uint32_t)i)
+                            : "memory");
+                        cnt += (mag >= tau_bits) ? 1 : 0;
                     }
                 }
             }
