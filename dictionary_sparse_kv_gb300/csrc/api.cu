@@ -120,6 +120,13 @@ bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
 
 }  // namespace
 
+// Records a message for fadkv_last_error on this host thread (used by entry
+// points defined in other translation units).
+void fadkv::set_last_error(const char* msg)
+{
+    snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+}
+
 struct ProfRec {
     int cls;
     cudaEvent_t start, stop;

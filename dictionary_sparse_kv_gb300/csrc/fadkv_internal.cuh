@@ -36,6 +36,9 @@ struct Shape {
     float lambda_abs, lambda_rel;
 };
 
+// Message for fadkv_last_error on the calling host thread.
+void set_last_error(const char* msg);
+
 // Element access for the two storage types.
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }

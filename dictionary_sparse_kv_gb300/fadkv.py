@@ -75,6 +75,9 @@ _SIGS = {
                      C.c_int),
     "fadkv_adapt": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                      C.c_void_p, C.c_void_p], C.c_int),
+    "fadkv_adapt_noalloc": ([C.POINTER(Params), C.c_void_p, C.c_void_p, C.POINTER(C.c_float), C.c_void_p,
+                             C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                             C.c_void_p], C.c_int),
     "fadkv_reconstruct": ([C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                            C.c_void_p], C.c_int),
     "fadkv_dict_stats": ([C.c_void_p, C.POINTER(C.c_int64), C.c_void_p], C.c_int),
@@ -165,6 +168,17 @@ def adapt(h: int, x, V: int, idx, coef, relres, repl_id, repl_coef, stream=None)
     st = _stream(stream, x, idx)
     _check("fadkv_adapt", lib().fadkv_adapt(h, _addr(x), V, _addr(idx), _addr(coef), _addr(relres),
                                             _addr(repl_id), _addr(repl_coef), st))
+
+
+def adapt_noalloc(p: Params, atoms, usage, delta, x, V: int, idx, coef, relres, repl_id, repl_coef,
+                  stream=None) -> None:
+    """Handle-free adaptation on the library's static scratch (no allocation)."""
+    arr = (C.c_float * len(delta))(*[float(v) for v in delta])
+    st = _stream(stream, atoms, x)
+    rc = lib().fadkv_adapt_noalloc(C.byref(p), _addr(atoms), _addr(usage), arr, _addr(x), V, _addr(idx),
+                                   _addr(coef), _addr(relres), _addr(repl_id), _addr(repl_coef), st)
+    if rc != 0:
+        raise FadkvError("fadkv_adapt_noalloc", rc, last_error())
 
 
 def reconstruct(h: int, V: int, idx, coef, repl_id, repl_coef, xhat, stream=None) -> None:

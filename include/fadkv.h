@@ -163,6 +163,38 @@ fadkv_status fadkv_adapt(fadkv_dict dict, const void* x, int32_t V, const int32_
                          const float* coef, const float* relres, int32_t* repl_id,
                          float* repl_coef, void* stream);
 
+/* Fixed-size adaptation without a handle and without caller scratch.  The
+   pages have no counterpart to this call: it runs the same adaptation as
+   fadkv_adapt (same kernel, same results) for callers that cannot give the
+   library any device memory of its own, e.g. a plain C runtime with a fixed
+   memory plan and no allocator, or a decode loop that must not call
+   cudaMalloc / cudaFree since either can synchronise the whole device.
+     params     shape and dtype (max_batch is not used; V is limited by the
+                scratch instead); the same checks as fadkv_workspace_bytes
+     atoms      [G][N][d] dictionary, 16-byte aligned (mutated)
+     usage      [G][N] int32 usage counts (mutated)
+     delta      HOST array [G] of thresholds, each >= 0
+     x, V, idx, coef, relres, repl_id, repl_coef: as for fadkv_adapt
+     stream     cudaStream_t as void*; NULL = legacy default stream
+   Scratch: one statically sized device array inside the library (4 MiB per
+   device) holds the inactive-atom list, the flagged-vector list and the
+   counters.  A call needs 256-rounded 4*G*N + 4*G*V bytes plus 64*G; more
+   than 4 MiB returns FADKV_ERR_WORKSPACE with the sizes in
+   fadkv_last_error(), before any CUDA call.  Nothing in the scratch has to
+   start at zero, and the library allocates and frees nothing.
+   The first call on a device looks up the scratch's address there
+   (cudaGetSymbolAddress, with that device current); a caller that records
+   its calls under stream capture should make one call on each device before
+   capture begins.  All calls on one device share the one scratch array:
+   calls that may run concurrently (different streams or host threads) race,
+   so issue them in order on one stream.  There is no sequence check and no
+   per-dictionary statistics: the caller keeps encode/adapt order itself.
+   Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+fadkv_status fadkv_adapt_noalloc(const fadkv_params* params, void* atoms, int32_t* usage,
+                                 const float* delta, const void* x, int32_t V, const int32_t* idx,
+                                 const float* coef, const float* relres, int32_t* repl_id,
+                                 float* repl_coef, void* stream);
+
 /* Sparse reconstruction (abstract: a sparse combination of atoms):
    xhat_v = sum_k coef[v][k] d_{idx[v][k]} + repl_coef[v] d_{repl_id[v]}.
    repl_id / repl_coef may both be NULL (no replacement terms); entries with
