@@ -249,6 +249,17 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
     });
 }
 
+// FADKV_GREEDY=tc selects the greedy with one tcgen05 GEMM per pick (binary16
+// dictionaries screened on the tensor cores); the default is the
+// pool-resident mma.sync kernel, FADKV_GREEDY=ffma the FP32-pipe kernel.
+bool use_greedy_tc(fadkv_dict h)
+{
+    if (!h->L.tc) return false;
+    const char* f = getenv("FADKV_GREEDY");
+    if (!(f && strcmp(f, "tc") == 0)) return false;
+    return greedy_tc_supported(h->sh);
+}
+
 GreedyArgs greedy_args(fadkv_dict h, const void* x, int32_t V, int v0, int Vc)
 {
     GreedyArgs a;
@@ -404,7 +415,25 @@ fadkv_status fadkv_encode(fadkv_dict h, const void* x, int32_t V, int32_t* idx, 
     for (int v0 = 0; v0 < V; v0 += chunk) {
         const int Vc = (V - v0 < chunk) ? V - v0 : chunk;
         cudaError_t e = run_screen(h, x, V, v0, Vc, nullptr, st);
-        if (e == cudaSuccess) {
+        if (e == cudaSuccess && use_greedy_tc(h)) {
+            int32_t* pool = (int32_t*)(h->ws + h->L.pool);
+            GreedyArgs fa = greedy_args(h, x, V, v0, Vc);
+            e = traced(h, FADKV_K_TOPN, st, [&] { return launch_pool_fixup(h->sh, fa, pool, h->sms, st); });
+            if (e == cudaSuccess) {
+                GreedyTCArgs ga;
+                ga.atoms = h->atoms;
+                ga.x = x;
+                ga.pool = pool;
+                ga.idx = idx;
+                ga.coef = coef;
+                ga.relres = relres;
+                ga.counters = counters(h);
+                ga.V = V;
+                ga.v0 = v0;
+                ga.Vc = Vc;
+                e = traced(h, FADKV_K_GREEDY, st, [&] { return launch_greedy_tc(h->sh, ga, h->sms, st); });
+            }
+        } else if (e == cudaSuccess) {
             GreedyArgs a = greedy_args(h, x, V, v0, Vc);
             a.idx = idx;
             a.coef = coef;

@@ -128,6 +128,28 @@ size_t greedy_smem_bytes(const Shape& sh);
 cudaError_t launch_greedy_mma(const Shape& sh, const GreedyArgs& a, cudaStream_t st);
 size_t greedy_mma_smem_bytes(const Shape& sh);
 
+// Greedy selection + ridge refit with the pool correlations on the tensor
+// cores: every pick is one GEMM of the residual tile (128 vectors) against
+// the dictionary, reduced to a masked argmax per vector (binary16
+// dictionaries).  Needs the exact pool of every vector in `pool` (run
+// launch_pool_fixup first).
+struct GreedyTCArgs {
+    const void* atoms;
+    const void* x;            // [G][V][d]
+    const int32_t* pool;      // [G][Vc][n]
+    int32_t* idx;             // [G][V][s]
+    float* coef;              // [G][V][s]
+    float* relres;            // [G][V]
+    long long* counters;      // [G][kCntFields]
+    int V, v0, Vc;
+};
+bool greedy_tc_supported(const Shape& sh);
+cudaError_t launch_greedy_tc(const Shape& sh, const GreedyTCArgs& a, int sms, cudaStream_t st);
+
+// Exact pool of the vectors the selection kernel left to the slow path
+// (pool[0] == -2): all N scores on the FP32 pipe, exact Top-n.
+cudaError_t launch_pool_fixup(const Shape& sh, const GreedyArgs& a, int32_t* pool, int sms, cudaStream_t st);
+
 // Fixed-size adaptation, one CTA per dictionary.
 struct AdaptArgs {
     void* atoms;

@@ -28,10 +28,7 @@
 // TMEM columns per CTA: two CTAs share an SM.  Every wait is bounded by a
 // wall-clock limit; on expiry the CTA sets FADKV_DEV_TIMEOUT in the status
 // word, drains its own copies and MMAs (bounded), frees TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "fadkv_internal.cuh"
+#include "tc_common.cuh"
 
 namespace fadkv {
 namespace {
@@ -41,118 +38,18 @@ constexpr int kTileV = 128;        // vectors per CTA (MMA M)
 constexpr int kChunk = 128;        // atoms per MMA chunk (MMA N)
 constexpr int kStages = 2;         // B (atom chunk) pipeline depth
 constexpr int kTmemCols = 2 * kChunk;
-constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;   // 200 ms
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+using namespace tc;
 
-__device__ __forceinline__ unsigned long long globaltimer()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait; returns false (and flags the status word) on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long* status)
-{
-    if (mbar_try(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try(bar, parity)) return true;
-        if ((i & 255u) == 255u && globaltimer() - t0 > kWaitNs) {
-            atomicOr(status, (unsigned long long)FADKV_DEV_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart; the start address advances 32 bytes per K = 16 step.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr)
-{
-    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)(16u >> 4) << 16;       // leading byte offset (unused with this swizzle)
-    d |= (uint64_t)(1024u >> 4) << 32;     // stride byte offset
-    d |= (uint64_t)1 << 46;                // descriptor version
-    d |= (uint64_t)2 << 61;                // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor: f16 x f16 -> f32, A and B K-major, M=128, N=128.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kChunk >> 3) << 17) | ((uint32_t)(kTileV >> 4) << 24);
+// Instruction descriptor: M = 128 vectors, N = 128 atoms.
+constexpr uint32_t kIdesc = idesc_f16(kTileV, kChunk);
 
 __device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t acc)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(dtmem), "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
-        : "memory");
+    mma_ss(dtmem, a, b, kIdesc, acc);
 }
-
-__device__ __forceinline__ void mma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
+__device__ __forceinline__ void tc_fence_before() { fence_before(); }
+__device__ __forceinline__ void tc_fence_after() { fence_after(); }
 
 template <int D>
 struct SmemLayout {
@@ -364,7 +261,27 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
 // host side
 // ---------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+template <int D, bool kDump>
+cudaError_t launch_t(const Shape& sh, const void* atoms, const void* x, int V, const ScreenTCArgs& a, int sms,
+                     cudaStream_t st)
+{
+    CUtensorMap mx, md;
+    if (!make_tma_map_f16(&mx, x, (long long)sh.G * V, D, 128) ||
+        !make_tma_map_f16(&md, atoms, (long long)sh.G * sh.N, D, 128))
+        return cudaErrorInvalidValue;
+    auto k = screen_tc_kernel<D, kDump>;
+    const int smem = SmemLayout<D>::alloc;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int tiles = (a.Vc + kTileV - 1) / kTileV;
+    dim3 grid(tiles * a.slices, sh.G);
+    k<<<grid, kThreads, smem, st>>>(mx, md, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tma_encode_fn()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -378,38 +295,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// [rows][d] binary16 matrix, boxes of 64 elements x 128 rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, long long rows, int d)
+bool make_tma_map_f16(CUtensorMap* m, const void* base, long long rows, int d, int box_rows)
 {
-    auto fn = encode_fn();
+    auto fn = tma_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-template <int D, bool kDump>
-cudaError_t launch_t(const Shape& sh, const void* atoms, const void* x, int V, const ScreenTCArgs& a, int sms,
-                     cudaStream_t st)
-{
-    CUtensorMap mx, md;
-    if (!make_map(&mx, x, (long long)sh.G * V, D) || !make_map(&md, atoms, (long long)sh.G * sh.N, D))
-        return cudaErrorInvalidValue;
-    auto k = screen_tc_kernel<D, kDump>;
-    const int smem = SmemLayout<D>::alloc;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    const int tiles = (a.Vc + kTileV - 1) / kTileV;
-    dim3 grid(tiles * a.slices, sh.G);
-    k<<<grid, kThreads, smem, st>>>(mx, md, a);
-    return cudaGetLastError();
-}
-
-}  // namespace
 
 int screen_tc_slices(const Shape& sh, int Vc, int sms)
 {

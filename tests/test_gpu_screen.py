@@ -118,16 +118,27 @@ def test_slow_path_short_and_overflowing_lists():
 
 @pytest.mark.parametrize("name,G,V", [("decode_3b", 3, 200), ("decode_8b", 2, 64)])
 def test_greedy_kernels_agree(monkeypatch, name, G, V):
-    """The tensor-core greedy kernel (binary16 pools as mma.sync operands,
-    residual split in two binary16 terms; 2 or 4 m16 tiles per warp) and the
-    FP32-pipe kernel give the same picks and coefficients within the parity
-    tolerance, and all match the oracle."""
+    """The greedy kernels all match the oracle: one tcgen05 GEMM per pick over
+    the whole dictionary with a pool-masked argmax (cluster size chosen by
+    the launcher, and forced to 1 and 3), the
+    pool-resident mma.sync kernel (2 or 4 m16 tiles per warp) and the
+    FP32-pipe kernel."""
     from dataclasses import replace
     w = replace(S.WORKLOADS[name], G=G)
     data = S.WorkloadData(w)
     x = data.inputs(0, V)
     outs = {}
-    for path in ("mma", "mma4", "ffma"):
+    paths = ("tc", "tc_c1", "tc_c3", "mma", "mma4", "ffma")
+    for path in paths:
+        if path == "tc":
+            monkeypatch.setenv("FADKV_GREEDY", "tc")
+        if path == "tc_c1":
+            monkeypatch.setenv("FADKV_GREEDY_CLUSTER", "1")
+        if path == "tc_c3":
+            monkeypatch.setenv("FADKV_GREEDY_CLUSTER", "3")
+        if path == "mma":
+            monkeypatch.delenv("FADKV_GREEDY_CLUSTER")
+            monkeypatch.setenv("FADKV_GREEDY", "mma")
         if path == "mma4":
             monkeypatch.setenv("FADKV_GREEDY_TILES", "4")
         if path == "ffma":
@@ -141,7 +152,7 @@ def test_greedy_kernels_agree(monkeypatch, name, G, V):
     p = PU.oparams(w)
     for g in range(w.G):
         res = O.encode_threaded(p, data.atoms[g], x[g], PU.THREADS)
-        for path in ("mma", "mma4", "ffma"):
+        for path in paths:
             idx, coef, rel = outs[path]
             PU.assert_encode_ok(PU.compare_encode(res, idx[g], coef[g], rel[g]))
 
