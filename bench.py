@@ -140,20 +140,20 @@ class ClockSampler:
 
 def kernel_work(w, kernel: str, vectors: int):
     """(bound, algorithmic units per launch, unit) for one launch that covers
-    `vectors` vectors of every dictionary (G * vectors vectors in total)."""
+    `vectors` vectors of every dictionary (G * vectors vectors in total).
+    Per-vector figures: screening streams the dictionary once per launch plus
+    the inputs (HBM); the greedy's contraction is (s - 1) n d multiply-adds
+    per vector over the pool (tensor pipe)."""
     G, N, d, n, s = w.G, w.N, w.d, w.n, w.s
     esz = 2 if w.dtype.__name__ == "float16" else 4
     nv = G * vectors
     if kernel == "screen":
-        # one pass over every dictionary plus the inputs; 2 N d flops per vector
-        return "alu", 2.0 * N * d * nv, "TFLOP/s"
+        return "hbm", float(G * N * d * esz + nv * d * esz), "GB/s"
     if kernel == "topn":
-        return "hbm", 4.0 * N * nv + 8.0 * n * nv, "GB/s"
+        # candidate keys in (about 2n per vector, 8 B each) and the pool out
+        return "hbm", (8.0 * 2 * n + 4.0 * n) * nv, "GB/s"
     if kernel == "greedy":
-        # correlations of the s-1 later picks over the pool, plus per step k
-        # the Gram row (k+1 dots), right-hand side (1 dot) and residual (k+1)
-        per = 2.0 * (s - 1) * n * d + sum(2.0 * d * (2 * (k + 1) + 1) for k in range(s))
-        return "alu", per * nv, "TFLOP/s"
+        return "tensor", 2.0 * (s - 1) * n * d * nv, "TFLOP/s"
     if kernel == "adapt":
         return "hbm", 4.0 * (s + 3) * nv + 4.0 * G * N, "GB/s"
     if kernel == "reconstruct":
@@ -170,8 +170,15 @@ def kernel_sources():
     return out
 
 
-KERNEL_FILES = {"screen": "k_screen_ffma.cu", "topn": "k_topn.cu", "greedy": "k_greedy.cu",
-                "adapt": "k_adapt_reconstruct.cu", "reconstruct": "k_adapt_reconstruct.cu"}
+def greedy_source() -> str:
+    f = os.environ.get("FADKV_GREEDY", "")
+    return {"tc": "k_greedy_tc.cu", "ffma": "k_greedy.cu"}.get(f, "k_greedy_mma.cu")
+
+
+def kernel_files():
+    """Source file of each kernel class on the binary16 path the bench runs."""
+    return {"screen": "k_screen_tc.cu", "topn": "k_select.cu", "greedy": greedy_source(),
+            "adapt": "k_adapt_reconstruct.cu", "reconstruct": "k_adapt_reconstruct.cu"}
 
 
 def traffic_for(kernel: str, w):
@@ -185,7 +192,7 @@ def traffic_for(kernel: str, w):
     ent = tab.get(w.name, {}).get(kernel)
     if not ent:
         return None
-    src = kernel_sources().get(KERNEL_FILES.get(kernel, ""), None)
+    src = kernel_sources().get(kernel_files().get(kernel, ""), None)
     if ent.get("source_sha256_16") != src:
         return None
     return ent.get("dram_bytes_per_launch")
@@ -214,9 +221,11 @@ def roofline(w, prof, vectors_per_launch, peaks, peak_kind, sm_count, sm_mhz_max
             peak = sm_count * 128 * 2 * sm_mhz_max * 1e6 / 1e12
             pk = f"fp32 fma: {sm_count} SMs x 128 lanes x 2 x {sm_mhz_max:.0f} MHz"
         else:
+            # binary16 inputs, fp32 accumulation: the dense bf16 rate (same
+            # nominal rate as fp16), burst figure for a kernel timed per launch
             peak = peaks["bf16_tflops"]
-            pk = f"bf16_tflops ({peak_kind})"
-    obj = {"kernel": kern, "bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": unit,
+            pk = f"bf16_tflops ({peak_kind}, burst; fp16 at the same nominal rate)"
+    obj = {"kernel": kern, "source": kernel_files().get(kern), "bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": unit,
            "frac": round(achieved / peak, 4), "traffic": traffic_for(kern, w), "peak_source": pk,
            "launch_ms": round(ms / n_launch, 5)}
     return obj, shares
