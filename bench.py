@@ -305,6 +305,32 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------
+# multi-rank plumbing (weak scaling: every rank owns its own dictionaries)
+# --------------------------------------------------------------------------
+
+def rank_workload(w0, rank: int):
+    """The workload a rank runs: the same shapes, its own dictionaries and
+    inputs (seed offset by rank)."""
+    return replace(w0, seed=w0.seed + 1000 * rank)
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest x over all ranks (the step time of the slowest rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, vectors_per_step: int, ms_max: float) -> float:
+    """Whole-job vectors/s: every rank's vectors over the slowest rank's time."""
+    return world * steps * vectors_per_step / (ms_max / 1e3)
+
+
+# --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
 
@@ -328,8 +354,7 @@ def run_ours(args):
         dist.barrier()
     F.lib()
 
-    w0 = S.WORKLOADS[args.workload]
-    w = replace(w0, seed=w0.seed + 1000 * rank)       # each rank its own dictionaries
+    w = rank_workload(S.WORKLOADS[args.workload], rank)
     data = S.WorkloadData(w)
     K, W = args.steps, max(3, args.warmup)
     G, V, d = w.G, w.V, w.d
@@ -367,11 +392,7 @@ def run_ours(args):
     clk = clocks.stop() if rank == 0 else None
     F.profile_enable(D.h, False)
     prof = F.profile_read(D.h, reset=True)
-    dev_ms = sum(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        tt = torch.tensor([dev_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        dev_ms = float(tt.item())
+    dev_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dev)
     launches = sum(n for n, _ in prof.values())
 
     # ---- end to end: pinned host inputs in, codes out, every step ----
@@ -393,11 +414,7 @@ def run_ours(args):
             o.copy_(c, non_blocking=True)
         ev2[t][1].record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev2), dev)
     stats = D.stats()
 
     if rank != 0:
@@ -405,8 +422,8 @@ def run_ours(args):
         return 0
 
     vectors_per_step = G * V
-    value = world * K * vectors_per_step / (dev_ms / 1e3)
-    e2e = world * K * vectors_per_step / (e2e_ms / 1e3)
+    value = job_throughput(world, K, vectors_per_step, dev_ms)
+    e2e = job_throughput(world, K, vectors_per_step, e2e_ms)
     peaks, peak_kind = load_peaks()
     props = torch.cuda.get_device_properties(dev)
     sm_max = float(peaks.get("sm_max_mhz") or clk.get("sm_max_mhz") or 2070.0)
