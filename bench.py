@@ -172,7 +172,7 @@ def kernel_sources():
 
 def greedy_source() -> str:
     f = os.environ.get("FADKV_GREEDY", "")
-    return {"tc": "k_greedy_tc.cu", "ffma": "k_greedy.cu"}.get(f, "k_greedy_mma.cu")
+    return {"tc": "k_greedy_tc.cu", "ffma": "k_greedy.cu", "mma": "k_greedy_mma.cu"}.get(f, "k_greedy_chol.cu")
 
 
 def kernel_files():

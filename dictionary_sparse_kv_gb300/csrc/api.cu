@@ -249,15 +249,19 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
     });
 }
 
-// FADKV_GREEDY=tc selects the greedy with one tcgen05 GEMM per pick (binary16
-// dictionaries screened on the tensor cores); the default is the
-// pool-resident mma.sync kernel, FADKV_GREEDY=ffma the FP32-pipe kernel.
-bool use_greedy_tc(fadkv_dict h)
+// Greedy kernel for binary16 dictionaries screened on the tensor cores: by
+// default the correlation-domain kernel (incremental Cholesky factor);
+// FADKV_GREEDY=tc selects one tcgen05 GEMM per pick, FADKV_GREEDY=mma the
+// residual-based mma.sync kernel and FADKV_GREEDY=ffma the FP32-pipe kernel.
+enum class GreedyPath { kChol, kTc, kClassic };
+
+GreedyPath greedy_path(fadkv_dict h)
 {
-    if (!h->L.tc) return false;
+    if (!h->L.tc) return GreedyPath::kClassic;
     const char* f = getenv("FADKV_GREEDY");
-    if (!(f && strcmp(f, "tc") == 0)) return false;
-    return greedy_tc_supported(h->sh);
+    if (f && strcmp(f, "tc") == 0) return greedy_tc_supported(h->sh) ? GreedyPath::kTc : GreedyPath::kClassic;
+    if (f && (strcmp(f, "mma") == 0 || strcmp(f, "ffma") == 0)) return GreedyPath::kClassic;
+    return greedy_chol_supported(h->sh) ? GreedyPath::kChol : GreedyPath::kClassic;
 }
 
 GreedyArgs greedy_args(fadkv_dict h, const void* x, int32_t V, int v0, int Vc)
@@ -415,11 +419,18 @@ fadkv_status fadkv_encode(fadkv_dict h, const void* x, int32_t V, int32_t* idx, 
     for (int v0 = 0; v0 < V; v0 += chunk) {
         const int Vc = (V - v0 < chunk) ? V - v0 : chunk;
         cudaError_t e = run_screen(h, x, V, v0, Vc, nullptr, st);
-        if (e == cudaSuccess && use_greedy_tc(h)) {
+        const GreedyPath gp = greedy_path(h);
+        if (e == cudaSuccess && gp != GreedyPath::kClassic) {
             int32_t* pool = (int32_t*)(h->ws + h->L.pool);
             GreedyArgs fa = greedy_args(h, x, V, v0, Vc);
             e = traced(h, FADKV_K_TOPN, st, [&] { return launch_pool_fixup(h->sh, fa, pool, h->sms, st); });
-            if (e == cudaSuccess) {
+            if (e == cudaSuccess && gp == GreedyPath::kChol) {
+                GreedyArgs ca = greedy_args(h, x, V, v0, Vc);
+                ca.idx = idx;
+                ca.coef = coef;
+                ca.relres = relres;
+                e = traced(h, FADKV_K_GREEDY, st, [&] { return launch_greedy_chol(h->sh, ca, st); });
+            } else if (e == cudaSuccess) {
                 GreedyTCArgs ga;
                 ga.atoms = h->atoms;
                 ga.x = x;

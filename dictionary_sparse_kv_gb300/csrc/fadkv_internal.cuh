@@ -146,6 +146,12 @@ struct GreedyTCArgs {
 bool greedy_tc_supported(const Shape& sh);
 cudaError_t launch_greedy_tc(const Shape& sh, const GreedyTCArgs& a, int sms, cudaStream_t st);
 
+// Greedy + ridge refit in the correlation domain (incremental Cholesky
+// factor, pool resident in registers; binary16, n <= 512, s <= 16).  Needs
+// the exact pool of every vector in a.pool_in (run launch_pool_fixup first).
+bool greedy_chol_supported(const Shape& sh);
+cudaError_t launch_greedy_chol(const Shape& sh, const GreedyArgs& a, cudaStream_t st);
+
 // Exact pool of the vectors the selection kernel left to the slow path
 // (pool[0] == -2): all N scores on the FP32 pipe, exact Top-n.
 cudaError_t launch_pool_fixup(const Shape& sh, const GreedyArgs& a, int32_t* pool, int sms, cudaStream_t st);

@@ -1,0 +1,382 @@
+// In-pool greedy selection with the ridge refit carried as an incremental
+// Cholesky factor in the correlation domain -- binary16 dictionaries, the
+// pool resident in registers as mma.sync operands.
+//
+// "FAD-KV: Adaptive Dictionary KV Caching for Efficient Reasoning Decoding":
+// abstract (screening-based sparse coding: a one-shot Top-n pool followed by
+// lightweight coefficient refinement) and Table 5 (ridge lambda = 1e-4 +
+// 0.20 diag(G)).  Greedy selection inside the pool and the lower-index tie
+// rule are conventions of this library.
+//
+// The step the method defines -- pick j* = argmax |<d_j, e_k>| over the
+// pool, refit (G_SS + diag(la + lr G_ii)) c = D_S x, e = x - D_S c -- is
+// carried without forming e (the way batch OMP carries plain OMP):
+// with A_SS = L L^T, z = L^-1 D_S^T x and l_j = L^-1 G_{S,j} for every pool
+// atom j,
+//   <d_j, e> = r_j - l_j . z                       (r = D x: the screening scores)
+//   picking j*:  L_kk = sqrt(G_j*j* (1 + lr) + la - |l_j*|^2),
+//                z_k  = <d_j*, e> / L_kk,
+//   every j:     l_j[k] = (G_{j,j*} - l_j* . l_j) / L_kk,
+//                <d_j, e> -= z_k l_j[k],
+//   at the end   c = L^-T z (back substitution), e = x - D_S c.
+// Per step the only contraction is the pick's Gram column G_{P,j*}: one
+// mma.sync pass of the register-resident pool against the pick's binary16
+// row (exact products, fp32 sums).
+//
+// One CTA of NW warps per vector; warp w holds pool slots 32w .. 32w+31 as
+// two m16 tiles of A fragments; lane (g8, t4) keeps the Cholesky state of
+// slot t4 of its row group (tile t4>>1, row g8 + 8 (t4&1)).  Each warp ends
+// a step by publishing its best slot (key, l vector, correlation, |l|^2,
+// G_jj and the atom's row), so one barrier per step suffices.
+#include <stdlib.h>
+#include <string.h>
+
+#include "fadkv_internal.cuh"
+
+namespace fadkv {
+namespace {
+
+constexpr int kMT = 2;   // m16 tiles per warp
+
+__device__ __forceinline__ void hmma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int D, int NW, int SMAX>
+__global__ void __launch_bounds__(NW * 32, NW <= 8 ? 2 : 1)
+greedy_chol_kernel(Shape sh, GreedyArgs a)
+{
+    constexpr int KT = D / 16, KP = D / 32, NT = NW * 32;
+    constexpr int SPW = kMT * 16, NPAD = NW * SPW;
+    constexpr int PL = SMAX + 4;                 // published floats: l[SMAX], corr, |l|^2, G_jj, slot
+    const int vc = blockIdx.x, g = blockIdx.y;
+    const int v = a.v0 + vc;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int n = sh.n, s = sh.s, N = sh.N;
+
+    __shared__ float xs[D];
+    __shared__ int pid[NPAD];
+    __shared__ __align__(16) __half bx[2 * D];         // first pass: x 2^p split in two binary16 terms
+    __shared__ __align__(16) __half zrow[D];           // a zero B column
+    __shared__ __align__(16) __half pub[2][NW][D];     // each warp's best atom row
+    __shared__ float publ[2][NW][PL];
+    __shared__ unsigned long long kred[2][NW];
+    __shared__ __align__(16) __half picked[SMAX][D];   // rows of the picks
+    __shared__ float zrec[SMAX], irec[SMAX], crec[SMAX], lrow[SMAX][SMAX + 1];
+    __shared__ int sslot[SMAX];
+    __shared__ float fred[NW];
+
+    const size_t gv = (size_t)g * a.Vc + vc;
+    const __half* X = (const __half*)a.x + ((size_t)g * a.V + v) * D;
+    const __half* Aglob = (const __half*)a.atoms + (size_t)g * N * D;
+    long long* cnt = a.counters + (size_t)g * kCntFields;
+    unsigned long long* status = (unsigned long long*)&cnt[kCntStatus];
+    const size_t out = (size_t)g * a.V + v;
+
+    // ---- x, its norm and finiteness; the pool ----
+    float xsq = 0.f;
+    int bad = 0;
+    for (int t = tid; t < D; t += NT) {
+        const float xv = __half2float(X[t]);
+        xs[t] = xv;
+        zrow[t] = __float2half_rn(0.f);
+        bad |= !isfinite(xv);
+        xsq = fmaf(xv, xv, xsq);
+    }
+    xsq = warp_sum(xsq);
+    if (lane == 0) fred[warp] = xsq;
+    for (int i = tid; i < NPAD; i += NT) pid[i] = (i < n) ? a.pool_in[gv * n + i] : -1;
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        for (int k = tid; k < s; k += NT) {
+            a.idx[out * s + k] = -1;
+            a.coef[out * s + k] = 0.f;
+        }
+        if (tid == 0) {
+            a.relres[out] = __int_as_float(0x7fc00000);
+            atomicAdd((unsigned long long*)&cnt[kCntNonfinite], 1ull);
+            atomicOr(status, (unsigned long long)FADKV_DEV_NONFINITE_INPUT);
+        }
+        return;
+    }
+    float xnorm2 = 0.f;
+    for (int w = 0; w < NW; ++w) xnorm2 += fred[w];
+
+    // ---- pool atoms -> A fragments; G_jj of this lane's slot ----
+    // Inside each 32-element block of the head dimension, thread t4 of a row
+    // holds elements 8 t4 .. 8 t4 + 7 (one 16-byte load): a permutation of the
+    // contraction index applied alike to A and B.
+    uint32_t Af[kMT][KT][4];
+    float gjj = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt) {
+        const int s0 = warp * SPW + mt * 16 + g8;
+        const int r0 = pid[s0], r1 = pid[s0 + 8];
+        float n0 = 0.f, n1 = 0.f;
+#pragma unroll
+        for (int kp = 0; kp < KP; ++kp) {
+            uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+            if (r0 >= 0) q0 = *reinterpret_cast<const uint4*>(Aglob + (size_t)r0 * D + 32 * kp + 8 * t4);
+            if (r1 >= 0) q1 = *reinterpret_cast<const uint4*>(Aglob + (size_t)r1 * D + 32 * kp + 8 * t4);
+            Af[mt][2 * kp][0] = q0.x;
+            Af[mt][2 * kp][2] = q0.y;
+            Af[mt][2 * kp + 1][0] = q0.z;
+            Af[mt][2 * kp + 1][2] = q0.w;
+            Af[mt][2 * kp][1] = q1.x;
+            Af[mt][2 * kp][3] = q1.y;
+            Af[mt][2 * kp + 1][1] = q1.z;
+            Af[mt][2 * kp + 1][3] = q1.w;
+            const __half2* h0 = reinterpret_cast<const __half2*>(&q0);
+            const __half2* h1 = reinterpret_cast<const __half2*>(&q1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f0 = __half22float2(h0[i]), f1 = __half22float2(h1[i]);
+                n0 = fmaf(f0.x, f0.x, fmaf(f0.y, f0.y, n0));
+                n1 = fmaf(f1.x, f1.x, fmaf(f1.y, f1.y, n1));
+            }
+        }
+        n0 += __shfl_xor_sync(0xffffffffu, n0, 1);
+        n0 += __shfl_xor_sync(0xffffffffu, n0, 2);
+        n1 += __shfl_xor_sync(0xffffffffu, n1, 1);
+        n1 += __shfl_xor_sync(0xffffffffu, n1, 2);
+        if (t4 == 2 * mt) gjj = n0;
+        if (t4 == 2 * mt + 1) gjj = n1;
+    }
+    const int myslot = warp * SPW + (t4 >> 1) * 16 + (t4 & 1) * 8 + g8;
+    const int myatom = pid[myslot];
+    bool live = myatom >= 0;
+
+    // scale 2^p with ||x|| < 2^ex: |x_t| 2^p < 2^14 (no binary16 overflow)
+    int ex = 0;
+    frexpf(sqrtf(xnorm2), &ex);
+    const float scale = (xnorm2 > 0.f) ? ldexpf(1.f, 14 - ex) : 1.f;
+    const float inv_scale = (xnorm2 > 0.f) ? ldexpf(1.f, ex - 14) : 1.f;
+    for (int t = tid; t < D; t += NT) {
+        const float sv = xs[t] * scale;
+        const __half hi = __float2half_rn(sv);
+        bx[t] = hi;
+        bx[D + t] = __float2half_rn(sv - __half2float(hi));
+    }
+    __syncthreads();
+
+    // pool rows x B (column g8 of this lane from `c0`, `c1` or zero) -> acc
+    float acc[kMT][4];
+    auto mma_pass = [&](const __half* c0, const __half* c1) {
+        const __half* bsrc = (g8 == 0) ? c0 : ((g8 == 1) ? c1 : zrow);
+        float part[kMT][2][4];
+#pragma unroll
+        for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) part[mt][ks][r] = 0.f;
+#pragma unroll
+        for (int kp = 0; kp < KP; ++kp) {
+            const uint4 qb = *reinterpret_cast<const uint4*>(bsrc + 32 * kp + 8 * t4);
+#pragma unroll
+            for (int mt = 0; mt < kMT; ++mt) {
+                hmma(part[mt][kp & 1], Af[mt][2 * kp], qb.x, qb.y);
+                hmma(part[mt][kp & 1], Af[mt][2 * kp + 1], qb.z, qb.w);
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[mt][r] = part[mt][0][r] + part[mt][1][r];
+    };
+    // value of column 0 (+ column 1 when `two`) for each of the row group's 4
+    // slots, handed to the lane that owns the slot (lane t4 <- slot t4)
+    auto to_owner = [&](bool two) -> float {
+        float vv[4];
+        vv[0] = two ? acc[0][0] + acc[0][1] : acc[0][0];
+        vv[1] = two ? acc[0][2] + acc[0][3] : acc[0][2];
+        vv[2] = two ? acc[1][0] + acc[1][1] : acc[1][0];
+        vv[3] = two ? acc[1][2] + acc[1][3] : acc[1][2];
+        float mine = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float t = __shfl_sync(0xffffffffu, vv[m], lane & ~3);
+            if (t4 == m) mine = t;
+        }
+        return mine;
+    };
+
+    // ---- first pass: r_j for the pool ----
+    mma_pass(bx, bx + D);
+    float corr = to_owner(true) * inv_scale;
+    float ll = 0.f;
+    float l[SMAX];
+#pragma unroll
+    for (int i = 0; i < SMAX; ++i) l[i] = 0.f;
+
+    // this warp's best live slot (larger |corr|, then the lower atom) -> publish
+    auto best_publish = [&](int par, int k) {
+        const uint32_t key = live ? (__float_as_uint(corr) & 0x7fffffffu) + 1u : 0u;
+        const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+        const uint32_t cand = (live && key == m) ? (uint32_t)myatom : 0xffffffffu;
+        const uint32_t amin = __reduce_min_sync(0xffffffffu, cand);
+        const bool win = m != 0u && live && key == m && (uint32_t)myatom == amin;
+        const unsigned wb = __ballot_sync(0xffffffffu, win);
+        if (lane == 0) kred[par][warp] = (m == 0u) ? 0ull : (((unsigned long long)m << 32) | (0xffffffffu - amin));
+        if (wb != 0u) {
+            const int wl = __ffs(wb) - 1;
+            const int mw = wl & 3, mt_w = mw >> 1, h_w = mw & 1;
+            if (g8 == (wl >> 2)) {
+                __half* dst = pub[par][warp];
+#pragma unroll
+                for (int mt = 0; mt < kMT; ++mt) {
+                    if (mt == mt_w) {
+#pragma unroll
+                        for (int kp = 0; kp < KP; ++kp) {
+                            const uint32_t w0 = h_w ? Af[mt][2 * kp][1] : Af[mt][2 * kp][0];
+                            const uint32_t w1 = h_w ? Af[mt][2 * kp][3] : Af[mt][2 * kp][2];
+                            const uint32_t w2 = h_w ? Af[mt][2 * kp + 1][1] : Af[mt][2 * kp + 1][0];
+                            const uint32_t w3 = h_w ? Af[mt][2 * kp + 1][3] : Af[mt][2 * kp + 1][2];
+                            *reinterpret_cast<uint4*>(dst + 32 * kp + 8 * t4) = make_uint4(w0, w1, w2, w3);
+                        }
+                    }
+                }
+            }
+            if (lane == wl) {
+                float* pl = publ[par][warp];
+#pragma unroll
+                for (int i = 0; i < SMAX; ++i)
+                    if (i < k) pl[i] = l[i];
+                pl[SMAX] = corr;
+                pl[SMAX + 1] = ll;
+                pl[SMAX + 2] = gjj;
+                pl[SMAX + 3] = __int_as_float(myslot);
+            }
+        }
+    };
+    best_publish(0, 0);
+    __syncthreads();
+
+    const float la = sh.lambda_abs, lr = sh.lambda_rel;
+    for (int k = 0; k < s; ++k) {
+        // ---- the pick: best of the warps' bests ----
+        const int par = k & 1;
+        unsigned long long win = 0ull;
+        int w_o = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const unsigned long long kv = kred[par][w];
+            if (kv > win) {
+                win = kv;
+                w_o = w;
+            }
+        }
+        const float* pl = publ[par][w_o];
+        const float cstar = pl[SMAX], llstar = pl[SMAX + 1], gstar = pl[SMAX + 2];
+        const int slot_o = __float_as_int(pl[SMAX + 3]);
+        float dk = fmaf(gstar, lr, gstar) + la - llstar;
+        if (!(dk > 0.f)) {
+            if (tid == 0) atomicOr(status, (unsigned long long)FADKV_DEV_NOT_SPD);
+            dk = 1e-30f;
+        }
+        const float inv = __frcp_rn(sqrtf(dk));
+        const float zk = cstar * inv;
+        if (live && myslot == slot_o) live = false;
+        if (warp == 0) {
+            // the factor's row k, z_k and the pick's row for the end
+            if (lane < k) lrow[k][lane] = pl[lane];
+            if (lane == 0) {
+                sslot[k] = slot_o;
+                zrec[k] = zk;
+                irec[k] = inv;
+            }
+            for (int t = lane; t < D / 8; t += 32)
+                reinterpret_cast<uint4*>(picked[k])[t] = reinterpret_cast<const uint4*>(pub[par][w_o])[t];
+        }
+        if (k + 1 == s) break;
+
+        // ---- Gram column of the pick; every slot's update ----
+        mma_pass(pub[par][w_o], zrow);
+        const float gj = to_owner(false);
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < SMAX; ++i)
+            if (i < k) dot = fmaf(pl[i], l[i], dot);
+        const float t = (gj - dot) * inv;
+#pragma unroll
+        for (int i = 0; i < SMAX; ++i)
+            if (i == k) l[i] = t;
+        ll = fmaf(t, t, ll);
+        corr = fmaf(-zk, t, corr);
+        best_publish(par ^ 1, k + 1);
+        __syncthreads();
+    }
+
+    // ---- coefficients c = L^-T z, residual and outputs (warp 0) ----
+    if (warp != 0) return;
+    __syncwarp();
+    if (lane == 0) {
+        for (int k = s - 1; k >= 0; --k) {
+            float acc0 = zrec[k];
+            for (int i = k + 1; i < s; ++i) acc0 = fmaf(-lrow[i][k], crec[i], acc0);
+            crec[k] = acc0 * irec[k];
+        }
+    }
+    __syncwarp();
+    float esq = 0.f;
+    for (int t = lane; t < D; t += 32) {
+        float e = xs[t];
+        for (int i = 0; i < s; ++i) e = fmaf(-crec[i], __half2float(picked[i][t]), e);
+        esq = fmaf(e, e, esq);
+    }
+    esq = warp_sum(esq);
+    if (lane == 0) a.relres[out] = (xnorm2 > 0.f) ? sqrtf(esq) / sqrtf(xnorm2) : 0.f;
+    for (int k = lane; k < s; k += 32) {
+        a.idx[out * s + k] = pid[sslot[k]];
+        a.coef[out * s + k] = crec[k];
+    }
+}
+
+template <int D, int NW, int SMAX>
+cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+{
+    dim3 grid(a.Vc, sh.G);
+    greedy_chol_kernel<D, NW, SMAX><<<grid, NW * 32, 0, st>>>(sh, a);
+    return cudaGetLastError();
+}
+
+template <int D, int NW>
+cudaError_t launch_s(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+{
+    return sh.s <= 8 ? launch_t<D, NW, 8>(sh, a, st) : launch_t<D, NW, 16>(sh, a, st);
+}
+
+template <int D>
+cudaError_t launch_d(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+{
+    return sh.n <= 256 ? launch_s<D, 8>(sh, a, st) : launch_s<D, 16>(sh, a, st);
+}
+
+}  // namespace
+
+bool greedy_chol_supported(const Shape& sh)
+{
+    return sh.dtype == FADKV_F16 && (sh.d == 64 || sh.d == 128) && sh.n <= 512 && sh.s <= 16;
+}
+
+cudaError_t launch_greedy_chol(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+{
+    if (a.Vc <= 0) return cudaSuccess;
+    if (!a.pool_in) return cudaErrorInvalidValue;
+    return sh.d == 128 ? launch_d<128>(sh, a, st) : launch_d<64>(sh, a, st);
+}
+
+}  // namespace fadkv

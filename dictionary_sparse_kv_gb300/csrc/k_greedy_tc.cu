@@ -52,12 +52,12 @@ using namespace tc;
 constexpr int kThreadsG = 256;
 constexpr int kTileG = 128;     // vectors per tile (MMA M)
 constexpr int kChunkG = 64;     // atoms per MMA (MMA N)
-constexpr int kStagesG = 3;     // atom-chunk pipeline depth
+constexpr int kStagesG = 2;     // atom-chunk pipeline depth
 constexpr int kTmemColsG = 256;
 constexpr int kMaxClusterG = 8;
 
 struct GtcLayout {
-    uint32_t b, mask, st, xch, bar, taddr, total, alloc;
+    uint32_t b, mask, st, gbuf, vec, stage, xch, bar, taddr, total, alloc;
 };
 
 // ns: atoms of the largest slice; C: CTAs per cluster.
@@ -68,6 +68,9 @@ __host__ __device__ inline GtcLayout gtc_layout(int d, int smax, int ns, int C)
     L.b = o;     o += (uint32_t)(kStagesG * (d / 64) * kChunkG * 128);          // 1024-byte multiples
     L.mask = o;  o += (uint32_t)((ns / 32) * kTileG * 4);                        // [word][row]
     L.st = o;    o += (uint32_t)((smax * (smax + 1) / 2 + 3 * smax) * kTileG * 4);  // M, z, c, picks: [entry][row]
+    L.gbuf = o;  o += (uint32_t)((smax + 2) * kTileG * 4);                       // Gram row, ||d||^2, <d,x>: [entry][row]
+    L.vec = o;   o += (uint32_t)(3 * kTileG * 4);                                // scale, ||x||^2, state: [row]
+    L.stage = o; o += (uint32_t)(4 * 2 * 32 * 32 * 2);                           // per warp: hi, lo [32 rows][32] binary16
     L.xch = o;   o += (uint32_t)(2 * C * kTileG * 8);                            // [parity][rank][row]
     o = (o + 7u) & ~7u;
     L.bar = o;   o += (uint32_t)((2 * kStagesG + 2 + 2 + 1 + 2) * 8);
@@ -216,90 +219,168 @@ greedy_tc_kernel(const __grid_constant__ CUtensorMap map_d, Shape sh, GreedyTCAr
             if (cc > 0) mbar_wait(accf_bar((cc - 1) & 1), (uint32_t)((cc - 1) >> 1) & 1u, status);
         }
     } else if (warp >= 4) {
-        // ---------------- one vector per thread ----------------
+        // ---------------- the vectors: warps 4..7, one TMEM lane quadrant each ----------------
+        // Thread-per-vector work (row r = TMEM lane): the sweep, the cluster
+        // exchange and the refit.  Warp-cooperative work (8 lanes per vector,
+        // 4 vectors at a time, each lane 4 consecutive elements of every
+        // 32-element quarter, so a row quarter is one 64-byte segment): the
+        // statistics of x, the pool masks, the Gram row of the pick and the
+        // residual, which is staged per quarter and written to TMEM by the
+        // lane owners.
         const int q = warp - 4;
         const int r = q * 32 + lane;                       // tile row = TMEM lane
-        const int vloc = tile * kTileG + r;                // vector inside this pass
-        const bool valid = vloc < a.Vc;
-        const int v = a.v0 + (valid ? vloc : 0);
+        const int gs = lane >> 3, l8 = lane & 7;           // vector slot of the group, lane in the group
+        const int rows = min(kTileG, a.Vc - tile * kTileG);
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const __half* Ag = (const __half*)a.atoms + (size_t)g * N * D;
-        const __half* xrow = (const __half*)a.x + ((size_t)g * a.V + v) * D;
+        const __half* Xt = (const __half*)a.x + ((size_t)g * a.V + a.v0 + (size_t)tile * kTileG) * D;   // row R at Xt + R D
         float* Mst = stf;                                  // [TRI][row]
         float* zst = stf + TRI * kTileG;                   // [SMAX][row]
         float* cst = zst + SMAX * kTileG;                  // [SMAX][row]
         int* pst = (int*)(cst + SMAX * kTileG);            // [SMAX][row]
+        float* gbuf = (float*)(smem + L.gbuf);             // [SMAX + 2][row]
+        float* vscale = (float*)(smem + L.vec);            // [row]
+        float* vxn2 = vscale + kTileG;                     // [row]
+        int* vstate = (int*)(vxn2 + kTileG);               // [row]: 0 none, 1 active, 2 non-finite
+        __half* stg_hi = (__half*)(smem + L.stage) + q * (2 * 32 * 32);
+        __half* stg_lo = stg_hi + 32 * 32;
         const float la = sh.lambda_abs, lr = sh.lambda_rel;
 
-        // x: finiteness, norm, scale 2^p with |e_t| 2^p < 2^14
-        float xn2 = 0.f;
-        bool bad = false;
-        if (valid) {
-            for (int t0 = 0; t0 < D; t0 += 8) {
-                float f[8];
-                load8(xrow + t0, f);
+        // 4 elements of a binary16 row at element e (8-byte load)
+        auto ld4 = [](const __half* p, float (&f)[4]) {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+            const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+            f[0] = a0.x; f[1] = a0.y; f[2] = a1.x; f[3] = a1.y;
+        };
+
+        // ---- x: finiteness, norm, scale 2^p with |e_t| 2^p < 2^14 ----
+#pragma unroll 1
+        for (int it = 0; it < 8; ++it) {
+            const int R = q * 32 + it * 4 + gs;
+            float sq = 0.f;
+            int bad = 0;
+            if (R < rows) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    bad |= !isfinite(f[u]);
-                    xn2 = fmaf(f[u], f[u], xn2);
+                for (int cq = 0; cq < D / 32; ++cq) {
+                    float f[4];
+                    ld4(Xt + (size_t)R * D + cq * 32 + 4 * l8, f);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        bad |= !isfinite(f[u]);
+                        sq = fmaf(f[u], f[u], sq);
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+            }
+            if (l8 == 0) {
+                int ex = 0;
+                frexpf(sqrtf(sq), &ex);
+                vscale[R] = (sq > 0.f) ? ldexpf(1.f, 14 - ex) : 1.f;
+                vxn2[R] = sq;
+                vstate[R] = (R < rows) ? (bad ? 2 : 1) : 0;
+            }
+        }
+
+        // ---- pool membership of this slice's atoms (bitmask per row) ----
+        for (int w = 0; w < 2 * nch; ++w) mask[w * kTileG + r] = 0u;
+        __syncwarp();
+        {
+            const unsigned span = (unsigned)(nch * kChunkG);
+#pragma unroll 1
+            for (int v = 0; v < 32; ++v) {
+                const int R = q * 32 + v;
+                if (R >= rows) break;
+                const int32_t* pl = a.pool + ((size_t)g * a.Vc + (size_t)tile * kTileG + R) * n;
+#pragma unroll 4
+                for (int i = lane; i < n; i += 32) {
+                    const int j = __ldg(pl + i) - atom0;
+                    if ((unsigned)j < span) atomicOr(&mask[(j >> 5) * kTileG + R], 1u << (j & 31));
                 }
             }
         }
-        bool active = valid && !bad;
-        int ex = 0;
-        frexpf(sqrtf(xn2), &ex);
-        const float scale = (xn2 > 0.f) ? ldexpf(1.f, 14 - ex) : 1.f;
+        __syncwarp();
 
-        // pool membership of this slice's atoms
-        for (int w = 0; w < 2 * nch; ++w) mask[w * kTileG + r] = 0u;
-        if (active) {
-            const int32_t* pl = a.pool + ((size_t)g * a.Vc + vloc) * n;
-            const unsigned span = (unsigned)(nch * kChunkG);
-#pragma unroll 4
-            for (int i = 0; i < n; ++i) {
-                const int j = __ldg(pl + i) - atom0;
-                if ((unsigned)j < span) mask[(j >> 5) * kTileG + r] |= 1u << (j & 31);
-            }
-        }
-
-        // e -> A operand (hi, lo) of this lane, 32 elements at a time
-        auto write_a = [&](int cb, const float (&e)[32]) {
-            uint32_t hi[16], lo[16];
+        // ---- residual with the first kk+1 picks -> A operand (or ||e||^2) ----
+        // kk = -1: e = x.  Row order: row 32q + 4 it + gs at staging row 4 it + gs.
+        float esq[8];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const float s0 = e[2 * u] * scale, s1 = e[2 * u + 1] * scale;
-                const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
-                const __half l0 = __float2half_rn(s0 - __half2float(h0));
-                const __half l1 = __float2half_rn(s1 - __half2float(h1));
-                const __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
-                hi[u] = *reinterpret_cast<const uint32_t*>(&hh);
-                lo[u] = *reinterpret_cast<const uint32_t*>(&ll);
-            }
-            tmem_st16(tbase + lane_off + (uint32_t)(cb * 16), hi);
-            tmem_st16(tbase + lane_off + (uint32_t)(ACOLS + cb * 16), lo);
-        };
+        for (int it = 0; it < 8; ++it) esq[it] = 0.f;
+        auto residual_pass = [&](int kk, bool to_tmem) {
 #pragma unroll 1
-        for (int cb = 0; cb < D / 32; ++cb) {
-            float e[32];
+            for (int cq = 0; cq < D / 32; ++cq) {
+#pragma unroll 2
+                for (int it = 0; it < 8; ++it) {
+                    const int lr_ = it * 4 + gs;
+                    const int R = q * 32 + lr_;
+                    const bool act = vstate[R] == 1;
+                    float e[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (act) {
+                        ld4(Xt + (size_t)R * D + cq * 32 + 4 * l8, e);
 #pragma unroll
-            for (int u8 = 0; u8 < 4; ++u8) {
-                float f[8];
-                if (active) load8(xrow + cb * 32 + u8 * 8, f);
+                        for (int i = 0; i < SMAX; ++i) {
+                            if (i <= kk) {
+                                const float ci = cst[i * kTileG + R];
+                                float f[4];
+                                ld4(Ag + (size_t)pst[i * kTileG + R] * D + cq * 32 + 4 * l8, f);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) e[u8 * 8 + u] = active ? f[u] : 0.f;
+                                for (int u = 0; u < 4; ++u) e[u] = fmaf(-ci, f[u], e[u]);
+                            }
+                        }
+                    }
+                    if (to_tmem) {
+                        const float sc = vscale[R];
+                        __half h[4], l[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float sv = e[u] * sc;
+                            h[u] = __float2half_rn(sv);
+                            l[u] = __float2half_rn(sv - __half2float(h[u]));
+                        }
+                        const __half2 h01 = __halves2half2(h[0], h[1]), h23 = __halves2half2(h[2], h[3]);
+                        const __half2 l01 = __halves2half2(l[0], l[1]), l23 = __halves2half2(l[2], l[3]);
+                        uint2 uh, ul;
+                        uh.x = *reinterpret_cast<const uint32_t*>(&h01);
+                        uh.y = *reinterpret_cast<const uint32_t*>(&h23);
+                        ul.x = *reinterpret_cast<const uint32_t*>(&l01);
+                        ul.y = *reinterpret_cast<const uint32_t*>(&l23);
+                        *reinterpret_cast<uint2*>(stg_hi + lr_ * 32 + 4 * l8) = uh;
+                        *reinterpret_cast<uint2*>(stg_lo + lr_ * 32 + 4 * l8) = ul;
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) esq[it] = fmaf(e[u], e[u], esq[it]);
+                    }
+                }
+                if (to_tmem) {
+                    __syncwarp();
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int w4 = 0; w4 < 4; ++w4) {
+                        const uint4 th = *reinterpret_cast<const uint4*>(stg_hi + lane * 32 + w4 * 8);
+                        const uint4 tl = *reinterpret_cast<const uint4*>(stg_lo + lane * 32 + w4 * 8);
+                        hi[w4 * 4 + 0] = th.x; hi[w4 * 4 + 1] = th.y; hi[w4 * 4 + 2] = th.z; hi[w4 * 4 + 3] = th.w;
+                        lo[w4 * 4 + 0] = tl.x; lo[w4 * 4 + 1] = tl.y; lo[w4 * 4 + 2] = tl.z; lo[w4 * 4 + 3] = tl.w;
+                    }
+                    tmem_st16(tbase + lane_off + (uint32_t)(cq * 16), hi);
+                    tmem_st16(tbase + lane_off + (uint32_t)(ACOLS + cq * 16), lo);
+                    __syncwarp();
+                }
             }
-            write_a(cb, e);
-        }
-        tmem_st_wait();
+            if (to_tmem) tmem_st_wait();
+        };
+        residual_pass(-1, true);
 
         int cc = 0;
         bool ok = true;
-        float esq = 0.f;
         for (int k = 0; k < s; ++k) {
             fence_before();
             mbar_arrive(afull_bar);                        // A_k is in TMEM
 
-            // ---- sweep: masked argmax over this slice ----
+            // ---- sweep: masked argmax over this slice (thread per vector) ----
             uint32_t best = 0u;                            // (|acc| bits) + 1 for pool atoms, 0 otherwise
             int bj = -1;
             for (int c = 0; c < nch; ++c) {
@@ -351,48 +432,81 @@ greedy_tc_kernel(const __grid_constant__ CUtensorMap map_d, Shape sh, GreedyTCAr
                     ok = false;
                 }
             }
-            if (!(best > 0u) || bj < 0 || bj >= N) active = false;   // no pool atom left (not reached for n >= s)
-            const int jk = bj;
-            if (active) {
-                const int jj = jk - atom0;
-                if ((unsigned)jj < (unsigned)(nch * kChunkG)) mask[(jj >> 5) * kTileG + r] &= ~(1u << (jj & 31));
-                pst[k * kTileG + r] = jk;
+            if (vstate[r] == 1) {
+                if (!(best > 0u) || bj < 0 || bj >= N) {
+                    vstate[r] = 0;                          // no pool atom left (not reached for n >= s)
+                } else {
+                    const int jj = bj - atom0;
+                    if ((unsigned)jj < (unsigned)(nch * kChunkG)) mask[(jj >> 5) * kTileG + r] &= ~(1u << (jj & 31));
+                    pst[k * kTileG + r] = bj;
+                }
+            }
+            __syncwarp();
 
-                // ---- Gram row of the pick, its norm and <d, x> ----
-                int pk[SMAX];
-#pragma unroll
-                for (int i = 0; i < SMAX; ++i) pk[i] = (i < k) ? pst[i * kTileG + r] : 0;
-                float bk = 0.f, gkk = 0.f, gr[SMAX];
-#pragma unroll
-                for (int i = 0; i < SMAX; ++i) gr[i] = 0.f;
-                const __half* dn = Ag + (size_t)jk * D;
+            // ---- Gram row of the pick, its norm and <d, x> (8 lanes per vector) ----
 #pragma unroll 1
-                for (int t0 = 0; t0 < D; t0 += 8) {
-                    float fn[8], fx[8];
-                    load8(dn + t0, fn);
-                    load8(xrow + t0, fx);
+            for (int it = 0; it < 8; ++it) {
+                const int R = q * 32 + it * 4 + gs;
+                const bool act = vstate[R] == 1;
+                float gp[SMAX];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        bk = fmaf(fn[u], fx[u], bk);
-                        gkk = fmaf(fn[u], fn[u], gkk);
-                    }
+                for (int i = 0; i < SMAX; ++i) gp[i] = 0.f;
+                float bp = 0.f, np = 0.f;
+                if (act) {
+                    const __half* dn = Ag + (size_t)pst[k * kTileG + R] * D;
+                    int pk[SMAX];
 #pragma unroll
-                    for (int i = 0; i < SMAX; ++i) {
-                        if (i < k) {
-                            float fi[8];
-                            load8(Ag + (size_t)pk[i] * D + t0, fi);
+                    for (int i = 0; i < SMAX; ++i) pk[i] = (i < k) ? pst[i * kTileG + R] : 0;
 #pragma unroll
-                            for (int u = 0; u < 8; ++u) gr[i] = fmaf(fn[u], fi[u], gr[i]);
+                    for (int cq = 0; cq < D / 32; ++cq) {
+                        const int e0 = cq * 32 + 4 * l8;
+                        float fn[4], fx[4];
+                        ld4(dn + e0, fn);
+                        ld4(Xt + (size_t)R * D + e0, fx);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            bp = fmaf(fn[u], fx[u], bp);
+                            np = fmaf(fn[u], fn[u], np);
+                        }
+#pragma unroll
+                        for (int i = 0; i < SMAX; ++i) {
+                            if (i < k) {
+                                float fi[4];
+                                ld4(Ag + (size_t)pk[i] * D + e0, fi);
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) gp[i] = fmaf(fn[u], fi[u], gp[i]);
+                            }
                         }
                     }
                 }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    bp += __shfl_xor_sync(0xffffffffu, bp, o);
+                    np += __shfl_xor_sync(0xffffffffu, np, o);
+#pragma unroll
+                    for (int i = 0; i < SMAX; ++i)
+                        if (i < k) gp[i] += __shfl_xor_sync(0xffffffffu, gp[i], o);
+                }
+                if (l8 == 0 && act) {
+#pragma unroll
+                    for (int i = 0; i < SMAX; ++i)
+                        if (i < k) gbuf[i * kTileG + R] = gp[i];
+                    gbuf[SMAX * kTileG + R] = np;
+                    gbuf[(SMAX + 1) * kTileG + R] = bp;
+                }
+            }
+            __syncwarp();
 
-                // ---- ridge refit: one row more of M = L^-1 ----
-                // A = G_SS + diag(lambda_abs + lambda_rel G_ii) = L L^T,
-                // z = M b, c = M^T z.  l = M g, L_kk = sqrt(gkk (1 + lr) + la - l.l),
-                // z_k = (b_k - l.z) / L_kk, new row w = -(l^T M) / L_kk,
-                // c <- c + z_k w, c_k = z_k / L_kk.
-                float l[SMAX];
+            // ---- ridge refit: one row more of M = L^-1 (thread per vector) ----
+            // A = G_SS + diag(lambda_abs + lambda_rel G_ii) = L L^T,
+            // z = M b, c = M^T z.  l = M g, L_kk = sqrt(gkk (1 + lr) + la - l.l),
+            // z_k = (b_k - l.z) / L_kk, new row w = -(l^T M) / L_kk,
+            // c <- c + z_k w, c_k = z_k / L_kk.
+            if (vstate[r] == 1) {
+                const float gkk = gbuf[SMAX * kTileG + r], bk = gbuf[(SMAX + 1) * kTileG + r];
+                float gr[SMAX], l[SMAX];
+#pragma unroll
+                for (int i = 0; i < SMAX; ++i) gr[i] = (i < k) ? gbuf[i * kTileG + r] : 0.f;
                 float ll = 0.f, lz = 0.f;
 #pragma unroll
                 for (int i = 0; i < SMAX; ++i) {
@@ -428,69 +542,44 @@ greedy_tc_kernel(const __grid_constant__ CUtensorMap map_d, Shape sh, GreedyTCAr
                 zst[k * kTileG + r] = zk;
                 cst[k * kTileG + r] = zk * inv;
             }
+            __syncwarp();
 
-            // ---- residual e_{k+1} = x - D_S c: the next A operand, or relres ----
-            const bool last = (k + 1 == s);
-            float cr[SMAX];
-            int pr[SMAX];
-#pragma unroll
-            for (int i = 0; i < SMAX; ++i) {
-                cr[i] = (active && i <= k) ? cst[i * kTileG + r] : 0.f;
-                pr[i] = (active && i <= k) ? pst[i * kTileG + r] : 0;
-            }
-#pragma unroll 1
-            for (int cb = 0; cb < D / 32; ++cb) {
-                float e[32];
-#pragma unroll
-                for (int u8 = 0; u8 < 4; ++u8) {
-                    float f[8];
-                    if (active) load8(xrow + cb * 32 + u8 * 8, f);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) e[u8 * 8 + u] = active ? f[u] : 0.f;
-                }
-                if (active) {
-#pragma unroll
-                    for (int i = 0; i < SMAX; ++i) {
-                        if (i <= k) {
-                            const __half* di = Ag + (size_t)pr[i] * D + cb * 32;
-#pragma unroll
-                            for (int u8 = 0; u8 < 4; ++u8) {
-                                float f[8];
-                                load8(di + u8 * 8, f);
-#pragma unroll
-                                for (int u = 0; u < 8; ++u) e[u8 * 8 + u] = fmaf(-cr[i], f[u], e[u8 * 8 + u]);
-                            }
-                        }
-                    }
-                }
-                if (!last) {
-                    write_a(cb, e);
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) esq = fmaf(e[u], e[u], esq);
-                }
-            }
-            if (!last) tmem_st_wait();
+            // ---- residual e_{k+1} = x - D_S c: the next A operand, or ||e_s||^2 ----
+            residual_pass(k, k + 1 < s);
         }
 
         // ---- outputs (cluster rank 0) ----
-        if (rank == 0 && valid) {
-            const size_t o = (size_t)g * a.V + v;
-            long long* cnt = a.counters + (size_t)g * kCntFields;
-            if (bad) {
-                for (int k = 0; k < s; ++k) {
-                    a.idx[o * s + k] = -1;
-                    a.coef[o * s + k] = 0.f;
+        if (rank == 0) {
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                float e2 = esq[it];
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) e2 += __shfl_xor_sync(0xffffffffu, e2, o);
+                const int R = q * 32 + it * 4 + gs;
+                if (l8 == 0 && R < rows && vstate[R] != 2) {
+                    const float xn2 = vxn2[R];
+                    a.relres[(size_t)g * a.V + a.v0 + (size_t)tile * kTileG + R] =
+                        (xn2 > 0.f) ? sqrtf(e2) / sqrtf(xn2) : 0.f;
                 }
-                a.relres[o] = __int_as_float(0x7fc00000);
-                atomicAdd((unsigned long long*)&cnt[kCntNonfinite], 1ull);
-                atomicOr((unsigned long long*)&cnt[kCntStatus], (unsigned long long)FADKV_DEV_NONFINITE_INPUT);
-            } else {
-                for (int k = 0; k < s; ++k) {
-                    a.idx[o * s + k] = active ? pst[k * kTileG + r] : -1;
-                    a.coef[o * s + k] = active ? cst[k * kTileG + r] : 0.f;
+            }
+            if (r < rows) {
+                const size_t o = (size_t)g * a.V + a.v0 + (size_t)tile * kTileG + r;
+                long long* cnt = a.counters + (size_t)g * kCntFields;
+                const int stt = vstate[r];
+                if (stt == 2) {
+                    for (int k = 0; k < s; ++k) {
+                        a.idx[o * s + k] = -1;
+                        a.coef[o * s + k] = 0.f;
+                    }
+                    a.relres[o] = __int_as_float(0x7fc00000);
+                    atomicAdd((unsigned long long*)&cnt[kCntNonfinite], 1ull);
+                    atomicOr((unsigned long long*)&cnt[kCntStatus], (unsigned long long)FADKV_DEV_NONFINITE_INPUT);
+                } else {
+                    for (int k = 0; k < s; ++k) {
+                        a.idx[o * s + k] = stt == 1 ? pst[k * kTileG + r] : -1;
+                        a.coef[o * s + k] = stt == 1 ? cst[k * kTileG + r] : 0.f;
+                    }
                 }
-                a.relres[o] = (xn2 > 0.f) ? sqrtf(esq) / sqrtf(xn2) : 0.f;
             }
         }
     }

@@ -118,17 +118,17 @@ def test_slow_path_short_and_overflowing_lists():
 
 @pytest.mark.parametrize("name,G,V", [("decode_3b", 3, 200), ("decode_8b", 2, 64)])
 def test_greedy_kernels_agree(monkeypatch, name, G, V):
-    """The greedy kernels all match the oracle: one tcgen05 GEMM per pick over
-    the whole dictionary with a pool-masked argmax (cluster size chosen by
-    the launcher, and forced to 1 and 3), the
-    pool-resident mma.sync kernel (2 or 4 m16 tiles per warp) and the
-    FP32-pipe kernel."""
+    """The greedy kernels all match the oracle: the correlation-domain kernel
+    with an incremental Cholesky factor (default), one tcgen05 GEMM per pick
+    over the whole dictionary with a pool-masked argmax (cluster size chosen
+    by the launcher, and forced to 1 and 3), the residual-based mma.sync
+    kernel (2 or 4 m16 tiles per warp) and the FP32-pipe kernel."""
     from dataclasses import replace
     w = replace(S.WORKLOADS[name], G=G)
     data = S.WorkloadData(w)
     x = data.inputs(0, V)
     outs = {}
-    paths = ("tc", "tc_c1", "tc_c3", "mma", "mma4", "ffma")
+    paths = ("chol", "tc", "tc_c1", "tc_c3", "mma", "mma4", "ffma")
     for path in paths:
         if path == "tc":
             monkeypatch.setenv("FADKV_GREEDY", "tc")
