@@ -75,7 +75,7 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     __shared__ float publ[2][NW][PL];
     __shared__ unsigned long long kred[2][NW];
     __shared__ __align__(16) __half picked[SMAX][D];   // rows of the picks
-    __shared__ float zrec[SMAX], irec[SMAX], crec[SMAX], lrow[SMAX][SMAX + 1];
+    __shared__ float zrec[SMAX], irec[SMAX], lrow[SMAX][SMAX + 1];
     __shared__ int sslot[SMAX];
     __shared__ float fred[NW];
 
@@ -267,18 +267,13 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
 
     const float la = sh.lambda_abs, lr = sh.lambda_rel;
     for (int k = 0; k < s; ++k) {
-        // ---- the pick: best of the warps' bests ----
+        // ---- the pick: best of the warps' bests (lane w reads warp w's key) ----
         const int par = k & 1;
-        unsigned long long win = 0ull;
-        int w_o = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const unsigned long long kv = kred[par][w];
-            if (kv > win) {
-                win = kv;
-                w_o = w;
-            }
-        }
+        const unsigned long long kv = (lane < NW) ? kred[par][lane] : 0ull;
+        const uint32_t khi = (uint32_t)(kv >> 32), klo = (uint32_t)kv;
+        const uint32_t mhi = __reduce_max_sync(0xffffffffu, khi);
+        const uint32_t mlo = __reduce_max_sync(0xffffffffu, khi == mhi ? klo : 0u);
+        const int w_o = __ffs(__ballot_sync(0xffffffffu, lane < NW && khi == mhi && klo == mlo)) - 1;
         const float* pl = publ[par][w_o];
         const float cstar = pl[SMAX], llstar = pl[SMAX + 1], gstar = pl[SMAX + 2];
         const int slot_o = __float_as_int(pl[SMAX + 3]);
@@ -287,7 +282,7 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
             if (tid == 0) atomicOr(status, (unsigned long long)FADKV_DEV_NOT_SPD);
             dk = 1e-30f;
         }
-        const float inv = __frcp_rn(sqrtf(dk));
+        const float inv = rsqrtf(dk);                  // 1 / L_kk
         const float zk = cstar * inv;
         if (live && myslot == slot_o) live = false;
         if (warp == 0) {
@@ -323,25 +318,44 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     // ---- coefficients c = L^-T z, residual and outputs (warp 0) ----
     if (warp != 0) return;
     __syncwarp();
-    if (lane == 0) {
-        for (int k = s - 1; k >= 0; --k) {
-            float acc0 = zrec[k];
-            for (int i = k + 1; i < s; ++i) acc0 = fmaf(-lrow[i][k], crec[i], acc0);
-            crec[k] = acc0 * irec[k];
+    // lane j holds c_j: for k = s-1 .. 0, c_k = acc_k / L_kk, then every
+    // lane j < k removes L[k][j] c_k from its acc_j
+    float accj = (lane < s) ? zrec[lane] : 0.f;
+    const float invj = (lane < s) ? irec[lane] : 0.f;
+    float cj = 0.f;
+#pragma unroll
+    for (int k = SMAX - 1; k >= 0; --k) {
+        if (k < s) {
+            const float ck = __shfl_sync(0xffffffffu, accj * invj, k);
+            if (lane == k) cj = ck;
+            if (lane < k) accj = fmaf(-lrow[k][lane], ck, accj);
         }
     }
-    __syncwarp();
-    float esq = 0.f;
-    for (int t = lane; t < D; t += 32) {
-        float e = xs[t];
-        for (int i = 0; i < s; ++i) e = fmaf(-crec[i], __half2float(picked[i][t]), e);
-        esq = fmaf(e, e, esq);
+    // e = x - D_S c on D/32 consecutive elements per lane
+    constexpr int EPL = D / 32;
+    float e[EPL];
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) e[u] = xs[lane * EPL + u];
+#pragma unroll
+    for (int i = 0; i < SMAX; ++i) {
+        const float ci = __shfl_sync(0xffffffffu, cj, i);
+        if (i < s) {
+#pragma unroll
+            for (int u = 0; u < EPL; u += 2) {
+                const float2 d2 = __half22float2(*reinterpret_cast<const __half2*>(&picked[i][lane * EPL + u]));
+                e[u] = fmaf(-ci, d2.x, e[u]);
+                e[u + 1] = fmaf(-ci, d2.y, e[u + 1]);
+            }
+        }
     }
+    float esq = 0.f;
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) esq = fmaf(e[u], e[u], esq);
     esq = warp_sum(esq);
     if (lane == 0) a.relres[out] = (xnorm2 > 0.f) ? sqrtf(esq) / sqrtf(xnorm2) : 0.f;
-    for (int k = lane; k < s; k += 32) {
-        a.idx[out * s + k] = pid[sslot[k]];
-        a.coef[out * s + k] = crec[k];
+    if (lane < s) {
+        a.idx[out * s + lane] = pid[sslot[lane]];
+        a.coef[out * s + lane] = cj;
     }
 }
 
