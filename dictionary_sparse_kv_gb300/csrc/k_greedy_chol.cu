@@ -24,10 +24,12 @@
 // row (exact products, fp32 sums).
 //
 // One CTA of NW warps per vector; warp w holds pool slots 32w .. 32w+31 as
-// two m16 tiles of A fragments; lane (g8, t4) keeps the Cholesky state of
-// slot t4 of its row group (tile t4>>1, row g8 + 8 (t4&1)).  Each warp ends
-// a step by publishing its best slot (key, l vector, correlation, |l|^2,
-// G_jj and the atom's row), so one barrier per step suffices.
+// two m16 tiles of A fragments (loaded from a copy of the pool's rows in
+// shared memory, which also serves the pick's row as the B column); lane
+// (g8, t4) keeps the Cholesky state of slot t4 of its row group (tile t4>>1,
+// row g8 + 8 (t4&1)).  Each warp ends a step by publishing its best slot
+// (key, l vector, correlation, |l|^2, G_jj), so one barrier per step
+// suffices.
 #include <stdlib.h>
 #include <string.h>
 
@@ -54,6 +56,17 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid)
+{
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+
+// Row stride (binary16 elements) of the pool's copy in shared memory: 16
+// bytes of padding keep the fragment loads free of bank conflicts.
+template <int D>
+constexpr int pool_rs() { return D + 8; }
+
 template <int D, int NW, int SMAX>
 __global__ void __launch_bounds__(NW * 32, NW <= 8 ? 2 : 1)
 greedy_chol_kernel(Shape sh, GreedyArgs a)
@@ -71,10 +84,11 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     __shared__ int pid[NPAD];
     __shared__ __align__(16) __half bx[2 * D];         // first pass: x 2^p split in two binary16 terms
     __shared__ __align__(16) __half zrow[D];           // a zero B column
-    __shared__ __align__(16) __half pub[2][NW][D];     // each warp's best atom row
-    __shared__ float publ[2][NW][PL];
+    __shared__ __align__(16) float publ[2][NW][PL];    // each warp's best: l, corr, |l|^2, G_jj, slot
     __shared__ unsigned long long kred[2][NW];
-    __shared__ __align__(16) __half picked[SMAX][D];   // rows of the picks
+    extern __shared__ __align__(16) unsigned char dsm[];
+    __half* prow = (__half*)dsm;                       // the pool's rows [NPAD][pool_rs<D>()]
+    constexpr int RS = pool_rs<D>();
     __shared__ float zrec[SMAX], irec[SMAX], lrow[SMAX][SMAX + 1];
     __shared__ int sslot[SMAX];
     __shared__ float fred[NW];
@@ -100,6 +114,16 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     if (lane == 0) fred[warp] = xsq;
     for (int i = tid; i < NPAD; i += NT) pid[i] = (i < n) ? a.pool_in[gv * n + i] : -1;
     bad = __syncthreads_or(bad);
+    if (!bad) {
+        // the pool's rows into shared memory (coalesced 16-byte copies)
+        for (int c = tid; c < NPAD * (D / 8); c += NT) {
+            const int row = c / (D / 8), part = c % (D / 8);
+            const int id = pid[row];
+            cp_async16(prow + (size_t)row * RS + 8 * part, Aglob + (size_t)(id >= 0 ? id : 0) * D + 8 * part, id >= 0);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
+    }
     if (bad) {
         for (int k = tid; k < s; k += NT) {
             a.idx[out * s + k] = -1;
@@ -124,13 +148,11 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt) {
         const int s0 = warp * SPW + mt * 16 + g8;
-        const int r0 = pid[s0], r1 = pid[s0 + 8];
         float n0 = 0.f, n1 = 0.f;
 #pragma unroll
         for (int kp = 0; kp < KP; ++kp) {
-            uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
-            if (r0 >= 0) q0 = *reinterpret_cast<const uint4*>(Aglob + (size_t)r0 * D + 32 * kp + 8 * t4);
-            if (r1 >= 0) q1 = *reinterpret_cast<const uint4*>(Aglob + (size_t)r1 * D + 32 * kp + 8 * t4);
+            const uint4 q0 = *reinterpret_cast<const uint4*>(prow + (size_t)s0 * RS + 32 * kp + 8 * t4);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(prow + (size_t)(s0 + 8) * RS + 32 * kp + 8 * t4);
             Af[mt][2 * kp][0] = q0.x;
             Af[mt][2 * kp][2] = q0.y;
             Af[mt][2 * kp + 1][0] = q0.z;
@@ -231,35 +253,15 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
         const bool win = m != 0u && live && key == m && (uint32_t)myatom == amin;
         const unsigned wb = __ballot_sync(0xffffffffu, win);
         if (lane == 0) kred[par][warp] = (m == 0u) ? 0ull : (((unsigned long long)m << 32) | (0xffffffffu - amin));
-        if (wb != 0u) {
-            const int wl = __ffs(wb) - 1;
-            const int mw = wl & 3, mt_w = mw >> 1, h_w = mw & 1;
-            if (g8 == (wl >> 2)) {
-                __half* dst = pub[par][warp];
+        if (wb != 0u && lane == __ffs(wb) - 1) {
+            float* pl = publ[par][warp];
 #pragma unroll
-                for (int mt = 0; mt < kMT; ++mt) {
-                    if (mt == mt_w) {
-#pragma unroll
-                        for (int kp = 0; kp < KP; ++kp) {
-                            const uint32_t w0 = h_w ? Af[mt][2 * kp][1] : Af[mt][2 * kp][0];
-                            const uint32_t w1 = h_w ? Af[mt][2 * kp][3] : Af[mt][2 * kp][2];
-                            const uint32_t w2 = h_w ? Af[mt][2 * kp + 1][1] : Af[mt][2 * kp + 1][0];
-                            const uint32_t w3 = h_w ? Af[mt][2 * kp + 1][3] : Af[mt][2 * kp + 1][2];
-                            *reinterpret_cast<uint4*>(dst + 32 * kp + 8 * t4) = make_uint4(w0, w1, w2, w3);
-                        }
-                    }
-                }
-            }
-            if (lane == wl) {
-                float* pl = publ[par][warp];
-#pragma unroll
-                for (int i = 0; i < SMAX; ++i)
-                    if (i < k) pl[i] = l[i];
-                pl[SMAX] = corr;
-                pl[SMAX + 1] = ll;
-                pl[SMAX + 2] = gjj;
-                pl[SMAX + 3] = __int_as_float(myslot);
-            }
+            for (int i = 0; i < SMAX; ++i)
+                if (i < k) pl[i] = l[i];
+            pl[SMAX] = corr;
+            pl[SMAX + 1] = ll;
+            pl[SMAX + 2] = gjj;
+            pl[SMAX + 3] = __int_as_float(myslot);
         }
     };
     best_publish(0, 0);
@@ -286,25 +288,30 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
         const float zk = cstar * inv;
         if (live && myslot == slot_o) live = false;
         if (warp == 0) {
-            // the factor's row k, z_k and the pick's row for the end
+            // the factor's row k and z_k for the end
             if (lane < k) lrow[k][lane] = pl[lane];
             if (lane == 0) {
                 sslot[k] = slot_o;
                 zrec[k] = zk;
                 irec[k] = inv;
             }
-            for (int t = lane; t < D / 8; t += 32)
-                reinterpret_cast<uint4*>(picked[k])[t] = reinterpret_cast<const uint4*>(pub[par][w_o])[t];
         }
         if (k + 1 == s) break;
 
         // ---- Gram column of the pick; every slot's update ----
-        mma_pass(pub[par][w_o], zrow);
+        mma_pass(prow + (size_t)slot_o * RS, zrow);
         const float gj = to_owner(false);
         float dot = 0.f;
 #pragma unroll
-        for (int i = 0; i < SMAX; ++i)
-            if (i < k) dot = fmaf(pl[i], l[i], dot);
+        for (int i4 = 0; i4 < SMAX; i4 += 4) {
+            if (i4 < k) {
+                const float4 q = *reinterpret_cast<const float4*>(pl + i4);
+                if (i4 + 0 < k) dot = fmaf(q.x, l[i4 + 0], dot);
+                if (i4 + 1 < k) dot = fmaf(q.y, l[i4 + 1], dot);
+                if (i4 + 2 < k) dot = fmaf(q.z, l[i4 + 2], dot);
+                if (i4 + 3 < k) dot = fmaf(q.w, l[i4 + 3], dot);
+            }
+        }
         const float t = (gj - dot) * inv;
 #pragma unroll
         for (int i = 0; i < SMAX; ++i)
@@ -342,7 +349,8 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
         if (i < s) {
 #pragma unroll
             for (int u = 0; u < EPL; u += 2) {
-                const float2 d2 = __half22float2(*reinterpret_cast<const __half2*>(&picked[i][lane * EPL + u]));
+                const float2 d2 = __half22float2(
+                    *reinterpret_cast<const __half2*>(prow + (size_t)sslot[i] * RS + lane * EPL + u));
                 e[u] = fmaf(-ci, d2.x, e[u]);
                 e[u + 1] = fmaf(-ci, d2.y, e[u + 1]);
             }
@@ -362,8 +370,12 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
 template <int D, int NW, int SMAX>
 cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 {
+    const size_t smem = (size_t)NW * kMT * 16 * pool_rs<D>() * 2;
+    auto k = greedy_chol_kernel<D, NW, SMAX>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     dim3 grid(a.Vc, sh.G);
-    greedy_chol_kernel<D, NW, SMAX><<<grid, NW * 32, 0, st>>>(sh, a);
+    k<<<grid, NW * 32, smem, st>>>(sh, a);
     return cudaGetLastError();
 }
 
