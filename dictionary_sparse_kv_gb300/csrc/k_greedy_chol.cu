@@ -62,13 +62,19 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
 }
 
-// Row stride (binary16 elements) of the pool's copy in shared memory: 16
-// bytes of padding keep the fragment loads free of bank conflicts.
-template <int D>
-constexpr int pool_rs() { return D + 8; }
+// The pool's copy in shared memory: row r (D binary16) holds its 16-byte
+// chunk c at position c ^ (r & 7), so the fragment loads of a warp (rows
+// g8 = 0..7, chunks t4 + 4 kp) spread over all banks.
+__device__ __forceinline__ const uint4* prow_chunk(const __half* prow, int D, int r, int c)
+{
+    return reinterpret_cast<const uint4*>(prow + (size_t)r * D + ((c ^ (r & 7)) << 3));
+}
 
-template <int D, int NW, int SMAX>
-__global__ void __launch_bounds__(NW * 32, NW <= 8 ? 2 : 1)
+// RT: m16 tiles per warp whose A fragments stay in registers (2: all; 1:
+// the second tile is read from the shared copy at every pass, which frees
+// the registers for three CTAs per SM).
+template <int D, int NW, int SMAX, int RT>
+__global__ void __launch_bounds__(NW * 32, NW <= 8 ? (RT == 2 ? 2 : 3) : 1)
 greedy_chol_kernel(Shape sh, GreedyArgs a)
 {
     constexpr int KT = D / 16, KP = D / 32, NT = NW * 32;
@@ -83,12 +89,10 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     __shared__ float xs[D];
     __shared__ int pid[NPAD];
     __shared__ __align__(16) __half bx[2 * D];         // first pass: x 2^p split in two binary16 terms
-    __shared__ __align__(16) __half zrow[D];           // a zero B column
     __shared__ __align__(16) float publ[2][NW][PL];    // each warp's best: l, corr, |l|^2, G_jj, slot
     __shared__ unsigned long long kred[2][NW];
     extern __shared__ __align__(16) unsigned char dsm[];
-    __half* prow = (__half*)dsm;                       // the pool's rows [NPAD][pool_rs<D>()]
-    constexpr int RS = pool_rs<D>();
+    __half* prow = (__half*)dsm;                       // the pool's rows [NPAD][D], chunk-swizzled
     __shared__ float zrec[SMAX], irec[SMAX], lrow[SMAX][SMAX + 1];
     __shared__ int sslot[SMAX];
     __shared__ float fred[NW];
@@ -106,7 +110,6 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     for (int t = tid; t < D; t += NT) {
         const float xv = __half2float(X[t]);
         xs[t] = xv;
-        zrow[t] = __float2half_rn(0.f);
         bad |= !isfinite(xv);
         xsq = fmaf(xv, xv, xsq);
     }
@@ -119,7 +122,8 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
         for (int c = tid; c < NPAD * (D / 8); c += NT) {
             const int row = c / (D / 8), part = c % (D / 8);
             const int id = pid[row];
-            cp_async16(prow + (size_t)row * RS + 8 * part, Aglob + (size_t)(id >= 0 ? id : 0) * D + 8 * part, id >= 0);
+            cp_async16(prow + (size_t)row * D + ((part ^ (row & 7)) << 3), Aglob + (size_t)(id >= 0 ? id : 0) * D + 8 * part,
+                       id >= 0);
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();
@@ -143,7 +147,7 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     // Inside each 32-element block of the head dimension, thread t4 of a row
     // holds elements 8 t4 .. 8 t4 + 7 (one 16-byte load): a permutation of the
     // contraction index applied alike to A and B.
-    uint32_t Af[kMT][KT][4];
+    uint32_t Af[RT][KT][4];
     float gjj = 0.f;
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt) {
@@ -151,16 +155,18 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
         float n0 = 0.f, n1 = 0.f;
 #pragma unroll
         for (int kp = 0; kp < KP; ++kp) {
-            const uint4 q0 = *reinterpret_cast<const uint4*>(prow + (size_t)s0 * RS + 32 * kp + 8 * t4);
-            const uint4 q1 = *reinterpret_cast<const uint4*>(prow + (size_t)(s0 + 8) * RS + 32 * kp + 8 * t4);
-            Af[mt][2 * kp][0] = q0.x;
-            Af[mt][2 * kp][2] = q0.y;
-            Af[mt][2 * kp + 1][0] = q0.z;
-            Af[mt][2 * kp + 1][2] = q0.w;
-            Af[mt][2 * kp][1] = q1.x;
-            Af[mt][2 * kp][3] = q1.y;
-            Af[mt][2 * kp + 1][1] = q1.z;
-            Af[mt][2 * kp + 1][3] = q1.w;
+            const uint4 q0 = *prow_chunk(prow, D, s0, 4 * kp + t4);
+            const uint4 q1 = *prow_chunk(prow, D, s0 + 8, 4 * kp + t4);
+            if (mt < RT) {
+                Af[mt < RT ? mt : 0][2 * kp][0] = q0.x;
+                Af[mt < RT ? mt : 0][2 * kp][2] = q0.y;
+                Af[mt < RT ? mt : 0][2 * kp + 1][0] = q0.z;
+                Af[mt < RT ? mt : 0][2 * kp + 1][2] = q0.w;
+                Af[mt < RT ? mt : 0][2 * kp][1] = q1.x;
+                Af[mt < RT ? mt : 0][2 * kp][3] = q1.y;
+                Af[mt < RT ? mt : 0][2 * kp + 1][1] = q1.z;
+                Af[mt < RT ? mt : 0][2 * kp + 1][3] = q1.w;
+            }
             const __half2* h0 = reinterpret_cast<const __half2*>(&q0);
             const __half2* h1 = reinterpret_cast<const __half2*>(&q1);
 #pragma unroll
@@ -194,10 +200,10 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     }
     __syncthreads();
 
-    // pool rows x B (column g8 of this lane from `c0`, `c1` or zero) -> acc
+    // pool rows x B -> acc; B column g8 of this lane: `bcol(kp)` for the
+    // lanes that carry data (g8 < ncols), zero otherwise
     float acc[kMT][4];
-    auto mma_pass = [&](const __half* c0, const __half* c1) {
-        const __half* bsrc = (g8 == 0) ? c0 : ((g8 == 1) ? c1 : zrow);
+    auto mma_pass = [&](auto bcol, int ncols) {
         float part[kMT][2][4];
 #pragma unroll
         for (int mt = 0; mt < kMT; ++mt)
@@ -207,11 +213,21 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
                 for (int r = 0; r < 4; ++r) part[mt][ks][r] = 0.f;
 #pragma unroll
         for (int kp = 0; kp < KP; ++kp) {
-            const uint4 qb = *reinterpret_cast<const uint4*>(bsrc + 32 * kp + 8 * t4);
+            const uint4 qb = (g8 < ncols) ? bcol(kp) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int mt = 0; mt < kMT; ++mt) {
-                hmma(part[mt][kp & 1], Af[mt][2 * kp], qb.x, qb.y);
-                hmma(part[mt][kp & 1], Af[mt][2 * kp + 1], qb.z, qb.w);
+                if (mt < RT) {
+                    hmma(part[mt][kp & 1], Af[mt < RT ? mt : 0][2 * kp], qb.x, qb.y);
+                    hmma(part[mt][kp & 1], Af[mt < RT ? mt : 0][2 * kp + 1], qb.z, qb.w);
+                } else {
+                    const int s0 = warp * SPW + mt * 16 + g8;
+                    const uint4 q0 = *prow_chunk(prow, D, s0, 4 * kp + t4);
+                    const uint4 q1 = *prow_chunk(prow, D, s0 + 8, 4 * kp + t4);
+                    const uint32_t f0[4] = {q0.x, q1.x, q0.y, q1.y};
+                    const uint32_t f1[4] = {q0.z, q1.z, q0.w, q1.w};
+                    hmma(part[mt][kp & 1], f0, qb.x, qb.y);
+                    hmma(part[mt][kp & 1], f1, qb.z, qb.w);
+                }
             }
         }
 #pragma unroll
@@ -237,7 +253,7 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     };
 
     // ---- first pass: r_j for the pool ----
-    mma_pass(bx, bx + D);
+    mma_pass([&](int kp) { return *reinterpret_cast<const uint4*>(bx + g8 * D + 32 * kp + 8 * t4); }, 2);
     float corr = to_owner(true) * inv_scale;
     float ll = 0.f;
     float l[SMAX];
@@ -299,7 +315,7 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
         if (k + 1 == s) break;
 
         // ---- Gram column of the pick; every slot's update ----
-        mma_pass(prow + (size_t)slot_o * RS, zrow);
+        mma_pass([&](int kp) { return *prow_chunk(prow, D, slot_o, 4 * kp + t4); }, 1);
         const float gj = to_owner(false);
         float dot = 0.f;
 #pragma unroll
@@ -349,8 +365,9 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
         if (i < s) {
 #pragma unroll
             for (int u = 0; u < EPL; u += 2) {
-                const float2 d2 = __half22float2(
-                    *reinterpret_cast<const __half2*>(prow + (size_t)sslot[i] * RS + lane * EPL + u));
+                const int r = sslot[i], e0 = lane * EPL + u;
+                const float2 d2 = __half22float2(*reinterpret_cast<const __half2*>(
+                    reinterpret_cast<const __half*>(prow_chunk(prow, D, r, e0 >> 3)) + (e0 & 7)));
                 e[u] = fmaf(-ci, d2.x, e[u]);
                 e[u + 1] = fmaf(-ci, d2.y, e[u + 1]);
             }
@@ -367,16 +384,31 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     }
 }
 
-template <int D, int NW, int SMAX>
-cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+// Both tiles in registers (two CTAs per SM) by default: measured faster on
+// decode shapes than FADKV_CHOL_RT=1 (three CTAs per SM, second tile read
+// from shared memory at every pass).
+int resident_tiles()
 {
-    const size_t smem = (size_t)NW * kMT * 16 * pool_rs<D>() * 2;
-    auto k = greedy_chol_kernel<D, NW, SMAX>;
+    const char* f = getenv("FADKV_CHOL_RT");
+    return (f && strcmp(f, "1") == 0) ? 1 : 2;
+}
+
+template <int D, int NW, int SMAX, int RT>
+cudaError_t launch_rt(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+{
+    const size_t smem = (size_t)NW * kMT * 16 * D * 2;
+    auto k = greedy_chol_kernel<D, NW, SMAX, RT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Vc, sh.G);
     k<<<grid, NW * 32, smem, st>>>(sh, a);
     return cudaGetLastError();
+}
+
+template <int D, int NW, int SMAX>
+cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
+{
+    return resident_tiles() == 2 ? launch_rt<D, NW, SMAX, 2>(sh, a, st) : launch_rt<D, NW, SMAX, 1>(sh, a, st);
 }
 
 template <int D, int NW>
