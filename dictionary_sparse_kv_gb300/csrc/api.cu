@@ -51,7 +51,7 @@ struct Layout {
     bool tc;     // screening on tensor cores with candidate filtering
     int chunk;   // vectors per dictionary per encode pass
     int cap;     // candidate capacity per vector
-    size_t counters, scores, cand, cand_count, pool, inactive, flagged, total;
+    size_t counters, scores, cand, cand_count, pool, inactive, flagged, slow, total;
 };
 
 Layout make_layout(const fadkv_params& p)
@@ -74,16 +74,19 @@ Layout make_layout(const fadkv_params& p)
     L.pool = o;       o = align_up(o + (L.tc ? G * chunk * (size_t)p.n * sizeof(int32_t) : 0), kAlign);
     L.inactive = o;   o = align_up(o + G * (size_t)p.N * sizeof(int32_t), kAlign);
     L.flagged = o;    o = align_up(o + G * mb * sizeof(int32_t), kAlign);
+    L.slow = o;       o = align_up(o + sizeof(uint32_t), kAlign);
     L.total = o;
     return L;
 }
 
-// alpha with P(|Z| >= alpha) = min(1, 2n/N) for a standard normal Z, by
+// alpha with P(|Z| >= alpha) = min(1, 1.5n/N) for a standard normal Z, by
 // bisection on erfc: an atom uncorrelated with x has |<d, x>| ~ ||x||/sqrt(d)
-// |Z|, so tau = alpha ||x|| / sqrt(d) keeps about 2n candidates per vector.
+// |Z|, so tau = alpha ||x|| / sqrt(d) keeps about 1.5n candidates per vector
+// (the count sits several standard deviations above n; a list that ends
+// short is redone exactly).
 float screen_alpha(int n, int N)
 {
-    double f = 2.0 * n / (double)N;
+    double f = 1.5 * n / (double)N;
     if (f >= 1.0) return 0.f;
     double lo = 0.0, hi = 40.0;
     for (int i = 0; i < 200; ++i) {
@@ -144,6 +147,7 @@ struct fadkv_dict_s {
     bool pending;      // an encode batch waits for its adapt
     int32_t pending_V;
     int sms;           // multiprocessors of the device (queried at first use)
+    uint32_t seq;      // screening passes issued (the slow-path flag names the pass)
     float alpha;       // screening threshold factor
     // tracing
     bool prof_on;
@@ -237,6 +241,9 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
         sa.cand = cand_buf(h);
         sa.cand_count = cand_count_buf(h);
         sa.pool = (int32_t*)(h->ws + h->L.pool);
+        if (++h->seq == 0) h->seq = 1;                 // 0 is the workspace's initial value
+        sa.slow_seq = (uint32_t*)(h->ws + h->L.slow);
+        sa.seq = h->seq;
         return traced(h, FADKV_K_TOPN, st, [&] { return launch_select(sa, st); });
     }
     float* scores = dump ? dump : (float*)(h->ws + h->L.scores);
@@ -343,6 +350,7 @@ fadkv_status fadkv_dict_create(const fadkv_params* p, void* atoms, int32_t* usag
     h->pending = false;
     h->pending_V = 0;
     h->sms = 0;
+    h->seq = 0;
     h->alpha = screen_alpha(p->n, p->N);
     h->prof_on = false;
     for (int i = 0; i < FADKV_PROFILE_KERNELS; ++i) {
@@ -423,7 +431,8 @@ fadkv_status fadkv_encode(fadkv_dict h, const void* x, int32_t V, int32_t* idx, 
         if (e == cudaSuccess && gp != GreedyPath::kClassic) {
             int32_t* pool = (int32_t*)(h->ws + h->L.pool);
             GreedyArgs fa = greedy_args(h, x, V, v0, Vc);
-            e = traced(h, FADKV_K_TOPN, st, [&] { return launch_pool_fixup(h->sh, fa, pool, h->sms, st); });
+            e = traced(h, FADKV_K_TOPN, st, [&] { return launch_pool_fixup(h->sh, fa, pool, (const uint32_t*)(h->ws + h->L.slow), h->seq, h->sms, st);
+            });
             if (e == cudaSuccess && gp == GreedyPath::kChol) {
                 GreedyArgs ca = greedy_args(h, x, V, v0, Vc);
                 ca.idx = idx;

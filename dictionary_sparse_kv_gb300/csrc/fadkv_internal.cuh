@@ -51,7 +51,7 @@ template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return
 // ---------------------------------------------------------------------------
 
 // Candidate capacity per vector: four times the pool size (the screening
-// threshold aims at about 2n candidates).  The list is split into
+// threshold aims at about 1.5n candidates).  The list is split into
 // 2 * slices regions (one per atom slice and accumulator buffer of the
 // screening kernel), each with its own count in cand_count[.][kCountSlots].
 __host__ __device__ inline int cand_cap(int n) { return 4 * n; }
@@ -97,6 +97,8 @@ struct SelectArgs {
     unsigned long long* cand; // [G][Vc][cap]
     int* cand_count;          // [G][Vc][kCountSlots]; reset to 0 once consumed
     int32_t* pool;            // [G][Vc][n]
+    uint32_t* slow_seq;       // set to `seq` when some vector of the pass needs the slow path
+    uint32_t seq;             // number of this screening pass (never 0)
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 size_t select_smem_bytes(int cap);
@@ -154,7 +156,8 @@ cudaError_t launch_greedy_chol(const Shape& sh, const GreedyArgs& a, cudaStream_
 
 // Exact pool of the vectors the selection kernel left to the slow path
 // (pool[0] == -2): all N scores on the FP32 pipe, exact Top-n.
-cudaError_t launch_pool_fixup(const Shape& sh, const GreedyArgs& a, int32_t* pool, int sms, cudaStream_t st);
+cudaError_t launch_pool_fixup(const Shape& sh, const GreedyArgs& a, int32_t* pool, const uint32_t* slow_seq,
+                              uint32_t seq, int sms, cudaStream_t st);
 
 // Fixed-size adaptation, one CTA per dictionary.
 struct AdaptArgs {

@@ -623,8 +623,9 @@ constexpr int kFixThreads = 256;
 
 template <int D>
 __global__ void __launch_bounds__(kFixThreads)
-pool_fixup_kernel(Shape sh, GreedyArgs a, int32_t* pool)
+pool_fixup_kernel(Shape sh, GreedyArgs a, int32_t* pool, const uint32_t* slow_seq, uint32_t seq)
 {
+    if (*slow_seq != seq) return;                      // no vector of this pass was flagged
     const FixupLayout<D> L = fixup_layout<D>(sh.N, sh.n, kFixThreads / 32);
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned long long* keys = (unsigned long long*)(smem + L.keys);
@@ -751,7 +752,8 @@ int choose_cluster(const Shape& sh, int tiles, int sms)
 }
 
 template <int D>
-cudaError_t launch_fixup_t(const Shape& sh, const GreedyArgs& a, int32_t* pool, int sms, cudaStream_t st)
+cudaError_t launch_fixup_t(const Shape& sh, const GreedyArgs& a, int32_t* pool, const uint32_t* slow_seq,
+                           uint32_t seq, int sms, cudaStream_t st)
 {
     const size_t smem = fixup_layout<D>(sh.N, sh.n, kFixThreads / 32).total;
     auto k = pool_fixup_kernel<D>;
@@ -761,7 +763,7 @@ cudaError_t launch_fixup_t(const Shape& sh, const GreedyArgs& a, int32_t* pool, 
     const long long blocks = (total + kFixThreads - 1) / kFixThreads;
     const long long want = 2LL * sms;
     const unsigned grid = (unsigned)(blocks < want ? blocks : want);
-    k<<<grid, kFixThreads, smem, st>>>(sh, a, pool);
+    k<<<grid, kFixThreads, smem, st>>>(sh, a, pool, slow_seq, seq);
     return cudaGetLastError();
 }
 
@@ -786,10 +788,12 @@ cudaError_t launch_greedy_tc(const Shape& sh, const GreedyTCArgs& a, int sms, cu
     return sh.s <= 8 ? launch_tc<64, 8>(sh, a, C, st) : launch_tc<64, 16>(sh, a, C, st);
 }
 
-cudaError_t launch_pool_fixup(const Shape& sh, const GreedyArgs& a, int32_t* pool, int sms, cudaStream_t st)
+cudaError_t launch_pool_fixup(const Shape& sh, const GreedyArgs& a, int32_t* pool, const uint32_t* slow_seq,
+                              uint32_t seq, int sms, cudaStream_t st)
 {
     if (a.Vc <= 0) return cudaSuccess;
-    return sh.d == 128 ? launch_fixup_t<128>(sh, a, pool, sms, st) : launch_fixup_t<64>(sh, a, pool, sms, st);
+    return sh.d == 128 ? launch_fixup_t<128>(sh, a, pool, slow_seq, seq, sms, st)
+                       : launch_fixup_t<64>(sh, a, pool, slow_seq, seq, sms, st);
 }
 
 }  // namespace fadkv

@@ -17,7 +17,7 @@
 // appends are plain stores, with no atomics and nothing to wait for; the
 // exact Top-n (ties to the lower index) is taken from the regions by the
 // consumer.  tau_v = alpha * ||x_v|| / sqrt(d), with alpha set on the host so
-// that an atom uncorrelated with x_v passes with probability ~2n/N; lists
+// that an atom uncorrelated with x_v passes with probability ~1.5n/N; lists
 // that end shorter than n or overflow a region are redone exactly by the
 // consumer.
 //

@@ -59,7 +59,10 @@ select_kernel(SelectArgs a)
         counts[lane] = 0;                              // consumed: ready for the next call
     }
     if (over || K < n) {
-        if (lane == 0) pool[0] = -2;                   // exact slow path in the greedy kernel
+        if (lane == 0) {
+            pool[0] = -2;                              // exact slow path (pool fixup, or the greedy kernel)
+            *a.slow_seq = a.seq;                       // every writer stores the same value
+        }
         return;
     }
     __syncwarp();
