@@ -200,10 +200,12 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     }
     __syncthreads();
 
-    // pool rows x B -> acc; B column g8 of this lane: `bcol(kp)` for the
-    // lanes that carry data (g8 < ncols), zero otherwise
+    // pool rows x B -> acc.  B column n of this lane (n = g8): `beven(kp)`
+    // for even n, `bodd(kp)` for odd n.  With the same data in columns 0, 2,
+    // 4, 6 (and 1, 3, 5, 7), lane (g8, t4) finds its slot's results in its
+    // own accumulators: column 2 t4 (+ 1) of row g8 / g8 + 8 of each tile.
     float acc[kMT][4];
-    auto mma_pass = [&](auto bcol, int ncols) {
+    auto mma_pass = [&](auto beven, auto bodd) {
         float part[kMT][2][4];
 #pragma unroll
         for (int mt = 0; mt < kMT; ++mt)
@@ -213,7 +215,7 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
                 for (int r = 0; r < 4; ++r) part[mt][ks][r] = 0.f;
 #pragma unroll
         for (int kp = 0; kp < KP; ++kp) {
-            const uint4 qb = (g8 < ncols) ? bcol(kp) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 qb = (g8 & 1) ? bodd(kp) : beven(kp);
 #pragma unroll
             for (int mt = 0; mt < kMT; ++mt) {
                 if (mt < RT) {
@@ -235,26 +237,21 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[mt][r] = part[mt][0][r] + part[mt][1][r];
     };
-    // value of column 0 (+ column 1 when `two`) for each of the row group's 4
-    // slots, handed to the lane that owns the slot (lane t4 <- slot t4)
-    auto to_owner = [&](bool two) -> float {
-        float vv[4];
-        vv[0] = two ? acc[0][0] + acc[0][1] : acc[0][0];
-        vv[1] = two ? acc[0][2] + acc[0][3] : acc[0][2];
-        vv[2] = two ? acc[1][0] + acc[1][1] : acc[1][0];
-        vv[3] = two ? acc[1][2] + acc[1][3] : acc[1][2];
-        float mine = 0.f;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float t = __shfl_sync(0xffffffffu, vv[m], lane & ~3);
-            if (t4 == m) mine = t;
-        }
-        return mine;
+    // this lane's slot (t4: tile t4 >> 1, row g8 + 8 (t4 & 1)): even column,
+    // plus the odd one when `two`
+    auto mine = [&](bool two) -> float {
+        const int h = t4 & 1;
+        const float* am = (t4 >> 1) ? acc[1] : acc[0];
+        const float e = h ? am[2] : am[0];
+        const float o = h ? am[3] : am[1];
+        return two ? e + o : e;
     };
+    const auto zero16 = [](int) { return make_uint4(0u, 0u, 0u, 0u); };
 
     // ---- first pass: r_j for the pool ----
-    mma_pass([&](int kp) { return *reinterpret_cast<const uint4*>(bx + g8 * D + 32 * kp + 8 * t4); }, 2);
-    float corr = to_owner(true) * inv_scale;
+    mma_pass([&](int kp) { return *reinterpret_cast<const uint4*>(bx + 32 * kp + 8 * t4); },
+             [&](int kp) { return *reinterpret_cast<const uint4*>(bx + D + 32 * kp + 8 * t4); });
+    float corr = mine(true) * inv_scale;
     float ll = 0.f;
     float l[SMAX];
 #pragma unroll
@@ -293,8 +290,9 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
         const uint32_t mlo = __reduce_max_sync(0xffffffffu, khi == mhi ? klo : 0u);
         const int w_o = __ffs(__ballot_sync(0xffffffffu, lane < NW && khi == mhi && klo == mlo)) - 1;
         const float* pl = publ[par][w_o];
-        const float cstar = pl[SMAX], llstar = pl[SMAX + 1], gstar = pl[SMAX + 2];
-        const int slot_o = __float_as_int(pl[SMAX + 3]);
+        const float4 pq = *reinterpret_cast<const float4*>(pl + SMAX);
+        const float cstar = pq.x, llstar = pq.y, gstar = pq.z;
+        const int slot_o = __float_as_int(pq.w);
         float dk = fmaf(gstar, lr, gstar) + la - llstar;
         if (!(dk > 0.f)) {
             if (tid == 0) atomicOr(status, (unsigned long long)FADKV_DEV_NOT_SPD);
@@ -315,8 +313,8 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
         if (k + 1 == s) break;
 
         // ---- Gram column of the pick; every slot's update ----
-        mma_pass([&](int kp) { return *prow_chunk(prow, D, slot_o, 4 * kp + t4); }, 1);
-        const float gj = to_owner(false);
+        mma_pass([&](int kp) { return *prow_chunk(prow, D, slot_o, 4 * kp + t4); }, zero16);
+        const float gj = mine(false);
         float dot = 0.f;
 #pragma unroll
         for (int i4 = 0; i4 < SMAX; i4 += 4) {
