@@ -61,7 +61,10 @@ Layout make_layout(const fadkv_params& p)
     L.cap = cand_cap(p.n);
     const size_t G = (size_t)p.num_dicts;
     const size_t mb = (size_t)(p.max_batch > 0 ? p.max_batch : 1);
-    size_t chunk = L.tc ? kCandBudget / (G * (size_t)L.cap * 8) : kScoreBudget / (G * (size_t)p.N * sizeof(float));
+    // candidate bytes per vector: the FP32 path's lists, or the tensor-core
+    // path's screening records (kRecBytes per 128 atoms)
+    const size_t cand_bytes = L.tc ? (size_t)(p.N / 128) * kRecBytes : (size_t)L.cap * 8;
+    size_t chunk = L.tc ? kCandBudget / (G * cand_bytes) : kScoreBudget / (G * (size_t)p.N * sizeof(float));
     if (chunk >= mb) chunk = mb;
     else if (chunk >= 256) chunk = chunk / 128 * 128;   // whole MMA tiles
     if (chunk < 1) chunk = 1;
@@ -69,7 +72,7 @@ Layout make_layout(const fadkv_params& p)
     size_t o = 0;
     L.counters = o;   o = align_up(o + G * kCntFields * sizeof(long long), kAlign);
     L.scores = o;     o = align_up(o + (L.tc ? 0 : G * chunk * (size_t)p.N * sizeof(float)), kAlign);
-    L.cand = o;       o = align_up(o + G * chunk * (size_t)L.cap * 8, kAlign);
+    L.cand = o;       o = align_up(o + G * chunk * cand_bytes, kAlign);
     L.cand_count = o; o = align_up(o + G * chunk * kCountSlots * sizeof(int), kAlign);
     L.pool = o;       o = align_up(o + (L.tc ? G * chunk * (size_t)p.n * sizeof(int32_t) : 0), kAlign);
     L.inactive = o;   o = align_up(o + G * (size_t)p.N * sizeof(int32_t), kAlign);
@@ -149,6 +152,7 @@ struct fadkv_dict_s {
     int sms;           // multiprocessors of the device (queried at first use)
     uint32_t seq;      // screening passes issued (the slow-path flag names the pass)
     float alpha;       // screening threshold factor
+    ScreenTCCache tc_cache;   // tensor maps of the screening kernel
     // tracing
     bool prof_on;
     int64_t launches[FADKV_PROFILE_KERNELS];
@@ -211,7 +215,6 @@ int* cand_count_buf(fadkv_dict h) { return (int*)(h->ws + h->L.cand_count); }
 // Screening of vectors [v0, v0+Vc) of every dictionary: candidate lists
 // (tensor-core path) or the exact Top-n keys (FP32 path).  With `dump` set,
 // writes all scores [G][Vc][N] instead (test hook).
-int slices_for(fadkv_dict h, int Vc) { return h->L.tc ? screen_tc_slices(h->sh, Vc, h->sms) : 1; }
 
 cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, float* dump, cudaStream_t st)
 {
@@ -219,27 +222,25 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
     if (e != cudaSuccess) return e;
     if (h->L.tc) {
         ScreenTCArgs a;
+        a.G = h->p.num_dicts;
         a.N = h->p.N;
         a.V = V;
         a.v0 = v0;
         a.Vc = Vc;
-        a.slices = slices_for(h, Vc);
+        a.x = x;
         a.alpha = h->alpha;
-        a.cap = h->L.cap;
-        a.cand = cand_buf(h);
-        a.cand_count = cand_count_buf(h);
+        a.rec = h->ws + h->L.cand;
         a.dump = dump;
         a.counters = counters(h);
-        e = traced(h, FADKV_K_SCREEN, st, [&] { return launch_screen_tc(h->sh, h->atoms, x, V, a, h->sms, st); });
+        e = traced(h, FADKV_K_SCREEN, st, [&] { return launch_screen_tc(h->sh, h->atoms, a, h->sms, &h->tc_cache, st); });
         if (e != cudaSuccess || dump) return e;
         SelectArgs sa;
         sa.G = h->p.num_dicts;
         sa.Vc = Vc;
+        sa.N = h->p.N;
         sa.n = h->p.n;
         sa.cap = h->L.cap;
-        sa.slices = a.slices;
-        sa.cand = cand_buf(h);
-        sa.cand_count = cand_count_buf(h);
+        sa.rec = h->ws + h->L.cand;
         sa.pool = (int32_t*)(h->ws + h->L.pool);
         if (++h->seq == 0) h->seq = 1;                 // 0 is the workspace's initial value
         sa.slow_seq = (uint32_t*)(h->ws + h->L.slow);
@@ -279,7 +280,6 @@ GreedyArgs greedy_args(fadkv_dict h, const void* x, int32_t V, int v0, int Vc)
     a.cand = cand_buf(h);
     a.cand_count = cand_count_buf(h);
     a.cap = h->L.cap;
-    a.slices = slices_for(h, Vc);
     a.pool_in = h->L.tc ? (const int32_t*)(h->ws + h->L.pool) : nullptr;
     a.idx = nullptr;
     a.coef = nullptr;

@@ -51,12 +51,23 @@ template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return
 // ---------------------------------------------------------------------------
 
 // Candidate capacity per vector: four times the pool size (the screening
-// threshold aims at about 1.5n candidates).  The list is split into
-// 2 * slices regions (one per atom slice and accumulator buffer of the
-// screening kernel), each with its own count in cand_count[.][kCountSlots].
+// threshold aims at about 1.5n candidates).  On the FP32 path a vector's list
+// is made of up to kCountSlots regions, each described by one slot word in
+// cand_count[.][kCountSlots]:
+//   bit 31      the region overflowed (the consumer redoes the vector exactly)
+//   bits 30..16 offset of the region in the vector's list (entries)
+//   bits 15..0  keys in the region
+// A zero word is an empty slot; consumers reset every word to zero.
 __host__ __device__ inline int cand_cap(int n) { return 4 * n; }
-constexpr int kMaxSlices = 16;
-constexpr int kCountSlots = 2 * kMaxSlices;
+constexpr int kCountSlots = 32;
+constexpr uint32_t kSlotOverflow = 0x80000000u;
+__host__ __device__ inline uint32_t slot_word(bool over, int offset, int count)
+{
+    return (over ? kSlotOverflow : 0u) | ((uint32_t)offset << 16) | (uint32_t)(count > 0xffff ? 0xffff : count);
+}
+__host__ __device__ inline int slot_count(uint32_t w) { return (int)(w & 0xffffu); }
+__host__ __device__ inline int slot_offset(uint32_t w) { return (int)((w >> 16) & 0x7fffu); }
+__host__ __device__ inline bool slot_over(uint32_t w) { return (w & kSlotOverflow) != 0u; }
 
 // Candidate keys: (bits(|r_j|) << 32) | (0xffffffff - j).  The larger key is
 // the larger |r|, then the lower atom index: the Top-n pool is the n largest
@@ -68,34 +79,58 @@ cudaError_t launch_screen_ffma(const Shape& sh, const void* atoms, const void* x
                                int v0, int Vc, float* scores, cudaStream_t st);
 
 // Exact Top-n of materialised scores: writes the n pool keys of every vector
-// to region 0 of its candidate list (one slice: regions of cap/2 entries)
-// with count n (0 for non-finite scores).
+// to the start of its candidate list, slot 0 = n keys at offset 0 (0 keys for
+// non-finite scores).
 cudaError_t launch_topn_radix(const Shape& sh, const float* scores, int Vc, unsigned long long* cand,
                               int* cand_count, int cap, cudaStream_t st);
 
 // Tensor-core screening with the fused |r| >= tau filter (binary16 only).
+// One CTA per SM; CTA b takes units [b*T/B, (b+1)*T/B) of the T = G * tiles *
+// (N/128) (dictionary, 128-vector tile, 128-atom chunk) units, chunk fastest.
+//
+// Output: per vector and 128-atom chunk c, one record of kRecBytes at
+// rec + ((g * Vc + v) * (N/128) + c) * kRecBytes, in 8-byte entries:
+//   entry 0     header: low word = overflow << 31 | count
+//   entries 1.. count candidate keys (0xffffffff - j) | (bits(r_j) << 32), in
+//               atom order (the high word keeps the sign of r_j)
+// A record with more than kRecKeys keys is flagged: the consumer redoes the
+// vector exactly.
+constexpr int kRecEntries = 32;
+constexpr int kRecBytes = kRecEntries * 8;
+constexpr int kRecKeys = kRecEntries - 1;
+__host__ __device__ inline uint32_t rec_header(bool over, int count)
+{
+    return (over ? 0x80000000u : 0u) | (uint32_t)count;
+}
 struct ScreenTCArgs {
-    int N, V, v0, Vc;         // V: vectors per dictionary of the whole call
-    int slices;               // atom slices per dictionary (grid = tiles*slices x G)
+    int G, N, V, v0, Vc;      // V: vectors per dictionary of the whole call
+    const void* x;            // [G][V][d] binary16 (read for ||x||)
     float alpha;              // tau = alpha * ||x|| / sqrt(d)
-    int cap;                  // candidate capacity per vector
-    unsigned long long* cand; // [G][Vc][cap], region r at [r * cap/(2*slices), ...)
-    int* cand_count;          // [G][Vc][kCountSlots], region counts
+    unsigned char* rec;       // [G][Vc][N/128] records of kRecBytes
     float* dump;              // test hook: if set, write all scores [G][Vc][N] instead
     long long* counters;      // [G][kCntFields] (status word)
 };
+// Host-side state a handle keeps between launches: the encoded tensor map of
+// the dictionaries (by base address and row count) and whether the kernel's
+// shared-memory limit was raised.
+struct ScreenTCCache {
+    alignas(64) unsigned char map_d[128];
+    const void* d_base = nullptr;
+    long long d_rows = -1;
+    bool attr_done[2] = {false, false};
+};
 bool screen_tc_supported(const Shape& sh);
-int screen_tc_slices(const Shape& sh, int Vc, int sms);
-cudaError_t launch_screen_tc(const Shape& sh, const void* atoms, const void* x, int V, const ScreenTCArgs& a,
-                             int sms, cudaStream_t st);
+int screen_tc_grid(const Shape& sh, int Vc, int sms);
+cudaError_t launch_screen_tc(const Shape& sh, const void* atoms, const ScreenTCArgs& a, int sms, ScreenTCCache* cache,
+                             cudaStream_t st);
 
-// Exact Top-n pool from the candidate lists, one warp per vector; pool
-// [G][Vc][n] atom ids, pool[0] = -2 where the greedy kernel must take the
-// exact slow path (list overflowed or shorter than n).
+// Exact Top-n pool from the screening records, one warp per vector; pool
+// [G][Vc][n] atom ids, pool[0] = -2 where the exact slow path must redo the
+// vector (a record overflowed or was clipped, fewer than n candidates, or
+// more than cap).
 struct SelectArgs {
-    int G, Vc, n, cap, slices;
-    unsigned long long* cand; // [G][Vc][cap]
-    int* cand_count;          // [G][Vc][kCountSlots]; reset to 0 once consumed
+    int G, Vc, N, n, cap;     // cap: the most candidates taken (else the slow path)
+    const unsigned char* rec; // [G][Vc][N/128] screening records
     int32_t* pool;            // [G][Vc][n]
     uint32_t* slow_seq;       // set to `seq` when some vector of the pass needs the slow path
     uint32_t seq;             // number of this screening pass (never 0)
@@ -111,9 +146,8 @@ struct GreedyArgs {
     const void* atoms;
     const void* x;
     unsigned long long* cand; // [G][Vc][cap]
-    int* cand_count;          // [G][Vc][kCountSlots]; reset to 0 once consumed
+    int* cand_count;          // [G][Vc][kCountSlots] slot words; reset to 0 once consumed
     int cap;
-    int slices;               // regions used: 2 * slices
     int32_t* idx;
     float* coef;
     float* relres;

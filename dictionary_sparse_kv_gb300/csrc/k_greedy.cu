@@ -69,7 +69,7 @@ __host__ __device__ inline GreedyLayout greedy_layout(int n, int d, int elem, in
     L.sslot = o; o += sizeof(int) * kMaxS;
     L.hist = o;  o += sizeof(uint32_t) * 256;
     L.scan = o;  o += sizeof(uint32_t) * kWarps;
-    L.misc = o;  o += sizeof(uint32_t) * (4 + kCountSlots);
+    L.misc = o;  o += sizeof(uint32_t) * (4 + 2 * kCountSlots);
     L.total = align_up(o, 16);
     return L;
 }

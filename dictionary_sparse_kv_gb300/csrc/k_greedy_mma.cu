@@ -76,7 +76,7 @@ __host__ __device__ inline MmaLayout<D> mma_layout(int n_pad, int N, int cap, in
     L.sslot = o; o += 4 * kMaxS;
     L.hist = o;  o += 4 * 256;
     L.scan = o;  o += 4 * nw;
-    L.misc = o;  o += 4 * (4 + kCountSlots);
+    L.misc = o;  o += 4 * (4 + 2 * kCountSlots);
     L.total = al(o, 16);
     return L;
 }

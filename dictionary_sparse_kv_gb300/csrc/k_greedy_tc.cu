@@ -612,7 +612,7 @@ __host__ __device__ inline FixupLayout<D> fixup_layout(int N, int n, int nw)
     L.mag = o;  o += 4 * (size_t)n;
     L.hist = o; o += 4 * 256;
     L.scan = o; o += 4 * (size_t)nw;
-    L.misc = o; o += 4 * (4 + kCountSlots);
+    L.misc = o; o += 4 * (4 + 2 * kCountSlots);
     o = (o + 7) & ~(size_t)7;
     L.pref = o; o += 8;
     L.total = o;
@@ -634,21 +634,23 @@ pool_fixup_kernel(Shape sh, GreedyArgs a, int32_t* pool, const uint32_t* slow_se
     float* mag = (float*)(smem + L.mag);
     sel::Scratch sc{(uint32_t*)(smem + L.hist), (uint32_t*)(smem + L.scan), (uint32_t*)(smem + L.misc),
                     (unsigned long long*)(smem + L.pref)};
-    __shared__ int flagged[kFixThreads];
+    __shared__ long long flagged[kFixThreads];
     __shared__ int nflagged;
     const int n = sh.n, N = sh.N;
     const long long total = (long long)sh.G * a.Vc;
-    for (long long base = (long long)blockIdx.x * kFixThreads; base < total;
-         base += (long long)gridDim.x * kFixThreads) {
-      // the flags of kFixThreads vectors at once, then the flagged ones in turn
+    // vector gv belongs to CTA gv mod gridDim: flagged vectors, which come in
+    // runs of neighbours, spread over the CTAs.  The flags of a CTA's next
+    // kFixThreads vectors are read at once, then the flagged ones in turn.
+    const long long stride = (long long)gridDim.x * kFixThreads;
+    for (long long base = blockIdx.x; base < total; base += stride) {
       if (threadIdx.x == 0) nflagged = 0;
       __syncthreads();
-      const long long mine = base + threadIdx.x;
-      if (mine < total && pool[mine * n] == -2) flagged[atomicAdd(&nflagged, 1)] = (int)threadIdx.x;
+      const long long mine = base + (long long)threadIdx.x * gridDim.x;
+      if (mine < total && pool[mine * n] == -2) flagged[atomicAdd(&nflagged, 1)] = mine;
       __syncthreads();
       const int nf = nflagged;
       for (int f = 0; f < nf; ++f) {
-        const long long gv = base + flagged[f];
+        const long long gv = flagged[f];
         const int g = (int)(gv / a.Vc), vc = (int)(gv % a.Vc);
         const __half* X = (const __half*)a.x + ((size_t)g * a.V + a.v0 + vc) * D;
         int bad = 0;
@@ -760,9 +762,8 @@ cudaError_t launch_fixup_t(const Shape& sh, const GreedyArgs& a, int32_t* pool, 
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long total = (long long)sh.G * a.Vc;
-    const long long blocks = (total + kFixThreads - 1) / kFixThreads;
     const long long want = 2LL * sms;
-    const unsigned grid = (unsigned)(blocks < want ? blocks : want);
+    const unsigned grid = (unsigned)(total < want ? total : want);
     k<<<grid, kFixThreads, smem, st>>>(sh, a, pool, slow_seq, seq);
     return cudaGetLastError();
 }

@@ -4,163 +4,246 @@
 // abstract: screening-based sparse coding correlates each incoming vector
 // with every atom, then a one-shot Top-n selection keeps a small pool.
 //
-// Per CTA: one dictionary g, a tile of 128 vectors (the MMA's M = TMEM
-// lanes) and a slice of the atoms, streamed in chunks of 128 atoms (N = 128
-// TMEM columns).  S[v][j] = sum_t X[v][t] D[j][t] is a K-major x K-major
-// product: A = the vector tile, B = the atom chunk, both binary16 in shared
-// memory with the 128-byte swizzle written by TMA; fp32 accumulation in TMEM,
-// two accumulator buffers so the epilogue of chunk c overlaps the MMAs of
-// chunk c+1.  Scores never reach HBM: the epilogue thread of vector v keeps
-// atom j only if |S[v][j]| >= tau_v and appends the 64-bit key
-// (bits(|S|) << 32) | (0xffffffff - j) to its own region of the vector's
-// candidate list -- one region per (atom slice, accumulator buffer), so
-// appends are plain stores, with no atomics and nothing to wait for; the
-// exact Top-n (ties to the lower index) is taken from the regions by the
-// consumer.  tau_v = alpha * ||x_v|| / sqrt(d), with alpha set on the host so
-// that an atom uncorrelated with x_v passes with probability ~1.5n/N; lists
-// that end shorter than n or overflow a region are redone exactly by the
-// consumer.
+// Work: the (dictionary g, tile of 128 vectors, chunk of 128 atoms) units,
+// chunk fastest, split evenly over one persistent CTA per SM: CTA b takes the
+// contiguous units [b*T/B, (b+1)*T/B), so every SM streams the same number
+// of atom chunks whatever G and the batch are.  A run of units of one
+// (g, tile) is a segment; its vector tile is the MMA's A operand (two
+// buffers, so the next segment's tile loads under the current one).
 //
-// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 issues MMAs
-// (one thread), warp 2 owns the TMEM allocation, warps 4..11 are the
-// epilogue (warp 4+e reads TMEM lanes 32(e%4).. and handles the chunks
-// whose accumulator buffer is e/4).  About 97 KB of shared memory and 256
-// TMEM columns per CTA: two CTAs share an SM.  Every wait is bounded by a
-// wall-clock limit; on expiry the CTA sets FADKV_DEV_TIMEOUT in the status
-// word, drains its own copies and MMAs (bounded), frees TMEM and returns.
+// S[v][j] = sum_t X[v][t] D[j][t] per unit: A = the vector tile (M = 128 TMEM
+// lanes), B = the atom chunk (N = 128 columns), both binary16 K-major with the
+// 128-byte swizzle written by TMA; fp32 accumulation in TMEM, two accumulator
+// buffers.  Scores never reach HBM.  The epilogue thread of vector v keeps
+// atom j if |S[v][j]| >= tau_v, tau_v = alpha * ||x_v|| / sqrt(d) with alpha
+// set on the host so that an atom uncorrelated with x_v passes with
+// probability ~1.5n/N.  Each kept score's key (0xffffffff - j) | (bits << 32)
+// is appended to the vector's record of the unit in shared memory: one
+// predicated 8-byte store per score.  After each unit the warp copies its 32
+// records out with 16-byte loads and stores, sixteen lanes on a record: the
+// candidate output lands as whole sectors.  A row with more than kRecKeys kept scores in a unit makes
+// the consumer redo the vector.
+//
+// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 issues MMAs (one
+// thread), warp 2 owns the TMEM allocation, warps 4..11 are the epilogue
+// (warp 4+e reads TMEM lanes 32(e%4).. and handles the units whose
+// accumulator buffer is e/4).  Every wait is bounded by a wall-clock limit;
+// on expiry the CTA sets FADKV_DEV_TIMEOUT in the status word, drains its own
+// copies and MMAs (bounded), frees TMEM and returns.
 #include "tc_common.cuh"
 
 namespace fadkv {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kTileV = 128;        // vectors per CTA (MMA M)
-constexpr int kChunk = 128;        // atoms per MMA chunk (MMA N)
-constexpr int kStages = 2;         // B (atom chunk) pipeline depth
-constexpr int kTmemCols = 2 * kChunk;
+constexpr int kThreads = 512;
+constexpr int kTileV = 128;        // vectors per tile (MMA M)
+constexpr int kChunk = 128;        // atoms per chunk (MMA N)
+constexpr int kStagesFor(int D) { return D == 64 ? 8 : 4; }   // atom chunk pipeline depth
+constexpr int kTmemCols = 512;     // two accumulator buffers (128 columns each), two vector tiles
+constexpr int kAcol = 2 * kChunk;  // first TMEM column of the vector tiles
+constexpr int kEpiWarps = 8;
+constexpr int kWarpStageEntries = 32 * kRecEntries + 32;  // a warp's 32 records + a guard of 32 entries
+static_assert(kRecEntries >= 32, "a row spills at most 32 entries, into the next record or the guard");
+static_assert(kRecBytes % 16 == 0, "records are copied in 16-byte pieces");
 
 using namespace tc;
 
 // Instruction descriptor: M = 128 vectors, N = 128 atoms.
 constexpr uint32_t kIdesc = idesc_f16(kTileV, kChunk);
 
-__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t acc)
-{
-    mma_ss(dtmem, a, b, kIdesc, acc);
-}
-__device__ __forceinline__ void tc_fence_before() { fence_before(); }
-__device__ __forceinline__ void tc_fence_after() { fence_after(); }
-
 template <int D>
 struct SmemLayout {
+    static constexpr int kStages = kStagesFor(D);
     static constexpr int KH = D / 64;                          // 64-element (128-byte) K halves
     static constexpr int kTileBytes = KH * kChunk * 128;       // one 128-row operand tile
-    static constexpr int a_off = 0;
-    static constexpr int b_off = kTileBytes;
-    static constexpr int bar_off = b_off + kStages * kTileBytes;
-    static constexpr int n_bars = 2 * kStages + 4 + 1;
+    static constexpr int b_off = 0;                            // kStages atom chunks
+    static constexpr int s_off = b_off + kStages * kTileBytes; // the epilogue warps' records
+    static constexpr int bar_off = s_off + kEpiWarps * kWarpStageEntries * 8;
+    static constexpr int n_bars = 2 * kStages + 8;
     static constexpr int taddr_off = bar_off + n_bars * 8;
     static constexpr int total = taddr_off + 16;
     static constexpr int alloc = total + 1024;                 // slack for 1024-byte alignment
 };
 
+// Walks a CTA's units in order without divisions: the unit's chunk c and its
+// (dictionary g, tile); pair = g * tiles + tile.
+struct UnitCursor {
+    int pair, c, g, tile, nch, tiles;
+    __device__ __forceinline__ void init(long long u, int nch_, int tiles_)
+    {
+        nch = nch_;
+        tiles = tiles_;
+        const long long p = u / nch;
+        pair = (int)p;
+        c = (int)(u - p * nch);
+        g = pair / tiles;
+        tile = pair - g * tiles;
+    }
+    __device__ __forceinline__ void advance(int k)
+    {
+        c += k;
+        while (c >= nch) {
+            c -= nch;
+            ++pair;
+            if (++tile == tiles) {
+                tile = 0;
+                ++g;
+            }
+        }
+    }
+};
+
 template <int D, bool kDump>
-__global__ void __launch_bounds__(kThreads, 2)
-screen_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_d,
-                 ScreenTCArgs a)
+__global__ void __launch_bounds__(kThreads, 1)
+screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
 {
     using L = SmemLayout<D>;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sA = sbase + L::a_off, sB = sbase + L::b_off;
+    const uint32_t sB = sbase + L::b_off;
     const uint32_t bar0 = sbase + L::bar_off;
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
-    auto empty_bar = [&](int i) { return bar0 + 8u * (kStages + i); };
-    auto tfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
-    auto tempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 + i); };
-    const uint32_t afull_bar = bar0 + 8u * (2 * kStages + 4);
+    auto empty_bar = [&](int i) { return bar0 + 8u * (L::kStages + i); };
+    auto tfull_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + i); };
+    auto tempty_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + 2 + i); };
+    auto afull_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + 4 + i); };
+    auto aempty_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + 6 + i); };
     uint32_t* taddr_slot = (uint32_t*)(smem + L::taddr_off);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blockIdx.y;
-    const int tile = blockIdx.x / a.slices, slice = blockIdx.x % a.slices;
-    const int nchunks_all = a.N / kChunk;
-    const int cps = (nchunks_all + a.slices - 1) / a.slices;
-    const int c0 = slice * cps;
-    const int nch = max(0, min(cps, nchunks_all - c0));
-    unsigned long long* status = (unsigned long long*)&a.counters[(size_t)g * kCntFields + kCntStatus];
+    const int nch = a.N / kChunk;
+    const int tiles = (a.Vc + kTileV - 1) / kTileV;
+    const long long T = (long long)a.G * tiles * nch;
+    const int B = (int)gridDim.x, b = (int)blockIdx.x;
+    const long long u0 = (long long)b * T / B, u1 = (long long)(b + 1) * T / B;
+    const int nu = (int)(u1 - u0);
+    const int g_first = (int)(u0 / nch / tiles);
+    unsigned long long* status = (unsigned long long*)&a.counters[(size_t)g_first * kCntFields + kCntStatus];
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_d)) : "memory");
+        for (int i = 0; i < L::kStages; ++i) {
             mbar_init(full_bar(i), 1);
             mbar_init(empty_bar(i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(tfull_bar(i), 1);
             mbar_init(tempty_bar(i), 128);
+            mbar_init(afull_bar(i), 128);
+            mbar_init(aempty_bar(i), 1);
         }
-        mbar_init(afull_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 2) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(taddr_slot)),
-                     "r"(kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = *taddr_slot;
-
-    const int row0 = g * a.V + a.v0 + tile * kTileV;   // first row of this tile in x viewed as [G*V][D]
+    // The TMEM allocation is published to the MMA and epilogue warps (and
+    // warp 2) by a named barrier: the producer starts streaming at once.
+    constexpr int kTmemSyncThreads = 32 * (2 + kEpiWarps + 4);
+    uint32_t tbase = 0;
+    if (warp != 0 && warp != 3) {
+        if (warp == 2) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(taddr_slot)),
+                         "r"(kTmemCols));
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        }
+        fence_before();
+        asm volatile("bar.sync 1, %0;" ::"n"(kTmemSyncThreads) : "memory");
+        fence_after();
+        tbase = *taddr_slot;
+    }
     constexpr uint32_t kTileBytes = (uint32_t)L::kTileBytes;
 
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
+        // ---------------- TMA producer (atom chunks) ----------------
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_d)) : "memory");
-            mbar_expect_tx(afull_bar, kTileBytes);
-            for (int h = 0; h < L::KH; ++h) tma_load_2d(sA + h * kChunk * 128, &map_x, h * 64, row0, afull_bar);
             int issued = 0;
             bool ok = true;
-            for (int c = 0; c < nch && ok; ++c) {
-                const int st = c % kStages;
-                const uint32_t ph = (uint32_t)(c / kStages) & 1u;
-                ok = mbar_wait(empty_bar(st), ph ^ 1u, status);
+            UnitCursor uc;
+            uc.init(u0, nch, tiles);
+            for (int i = 0; i < nu && ok; ++i, uc.advance(1)) {
+                const int st = i % L::kStages;
+                ok = mbar_wait(empty_bar(st), ((uint32_t)(i / L::kStages) & 1u) ^ 1u, status);
                 if (!ok) break;
                 mbar_expect_tx(full_bar(st), kTileBytes);
-                const int arow = g * a.N + (c0 + c) * kChunk;
+                const int arow = uc.g * a.N + uc.c * kChunk;
                 for (int h = 0; h < L::KH; ++h)
                     tma_load_2d(sB + st * kTileBytes + h * kChunk * 128, &map_d, h * 64, arow, full_bar(st));
                 ++issued;
             }
             // drain: every issued load must have landed before the CTA exits
-            mbar_wait(afull_bar, 0, status);
-            for (int c = max(0, issued - kStages); c < issued; ++c)
-                mbar_wait(full_bar(c % kStages), (uint32_t)(c / kStages) & 1u, status);
+            for (int i = max(0, issued - L::kStages); i < issued; ++i)
+                mbar_wait(full_bar(i % L::kStages), (uint32_t)(i / L::kStages) & 1u, status);
+        }
+    } else if (warp >= 4 + kEpiWarps) {
+        // ---------------- vector tiles into TMEM ----------------
+        // Warp 12+q writes rows 32q.. of each segment's tile (binary16 pairs,
+        // K-major: column k holds elements 2k, 2k+1) into its TMEM buffer,
+        // the MMAs' A operand; rows past the batch are zeros.
+        const int q = warp - 4 - kEpiWarps;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        int prev = -1, seg = -1;
+        bool ok = true;
+        UnitCursor uc;
+        uc.init(u0, nch, tiles);
+        for (int i = 0; i < nu && ok; ++i, uc.advance(1)) {
+            if (uc.pair == prev) continue;
+            prev = uc.pair;
+            ++seg;
+            const int ab = seg & 1;
+            // the buffer's previous tile (segment seg-2) must be done with
+            if (seg >= 2) ok = mbar_wait(aempty_bar(ab), (uint32_t)((seg >> 1) - 1) & 1u, status);
+            if (!ok) break;
+            fence_after();
+            const int vloc = uc.tile * kTileV + q * 32 + lane;
+            const uint4* xr = reinterpret_cast<const uint4*>((const __half*)a.x +
+                                                             ((size_t)uc.g * a.V + a.v0 + (vloc < a.Vc ? vloc : 0)) * D);
+#pragma unroll
+            for (int h = 0; h < D / 32; ++h) {
+                uint32_t w[16];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 t = vloc < a.Vc ? __ldg(xr + h * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
+                    w[4 * k + 0] = t.x;
+                    w[4 * k + 1] = t.y;
+                    w[4 * k + 2] = t.z;
+                    w[4 * k + 3] = t.w;
+                }
+                tmem_st16(tbase + lane_off + (uint32_t)(kAcol + ab * (D / 2) + h * 16), w);
+            }
+            tmem_st_wait();
+            fence_before();
+            mbar_arrive(afull_bar(ab));
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            bool ok = mbar_wait(afull_bar, 0, status);
-            int issued = 0;
-            for (int c = 0; c < nch && ok; ++c) {
-                const int st = c % kStages;
-                const uint32_t ph = (uint32_t)(c / kStages) & 1u;
-                const int buf = c & 1;
-                const uint32_t bph = (uint32_t)(c >> 1) & 1u;
-                ok = mbar_wait(tempty_bar(buf), bph ^ 1u, status);
+            int prev = -1, seg = -1, issued = 0;
+            bool ok = true;
+            UnitCursor uc;
+            uc.init(u0, nch, tiles);
+            for (int i = 0; i < nu && ok; ++i, uc.advance(1)) {
+                if (uc.pair != prev) {
+                    // the previous segment's tile is free once its MMAs complete
+                    if (seg >= 0) mma_commit(aempty_bar(seg & 1));
+                    prev = uc.pair;
+                    ++seg;
+                    ok = mbar_wait(afull_bar(seg & 1), (uint32_t)(seg >> 1) & 1u, status);
+                    if (!ok) break;
+                }
+                const int buf = i & 1;
+                ok = mbar_wait(tempty_bar(buf), ((uint32_t)(i >> 1) & 1u) ^ 1u, status);
                 if (!ok) break;
-                ok = mbar_wait(full_bar(st), ph, status);
+                const int st = i % L::kStages;
+                ok = mbar_wait(full_bar(st), (uint32_t)(i / L::kStages) & 1u, status);
                 if (!ok) break;
-                tc_fence_after();
+                fence_after();
                 const uint32_t dt = tbase + (uint32_t)(buf * kChunk);
+                const uint32_t at = tbase + (uint32_t)(kAcol + (seg & 1) * (D / 2));
+                const uint32_t aB = sB + (uint32_t)st * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = (uint32_t)((kk >> 2) * kChunk * 128 + (kk & 3) * 32);
-                    mma_f16(dt, sdesc(sA + koff), sdesc(sB + st * kTileBytes + koff), kk > 0 ? 1u : 0u);
+                    mma_ts(dt, at + (uint32_t)(kk * 8), sdesc(aB + koff), kIdesc, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(empty_bar(st));
                 mma_commit(tfull_bar(buf));
@@ -175,84 +258,122 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
         const int q = e & 3;                                // TMEM lane group
         const int hb = e >> 2;                              // accumulator buffer handled
         const int r = q * 32 + lane;                        // TMEM lane = row of the vector tile
-        const int vloc = tile * kTileV + r;                 // vector index inside the chunk
-        const bool valid = vloc < a.Vc;
-        const int region = slice * 2 + hb;
-        const int cs = a.cap / (2 * a.slices);              // entries per region
-        unsigned long long* list =
-            a.cand + ((size_t)g * a.Vc + (valid ? vloc : 0)) * a.cap + (size_t)region * cs;
-        uint32_t tau_bits = 0u;
-        int cnt = 0;
-        bool ok = mbar_wait(afull_bar, 0, status);
-        if (ok && !kDump) {
-            // ||x||^2 from this row of the swizzled A tile (all 16-byte chunks
-            // of the row, whatever their swizzled order)
-            float sq = 0.f;
+        uint2* const recs = reinterpret_cast<uint2*>(smem + L::s_off) + e * kWarpStageEntries;
+        uint2* const myrec = recs + lane * kRecEntries;      // entry 0 header, then the keys
+        int cur = -1, g = 0, vloc = 0;
+        bool valid = false, ok = true;
+        float tau = __int_as_float(0x7fffffff);
+        UnitCursor uc;
+        uc.init(u0 + hb, nch, tiles);
+        for (int i = hb; i < nu && ok; i += 2, uc.advance(2)) {
+            const int c = uc.c;
+            if (uc.pair != cur) {
+                cur = uc.pair;
+                g = uc.g;
+                vloc = uc.tile * kTileV + r;
+                valid = vloc < a.Vc;
+                // tau from ||x||^2 (rows past the batch: NaN, never passes)
+                tau = __int_as_float(0x7fffffff);
+                if (valid && !kDump) {
+                    const uint4* xr =
+                        reinterpret_cast<const uint4*>((const __half*)a.x + ((size_t)g * a.V + a.v0 + vloc) * D);
+                    float sq = 0.f;
 #pragma unroll
-            for (int h = 0; h < L::KH; ++h) {
+                    for (int k = 0; k < D / 8; ++k) {
+                        const uint4 w = __ldg(xr + k);
+                        const __half2* hv = reinterpret_cast<const __half2*>(&w);
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(
-                        smem + L::a_off + h * kChunk * 128 + r * 128 + ((ch ^ (r & 7)) * 16));
-                    const __half2* hv = reinterpret_cast<const __half2*>(&w);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f = __half22float2(hv[i]);
-                        sq = fmaf(f.x, f.x, sq);
-                        sq = fmaf(f.y, f.y, sq);
+                        for (int t = 0; t < 4; ++t) {
+                            const float2 f = __half22float2(hv[t]);
+                            sq = fmaf(f.x, f.x, sq);
+                            sq = fmaf(f.y, f.y, sq);
+                        }
                     }
+                    tau = a.alpha * sqrtf(sq * (1.0f / (float)D));
                 }
             }
-            // rows past the batch never pass (|S| bits are below 0xffffffff)
-            tau_bits = valid ? __float_as_uint(a.alpha * sqrtf(sq * (1.0f / (float)D))) : 0xffffffffu;
-        }
-        for (int c = hb; c < nch && ok; c += 2) {
-            const uint32_t bph = (uint32_t)(c >> 1) & 1u;
-            ok = mbar_wait(tfull_bar(hb), bph, status);
+            const int buf = i & 1;
+            ok = mbar_wait(tfull_bar(buf), (uint32_t)(i >> 1) & 1u, status);
             if (!ok) break;
-            tc_fence_after();
-            const int atom0 = (c0 + c) * kChunk;
-#pragma unroll
-            for (int qq = 0; qq < kChunk / 32; ++qq) {
-                uint32_t v[32];
-                tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(hb * kChunk + qq * 32), v);
+            fence_after();
+            const uint32_t tcol = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kChunk);
+            const uint32_t lo0 = 0xffffffffu - (uint32_t)(c * kChunk);
+            int k = 1;                                      // next entry of this row's record
+            bool ovf = false;
+            // one 32-column group: append the keys of the kept scores
+            auto stage = [&](const uint32_t (&v)[32], int qq) {
                 if (kDump) {
                     if (valid) {
-                        float* out = a.dump + ((size_t)g * a.Vc + vloc) * a.N + atom0 + qq * 32;
+                        float* out = a.dump + ((size_t)g * a.Vc + vloc) * a.N + c * kChunk + qq * 32;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(v[i]);
+                        for (int t = 0; t < 32; ++t) out[t] = __uint_as_float(v[t]);
                     }
-                } else {
-                    const uint32_t lo0 = 0xffffffffu - (uint32_t)(atom0 + qq * 32);
+                    return;
+                }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        // branch-free: a predicated store, then the count.  Past
-                        // the region's end the last slot is reused: the count
-                        // then exceeds the region and the consumer redoes the
-                        // vector exactly.
-                        const uint32_t mag = v[i] & 0x7fffffffu;
-                        unsigned long long* slot = list + min(cnt, cs - 1);
-                        asm volatile(
-                            "{\n\t.reg .pred p;\n\t"
-                            "setp.ge.u32 p, %0, %1;\n\t"
-                            "@p st.global.v2.u32 [%2], {%3, %0};\n\t}"
-                            ::"r"(mag), "r"(tau_bits), "l"(slot), "r"(lo0 - (uint32_t)i)
-                            : "memory");
-                        cnt += (mag >= tau_bits) ? 1 : 0;
+                for (int t = 0; t < 32; ++t) {
+                    if (fabsf(__uint_as_float(v[t])) >= tau) {
+                        myrec[k] = make_uint2(lo0 - (uint32_t)(qq * 32 + t), v[t]);
+                        ++k;
                     }
                 }
+                // a row may run past its record by at most 32 entries (into the
+                // next row's record, or the warp's guard after row 31): flagged
+                // below
+                ovf |= k > kRecEntries;
+                k = min(k, kRecEntries);
+            };
+            // TMEM loads double-buffered in registers: group g+1 is in flight
+            // while group g is filtered
+            static_assert(kChunk == 128, "four 32-column groups per unit");
+            uint32_t va[32], vb[32];
+            tmem_ld32_async(tcol, va);
+            tmem_wait32(va);
+            tmem_ld32_async(tcol + 32, vb);
+            stage(va, 0);
+            tmem_wait32(vb);
+            tmem_ld32_async(tcol + 64, va);
+            stage(vb, 1);
+            tmem_wait32(va);
+            tmem_ld32_async(tcol + 96, vb);
+            stage(va, 2);
+            tmem_wait32(vb);
+            // every column of this buffer is in registers: hand it back
+            fence_before();
+            mbar_arrive(tempty_bar(buf));
+            stage(vb, 3);
+            if (kDump) continue;
+            // a row that ran past its record spilled into the next row's record
+            // only (the group clamp bounds the spill to one record): both are
+            // flagged
+            const int prev_ovf = __shfl_up_sync(0xffffffffu, ovf ? 1 : 0, 1);   // every lane takes part
+            const bool over = ovf || (lane > 0 && prev_ovf != 0);
+            const int cnt = k - 1;
+            myrec[0] = make_uint2(rec_header(over, cnt), 0u);
+            __syncwarp();
+            // copy the 32 records out: sixteen lanes on a record (16 bytes
+            // each), two records at a time, only the pieces holding entries
+            const int part = lane & 15, rsub = lane >> 4;
+            const int pieces = valid ? (cnt + 2) / 2 : 0;
+            unsigned char* const out = a.rec + ((size_t)g * a.Vc + (size_t)(vloc - lane)) * nch * kRecBytes +
+                                       (size_t)c * kRecBytes;
+#pragma unroll
+            for (int it = 0; it < 16; ++it) {
+                const int j = it * 2 + rsub;
+                const int pj = __shfl_sync(0xffffffffu, pieces, j);
+                if (part < pj) {
+                    const uint4 w = reinterpret_cast<const uint4*>(recs + j * kRecEntries)[part];
+                    *reinterpret_cast<uint4*>(out + (size_t)j * nch * kRecBytes + part * 16) = w;
+                }
             }
-            tc_fence_before();
-            mbar_arrive(tempty_bar(hb));
+            __syncwarp();
         }
-        if (valid && !kDump)
-            a.cand_count[((size_t)g * a.Vc + vloc) * kCountSlots + region] = cnt;
     }
 
-    tc_fence_before();
+    fence_before();
     __syncthreads();
     if (warp == 2) {
-        tc_fence_after();
+        fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols));
     }
 }
@@ -262,20 +383,26 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constan
 // ---------------------------------------------------------------------------
 
 template <int D, bool kDump>
-cudaError_t launch_t(const Shape& sh, const void* atoms, const void* x, int V, const ScreenTCArgs& a, int sms,
+cudaError_t launch_t(const Shape& sh, const void* atoms, const ScreenTCArgs& a, int sms, ScreenTCCache* cache,
                      cudaStream_t st)
 {
-    CUtensorMap mx, md;
-    if (!make_tma_map_f16(&mx, x, (long long)sh.G * V, D, 128) ||
-        !make_tma_map_f16(&md, atoms, (long long)sh.G * sh.N, D, 128))
-        return cudaErrorInvalidValue;
+    static_assert(sizeof(CUtensorMap) <= sizeof(cache->map_d), "tensor map size");
+    CUtensorMap* md = reinterpret_cast<CUtensorMap*>(cache->map_d);
+    const long long drows = (long long)sh.G * sh.N;
+    if (cache->d_base != atoms || cache->d_rows != drows) {
+        cache->d_base = nullptr;
+        if (!make_tma_map_f16(md, atoms, drows, D, 128)) return cudaErrorInvalidValue;
+        cache->d_base = atoms;
+        cache->d_rows = drows;
+    }
     auto k = screen_tc_kernel<D, kDump>;
     const int smem = SmemLayout<D>::alloc;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    const int tiles = (a.Vc + kTileV - 1) / kTileV;
-    dim3 grid(tiles * a.slices, sh.G);
-    k<<<grid, kThreads, smem, st>>>(mx, md, a);
+    if (!cache->attr_done[kDump ? 1 : 0]) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        cache->attr_done[kDump ? 1 : 0] = true;
+    }
+    k<<<screen_tc_grid(sh, a.Vc, sms), kThreads, smem, st>>>(*md, a);
     return cudaGetLastError();
 }
 
@@ -308,18 +435,12 @@ bool make_tma_map_f16(CUtensorMap* m, const void* base, long long rows, int d, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int screen_tc_slices(const Shape& sh, int Vc, int sms)
+int screen_tc_grid(const Shape& sh, int Vc, int sms)
 {
-    // two CTAs per SM; at least 64 entries per candidate region
+    // one CTA per SM (fewer if there are fewer units than SMs)
     const int tiles = (Vc + kTileV - 1) / kTileV;
-    const int nchunks = sh.N / kChunk;
-    int s = 2 * sms / (sh.G * tiles);
-    const int by_cap = cand_cap(sh.n) / 128;
-    if (s > by_cap) s = by_cap;
-    if (s > kMaxSlices) s = kMaxSlices;
-    if (s > nchunks) s = nchunks;
-    if (s < 1) s = 1;
-    return s;
+    const long long T = (long long)sh.G * tiles * (sh.N / kChunk);
+    return (int)(T < sms ? (T > 0 ? T : 1) : sms);
 }
 
 bool screen_tc_supported(const Shape& sh)
@@ -327,14 +448,15 @@ bool screen_tc_supported(const Shape& sh)
     return sh.dtype == FADKV_F16 && (sh.d == 64 || sh.d == 128) && sh.N % kChunk == 0;
 }
 
-cudaError_t launch_screen_tc(const Shape& sh, const void* atoms, const void* x, int V, const ScreenTCArgs& a,
-                             int sms, cudaStream_t st)
+cudaError_t launch_screen_tc(const Shape& sh, const void* atoms, const ScreenTCArgs& a, int sms, ScreenTCCache* cache,
+                             cudaStream_t st)
 {
     if (a.Vc <= 0) return cudaSuccess;
     const bool dump = a.dump != nullptr;
     if (sh.d == 128)
-        return dump ? launch_t<128, true>(sh, atoms, x, V, a, sms, st) : launch_t<128, false>(sh, atoms, x, V, a, sms, st);
-    return dump ? launch_t<64, true>(sh, atoms, x, V, a, sms, st) : launch_t<64, false>(sh, atoms, x, V, a, sms, st);
+        return dump ? launch_t<128, true>(sh, atoms, a, sms, cache, st)
+                    : launch_t<128, false>(sh, atoms, a, sms, cache, st);
+    return dump ? launch_t<64, true>(sh, atoms, a, sms, cache, st) : launch_t<64, false>(sh, atoms, a, sms, cache, st);
 }
 
 }  // namespace fadkv

@@ -4,10 +4,10 @@
 // abstract: a one-shot Top-n selection identifies a small candidate pool;
 // ties go to the lower atom index (a convention of this library).
 //
-// The candidates of a vector arrive as 64-bit keys (bits(|r_j|) << 32) |
-// (0xffffffff - j) split into regions with one count each.  A warp gathers
-// them into its slice of shared memory (asynchronous copies, all in flight
-// at once), then:
+// The candidates of a vector arrive as the screening kernel's records: per
+// 128-atom chunk a header and the kept atoms' keys.  A warp gathers them as
+// 64-bit keys (bits(|r_j|) << 32) | (0xffffffff - j) in its slice of shared
+// memory, then:
 //   1. buckets the keys by |r| on a linear grid of 256 buckets over
 //      [min |r|, max |r|] of the list (monotone in |r|, so every key of a
 //      higher bucket beats every key of a lower one);
@@ -31,54 +31,84 @@ select_kernel(SelectArgs a)
 {
     extern __shared__ unsigned long long kbuf_all[];   // [kWarpsPerCta][cap]
     __shared__ uint32_t hist_all[kWarpsPerCta][256];
-    __shared__ int offs_all[kWarpsPerCta][kCountSlots + 1];
     const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
     const long long gw = (long long)blockIdx.x * kWarpsPerCta + wl;   // (g, vc) flattened
     if (gw >= (long long)a.G * a.Vc) return;
     uint32_t* hist = hist_all[wl];
-    int* offs = offs_all[wl];
     unsigned long long* keys = kbuf_all + (size_t)wl * a.cap;
     const int n = a.n;
     int32_t* pool = a.pool + gw * n;
 
-    // region counts -> total and region offsets
-    const int nreg = 2 * a.slices;
-    const int cs = a.cap / nreg;
-    int* counts = a.cand_count + gw * kCountSlots;
-    const int c = (lane < nreg) ? counts[lane] : 0;
-    const int over = __any_sync(0xffffffffu, c > cs);
-    int incl = c;
+    // the screening records of this vector: headers first (count, overflow)
+    const int nch = a.N / 128;
+    const unsigned char* rec = a.rec + (size_t)gw * nch * kRecBytes;
+    int K = 0;
+    bool bad = false;
+    for (int cg = 0; cg < nch; cg += 32) {
+        const int cc = cg + lane;
+        const uint32_t h = cc < nch ? __ldg(reinterpret_cast<const uint32_t*>(rec + (size_t)cc * kRecBytes)) : 0u;
+        bad |= (h >> 31) != 0u;
+        K += (int)(h & 0xffffu);
+    }
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    const int K = __shfl_sync(0xffffffffu, incl, 31);
-    if (lane < nreg) {
-        offs[lane] = incl - c;
-        counts[lane] = 0;                              // consumed: ready for the next call
-    }
-    if (over || K < n) {
+    for (int o = 16; o > 0; o >>= 1) K += __shfl_xor_sync(0xffffffffu, K, o);
+    bad = __any_sync(0xffffffffu, bad);
+    auto slow = [&]() {
         if (lane == 0) {
             pool[0] = -2;                              // exact slow path (pool fixup, or the greedy kernel)
             *a.slow_seq = a.seq;                       // every writer stores the same value
         }
+    };
+    if (bad || K < n || K > a.cap) {
+        slow();
         return;
     }
-    __syncwarp();
 
-    // gather the regions back to back (8-byte asynchronous copies)
-    const unsigned long long* src = a.cand + gw * a.cap;
-    for (int r = 0; r < nreg; ++r) {
-        const int o0 = offs[r];
-        const int len = (r + 1 < nreg ? offs[r + 1] : K) - o0;
-        for (int i = lane; i < len; i += 32) {
-            const uint32_t dst = (uint32_t)__cvta_generic_to_shared(keys + o0 + i);
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src + (size_t)r * cs + i)
-                         : "memory");
+    // gather: record c's keys at the sum of the counts of the records
+    // before it; sixteen lanes copy a record (two keys each), two records at
+    // a time
+    const int part = lane & 15, rsub = lane >> 4;
+    const uint32_t lo_min = 0xffffffffu - (uint32_t)(a.N - 1);   // keys of atoms j < N
+    bool foreign = false;
+    int gbase = 0;
+    for (int cg = 0; cg < nch; cg += 32) {
+        const int cc = cg + lane;
+        const uint32_t h = cc < nch ? __ldg(reinterpret_cast<const uint32_t*>(rec + (size_t)cc * kRecBytes)) : 0u;
+        const int cnt = (int)(h & 0xffffu);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
         }
+        const int off = gbase + incl - cnt;
+#pragma unroll 4
+        for (int it = 0; it < 16; ++it) {
+            const int j = it * 2 + rsub;
+            const int cj = __shfl_sync(0xffffffffu, cnt, j);
+            const int oj = __shfl_sync(0xffffffffu, off, j);
+            // entries 2*part, 2*part+1 of record j; entry 0 is the header
+            if (cg + j < nch && 2 * part <= cj) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(rec + (size_t)(cg + j) * kRecBytes) + part);
+                const int e0 = 2 * part - 1, e1 = 2 * part;
+                if (e0 >= 0) {
+                    keys[oj + e0] = ((unsigned long long)(w.y & 0x7fffffffu) << 32) | w.x;
+                    foreign |= w.x < lo_min;
+                }
+                if (e1 < cj) {
+                    keys[oj + e1] = ((unsigned long long)(w.w & 0x7fffffffu) << 32) | w.z;
+                    foreign |= w.z < lo_min;
+                }
+            }
+        }
+        gbase = __shfl_sync(0xffffffffu, off + cnt, 31);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    // an atom index outside the dictionary can only come from a damaged
+    // record: never let it reach the pool
+    if (__any_sync(0xffffffffu, foreign)) {
+        slow();
+        return;
+    }
     __syncwarp();
 
     // 1. range of |r| and the bucket grid

@@ -96,31 +96,33 @@ __device__ __forceinline__ float row_dot_f32<float, 64>(const float* row, const 
 struct Scratch {
     uint32_t* hist;             // [256]
     uint32_t* scan;             // [nwarps]
-    uint32_t* misc;             // [4 + kCountSlots]
+    uint32_t* misc;             // [4 + 2 * kCountSlots]
     unsigned long long* pref;   // [1]
 };
 
-// Reads the region counts of this vector's candidate list and resets them.
-// Returns the total count, or -1 if a region overflowed.  Region offsets are
-// left in misc[3 ..].  Whole block calls it; ends with a barrier.
+// Reads the slot words of this vector's candidate list and resets them.
+// Returns the total count (also left in misc[0]), or -1 if a region
+// overflowed.  The regions' offsets in the gathered key array are left in
+// misc[4 ..] and their offsets in the list in misc[4 + kCountSlots ..].
+// Whole block calls it; ends with a barrier.
 __device__ __forceinline__ int intake_counts(const GreedyArgs& a, size_t gv, Scratch sc)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nreg = 2 * a.slices;
-    const int cs = a.cap / nreg;
     int* counts = a.cand_count + gv * kCountSlots;
     if (warp == 0) {
-        const int c = (lane < nreg) ? counts[lane] : 0;
-        const int over = __any_sync(0xffffffffu, c > cs);
+        const uint32_t wd = (uint32_t)counts[lane];
+        const int c = slot_count(wd);
+        const int over = __any_sync(0xffffffffu, slot_over(wd));
         int incl = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int t = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += t;
         }
-        if (lane < nreg) sc.misc[3 + lane] = (uint32_t)(incl - c);
+        sc.misc[4 + lane] = (uint32_t)(incl - c);
+        sc.misc[4 + kCountSlots + lane] = (uint32_t)slot_offset(wd);
         if (lane == 31) sc.misc[0] = over ? 0xffffffffu : (uint32_t)incl;
-        if (lane < nreg) counts[lane] = 0;   // consumed: ready for the next call
+        counts[lane] = 0;   // consumed: ready for the next call
     }
     __syncthreads();
     return (int)sc.misc[0];
@@ -137,13 +139,12 @@ __device__ __forceinline__ int intake_keys(const GreedyArgs& a, size_t gv, int c
     int K;
     if (count >= n) {
         K = count;
-        const int nreg = 2 * a.slices;
-        const int cs = a.cap / nreg;
         const unsigned long long* src = a.cand + gv * a.cap;
-        for (int r = 0; r < nreg; ++r) {
-            const int off = (int)sc.misc[3 + r];
-            const int len = (r + 1 < nreg ? (int)sc.misc[4 + r] : K) - off;
-            for (int i = tid; i < len; i += nt) keys[off + i] = src[(size_t)r * cs + i];
+        for (int r = 0; r < kCountSlots; ++r) {
+            const int off = (int)sc.misc[4 + r];
+            const int len = (r + 1 < kCountSlots ? (int)sc.misc[5 + r] : K) - off;
+            const int so = (int)sc.misc[4 + kCountSlots + r];
+            for (int i = tid; i < len; i += nt) keys[off + i] = src[so + i];
         }
     } else {
         K = N;
