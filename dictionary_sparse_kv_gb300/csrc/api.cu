@@ -239,7 +239,7 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
         sa.Vc = Vc;
         sa.N = h->p.N;
         sa.n = h->p.n;
-        sa.cap = h->L.cap;
+        sa.cap = select_cap(h->p.n);
         sa.rec = h->ws + h->L.cand;
         sa.pool = (int32_t*)(h->ws + h->L.pool);
         if (++h->seq == 0) h->seq = 1;                 // 0 is the workspace's initial value

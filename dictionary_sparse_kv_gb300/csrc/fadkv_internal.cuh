@@ -137,6 +137,9 @@ struct SelectArgs {
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 size_t select_smem_bytes(int cap);
+// Keys a selection warp holds: the screening threshold aims at 1.5n
+// candidates, so 2n leaves room for the spread; more take the slow path.
+__host__ __device__ inline int select_cap(int n) { return 2 * n; }
 
 // Exact Top-n from the candidate lists (slow exact path for lists shorter
 // than n or longer than cap), then greedy selection inside the pool plus

@@ -39,41 +39,29 @@ select_kernel(SelectArgs a)
     const int n = a.n;
     int32_t* pool = a.pool + gw * n;
 
-    // the screening records of this vector: headers first (count, overflow)
+    // the screening records of this vector, 32 at a time: every record's
+    // header and all of its 16-byte pieces are loaded in one batch (sixteen
+    // lanes on a record, two records per load), then record c's keys go to
+    // the sum of the counts of the records before it
     const int nch = a.N / 128;
     const unsigned char* rec = a.rec + (size_t)gw * nch * kRecBytes;
-    int K = 0;
-    bool bad = false;
-    for (int cg = 0; cg < nch; cg += 32) {
-        const int cc = cg + lane;
-        const uint32_t h = cc < nch ? __ldg(reinterpret_cast<const uint32_t*>(rec + (size_t)cc * kRecBytes)) : 0u;
-        bad |= (h >> 31) != 0u;
-        K += (int)(h & 0xffffu);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) K += __shfl_xor_sync(0xffffffffu, K, o);
-    bad = __any_sync(0xffffffffu, bad);
-    auto slow = [&]() {
-        if (lane == 0) {
-            pool[0] = -2;                              // exact slow path (pool fixup, or the greedy kernel)
-            *a.slow_seq = a.seq;                       // every writer stores the same value
-        }
-    };
-    if (bad || K < n || K > a.cap) {
-        slow();
-        return;
-    }
-
-    // gather: record c's keys at the sum of the counts of the records
-    // before it; sixteen lanes copy a record (two keys each), two records at
-    // a time
     const int part = lane & 15, rsub = lane >> 4;
     const uint32_t lo_min = 0xffffffffu - (uint32_t)(a.N - 1);   // keys of atoms j < N
-    bool foreign = false;
+    bool bad = false, foreign = false;
     int gbase = 0;
+    constexpr int kIt = 16;                 // loads per lane: 32 records x 16 pieces over 32 lanes
+    static_assert(kRecBytes / 16 == 16, "sixteen lanes cover a record");
     for (int cg = 0; cg < nch; cg += 32) {
         const int cc = cg + lane;
         const uint32_t h = cc < nch ? __ldg(reinterpret_cast<const uint32_t*>(rec + (size_t)cc * kRecBytes)) : 0u;
+        uint4 w[kIt];
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int j = cg + it * 2 + rsub;
+            w[it] = j < nch ? __ldg(reinterpret_cast<const uint4*>(rec + (size_t)j * kRecBytes) + part)
+                            : make_uint4(0u, 0u, 0u, 0u);
+        }
+        bad |= (h >> 31) != 0u;
         const int cnt = (int)(h & 0xffffu);
         int incl = cnt;
 #pragma unroll
@@ -82,30 +70,36 @@ select_kernel(SelectArgs a)
             if (lane >= o) incl += t;
         }
         const int off = gbase + incl - cnt;
-#pragma unroll 4
-        for (int it = 0; it < 16; ++it) {
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
             const int j = it * 2 + rsub;
             const int cj = __shfl_sync(0xffffffffu, cnt, j);
             const int oj = __shfl_sync(0xffffffffu, off, j);
-            // entries 2*part, 2*part+1 of record j; entry 0 is the header
-            if (cg + j < nch && 2 * part <= cj) {
-                const uint4 w = __ldg(reinterpret_cast<const uint4*>(rec + (size_t)(cg + j) * kRecBytes) + part);
-                const int e0 = 2 * part - 1, e1 = 2 * part;
-                if (e0 >= 0) {
-                    keys[oj + e0] = ((unsigned long long)(w.y & 0x7fffffffu) << 32) | w.x;
-                    foreign |= w.x < lo_min;
-                }
-                if (e1 < cj) {
-                    keys[oj + e1] = ((unsigned long long)(w.w & 0x7fffffffu) << 32) | w.z;
-                    foreign |= w.z < lo_min;
-                }
+            // entries 2*part, 2*part+1 of record j are keys 2*part-1, 2*part
+            // (entry 0 is the header); keys past the buffer are dropped, the
+            // vector then takes the slow path below
+            const int e0 = 2 * part - 1, e1 = 2 * part;
+            if (e0 >= 0 && e0 < cj && oj + e0 < a.cap) {
+                keys[oj + e0] = ((unsigned long long)(w[it].y & 0x7fffffffu) << 32) | w[it].x;
+                foreign |= w[it].x < lo_min;
+            }
+            if (e1 < cj && oj + e1 < a.cap) {
+                keys[oj + e1] = ((unsigned long long)(w[it].w & 0x7fffffffu) << 32) | w[it].z;
+                foreign |= w[it].z < lo_min;
             }
         }
         gbase = __shfl_sync(0xffffffffu, off + cnt, 31);
     }
-    // an atom index outside the dictionary can only come from a damaged
-    // record: never let it reach the pool
-    if (__any_sync(0xffffffffu, foreign)) {
+    const int K = gbase;
+    auto slow = [&]() {
+        if (lane == 0) {
+            pool[0] = -2;                              // exact slow path (pool fixup, or the greedy kernel)
+            *a.slow_seq = a.seq;                       // every writer stores the same value
+        }
+    };
+    // an overflowed record, too few or too many keys, or an atom index
+    // outside the dictionary (only a damaged record has one): the slow path
+    if (__any_sync(0xffffffffu, bad || foreign) || K < n || K > a.cap) {
         slow();
         return;
     }
