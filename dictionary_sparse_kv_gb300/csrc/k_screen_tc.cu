@@ -42,8 +42,14 @@ constexpr int kStagesFor(int D) { return D == 64 ? 8 : 4; }   // atom chunk pipe
 constexpr int kTmemCols = 512;     // two accumulator buffers (128 columns each), two vector tiles
 constexpr int kAcol = 2 * kChunk;  // first TMEM column of the vector tiles
 constexpr int kEpiWarps = 8;
-constexpr int kWarpStageEntries = 32 * kRecEntries + 32;  // a warp's 32 records + a guard of 32 entries
-static_assert(kRecEntries >= 32, "a row spills at most 32 entries, into the next record or the guard");
+// A row's record in shared memory sits in a slot of kRecEntries + 2 entries
+// (272 bytes): consecutive rows start 4 banks apart, so the rows' appends,
+// which advance at similar rates, rarely hit the same bank.
+constexpr int kSlotEntries = kRecEntries + 2;
+constexpr int kWarpStageEntries = 32 * kSlotEntries + 32;  // a warp's 32 slots + a guard of 32 entries
+static_assert(kRecEntries >= 32 && kSlotEntries - kRecEntries <= 32,
+              "a row spills at most 32 entries past its record: into the next slot or the guard");
+static_assert(kSlotEntries * 8 % 16 == 0, "slots are read in 16-byte pieces");
 static_assert(kRecBytes % 16 == 0, "records are copied in 16-byte pieces");
 
 using namespace tc;
@@ -259,7 +265,7 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
         const int hb = e >> 2;                              // accumulator buffer handled
         const int r = q * 32 + lane;                        // TMEM lane = row of the vector tile
         uint2* const recs = reinterpret_cast<uint2*>(smem + L::s_off) + e * kWarpStageEntries;
-        uint2* const myrec = recs + lane * kRecEntries;      // entry 0 header, then the keys
+        uint2* const myrec = recs + lane * kSlotEntries;     // entry 0 header, then the keys
         int cur = -1, g = 0, vloc = 0;
         bool valid = false, ok = true;
         float tau = __int_as_float(0x7fffffff);
@@ -362,7 +368,7 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
                 const int j = it * 2 + rsub;
                 const int pj = __shfl_sync(0xffffffffu, pieces, j);
                 if (part < pj) {
-                    const uint4 w = reinterpret_cast<const uint4*>(recs + j * kRecEntries)[part];
+                    const uint4 w = reinterpret_cast<const uint4*>(recs + j * kSlotEntries)[part];
                     *reinterpret_cast<uint4*>(out + (size_t)j * nch * kRecBytes + part * 16) = w;
                 }
             }
