@@ -82,9 +82,11 @@ adapt_kernel(Shape sh, AdaptArgs a, DeltaTable delta, int max_batch)
     }
     __syncthreads();
 
-    // 2. inactive atoms in ascending id; 3. flagged vectors in ascending v
-    const int nL = block_compact(N, [&](int j) { return usage[j] == 0; }, inactive, ws);
+    // 2. flagged vectors in ascending v; 3. inactive atoms in ascending id
+    //    (only needed when some vector is flagged: the N-wide scan is skipped
+    //    in the common step with no replacement)
     const int nF = block_compact(V, [&](int v) { return relres[v] > dg; }, flagged, ws);
+    const int nL = nF > 0 ? block_compact(N, [&](int j) { return usage[j] == 0; }, inactive, ws) : 0;
     const int m = min(nL, nF);
 
     // 4. the r-th flagged vector takes the r-th inactive atom (one warp each).
@@ -125,6 +127,39 @@ adapt_kernel(Shape sh, AdaptArgs a, DeltaTable delta, int max_batch)
     }
 }
 
+// PL consecutive elements of a row as fp32, one vector load (rows are
+// 16-byte aligned: atoms are, and a row is 128 or 256 bytes).
+template <int PL>
+__device__ __forceinline__ void load_row(const __half* p, float (&r)[PL])
+{
+    static_assert(PL == 2 || PL == 4, "64 or 128 elements per row");
+    if constexpr (PL == 4) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        r[0] = a.x; r[1] = a.y; r[2] = b.x; r[3] = b.y;
+    } else {
+        const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(p));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u));
+        r[0] = a.x; r[1] = a.y;
+    }
+}
+template <int PL>
+__device__ __forceinline__ void load_row(const float* p, float (&r)[PL])
+{
+    if constexpr (PL == 4) {
+        const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+        r[0] = u.x; r[1] = u.y; r[2] = u.z; r[3] = u.w;
+    } else {
+        const float2 u = __ldg(reinterpret_cast<const float2*>(p));
+        r[0] = u.x; r[1] = u.y;
+    }
+}
+
+// x_hat = D_S c (+ repl_coef d_repl), one warp per vector: lane k reads
+// term k's atom id and coefficient and every lane the replacement's, then
+// every term's row is loaded at once, each lane taking D/32 consecutive
+// elements.
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
 reconstruct_kernel(const T* __restrict__ atoms, int G, int N, int s, int V, const int32_t* __restrict__ idx,
@@ -132,31 +167,58 @@ reconstruct_kernel(const T* __restrict__ atoms, int G, int N, int s, int V, cons
                    const float* __restrict__ repl_coef, float* __restrict__ xhat)
 {
     constexpr int PL = D / 32;
+    static_assert(kMaxS <= 32, "one term per lane");
     const int lane = threadIdx.x & 31;
     const long long gv = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (gv >= (long long)G * V) return;
     const int g = (int)(gv / V);
     const T* A = atoms + (size_t)g * N * D;
-    float acc[PL];
-#pragma unroll
-    for (int q = 0; q < PL; ++q) acc[q] = 0.f;
-    for (int k = 0; k < s; ++k) {
-        const int j = idx[gv * s + k];
-        if (j < 0 || j >= N) continue;
-        const float c = coef[gv * s + k];
-#pragma unroll
-        for (int q = 0; q < PL; ++q) acc[q] = fmaf(c, to_f32(A[(size_t)j * D + lane + 32 * q]), acc[q]);
+    int jt = -1, jr = -1;
+    float ct = 0.f, cr = 0.f;
+    if (lane < s) {
+        jt = idx[gv * s + lane];
+        ct = coef[gv * s + lane];
     }
     if (repl_id) {
-        const int j = repl_id[gv];
-        if (j >= 0 && j < N) {
-            const float c = repl_coef[gv];
-#pragma unroll
-            for (int q = 0; q < PL; ++q) acc[q] = fmaf(c, to_f32(A[(size_t)j * D + lane + 32 * q]), acc[q]);
-        }
+        jr = repl_id[gv];
+        cr = repl_coef[gv];
     }
+    // skipped terms: a valid row weighted by zero
+    if (jt < 0 || jt >= N) {
+        jt = 0;
+        ct = 0.f;
+    }
+    if (jr < 0 || jr >= N) {
+        jr = 0;
+        cr = 0.f;
+    }
+    float acc[PL];
+    {
+        float r[PL];
+        load_row(A + (size_t)jr * D + lane * PL, r);
 #pragma unroll
-    for (int q = 0; q < PL; ++q) xhat[gv * D + lane + 32 * q] = acc[q];
+        for (int q = 0; q < PL; ++q) acc[q] = cr * r[q];
+    }
+    // terms in batches of 8: all eight rows are loaded before any is used
+    // (terms past s read row 0 with weight 0)
+    for (int k0 = 0; k0 < s; k0 += 8) {
+        float r[8][PL];
+        float c8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = __shfl_sync(0xffffffffu, jt, (k0 + u) & 31);
+            c8[u] = __shfl_sync(0xffffffffu, ct, (k0 + u) & 31);
+            load_row(A + (size_t)(k0 + u < s ? j : 0) * D + lane * PL, r[u]);
+            if (k0 + u >= s) c8[u] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int q = 0; q < PL; ++q) acc[q] = fmaf(c8[u], r[u][q], acc[q]);
+    }
+    float* out = xhat + gv * D + lane * PL;
+#pragma unroll
+    for (int q = 0; q < PL; ++q) out[q] = acc[q];
 }
 
 template <typename T, int D>

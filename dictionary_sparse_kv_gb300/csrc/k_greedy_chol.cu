@@ -118,11 +118,14 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     for (int i = tid; i < NPAD; i += NT) pid[i] = (i < n) ? a.pool_in[gv * n + i] : -1;
     bad = __syncthreads_or(bad);
     if (!bad) {
-        // the pool's rows into shared memory (coalesced 16-byte copies)
-        for (int c = tid; c < NPAD * (D / 8); c += NT) {
-            const int row = c / (D / 8), part = c % (D / 8);
+        // the pool's rows into shared memory (coalesced 16-byte copies; a
+        // thread keeps one 16-byte column of the rows)
+        static_assert(NT % (D / 8) == 0, "whole rows per pass");
+        const int part = tid % (D / 8);
+        const __half* src0 = Aglob + 8 * part;
+        for (int row = tid / (D / 8); row < NPAD; row += NT / (D / 8)) {
             const int id = pid[row];
-            cp_async16(prow + (size_t)row * D + ((part ^ (row & 7)) << 3), Aglob + (size_t)(id >= 0 ? id : 0) * D + 8 * part,
+            cp_async16(prow + (size_t)row * D + ((part ^ (row & 7)) << 3), src0 + (size_t)(id >= 0 ? id : 0) * D,
                        id >= 0);
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
@@ -148,40 +151,50 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     // holds elements 8 t4 .. 8 t4 + 7 (one 16-byte load): a permutation of the
     // contraction index applied alike to A and B.
     uint32_t Af[RT][KT][4];
-    float gjj = 0.f;
+    float dlo[kMT], dhi[kMT];         // diag(A A^T) of rows g8 and g8 + 8 (lanes with t4 = g8 / 2)
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt) {
         const int s0 = warp * SPW + mt * 16 + g8;
-        float n0 = 0.f, n1 = 0.f;
+        uint32_t fr[KT][4];
 #pragma unroll
         for (int kp = 0; kp < KP; ++kp) {
             const uint4 q0 = *prow_chunk(prow, D, s0, 4 * kp + t4);
             const uint4 q1 = *prow_chunk(prow, D, s0 + 8, 4 * kp + t4);
-            if (mt < RT) {
-                Af[mt < RT ? mt : 0][2 * kp][0] = q0.x;
-                Af[mt < RT ? mt : 0][2 * kp][2] = q0.y;
-                Af[mt < RT ? mt : 0][2 * kp + 1][0] = q0.z;
-                Af[mt < RT ? mt : 0][2 * kp + 1][2] = q0.w;
-                Af[mt < RT ? mt : 0][2 * kp][1] = q1.x;
-                Af[mt < RT ? mt : 0][2 * kp][3] = q1.y;
-                Af[mt < RT ? mt : 0][2 * kp + 1][1] = q1.z;
-                Af[mt < RT ? mt : 0][2 * kp + 1][3] = q1.w;
-            }
-            const __half2* h0 = reinterpret_cast<const __half2*>(&q0);
-            const __half2* h1 = reinterpret_cast<const __half2*>(&q1);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 f0 = __half22float2(h0[i]), f1 = __half22float2(h1[i]);
-                n0 = fmaf(f0.x, f0.x, fmaf(f0.y, f0.y, n0));
-                n1 = fmaf(f1.x, f1.x, fmaf(f1.y, f1.y, n1));
-            }
+            fr[2 * kp][0] = q0.x;
+            fr[2 * kp][2] = q0.y;
+            fr[2 * kp + 1][0] = q0.z;
+            fr[2 * kp + 1][2] = q0.w;
+            fr[2 * kp][1] = q1.x;
+            fr[2 * kp][3] = q1.y;
+            fr[2 * kp + 1][1] = q1.z;
+            fr[2 * kp + 1][3] = q1.w;
         }
-        n0 += __shfl_xor_sync(0xffffffffu, n0, 1);
-        n0 += __shfl_xor_sync(0xffffffffu, n0, 2);
-        n1 += __shfl_xor_sync(0xffffffffu, n1, 1);
-        n1 += __shfl_xor_sync(0xffffffffu, n1, 2);
-        if (t4 == 2 * mt) gjj = n0;
-        if (t4 == 2 * mt + 1) gjj = n1;
+        // A A^T on the tensor pipe: the B fragment of "columns = rows 0..7 of
+        // the tile" is (a0, a2) of the same lane, of "rows 8..15" (a1, a3);
+        // the diagonal lands in the lanes with 2 t4 = g8 or 2 t4 + 1 = g8
+        float plo[2][4] = {}, phi[2][4] = {};
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+            hmma(plo[kt & 1], fr[kt], fr[kt][0], fr[kt][2]);
+            hmma(phi[kt & 1], fr[kt], fr[kt][1], fr[kt][3]);
+        }
+        dlo[mt] = (g8 & 1) ? plo[0][1] + plo[1][1] : plo[0][0] + plo[1][0];
+        dhi[mt] = (g8 & 1) ? phi[0][3] + phi[1][3] : phi[0][2] + phi[1][2];
+        if (mt < RT) {
+#pragma unroll
+            for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) Af[mt < RT ? mt : 0][kt][r] = fr[kt][r];
+        }
+    }
+    // this lane's slot is row (t4 & 1) * 8 + g8 of tile t4 >> 1; its G_jj is
+    // held by lane (g8, t4 = g8 / 2)
+    float gjj;
+    {
+        const int src = 4 * g8 + (g8 >> 1);
+        const float l0 = __shfl_sync(0xffffffffu, dlo[0], src), l1 = __shfl_sync(0xffffffffu, dlo[1], src);
+        const float h0 = __shfl_sync(0xffffffffu, dhi[0], src), h1 = __shfl_sync(0xffffffffu, dhi[1], src);
+        gjj = (t4 >> 1) ? ((t4 & 1) ? h1 : l1) : ((t4 & 1) ? h0 : l0);
     }
     const int myslot = warp * SPW + (t4 >> 1) * 16 + (t4 & 1) * 8 + g8;
     const int myatom = pid[myslot];
