@@ -39,10 +39,10 @@ select_kernel(SelectArgs a)
     const int n = a.n;
     int32_t* pool = a.pool + gw * n;
 
-    // the screening records of this vector, 32 at a time: every record's
-    // header and all of its 16-byte pieces are loaded in one batch (sixteen
-    // lanes on a record, two records per load), then record c's keys go to
-    // the sum of the counts of the records before it
+    // the screening records of this vector, 32 at a time: the headers, then
+    // the records' 16-byte pieces in two batches of eight loads (sixteen
+    // lanes on a record, two records per load); record c's keys go to the
+    // sum of the counts of the records before it
     const int nch = a.N / 128;
     const unsigned char* rec = a.rec + (size_t)gw * nch * kRecBytes;
     const int part = lane & 15, rsub = lane >> 4;
@@ -54,13 +54,17 @@ select_kernel(SelectArgs a)
     for (int cg = 0; cg < nch; cg += 32) {
         const int cc = cg + lane;
         const uint32_t h = cc < nch ? __ldg(reinterpret_cast<const uint32_t*>(rec + (size_t)cc * kRecBytes)) : 0u;
-        uint4 w[kIt];
+        constexpr int kB = kIt / 2;
+        auto load_batch = [&](int b, uint4 (&w)[kB]) {
 #pragma unroll
-        for (int it = 0; it < kIt; ++it) {
-            const int j = cg + it * 2 + rsub;
-            w[it] = j < nch ? __ldg(reinterpret_cast<const uint4*>(rec + (size_t)j * kRecBytes) + part)
-                            : make_uint4(0u, 0u, 0u, 0u);
-        }
+            for (int u = 0; u < kB; ++u) {
+                const int j = cg + (b + u) * 2 + rsub;
+                w[u] = j < nch ? __ldg(reinterpret_cast<const uint4*>(rec + (size_t)j * kRecBytes) + part)
+                               : make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        uint4 w[kB];
+        load_batch(0, w);                               // in flight with the headers
         bad |= (h >> 31) != 0u;
         const int cnt = (int)(h & 0xffffu);
         int incl = cnt;
@@ -70,22 +74,27 @@ select_kernel(SelectArgs a)
             if (lane >= o) incl += t;
         }
         const int off = gbase + incl - cnt;
+        // two batches of eight loads (registers for more resident warps)
 #pragma unroll
-        for (int it = 0; it < kIt; ++it) {
-            const int j = it * 2 + rsub;
-            const int cj = __shfl_sync(0xffffffffu, cnt, j);
-            const int oj = __shfl_sync(0xffffffffu, off, j);
-            // entries 2*part, 2*part+1 of record j are keys 2*part-1, 2*part
-            // (entry 0 is the header); keys past the buffer are dropped, the
-            // vector then takes the slow path below
-            const int e0 = 2 * part - 1, e1 = 2 * part;
-            if (e0 >= 0 && e0 < cj && oj + e0 < a.cap) {
-                keys[oj + e0] = ((unsigned long long)(w[it].y & 0x7fffffffu) << 32) | w[it].x;
-                foreign |= w[it].x < lo_min;
-            }
-            if (e1 < cj && oj + e1 < a.cap) {
-                keys[oj + e1] = ((unsigned long long)(w[it].w & 0x7fffffffu) << 32) | w[it].z;
-                foreign |= w[it].z < lo_min;
+        for (int b = 0; b < kIt; b += kB) {
+            if (b > 0) load_batch(b, w);
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int j = (b + u) * 2 + rsub;
+                const int cj = __shfl_sync(0xffffffffu, cnt, j);
+                const int oj = __shfl_sync(0xffffffffu, off, j);
+                // entries 2*part, 2*part+1 of record j are keys 2*part-1, 2*part
+                // (entry 0 is the header); keys past the buffer are dropped, the
+                // vector then takes the slow path below
+                const int e0 = 2 * part - 1, e1 = 2 * part;
+                if (e0 >= 0 && e0 < cj && oj + e0 < a.cap) {
+                    keys[oj + e0] = ((unsigned long long)(w[u].y & 0x7fffffffu) << 32) | w[u].x;
+                    foreign |= w[u].x < lo_min;
+                }
+                if (e1 < cj && oj + e1 < a.cap) {
+                    keys[oj + e1] = ((unsigned long long)(w[u].w & 0x7fffffffu) << 32) | w[u].z;
+                    foreign |= w[u].z < lo_min;
+                }
             }
         }
         gbase = __shfl_sync(0xffffffffu, off + cnt, 31);
