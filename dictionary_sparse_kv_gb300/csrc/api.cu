@@ -155,6 +155,7 @@ struct fadkv_dict_s {
     ScreenTCCache tc_cache;   // tensor maps of the screening kernel
     // tracing
     bool prof_on;
+    uint32_t prof_mask;    // kernel classes bracketed while profiling
     int64_t launches[FADKV_PROFILE_KERNELS];
     double ms[FADKV_PROFILE_KERNELS];
     std::vector<ProfRec> prof_pending;
@@ -182,7 +183,7 @@ template <typename F>
 cudaError_t traced(fadkv_dict h, int cls, cudaStream_t st, F&& launch)
 {
     cudaEvent_t a = nullptr, b = nullptr;
-    if (h->prof_on) {
+    if (h->prof_on && ((h->prof_mask >> cls) & 1u)) {
         a = prof_event(h);
         b = prof_event(h);
         if (a && b) cudaEventRecord(a, st);
@@ -353,6 +354,7 @@ fadkv_status fadkv_dict_create(const fadkv_params* p, void* atoms, int32_t* usag
     h->seq = 0;
     h->alpha = screen_alpha(p->n, p->N);
     h->prof_on = false;
+    h->prof_mask = 0xffffffffu;
     for (int i = 0; i < FADKV_PROFILE_KERNELS; ++i) {
         h->launches[i] = 0;
         h->ms[i] = 0.0;
@@ -377,6 +379,13 @@ fadkv_status fadkv_profile_enable(fadkv_dict h, int32_t enable)
 {
     if (!h) return FADKV_ERR_INVALID_ARG;
     h->prof_on = enable != 0;
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_profile_select(fadkv_dict h, uint32_t class_mask)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    h->prof_mask = class_mask;
     return FADKV_OK;
 }
 

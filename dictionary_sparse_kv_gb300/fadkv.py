@@ -84,6 +84,7 @@ _SIGS = {
     "fadkv_debug_pool": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "fadkv_debug_scores": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p], C.c_int),
     "fadkv_profile_enable": ([C.c_void_p, C.c_int32], C.c_int),
+    "fadkv_profile_select": ([C.c_void_p, C.c_uint32], C.c_int),
     "fadkv_profile_read": ([C.c_void_p, C.POINTER(C.c_int64), C.POINTER(C.c_double), C.c_int32], C.c_int),
 }
 
@@ -209,6 +210,18 @@ def debug_scores(h: int, x, V: int, scores, stream=None) -> None:
 
 def profile_enable(h: int, enable: bool = True) -> None:
     _check("fadkv_profile_enable", lib().fadkv_profile_enable(h, 1 if enable else 0))
+
+
+def profile_select(h: int, classes=None) -> None:
+    """Kernel classes bracketed with events while profiling (names from
+    KERNEL_NAMES or class numbers); None selects all."""
+    if classes is None:
+        mask = 0xFFFFFFFF
+    else:
+        mask = 0
+        for c in classes:
+            mask |= 1 << (KERNEL_NAMES.index(c) if isinstance(c, str) else int(c))
+    _check("fadkv_profile_select", lib().fadkv_profile_select(h, C.c_uint32(mask)))
 
 
 def profile_read(h: int, reset: bool = False):

@@ -229,7 +229,8 @@ fadkv_status fadkv_debug_scores(fadkv_dict dict, const void* x, int32_t V, float
 /* Kernel classes reported by fadkv_profile_read. */
 #define FADKV_PROFILE_KERNELS 8
 #define FADKV_K_SCREEN 0       /* screening (tensor cores + candidate filter, or FP32 scores) */
-#define FADKV_K_TOPN 1         /* Top-n over materialised FP32 scores (binary32 dictionaries) */
+#define FADKV_K_TOPN 1         /* Top-n: the selection from the screening records and the exact
+                                  pool fixup, or the radix Top-n over FP32 scores (binary32) */
 #define FADKV_K_GREEDY 2       /* in-pool greedy selection + ridge refit */
 #define FADKV_K_ADAPT 3        /* fixed-size adaptation */
 #define FADKV_K_RECONSTRUCT 4  /* sparse reconstruction */
@@ -239,6 +240,13 @@ fadkv_status fadkv_debug_scores(fadkv_dict dict, const void* x, int32_t V, float
    recorded on the launch stream and accumulates the device time between
    them.  Not for use inside CUDA-graph capture.  Errors: INVALID_ARG. */
 fadkv_status fadkv_profile_enable(fadkv_dict dict, int32_t enable);
+
+/* The kernel classes that profiling brackets with events: bit k of
+   class_mask stands for class k (FADKV_K_*); all classes by default.  Launch
+   counts are kept for every class regardless.  Bracketing fewer launches
+   leaves the others back to back on the stream, so a timed step is
+   perturbed less.  Errors: INVALID_ARG. */
+fadkv_status fadkv_profile_select(fadkv_dict dict, uint32_t class_mask);
 
 /* Launch counts and device milliseconds per kernel class since the last
    reset, written to HOST arrays launches[FADKV_PROFILE_KERNELS] and

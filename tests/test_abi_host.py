@@ -108,6 +108,28 @@ def test_create_checks_without_gpu(L):
         F.dict_destroy(h)
 
 
+def test_profile_controls_without_gpu(L):
+    p = F.params(1, 512, 64, 32, 4, F.F32, 16)
+    ws = F.workspace_bytes(p)
+    fake = 0x10000
+    h = F.dict_create(p, fake, fake, [0.5], fake, ws)
+    try:
+        F.profile_select(h, ["greedy"])
+        F.profile_select(h, [0, "adapt"])
+        F.profile_select(h, None)
+        F.profile_enable(h, True)
+        F.profile_enable(h, False)
+        # nothing traced, nothing launched: all zero
+        assert F.profile_read(h, reset=True) == {}
+        with pytest.raises(ValueError):
+            F.profile_select(h, ["no_such_kernel"])
+    finally:
+        F.dict_destroy(h)
+    with pytest.raises(F.FadkvError) as e:
+        F.profile_select(0, None)
+    assert e.value.status == 1
+
+
 def test_fault_injection_leaves_state(L, monkeypatch):
     p = F.params(1, 512, 64, 32, 4, F.F32, 16)
     ws = F.workspace_bytes(p)

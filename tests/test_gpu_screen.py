@@ -116,6 +116,38 @@ def test_slow_path_short_and_overflowing_lists():
         assert abs(rel[v] - res.relres[v]) <= PU.RELRES_TOL * res.relres[v] + 1e-7
 
 
+def test_more_candidates_than_the_selection_holds():
+    """A vector with far more candidates than the selection kernel's 2n-key
+    buffer, none of its 128-atom records overflowing (512 near-copies of x's
+    direction, one in every 8 atoms): the selection hands it to the exact
+    slow path, and pool and code match the oracle."""
+    d, N, n, s = 128, 4096, 128, 8
+    g = np.random.default_rng(13)
+    A = g.standard_normal((N, d))
+    u = g.standard_normal(d)
+    u /= np.linalg.norm(u)
+    near = np.arange(0, N, 8)
+    A[near] = u + g.standard_normal((near.size, d)) / np.sqrt(d)
+    A = (A / np.linalg.norm(A, axis=1, keepdims=True)).astype(np.float16)
+    x = np.empty((1, 2, d), np.float16)
+    x[0, 0] = (3.0 * u).astype(np.float16)
+    x[0, 1] = S.make_sparse_inputs(A, 1, s, 7)[0]      # an ordinary vector beside it
+    D = _dict(A[None], np.ones((1, N), np.int32), [0.5], n, s, 2)
+    pool = D.pool(_t(x))[0].cpu().numpy()[0]
+    c = D.new_codes(2)
+    D.encode(_t(x), c)
+    torch.cuda.synchronize()
+    assert D.stats()[0]["topn_slow_path"] >= 2            # pool() and encode(): vector 0
+    p = O.Params(N, d, n, s)
+    res = O.encode(p, A, x[0])
+    ok = ~PU.exempt_mask(res)                              # no near tie at the Top-n cut
+    for v in range(2):
+        if ok[v]:
+            assert np.array_equal(np.sort(pool[v]), np.sort(res.pool[v])), v
+    idx, coef, rel = (t.cpu().numpy()[0] for t in (c.idx, c.coef, c.relres))
+    PU.assert_encode_ok(PU.compare_encode(res, idx, coef, rel, pool, p, A, x[0]))
+
+
 @pytest.mark.parametrize("name,G,V", [("decode_3b", 3, 200), ("decode_8b", 2, 64)])
 def test_greedy_kernels_agree(monkeypatch, name, G, V):
     """The greedy kernels all match the oracle: the correlation-domain kernel
