@@ -128,6 +128,15 @@ bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
 
 // Records a message for fadkv_last_error on this host thread (used by entry
 // points defined in other translation units).
+bool fadkv::pdl_enabled()
+{
+    static const bool on = [] {
+        const char* f = getenv("FADKV_PDL");
+        return !(f && strcmp(f, "0") == 0);
+    }();
+    return on;
+}
+
 void fadkv::set_last_error(const char* msg)
 {
     snprintf(g_last_error, sizeof(g_last_error), "%s", msg);

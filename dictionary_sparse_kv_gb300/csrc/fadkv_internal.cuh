@@ -39,6 +39,36 @@ struct Shape {
 // Message for fadkv_last_error on the calling host thread.
 void set_last_error(const char* msg);
 
+// Programmatic dependent launch between the kernels of a step: a kernel may
+// be scheduled while its predecessor on the stream drains.  pdl_begin()
+// waits until the predecessor's results are in global memory (a no-op when
+// the kernel was launched normally) and lets the successor be scheduled; every
+// kernel launched with launch_pdl calls it before its first global access.
+// FADKV_PDL=0 launches normally.
+__device__ __forceinline__ void pdl_begin()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Element access for the two storage types.
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }

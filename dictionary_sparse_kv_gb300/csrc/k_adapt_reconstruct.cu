@@ -55,6 +55,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kAdaptThreads)
 adapt_kernel(Shape sh, AdaptArgs a, DeltaTable delta, int max_batch)
 {
+    pdl_begin();
     __shared__ int ws[kAdaptWarps];
     const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int N = sh.N, s = sh.s, V = a.V;
@@ -166,6 +167,7 @@ reconstruct_kernel(const T* __restrict__ atoms, int G, int N, int s, int V, cons
                    const float* __restrict__ coef, const int32_t* __restrict__ repl_id,
                    const float* __restrict__ repl_coef, float* __restrict__ xhat)
 {
+    pdl_begin();
     constexpr int PL = D / 32;
     static_assert(kMaxS <= 32, "one term per lane");
     const int lane = threadIdx.x & 31;
@@ -225,8 +227,7 @@ template <typename T, int D>
 cudaError_t adapt_t(const Shape& sh, const AdaptArgs& a, const DeltaTable& delta, int max_batch,
                     cudaStream_t st)
 {
-    adapt_kernel<T, D><<<sh.G, kAdaptThreads, 0, st>>>(sh, a, delta, max_batch);
-    return cudaGetLastError();
+    return launch_pdl(adapt_kernel<T, D>, dim3(sh.G), dim3(kAdaptThreads), 0, st, sh, a, delta, max_batch);
 }
 
 template <typename T, int D>
@@ -235,9 +236,8 @@ cudaError_t reconstruct_t(const Shape& sh, const void* atoms, int V, const int32
 {
     const long long warps = (long long)sh.G * V;
     const unsigned blocks = (unsigned)((warps + 7) / 8);
-    reconstruct_kernel<T, D><<<blocks, 256, 0, st>>>((const T*)atoms, sh.G, sh.N, sh.s, V, idx, coef,
-                                                     repl_id, repl_coef, xhat);
-    return cudaGetLastError();
+    return launch_pdl(reconstruct_kernel<T, D>, dim3(blocks), dim3(256), 0, st, (const T*)atoms, sh.G, sh.N, sh.s, V,
+                      idx, coef, repl_id, repl_coef, xhat);
 }
 
 }  // namespace

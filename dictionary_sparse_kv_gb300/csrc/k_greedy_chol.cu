@@ -77,6 +77,7 @@ template <int D, int NW, int SMAX, int RT>
 __global__ void __launch_bounds__(NW * 32, NW <= 8 ? (RT == 2 ? 2 : 3) : 1)
 greedy_chol_kernel(Shape sh, GreedyArgs a)
 {
+    pdl_begin();
     constexpr int KT = D / 16, KP = D / 32, NT = NW * 32;
     constexpr int SPW = kMT * 16, NPAD = NW * SPW;
     constexpr int PL = SMAX + 4;                 // published floats: l[SMAX], corr, |l|^2, G_jj, slot
@@ -412,8 +413,7 @@ cudaError_t launch_rt(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Vc, sh.G);
-    k<<<grid, NW * 32, smem, st>>>(sh, a);
-    return cudaGetLastError();
+    return launch_pdl(k, grid, dim3(NW * 32), smem, st, sh, a);
 }
 
 template <int D, int NW, int SMAX>

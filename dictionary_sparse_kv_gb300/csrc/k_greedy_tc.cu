@@ -625,6 +625,7 @@ template <int D>
 __global__ void __launch_bounds__(kFixThreads)
 pool_fixup_kernel(Shape sh, GreedyArgs a, int32_t* pool, const uint32_t* slow_seq, uint32_t seq)
 {
+    pdl_begin();
     if (*slow_seq != seq) return;                      // no vector of this pass was flagged
     const FixupLayout<D> L = fixup_layout<D>(sh.N, sh.n, kFixThreads / 32);
     extern __shared__ __align__(16) unsigned char smem[];
@@ -764,8 +765,7 @@ cudaError_t launch_fixup_t(const Shape& sh, const GreedyArgs& a, int32_t* pool, 
     const long long total = (long long)sh.G * a.Vc;
     const long long want = 2LL * sms;
     const unsigned grid = (unsigned)(total < want ? total : want);
-    k<<<grid, kFixThreads, smem, st>>>(sh, a, pool, slow_seq, seq);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(kFixThreads), smem, st, sh, a, pool, slow_seq, seq);
 }
 
 }  // namespace

@@ -142,6 +142,7 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    pdl_begin();                      // the predecessor's writes (x, atoms) are visible from here
     // The TMEM allocation is published to the MMA and epilogue warps (and
     // warp 2) by a named barrier: the producer starts streaming at once.
     constexpr int kTmemSyncThreads = 32 * (2 + kEpiWarps + 4);
@@ -408,8 +409,7 @@ cudaError_t launch_t(const Shape& sh, const void* atoms, const ScreenTCArgs& a, 
         if (e != cudaSuccess) return e;
         cache->attr_done[kDump ? 1 : 0] = true;
     }
-    k<<<screen_tc_grid(sh, a.Vc, sms), kThreads, smem, st>>>(*md, a);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(screen_tc_grid(sh, a.Vc, sms)), dim3(kThreads), smem, st, *md, a);
 }
 
 }  // namespace

@@ -29,6 +29,7 @@ constexpr int kWarpsPerCta = 4;
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 select_kernel(SelectArgs a)
 {
+    pdl_begin();
     extern __shared__ unsigned long long kbuf_all[];   // [kWarpsPerCta][cap]
     __shared__ uint32_t hist_all[kWarpsPerCta][256];
     const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
@@ -287,8 +288,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
-    select_kernel<<<blocks, kWarpsPerCta * 32, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(select_kernel, dim3(blocks), dim3(kWarpsPerCta * 32), smem, st, a);
 }
 
 }  // namespace fadkv
