@@ -119,18 +119,24 @@ cudaError_t launch_topn_radix(const Shape& sh, const float* scores, int Vc, unsi
 // (N/128) (dictionary, 128-vector tile, 128-atom chunk) units, chunk fastest.
 //
 // Output: per vector and 128-atom chunk c, one record of kRecBytes at
-// rec + ((g * Vc + v) * (N/128) + c) * kRecBytes, in 8-byte entries:
-//   entry 0     header: low word = overflow << 31 | count
-//   entries 1.. count candidate keys (0xffffffff - j) | (bits(r_j) << 32), in
-//               atom order (the high word keeps the sign of r_j)
-// A record with more than kRecKeys keys is flagged: the consumer redoes the
-// vector exactly.
-constexpr int kRecEntries = 32;
-constexpr int kRecBytes = kRecEntries * 8;
-constexpr int kRecKeys = kRecEntries - 1;
-__host__ __device__ inline uint32_t rec_header(bool over, int count)
+// rec + ((g * Vc + v) * (N/128) + c) * kRecBytes, in 32-bit words:
+//   word 0      header: overflow << 31 | eb << 16 | k0 << 8 | count
+//   words 1..   count packed keys, those of atoms c*128 + [0, 64) first (k0
+//               of them), then those of c*128 + [64, 128)
+// A packed key holds |r_j| exactly relative to eb, the exponent field of the
+// vector's threshold tau (every kept |r| >= tau >= 2^(eb-127)):
+//   packed = bits(min(|r|, top)) - (eb << 23) + (col << 26),
+//   col = the atom's index within its 64-atom half, top = the float with bits
+//   (eb << 23) + 2^26 - 1 (|r| < 2^(eb-119): eight binades above tau's).  A
+//   key at top may have been clipped, and a record with more than kRecKeys
+//   keys is flagged: the consumer redoes such a vector exactly.
+constexpr int kRecWords = 32;
+constexpr int kRecBytes = kRecWords * 4;
+constexpr int kRecKeys = kRecWords - 1;
+constexpr uint32_t kRecValueMask = (1u << 26) - 1u;
+__host__ __device__ inline uint32_t rec_header(bool over, uint32_t eb, int k0, int count)
 {
-    return (over ? 0x80000000u : 0u) | (uint32_t)count;
+    return (over ? 0x80000000u : 0u) | (eb << 16) | ((uint32_t)k0 << 8) | (uint32_t)count;
 }
 struct ScreenTCArgs {
     int G, N, V, v0, Vc;      // V: vectors per dictionary of the whole call

@@ -17,11 +17,12 @@
 // buffers.  Scores never reach HBM.  The epilogue thread of vector v keeps
 // atom j if |S[v][j]| >= tau_v, tau_v = alpha * ||x_v|| / sqrt(d) with alpha
 // set on the host so that an atom uncorrelated with x_v passes with
-// probability ~1.5n/N.  Each kept score's key (0xffffffff - j) | (bits << 32)
-// is appended to the vector's record of the unit in shared memory: one
-// predicated 8-byte store per score.  After each unit the warp copies its 32
-// records out with 16-byte loads and stores, sixteen lanes on a record: the
-// candidate output lands as whole sectors.  A row with more than kRecKeys kept scores in a unit makes
+// probability ~1.5n/N.  Each kept score becomes a 32-bit packed key (|S|
+// exactly, relative to the exponent of tau_v, and the atom's column; see
+// ScreenTCArgs) appended to the vector's record of the unit in shared
+// memory: one predicated 4-byte store per score.  After each unit the warp
+// copies its 32 records out with 16-byte loads and stores, eight lanes on a
+// record: the candidate output lands as whole sectors.  A row with more than kRecKeys kept scores in a unit makes
 // the consumer redo the vector.
 //
 // Warp roles (384 threads): warp 0 issues TMA loads, warp 1 issues MMAs (one
@@ -38,19 +39,18 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kTileV = 128;        // vectors per tile (MMA M)
 constexpr int kChunk = 128;        // atoms per chunk (MMA N)
-constexpr int kStagesFor(int D) { return D == 64 ? 8 : 4; }   // atom chunk pipeline depth
+constexpr int kStagesFor(int D) { return D == 64 ? 10 : 5; }  // atom chunk pipeline depth
 constexpr int kTmemCols = 512;     // two accumulator buffers (128 columns each), two vector tiles
 constexpr int kAcol = 2 * kChunk;  // first TMEM column of the vector tiles
 constexpr int kEpiWarps = 8;
-// A row's record in shared memory sits in a slot of kRecEntries + 2 entries
-// (272 bytes): consecutive rows start 4 banks apart, so the rows' appends,
+// A row's record in shared memory sits in a slot of kRecWords + 4 words
+// (144 bytes): consecutive rows start 4 banks apart, so the rows' appends,
 // which advance at similar rates, rarely hit the same bank.
-constexpr int kSlotEntries = kRecEntries + 2;
-constexpr int kWarpStageEntries = 32 * kSlotEntries + 32;  // a warp's 32 slots + a guard of 32 entries
-static_assert(kRecEntries >= 32 && kSlotEntries - kRecEntries <= 32,
-              "a row spills at most 32 entries past its record: into the next slot or the guard");
-static_assert(kSlotEntries * 8 % 16 == 0, "slots are read in 16-byte pieces");
-static_assert(kRecBytes % 16 == 0, "records are copied in 16-byte pieces");
+constexpr int kSlotWords = kRecWords + 4;
+constexpr int kWarpStageWords = 32 * kSlotWords + 32;      // a warp's 32 slots + a guard of 32 words
+static_assert(kRecWords >= 32 && kSlotWords - kRecWords <= 32,
+              "a row spills at most 32 words past its record: into the next slot or the guard");
+static_assert(kSlotWords * 4 % 16 == 0 && kRecBytes % 16 == 0, "records are copied in 16-byte pieces");
 
 using namespace tc;
 
@@ -64,7 +64,7 @@ struct SmemLayout {
     static constexpr int kTileBytes = KH * kChunk * 128;       // one 128-row operand tile
     static constexpr int b_off = 0;                            // kStages atom chunks
     static constexpr int s_off = b_off + kStages * kTileBytes; // the epilogue warps' records
-    static constexpr int bar_off = s_off + kEpiWarps * kWarpStageEntries * 8;
+    static constexpr int bar_off = s_off + kEpiWarps * kWarpStageWords * 4;
     static constexpr int n_bars = 2 * kStages + 8;
     static constexpr int taddr_off = bar_off + n_bars * 8;
     static constexpr int total = taddr_off + 16;
@@ -265,11 +265,12 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
         const int q = e & 3;                                // TMEM lane group
         const int hb = e >> 2;                              // accumulator buffer handled
         const int r = q * 32 + lane;                        // TMEM lane = row of the vector tile
-        uint2* const recs = reinterpret_cast<uint2*>(smem + L::s_off) + e * kWarpStageEntries;
-        uint2* const myrec = recs + lane * kSlotEntries;     // entry 0 header, then the keys
+        uint32_t* const recs = reinterpret_cast<uint32_t*>(smem + L::s_off) + e * kWarpStageWords;
+        uint32_t* const myrec = recs + lane * kSlotWords;    // word 0 header, then the keys
         int cur = -1, g = 0, vloc = 0;
         bool valid = false, ok = true;
-        float tau = __int_as_float(0x7fffffff);
+        float tau = __int_as_float(0x7fffffff), top = 0.f;
+        uint32_t eb = 0, nbase = 0;
         UnitCursor uc;
         uc.init(u0 + hb, nch, tiles);
         for (int i = hb; i < nu && ok; i += 2, uc.advance(2)) {
@@ -298,16 +299,21 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
                     }
                     tau = a.alpha * sqrtf(sq * (1.0f / (float)D));
                 }
+                // the key window: tau's exponent field, the largest value kept exactly
+                const uint32_t base_bits = __float_as_uint(tau) & 0x7f800000u;
+                eb = base_bits >> 23;
+                nbase = 0u - base_bits;
+                top = __uint_as_float(base_bits + kRecValueMask);
             }
             const int buf = i & 1;
             ok = mbar_wait(tfull_bar(buf), (uint32_t)(i >> 1) & 1u, status);
             if (!ok) break;
             fence_after();
             const uint32_t tcol = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kChunk);
-            const uint32_t lo0 = 0xffffffffu - (uint32_t)(c * kChunk);
-            int k = 1;                                      // next entry of this row's record
+            int k = 1;                                      // next word of this row's record
+            int k0 = 0;                                     // keys of atoms c*128 + [0, 64)
             bool ovf = false;
-            // one 32-column group: append the keys of the kept scores
+            // one 32-column group: append the packed keys of the kept scores
             auto stage = [&](const uint32_t (&v)[32], int qq) {
                 if (kDump) {
                     if (valid) {
@@ -319,16 +325,18 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
                 }
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
-                    if (fabsf(__uint_as_float(v[t])) >= tau) {
-                        myrec[k] = make_uint2(lo0 - (uint32_t)(qq * 32 + t), v[t]);
+                    const float f = fabsf(__uint_as_float(v[t]));
+                    if (f >= tau) {
+                        myrec[k] = __float_as_uint(fminf(f, top)) + ((uint32_t)((qq & 1) * 32 + t) << 26) + nbase;
                         ++k;
                     }
                 }
-                // a row may run past its record by at most 32 entries (into the
-                // next row's record, or the warp's guard after row 31): flagged
+                // a row may run past its record by at most 32 words (into the
+                // next row's slot, or the warp's guard after row 31): flagged
                 // below
-                ovf |= k > kRecEntries;
-                k = min(k, kRecEntries);
+                ovf |= k > kRecWords;
+                k = min(k, kRecWords);
+                if (qq == 1) k0 = k - 1;
             };
             // TMEM loads double-buffered in registers: group g+1 is in flight
             // while group g is filtered
@@ -356,20 +364,20 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
             const int prev_ovf = __shfl_up_sync(0xffffffffu, ovf ? 1 : 0, 1);   // every lane takes part
             const bool over = ovf || (lane > 0 && prev_ovf != 0);
             const int cnt = k - 1;
-            myrec[0] = make_uint2(rec_header(over, cnt), 0u);
+            myrec[0] = rec_header(over, eb, k0, cnt);
             __syncwarp();
-            // copy the 32 records out: sixteen lanes on a record (16 bytes
-            // each), two records at a time, only the pieces holding entries
-            const int part = lane & 15, rsub = lane >> 4;
-            const int pieces = valid ? (cnt + 2) / 2 : 0;
+            // copy the 32 records out: eight lanes on a record (16 bytes each),
+            // four records at a time, only the pieces holding words
+            const int part = lane & 7, rsub = lane >> 3;
+            const int pieces = valid ? (cnt + 4) / 4 : 0;
             unsigned char* const out = a.rec + ((size_t)g * a.Vc + (size_t)(vloc - lane)) * nch * kRecBytes +
                                        (size_t)c * kRecBytes;
 #pragma unroll
-            for (int it = 0; it < 16; ++it) {
-                const int j = it * 2 + rsub;
+            for (int it = 0; it < 8; ++it) {
+                const int j = it * 4 + rsub;
                 const int pj = __shfl_sync(0xffffffffu, pieces, j);
                 if (part < pj) {
-                    const uint4 w = reinterpret_cast<const uint4*>(recs + j * kSlotEntries)[part];
+                    const uint4 w = reinterpret_cast<const uint4*>(recs + j * kSlotWords)[part];
                     *reinterpret_cast<uint4*>(out + (size_t)j * nch * kRecBytes + part * 16) = w;
                 }
             }

@@ -5,9 +5,9 @@
 // ties go to the lower atom index (a convention of this library).
 //
 // The candidates of a vector arrive as the screening kernel's records: per
-// 128-atom chunk a header and the kept atoms' keys.  A warp gathers them as
-// 64-bit keys (bits(|r_j|) << 32) | (0xffffffff - j) in its slice of shared
-// memory, then:
+// 128-atom chunk a header and the kept atoms' packed keys.  A warp decodes
+// them into 64-bit keys (bits(|r_j|) << 32) | (0xffffffff - j) in its slice
+// of shared memory, then:
 //   1. buckets the keys by |r| on a linear grid of 256 buckets over
 //      [min |r|, max |r|] of the list (monotone in |r|, so every key of a
 //      higher bucket beats every key of a lower one);
@@ -40,34 +40,31 @@ select_kernel(SelectArgs a)
     const int n = a.n;
     int32_t* pool = a.pool + gw * n;
 
-    // the screening records of this vector, 32 at a time: the headers, then
-    // the records' 16-byte pieces in two batches of eight loads (sixteen
-    // lanes on a record, two records per load); record c's keys go to the
-    // sum of the counts of the records before it
+    // the screening records of this vector, 32 at a time: the headers and
+    // every record's 16-byte pieces in one batch of loads (eight lanes on a
+    // record, four records per load); record c's keys go to the sum of the
+    // counts of the records before it, decoded:
+    //   |r| bits = (packed & (2^26 - 1)) + (eb << 23), atom = 128 c + 64 h + (packed >> 26)
+    // with h = 1 for the keys past the record's first k0
     const int nch = a.N / 128;
     const unsigned char* rec = a.rec + (size_t)gw * nch * kRecBytes;
-    const int part = lane & 15, rsub = lane >> 4;
-    const uint32_t lo_min = 0xffffffffu - (uint32_t)(a.N - 1);   // keys of atoms j < N
-    bool bad = false, foreign = false;
+    const int part = lane & 7, rsub = lane >> 3;
+    constexpr int kIt = 8;                  // loads per lane: 32 records x 8 pieces over 32 lanes
+    static_assert(kRecBytes / 16 == 8, "eight lanes cover a record");
+    bool bad = false, clipped = false;
     int gbase = 0;
-    constexpr int kIt = 16;                 // loads per lane: 32 records x 16 pieces over 32 lanes
-    static_assert(kRecBytes / 16 == 16, "sixteen lanes cover a record");
     for (int cg = 0; cg < nch; cg += 32) {
         const int cc = cg + lane;
         const uint32_t h = cc < nch ? __ldg(reinterpret_cast<const uint32_t*>(rec + (size_t)cc * kRecBytes)) : 0u;
-        constexpr int kB = kIt / 2;
-        auto load_batch = [&](int b, uint4 (&w)[kB]) {
+        uint4 w[kIt];
 #pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int j = cg + (b + u) * 2 + rsub;
-                w[u] = j < nch ? __ldg(reinterpret_cast<const uint4*>(rec + (size_t)j * kRecBytes) + part)
-                               : make_uint4(0u, 0u, 0u, 0u);
-            }
-        };
-        uint4 w[kB];
-        load_batch(0, w);                               // in flight with the headers
+        for (int it = 0; it < kIt; ++it) {
+            const int j = cg + it * 4 + rsub;
+            w[it] = j < nch ? __ldg(reinterpret_cast<const uint4*>(rec + (size_t)j * kRecBytes) + part)
+                            : make_uint4(0u, 0u, 0u, 0u);
+        }
         bad |= (h >> 31) != 0u;
-        const int cnt = (int)(h & 0xffffu);
+        const int cnt = (int)(h & 0xffu);
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -75,26 +72,26 @@ select_kernel(SelectArgs a)
             if (lane >= o) incl += t;
         }
         const int off = gbase + incl - cnt;
-        // two batches of eight loads (registers for more resident warps)
 #pragma unroll
-        for (int b = 0; b < kIt; b += kB) {
-            if (b > 0) load_batch(b, w);
+        for (int it = 0; it < kIt; ++it) {
+            const int j = it * 4 + rsub;
+            const uint32_t hj = __shfl_sync(0xffffffffu, h, j);
+            const int oj = __shfl_sync(0xffffffffu, off, j);
+            const int cj = (int)(hj & 0xffu), k0 = (int)((hj >> 8) & 0xffu);
+            const uint32_t ebits = ((hj >> 16) & 0xffu) << 23;
+            const uint32_t jbase = (uint32_t)(cg + j) * 128u;
+            const uint32_t wv[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
 #pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int j = (b + u) * 2 + rsub;
-                const int cj = __shfl_sync(0xffffffffu, cnt, j);
-                const int oj = __shfl_sync(0xffffffffu, off, j);
-                // entries 2*part, 2*part+1 of record j are keys 2*part-1, 2*part
-                // (entry 0 is the header); keys past the buffer are dropped, the
-                // vector then takes the slow path below
-                const int e0 = 2 * part - 1, e1 = 2 * part;
-                if (e0 >= 0 && e0 < cj && oj + e0 < a.cap) {
-                    keys[oj + e0] = ((unsigned long long)(w[u].y & 0x7fffffffu) << 32) | w[u].x;
-                    foreign |= w[u].x < lo_min;
-                }
-                if (e1 < cj && oj + e1 < a.cap) {
-                    keys[oj + e1] = ((unsigned long long)(w[u].w & 0x7fffffffu) << 32) | w[u].z;
-                    foreign |= w[u].z < lo_min;
+            for (int q = 0; q < 4; ++q) {
+                // word 4*part+q of record j is key 4*part+q-1 (word 0 is the
+                // header); keys past the buffer are dropped, the vector then
+                // takes the slow path below
+                const int kk = 4 * part + q - 1;
+                if (kk >= 0 && kk < cj && oj + kk < a.cap) {
+                    const uint32_t val = wv[q] & kRecValueMask;
+                    clipped |= val == kRecValueMask;
+                    const uint32_t atom = jbase + (kk >= k0 ? 64u : 0u) + (wv[q] >> 26);
+                    keys[oj + kk] = ((unsigned long long)(val + ebits) << 32) | (0xffffffffu - atom);
                 }
             }
         }
@@ -107,9 +104,9 @@ select_kernel(SelectArgs a)
             *a.slow_seq = a.seq;                       // every writer stores the same value
         }
     };
-    // an overflowed record, too few or too many keys, or an atom index
-    // outside the dictionary (only a damaged record has one): the slow path
-    if (__any_sync(0xffffffffu, bad || foreign) || K < n || K > a.cap) {
+    // an overflowed record, a key that may have been clipped at the top of its
+    // window, too few or too many keys: the slow path
+    if (__any_sync(0xffffffffu, bad || clipped) || K < n || K > a.cap) {
         slow();
         return;
     }
