@@ -148,6 +148,37 @@ def test_more_candidates_than_the_selection_holds():
     PU.assert_encode_ok(PU.compare_encode(res, idx, coef, rel, pool, p, A, x[0]))
 
 
+def test_score_beyond_the_key_window():
+    """A dictionary with one atom 300 times longer than the others: the
+    vector along it scores far more than eight binades above its threshold,
+    so its packed key is clipped and the selection hands the vector to the
+    exact slow path; an ordinary vector beside it is not.  Pools and codes
+    match the oracle."""
+    d, N, n, s = 128, 4096, 256, 8
+    g = np.random.default_rng(14)
+    A = g.standard_normal((N, d))
+    A /= np.linalg.norm(A, axis=1, keepdims=True)
+    A[777] *= 300.0
+    A = A.astype(np.float16)
+    x = np.empty((1, 2, d), np.float16)
+    x[0, 0] = (A[777].astype(np.float64) / 300.0 + 0.05 * g.standard_normal(d) / np.sqrt(d)).astype(np.float16)
+    x[0, 1] = S.make_sparse_inputs(A[:700], 1, s, 8)[0]
+    D = _dict(A[None], np.ones((1, N), np.int32), [0.5], n, s, 2)
+    pool = D.pool(_t(x))[0].cpu().numpy()[0]
+    c = D.new_codes(2)
+    D.encode(_t(x), c)
+    torch.cuda.synchronize()
+    assert D.stats()[0]["topn_slow_path"] == 2             # vector 0 in pool() and in encode()
+    p = O.Params(N, d, n, s)
+    res = O.encode(p, A, x[0])
+    ok = ~PU.exempt_mask(res)
+    for v in range(2):
+        if ok[v]:
+            assert np.array_equal(np.sort(pool[v]), np.sort(res.pool[v])), v
+    idx, coef, rel = (t.cpu().numpy()[0] for t in (c.idx, c.coef, c.relres))
+    PU.assert_encode_ok(PU.compare_encode(res, idx, coef, rel, pool, p, A, x[0]))
+
+
 @pytest.mark.parametrize("name,G,V", [("decode_3b", 3, 200), ("decode_8b", 2, 64)])
 def test_greedy_kernels_agree(monkeypatch, name, G, V):
     """The greedy kernels all match the oracle: the correlation-domain kernel
