@@ -72,8 +72,10 @@ __device__ __forceinline__ const uint4* prow_chunk(const __half* prow, int D, in
 
 // RT: m16 tiles per warp whose A fragments stay in registers (2: all; 1:
 // the second tile is read from the shared copy at every pass, which frees
-// the registers for three CTAs per SM).
-template <int D, int NW, int SMAX, int RT>
+// the registers for three CTAs per SM).  FIXED: s == SMAX, known at compile
+// time, so the pick loop unrolls and every index into the per-slot factor
+// row is a constant.
+template <int D, int NW, int SMAX, int RT, bool FIXED>
 __global__ void __launch_bounds__(NW * 32, NW <= 8 ? (RT == 2 ? 2 : 3) : 1)
 greedy_chol_kernel(Shape sh, GreedyArgs a)
 {
@@ -85,7 +87,7 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     const int v = a.v0 + vc;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, t4 = lane & 3;
-    const int n = sh.n, s = sh.s, N = sh.N;
+    const int n = sh.n, s = FIXED ? SMAX : sh.s, N = sh.N;
 
     __shared__ float xs[D];
     __shared__ int pid[NPAD];
@@ -295,6 +297,7 @@ greedy_chol_kernel(Shape sh, GreedyArgs a)
     __syncthreads();
 
     const float la = sh.lambda_abs, lr = sh.lambda_rel;
+#pragma unroll (FIXED ? SMAX : 1)
     for (int k = 0; k < s; ++k) {
         // ---- the pick: best of the warps' bests (lane w reads warp w's key) ----
         const int par = k & 1;
@@ -409,7 +412,7 @@ template <int D, int NW, int SMAX, int RT>
 cudaError_t launch_rt(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 {
     const size_t smem = (size_t)NW * kMT * 16 * D * 2;
-    auto k = greedy_chol_kernel<D, NW, SMAX, RT>;
+    auto k = sh.s == SMAX ? greedy_chol_kernel<D, NW, SMAX, RT, true> : greedy_chol_kernel<D, NW, SMAX, RT, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Vc, sh.G);
