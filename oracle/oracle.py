@@ -97,6 +97,9 @@ def load(path: str):
     L.oracle_greedy_on_pool.argtypes = [P(_Params), C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p,
                                         C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
     L.oracle_greedy_on_pool.restype = C.c_int
+    L.oracle_encode_pl.argtypes = [P(_Params), C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p,
+                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+    L.oracle_encode_pl.restype = C.c_int
     L.oracle_half_to_double.argtypes = [C.c_uint16]
     L.oracle_half_to_double.restype = C.c_double
     L.oracle_double_to_half.argtypes = [C.c_double]
@@ -123,7 +126,7 @@ class Variant:
         import types
         mod = globals()
         for name in ("encode", "adapt", "reconstruct", "half_to_double", "double_to_half",
-                     "encode_threaded", "greedy_on_pool"):
+                     "encode_threaded", "greedy_on_pool", "encode_pl"):
             fn = mod[name]
             setattr(self, name, types.FunctionType(fn.__code__, dict(mod, lib=lambda: self._L),
                                                    fn.__name__, fn.__defaults__, fn.__closure__))
@@ -191,6 +194,28 @@ def greedy_on_pool(p: Params, atoms: np.ndarray, x: np.ndarray, pool: np.ndarray
     if rc != 0:
         raise RuntimeError(f"oracle_greedy_on_pool failed: {rc}")
     return EncodeResult(idx, coef, rel, pool, np.full(V, np.nan), gap, 0)
+
+
+def encode_pl(p: Params, atoms: np.ndarray, x: np.ndarray) -> EncodeResult:
+    """PL encode of the rows of ``x``: the s atoms of largest |r| (ties to
+    the lower index), in ascending atom order, and one ridge fit over them.
+    ``cut_gap`` is the relative margin of the Top-s cut; pool and pick_gap
+    of the result are empty."""
+    _check_store(atoms, p, "atoms")
+    _check_store(x, p, "x")
+    V = x.shape[0]
+    idx = np.empty((V, p.s), np.int32)
+    coef = np.empty((V, p.s), np.float64)
+    rel = np.empty(V, np.float64)
+    cut = np.empty(V, np.float64)
+    macs = C.c_int64(0)
+    pc = p.c()
+    rc = lib().oracle_encode_pl(C.byref(pc), _ptr(atoms), _ptr(x), V, _ptr(idx), _ptr(coef),
+                                _ptr(rel), _ptr(cut), C.addressof(macs))
+    if rc != 0:
+        raise RuntimeError(f"oracle_encode_pl failed: {rc}")
+    return EncodeResult(idx, coef, rel, np.empty((V, 0), np.int32), cut,
+                        np.empty((V, 0), np.float64), int(macs.value))
 
 
 def encode_threaded(p: Params, atoms: np.ndarray, x: np.ndarray, threads: int) -> EncodeResult:

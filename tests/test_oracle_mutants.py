@@ -37,6 +37,10 @@ MUTANTS = [
     ("reconstruct drops replacement", "acc += repl_coef[v] * load_elem", "acc += 0.0 * load_elem"),
     ("half rounding truncates", "double q = nearbyint(ldexp(a, 10 - E));", "double q = floor(ldexp(a, 10 - E));"),
     ("half subnormal scale", "v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    ("PL takes ranks 1..s", "for (int k = 0; k < s; ++k) S[k] = rk[k].id;", "for (int k = 0; k < s; ++k) S[k] = rk[k + 1].id;"),
+    ("PL ids left in rank order", "qsort(S, (size_t)s, sizeof(int32_t), cmp_i32);", ";"),
+    ("PL residual drops the last atom", "for (int k = 0; k < s; ++k)\n                acc -= c[k]", "for (int k = 0; k + 1 < s; ++k)\n                acc -= c[k]"),
+    ("PL relres squared norm", "sqrt(en2) / xn", "en2 / xn"),
 ]
 
 PIN_TESTS = [
@@ -55,6 +59,12 @@ PIN_TESTS = [
     pins.test_adapt_golden_cases,
     pins.test_adapt_invariants_random,
     pins.test_reconstruct_consistency,
+    pins.test_table4_pl_cost_reproduced_by_operation_count,
+    pins.test_pl_weighted_orthogonal_closed_form,
+    lambda O: pins.test_pl_with_one_atom_is_the_first_greedy_pick(O, pins.np.float32),
+    pins.test_pl_is_greedy_over_a_pool_of_s,
+    pins.test_pl_fit_matches_normal_equations,
+    pins.test_pl_zero_and_nonfinite_inputs,
 ]
 
 

@@ -330,6 +330,126 @@ def test_zero_and_nonfinite_inputs(oracle_lib):
 
 
 # --------------------------------------------------------------------------
+# PL encode: screening + one ridge fit (the PL rows of Tables 1-4)
+# --------------------------------------------------------------------------
+
+def test_table4_pl_cost_reproduced_by_operation_count(oracle_lib):
+    """Table 4 prints Cost 0.13 for PL.  Screening (N d) plus one fit over
+    s atoms (s(s+1)/2 Gram entries, s right-hand sides, s residual terms,
+    each d long), against the oracle's count for OMP over the whole
+    dictionary, must give that to two decimals."""
+    O = oracle_lib
+    g = _golden("table4_cost.json")
+    sh = g["shape"]
+    N, d, n, s = sh["N"], sh["d"], sh["n"], sh["s"]
+    p = O.Params(N, d, n, s)
+    D = S.make_dictionary(N, d, np.float16, 11)
+    x = S.make_sparse_inputs(D, 3, s, 12)
+    pl = O.encode_pl(p, D, x)
+    omp = O.encode(p, D, x, full_omp=True)
+    assert round(pl.macs / omp.macs, 2) == g["PL"]
+    assert pl.macs == 3 * (N * d + (s * (s + 1) // 2 + 2 * s) * d)
+
+
+def test_pl_weighted_orthogonal_closed_form(oracle_lib):
+    """Orthogonal atoms w_j e_j: r_j = w_j x_j, the fit decouples into
+    c_j = r_j / (w_j^2 (1 + lambda_rel) + lambda_abs), and the residual is
+    known exactly.  The support holds a tie in |r| at the Top-s cut (atoms
+    11 and 27, |r| = 2 each), which the lower id must win; idx comes out in
+    ascending atom order."""
+    O = oracle_lib
+    d = N = 32
+    w = np.array([0.5, 1.0, 2.0, 1.5] * 8)
+    D = np.diag(w).astype(np.float32)
+    # |r_j| = |x_j| w_j: 3 (atom 6), 2 (atoms 11, 27), 4.5 (atom 15),
+    # 1.5 (atom 20), 1 (atom 2), 6 (atom 30)
+    x = np.zeros(d)
+    for j, r in [(6, -3.0), (11, 2.0), (27, -2.0), (15, 4.5), (20, -1.5), (2, 1.0), (30, 6.0)]:
+        x[j] = r / w[j]
+    x32 = x.astype(np.float32)[None]
+    x = x32[0].astype(np.float64)                  # the stored values, exactly
+    s = 4
+    r = O.encode_pl(O.Params(N, d, 8, s, dtype=O.F32), D, x32)
+    assert list(r.idx[0]) == [6, 11, 15, 30]
+    e = x.copy()
+    for k, j in enumerate(r.idx[0]):
+        rj = w[j] * x[j]
+        assert r.coef[0, k] == pytest.approx(rj / (w[j] ** 2 * (1 + LR) + LA), rel=1e-13)
+        e[j] -= r.coef[0, k] * w[j]
+    assert r.relres[0] == pytest.approx(np.linalg.norm(e) / np.linalg.norm(x), rel=1e-13)
+    assert r.cut_gap[0] == 0.0                     # |r|_(4) = |r|_(5) = 2
+
+
+@pytest.mark.parametrize("dt", [np.float16, np.float32])
+def test_pl_with_one_atom_is_the_first_greedy_pick(oracle_lib, dt):
+    """With s = 1 the greedy coder's only pick is the atom of largest |r|
+    and its refit is the same one-atom fit: PL and GM agree bit for bit."""
+    O = oracle_lib
+    N, d = 512, 64
+    kind = O.F16 if dt == np.float16 else O.F32
+    D = S.make_dictionary(N, d, dt, 31)
+    x = S.make_sparse_inputs(D, 40, 3, 32, dtype=dt)
+    p = O.Params(N, d, 16, 1, dtype=kind)
+    pl = O.encode_pl(p, D, x)
+    gm = O.encode(p, D, x)
+    assert (pl.idx == gm.idx).all()
+    assert (pl.coef == gm.coef).all() and (pl.relres == gm.relres).all()
+
+
+def test_pl_is_greedy_over_a_pool_of_s(oracle_lib):
+    """A greedy coder whose pool holds exactly s atoms picks all of them, and
+    its last refit is the ridge fit over that pool: PL gives the same set,
+    the same coefficients per atom and the same relres (up to rounding
+    order)."""
+    O = oracle_lib
+    N, d, s = 1024, 128, 8
+    D = S.make_dictionary(N, d, np.float16, 41)
+    x = S.make_sparse_inputs(D, 30, s, 42)
+    p = O.Params(N, d, s, s)
+    pl = O.encode_pl(p, D, x)
+    gm = O.encode(p, D, x)
+    for v in range(x.shape[0]):
+        assert list(pl.idx[v]) == sorted(gm.idx[v])
+        order = np.argsort(gm.idx[v])
+        np.testing.assert_allclose(pl.coef[v], gm.coef[v][order], rtol=1e-11, atol=1e-13)
+        assert pl.relres[v] == pytest.approx(gm.relres[v], rel=1e-11)
+        # the cut is the one the greedy coder's pool was cut at
+        assert pl.cut_gap[v] == gm.cut_gap[v]
+
+
+def test_pl_fit_matches_normal_equations(oracle_lib):
+    """The fit on the Top-s set against numpy's solve of the same normal
+    equations, with the Top-s set from a full stable sort."""
+    O = oracle_lib
+    N, d, s = 512, 64, 6
+    D = S.make_dictionary(N, d, np.float32, 51)
+    x = S.make_sparse_inputs(D, 25, 4, 52, dtype=np.float32)
+    r = O.encode_pl(O.Params(N, d, 32, s, dtype=O.F32), D, x)
+    R = x.astype(np.float64) @ D.astype(np.float64).T
+    for v in range(x.shape[0]):
+        top = np.sort(np.lexsort((np.arange(N), -np.abs(R[v])))[:s])
+        assert list(r.idx[v]) == list(top)
+        c = _ridge_closed_form(D, top, x[v])
+        np.testing.assert_allclose(r.coef[v], c, rtol=1e-9, atol=1e-12)
+        e = x[v].astype(np.float64) - c @ D[top].astype(np.float64)
+        xn = np.linalg.norm(x[v].astype(np.float64))
+        assert r.relres[v] == pytest.approx(np.linalg.norm(e) / xn, rel=1e-9)
+
+
+def test_pl_zero_and_nonfinite_inputs(oracle_lib):
+    O = oracle_lib
+    p = O.Params(512, 64, 32, 4, dtype=O.F32)
+    D = S.make_dictionary(512, 64, np.float32, 0)
+    x = np.zeros((3, 64), np.float32)
+    x[1, 5] = np.nan
+    x[2, 9] = -np.inf
+    r = O.encode_pl(p, D, x)
+    assert list(r.idx[0]) == [0, 1, 2, 3] and (r.coef[0] == 0).all() and r.relres[0] == 0
+    for v in (1, 2):
+        assert (r.idx[v] == -1).all() and (r.coef[v] == 0).all() and math.isnan(r.relres[v])
+
+
+# --------------------------------------------------------------------------
 # adapt: hand-derived cases and invariants
 # --------------------------------------------------------------------------
 
