@@ -8,7 +8,10 @@ pool, greedy + ridge), fixed-size adaptation and sparse reconstruction,
 through the C ABI.  Inputs are synthetic (seeded sparse mixtures, see
 dictionary_sparse_kv_gb300/synthetic.py).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--coder gm|pl]
+
+--coder pl times the PL coder instead (the Top-s atoms and one ridge fit in
+place of the greedy selection; Tables 1-4's "PL" rows).
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its
 own 56 dictionaries (weak scaling, no collective on the data path); the time
@@ -32,6 +35,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "KV vectors encoded/s at N=4096,d=128,n=256,s=8; % HBM / tensor-pipe roofline"
+METRIC_PL = "KV vectors encoded/s, PL coder (Top-s + one ridge fit) at N=4096,d=128,s=8; % HBM roofline"
 UNIT = "vectors/s"
 WORKLOAD = "decode_3b"
 L2_FLUSH_BYTES = 256 << 20           # twice the 129 MB L2
@@ -47,6 +51,7 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--coder", choices=["gm", "pl"], default="gm")
     return ap.parse_args(argv)
 
 
@@ -55,8 +60,9 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def workload_config(w, vectors_per_step):
+def workload_config(w, vectors_per_step, coder="gm"):
     return {
+        "coder": "greedy in the Top-n pool + ridge refit" if coder == "gm" else "PL: Top-s + one ridge fit",
         "workload": f"{w.name}: {w.G} dictionaries (layers x K,V), N={w.N}, d={w.d}, n={w.n}, s={w.s}, "
                     f"{w.V} vectors per dictionary per step (8 KV heads x {w.V // 8} sequences)",
         "vectors_per_step": vectors_per_step,
@@ -138,7 +144,7 @@ class ClockSampler:
 # algorithmic work per kernel launch (the roofline numerators)
 # --------------------------------------------------------------------------
 
-def kernel_work(w, kernel: str, vectors: int):
+def kernel_work(w, kernel: str, vectors: int, coder: str = "gm"):
     """(bound, algorithmic units per launch, unit) for one launch that covers
     `vectors` vectors of every dictionary (G * vectors vectors in total).
     Per-vector figures: screening streams the dictionary once per launch plus
@@ -151,7 +157,11 @@ def kernel_work(w, kernel: str, vectors: int):
         return "hbm", float(G * N * d * esz + nv * d * esz), "GB/s"
     if kernel == "topn":
         # candidate keys in (about 2n per vector, 8 B each) and the pool out
-        return "hbm", (8.0 * 2 * n + 4.0 * n) * nv, "GB/s"
+        # (n ids; s for the PL coder)
+        return "hbm", (8.0 * 2 * n + 4.0 * (s if coder == "pl" else n)) * nv, "GB/s"
+    if kernel == "greedy" and coder == "pl":
+        # the fit: the s rows and x in, ids, coefficients and relres out
+        return "hbm", ((s + 1) * d * esz + 8.0 * s + 4.0) * nv, "GB/s"
     if kernel == "greedy":
         return "tensor", 2.0 * (s - 1) * n * d * nv, "TFLOP/s"
     if kernel == "adapt":
@@ -175,24 +185,26 @@ def greedy_source() -> str:
     return {"tc": "k_greedy_tc.cu", "ffma": "k_greedy.cu", "mma": "k_greedy_mma.cu"}.get(f, "k_greedy_chol.cu")
 
 
-def kernel_files():
+def kernel_files(coder: str = "gm"):
     """Source file of each kernel class on the binary16 path the bench runs."""
-    return {"screen": "k_screen_tc.cu", "topn": "k_select.cu", "greedy": greedy_source(),
+    return {"screen": "k_screen_tc.cu", "topn": "k_select.cu",
+            "greedy": "k_pl.cu" if coder == "pl" else greedy_source(),
             "adapt": "k_adapt_reconstruct.cu", "reconstruct": "k_adapt_reconstruct.cu"}
 
 
-def traffic_for(kernel: str, w):
+def traffic_for(kernel: str, w, coder: str = "gm"):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of that kernel (profiles/traffic.json)."""
+    the current source of that kernel (profiles/traffic.json; the PL coder's
+    entries sit under "<workload>+pl")."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         tab = json.load(f)
-    ent = tab.get(w.name, {}).get(kernel)
+    ent = tab.get(w.name + ("+pl" if coder == "pl" else ""), {}).get(kernel)
     if not ent:
         return None
-    src = kernel_sources().get(kernel_files().get(kernel, ""), None)
+    src = kernel_sources().get(kernel_files(coder).get(kernel, ""), None)
     if ent.get("source_sha256_16") != src:
         return None
     return ent.get("dram_bytes_per_launch")
@@ -203,7 +215,7 @@ def dominant_kernel(prof):
     return max(prof, key=lambda k: prof[k][1]) if prof else None
 
 
-def roofline(w, prof, timed, vectors_per_launch, peaks, peak_kind, sm_count, sm_mhz_max):
+def roofline(w, prof, timed, vectors_per_launch, peaks, peak_kind, sm_count, sm_mhz_max, coder="gm"):
     """Roofline object for the kernel with the largest share of device time
     (shares from `prof`, a pass with every launch bracketed; the kernel's
     launch duration from `timed`, the timed region, where only it is)."""
@@ -215,7 +227,7 @@ def roofline(w, prof, timed, vectors_per_launch, peaks, peak_kind, sm_count, sm_
     for k, (n_l, ms) in prof.items():
         shares[k] = {"launches": n_l, "ms_total": round(ms, 4), "share": round(ms / tot, 4)}
     n_launch, ms = timed[kern] if timed.get(kern, (0, 0.0))[1] > 0 else prof[kern]
-    bound, work, unit = kernel_work(w, kern, vectors_per_launch)
+    bound, work, unit = kernel_work(w, kern, vectors_per_launch, coder)
     sec = ms / 1e3 / n_launch
     if unit == "GB/s":
         achieved = work / sec / 1e9
@@ -232,8 +244,9 @@ def roofline(w, prof, timed, vectors_per_launch, peaks, peak_kind, sm_count, sm_
             # nominal rate as fp16), burst figure for a kernel timed per launch
             peak = peaks["bf16_tflops"]
             pk = f"bf16_tflops ({peak_kind}, burst; fp16 at the same nominal rate)"
-    obj = {"kernel": kern, "source": kernel_files().get(kern), "bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": unit,
-           "frac": round(achieved / peak, 4), "traffic": traffic_for(kern, w), "peak_source": pk,
+    obj = {"kernel": kern, "source": kernel_files(coder).get(kern), "bound": bound, "achieved": round(achieved, 3),
+           "peak": round(peak, 3), "unit": unit, "frac": round(achieved / peak, 4),
+           "traffic": traffic_for(kern, w, coder), "peak_source": pk,
            "launch_ms": round(ms / n_launch, 5)}
     return obj, shares
 
@@ -242,7 +255,7 @@ def roofline(w, prof, timed, vectors_per_launch, peaks, peak_kind, sm_count, sm_
 # oracle timing (CPU baseline and the reference arm)
 # --------------------------------------------------------------------------
 
-def oracle_steps(w, data, steps, threads):
+def oracle_steps(w, data, steps, threads, coder="gm"):
     """Run the oracle over `steps` decode steps of every dictionary of `data`
     (encode on `threads` host threads, then the sequential adapt and
     reconstruct).  Returns
@@ -258,7 +271,7 @@ def oracle_steps(w, data, steps, threads):
     for t in range(steps):
         x = xs[t]
         for g in range(len(data.dicts)):
-            r = O.encode_threaded(p, atoms[g], x[g], threads)
+            r = O.encode_threaded(p, atoms[g], x[g], threads, coder)
             a = O.adapt(p, atoms[g], usage[g], x[g], r.idx, r.coef, r.relres, data.deltas()[g])
             O.reconstruct(p, atoms[g], r.idx, r.coef, a.repl_id, a.repl_coef)
             nvec += x.shape[1]
@@ -293,14 +306,14 @@ def run_reference(args):
     data = S.WorkloadData(w)
     threads = os.cpu_count() or 1
     # warm-up steps, then K timed steps; each step is one full decode step
-    oracle_steps(w, data, max(0, min(args.warmup, 1)), threads)
-    nvec, sec = oracle_steps(w, data, args.steps, threads)
+    oracle_steps(w, data, max(0, min(args.warmup, 1)), threads, args.coder)
+    nvec, sec = oracle_steps(w, data, args.steps, threads, args.coder)
     value = nvec / sec
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_PL if args.coder == "pl" else METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, w.G * w.V),
+        "config": workload_config(w, w.G * w.V, args.coder),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{args.steps} full decode steps ({w.G} x {w.V} vectors each), "
                                    f"plain C double-precision oracle, encode split over {threads} host "
@@ -375,7 +388,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     for t in range(W):
-        D.step(xs_dev[t], codes, xhat)
+        D.step(xs_dev[t], codes, xhat, coder=args.coder)
     torch.cuda.synchronize(dev)
     F.profile_read(D.h, reset=True)
 
@@ -383,7 +396,7 @@ def run_ours(args):
     F.profile_enable(D.h, True)
     for t in range(min(K, 10)):
         flush.fill_(float(t))
-        D.step(xs_dev[W + t], codes, xhat)
+        D.step(xs_dev[W + t], codes, xhat, coder=args.coder)
     torch.cuda.synchronize(dev)
     F.profile_enable(D.h, False)
     prof_all = F.profile_read(D.h, reset=True)
@@ -404,7 +417,7 @@ def run_ours(args):
     for t in range(K):
         flush.fill_(float(t))
         ev[t][0].record(stream)
-        D.step(xs_dev[W + t], codes, xhat)
+        D.step(xs_dev[W + t], codes, xhat, coder=args.coder)
         ev[t][1].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -429,7 +442,7 @@ def run_ours(args):
         flush.fill_(float(t))
         ev2[t][0].record(stream)
         xin.copy_(xs_host[W + t], non_blocking=True)
-        D.step(xin, codes, xhat)
+        D.step(xin, codes, xhat, coder=args.coder)
         for o, c in zip(outs, (codes.idx, codes.coef, codes.relres, codes.repl_id, codes.repl_coef)):
             o.copy_(c, non_blocking=True)
         ev2[t][1].record(stream)
@@ -447,20 +460,22 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
     props = torch.cuda.get_device_properties(dev)
     sm_max = float(peaks.get("sm_max_mhz") or clk.get("sm_max_mhz") or 2070.0)
-    roof, shares = roofline(w, prof_all, prof, V, peaks, peak_kind, props.multi_processor_count, sm_max)
+    roof, shares = roofline(w, prof_all, prof, V, peaks, peak_kind, props.multi_processor_count, sm_max,
+                            args.coder)
 
     cpu = None
     if not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         sub = S.WorkloadData(w)
-        nvec, sec = oracle_steps(w, sub, 2, threads)
+        nvec, sec = oracle_steps(w, sub, 2, threads, args.coder)
         cpu = {"value": round(nvec / sec, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"first 2 decode steps of all {w.G} dictionaries ({nvec} vectors), oracle encode "
                          f"over {threads} host threads + sequential adapt; CPU: {cpu_model()}"}
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "metric": METRIC_PL if args.coder == "pl" else METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(dev_ms / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic", "config": workload_config(w, vectors_per_step),
+        "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, vectors_per_step, args.coder),
         "e2e": {"value": round(e2e, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches, "roofline": roof, "kernels": shares, "clocks": clk, "cpu_baseline": cpu,
         "wall_s_timed": round(wall, 4),

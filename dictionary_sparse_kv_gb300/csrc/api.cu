@@ -226,7 +226,10 @@ int* cand_count_buf(fadkv_dict h) { return (int*)(h->ws + h->L.cand_count); }
 // (tensor-core path) or the exact Top-n keys (FP32 path).  With `dump` set,
 // writes all scores [G][Vc][N] instead (test hook).
 
-cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, float* dump, cudaStream_t st)
+// n_sel: the pool size to select (the handle's n for the greedy coder, s
+// for the PL fit).
+cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, float* dump, cudaStream_t st,
+                       int n_sel)
 {
     cudaError_t e = ensure_device_info(h);
     if (e != cudaSuccess) return e;
@@ -248,7 +251,7 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
         sa.G = h->p.num_dicts;
         sa.Vc = Vc;
         sa.N = h->p.N;
-        sa.n = h->p.n;
+        sa.n = n_sel;
         sa.cap = select_cap(h->p.n);
         sa.rec = h->ws + h->L.cand;
         sa.pool = (int32_t*)(h->ws + h->L.pool);
@@ -262,8 +265,10 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
         return launch_screen_ffma(h->sh, h->atoms, x, (int64_t)V * h->p.d, v0, Vc, scores, st);
     });
     if (e != cudaSuccess || dump) return e;
+    Shape sh = h->sh;
+    sh.n = n_sel;
     return traced(h, FADKV_K_TOPN, st, [&] {
-        return launch_topn_radix(h->sh, scores, Vc, cand_buf(h), cand_count_buf(h), h->L.cap, st);
+        return launch_topn_radix(sh, scores, Vc, cand_buf(h), cand_count_buf(h), h->L.cap, st);
     });
 }
 
@@ -444,7 +449,7 @@ fadkv_status fadkv_encode(fadkv_dict h, const void* x, int32_t V, int32_t* idx, 
     const int chunk = h->L.chunk;
     for (int v0 = 0; v0 < V; v0 += chunk) {
         const int Vc = (V - v0 < chunk) ? V - v0 : chunk;
-        cudaError_t e = run_screen(h, x, V, v0, Vc, nullptr, st);
+        cudaError_t e = run_screen(h, x, V, v0, Vc, nullptr, st, h->p.n);
         const GreedyPath gp = greedy_path(h);
         if (e == cudaSuccess && gp != GreedyPath::kClassic) {
             int32_t* pool = (int32_t*)(h->ws + h->L.pool);
@@ -480,6 +485,59 @@ fadkv_status fadkv_encode(fadkv_dict h, const void* x, int32_t V, int32_t* idx, 
         }
         if (e != cudaSuccess) {
             set_error("fadkv_encode", e);
+            return FADKV_ERR_CUDA;
+        }
+    }
+    h->pending = true;
+    h->pending_V = V;
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_encode_pl(fadkv_dict h, const void* x, int32_t V, int32_t* idx, float* coef,
+                             float* relres, void* stream)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    if (V < 0 || V > h->p.max_batch) return FADKV_ERR_INVALID_ARG;
+    if (V > 0 && (!x || !idx || !coef || !relres)) return FADKV_ERR_INVALID_ARG;
+    if (V > 0 && (!aligned(x, 16) || !aligned(idx, 4) || !aligned(coef, 4) || !aligned(relres, 4)))
+        return FADKV_ERR_INVALID_ARG;
+    if (h->pending) return FADKV_ERR_SEQUENCE;
+    if (fault_injected()) {
+        set_error("fadkv_encode_pl", cudaErrorLaunchFailure);
+        return FADKV_ERR_CUDA;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    Shape sh = h->sh;
+    sh.n = h->p.s;                                     // the Top-s set
+    const int chunk = h->L.chunk;
+    for (int v0 = 0; v0 < V; v0 += chunk) {
+        const int Vc = (V - v0 < chunk) ? V - v0 : chunk;
+        cudaError_t e = run_screen(h, x, V, v0, Vc, nullptr, st, h->p.s);
+        PlArgs pa;
+        pa.atoms = h->atoms;
+        pa.x = x;
+        pa.pool = nullptr;
+        pa.cand = cand_buf(h);
+        pa.cand_count = cand_count_buf(h);
+        pa.cap = h->L.cap;
+        pa.idx = idx;
+        pa.coef = coef;
+        pa.relres = relres;
+        pa.counters = counters(h);
+        pa.V = V;
+        pa.v0 = v0;
+        pa.Vc = Vc;
+        if (e == cudaSuccess && h->L.tc) {
+            int32_t* pool = (int32_t*)(h->ws + h->L.pool);
+            GreedyArgs fa = greedy_args(h, x, V, v0, Vc);
+            e = traced(h, FADKV_K_TOPN, st, [&] {
+                return launch_pool_fixup(sh, fa, pool, (const uint32_t*)(h->ws + h->L.slow), h->seq, h->sms, st);
+            });
+            pa.pool = pool;
+        }
+        if (e == cudaSuccess) e = traced(h, FADKV_K_GREEDY, st, [&] { return launch_pl_fit(h->sh, pa, st); });
+        if (e != cudaSuccess) {
+            set_error("fadkv_encode_pl", e);
             return FADKV_ERR_CUDA;
         }
     }
@@ -576,7 +634,7 @@ fadkv_status fadkv_debug_pool(fadkv_dict h, const void* x, int32_t V, int32_t* p
     const int chunk = h->L.chunk;
     for (int v0 = 0; v0 < V; v0 += chunk) {
         const int Vc = (V - v0 < chunk) ? V - v0 : chunk;
-        cudaError_t e = run_screen(h, x, V, v0, Vc, nullptr, st);
+        cudaError_t e = run_screen(h, x, V, v0, Vc, nullptr, st, h->p.n);
         if (e == cudaSuccess) {
             GreedyArgs a = greedy_args(h, x, V, v0, Vc);
             a.pool_out = pool;
@@ -602,7 +660,7 @@ fadkv_status fadkv_debug_scores(fadkv_dict h, const void* x, int32_t V, float* s
         return FADKV_ERR_CUDA;
     }
     if (V == 0) return FADKV_OK;
-    const cudaError_t e = run_screen(h, x, V, 0, V, scores, (cudaStream_t)stream);
+    const cudaError_t e = run_screen(h, x, V, 0, V, scores, (cudaStream_t)stream, h->p.n);
     if (e != cudaSuccess) {
         set_error("fadkv_debug_scores", e);
         return FADKV_ERR_CUDA;

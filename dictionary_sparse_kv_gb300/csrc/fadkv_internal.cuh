@@ -232,6 +232,27 @@ cudaError_t launch_greedy_chol(const Shape& sh, const GreedyArgs& a, cudaStream_
 cudaError_t launch_pool_fixup(const Shape& sh, const GreedyArgs& a, int32_t* pool, const uint32_t* slow_seq,
                               uint32_t seq, int sms, cudaStream_t st);
 
+// PL encode's fit: the s atoms of the Top-s set in ascending order and one
+// ridge fit over them, one warp per vector.  The set comes from `pool`
+// ([G][Vc][s] ids in any order; the selection + pool fixup with n = s) or,
+// when pool is null, from the FP32 path's candidate keys (cand, cand_count,
+// cap; the radix Top-n with n = s writes them in ascending atom order).
+struct PlArgs {
+    const void* atoms;
+    const void* x;
+    const int32_t* pool;
+    const unsigned long long* cand;
+    const int* cand_count;
+    int cap;
+    int32_t* idx;
+    float* coef;
+    float* relres;
+    long long* counters;      // [G][kCntFields]
+    int V;                    // vectors per dictionary in the whole call
+    int v0, Vc;
+};
+cudaError_t launch_pl_fit(const Shape& sh, const PlArgs& a, cudaStream_t st);
+
 // Fixed-size adaptation, one CTA per dictionary.
 struct AdaptArgs {
     void* atoms;

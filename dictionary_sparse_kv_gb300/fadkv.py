@@ -73,6 +73,8 @@ _SIGS = {
     "fadkv_dict_destroy": ([C.c_void_p], C.c_int),
     "fadkv_encode": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p],
                      C.c_int),
+    "fadkv_encode_pl": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p],
+                     C.c_int),
     "fadkv_adapt": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                      C.c_void_p, C.c_void_p], C.c_int),
     "fadkv_adapt_noalloc": ([C.POINTER(Params), C.c_void_p, C.c_void_p, C.POINTER(C.c_float), C.c_void_p,
@@ -163,6 +165,12 @@ def dict_destroy(h: int) -> None:
 def encode(h: int, x, V: int, idx, coef, relres, stream=None) -> None:
     st = _stream(stream, x, idx)
     _check("fadkv_encode", lib().fadkv_encode(h, _addr(x), V, _addr(idx), _addr(coef), _addr(relres), st))
+
+
+def encode_pl(h: int, x, V: int, idx, coef, relres, stream=None) -> None:
+    """PL encode: Top-s atoms (ascending ids) and one ridge fit."""
+    st = _stream(stream, x, idx)
+    _check("fadkv_encode_pl", lib().fadkv_encode_pl(h, _addr(x), V, _addr(idx), _addr(coef), _addr(relres), st))
 
 
 def adapt(h: int, x, V: int, idx, coef, relres, repl_id, repl_coef, stream=None) -> None:
@@ -291,6 +299,10 @@ class Dictionary:
         V = x.shape[1]
         encode(self.h, x, V, codes.idx, codes.coef, codes.relres, stream)
 
+    def encode_pl(self, x, codes: Codes, stream=None):
+        V = x.shape[1]
+        encode_pl(self.h, x, V, codes.idx, codes.coef, codes.relres, stream)
+
     def adapt(self, x, codes: Codes, stream=None):
         V = x.shape[1]
         adapt(self.h, x, V, codes.idx, codes.coef, codes.relres, codes.repl_id, codes.repl_coef, stream)
@@ -300,9 +312,15 @@ class Dictionary:
         reconstruct(self.h, V, codes.idx, codes.coef, codes.repl_id if with_replacement else None,
                     codes.repl_coef if with_replacement else None, xhat, stream)
 
-    def step(self, x, codes: Codes, xhat=None, stream=None):
-        """One decode step: encode, adapt and (optionally) reconstruct."""
-        self.encode(x, codes, stream)
+    def step(self, x, codes: Codes, xhat=None, stream=None, coder: str = "gm"):
+        """One decode step: encode (coder "gm": greedy in the pool, "pl":
+        Top-s and one fit), adapt and (optionally) reconstruct."""
+        if coder == "pl":
+            self.encode_pl(x, codes, stream)
+        elif coder == "gm":
+            self.encode(x, codes, stream)
+        else:
+            raise ValueError(f"unknown coder {coder!r}")
         self.adapt(x, codes, stream)
         if xhat is not None:
             self.reconstruct(codes, xhat, True, stream)

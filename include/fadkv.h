@@ -149,6 +149,23 @@ fadkv_status fadkv_dict_destroy(fadkv_dict dict);
 fadkv_status fadkv_encode(fadkv_dict dict, const void* x, int32_t V, int32_t* idx, float* coef,
                           float* relres, void* stream);
 
+/* PL encode: the cheaper coder of the "PL (ours)" rows of Tables 1-4 (Table 4:
+   Cost 0.13 of OMP, against 0.19 for the greedy coder).  The pages name it
+   without spelling it out; this library reads it as screening plus a single
+   ridge fit, the reading that cost supports: for every x, scores r = D x;
+   S = the s atoms with the largest |r_j| (ties to the lower j); one solve
+   (G + diag(lambda_abs + lambda_rel G_ii)) c = D_S x with G = D_S D_S^T;
+   relres = ||x - D_S c|| / ||x|| (0 if x = 0).
+     x [G][V][d]; outputs idx [G][V][s] in ASCENDING atom order (not a pick
+     order), coef [G][V][s] aligned with idx, relres [G][V].
+   Arguments, ordering and errors as for fadkv_encode: the batch counts as
+   an encode and must be passed to fadkv_adapt (which works the same on
+   either coder's output) before the next encode; a non-finite x gets
+   idx = -1, coef = 0, relres = NaN.  The handle's n is not used.
+   Errors: INVALID_ARG, SEQUENCE, CUDA. */
+fadkv_status fadkv_encode_pl(fadkv_dict dict, const void* x, int32_t V, int32_t* idx, float* coef,
+                             float* relres, void* stream);
+
 /* Fixed-size adaptation of the batch just encoded (abstract; Fig. 2 caption).
    usage[idx] += 1 for every selected atom; then the m-th vector with
    relres > delta[g] (ascending v) takes the m-th atom with usage == 0
@@ -231,7 +248,8 @@ fadkv_status fadkv_debug_scores(fadkv_dict dict, const void* x, int32_t V, float
 #define FADKV_K_SCREEN 0       /* screening (tensor cores + candidate filter, or FP32 scores) */
 #define FADKV_K_TOPN 1         /* Top-n: the selection from the screening records and the exact
                                   pool fixup, or the radix Top-n over FP32 scores (binary32) */
-#define FADKV_K_GREEDY 2       /* in-pool greedy selection + ridge refit */
+#define FADKV_K_GREEDY 2       /* in-pool greedy selection + ridge refit (the PL fit for
+                                  fadkv_encode_pl) */
 #define FADKV_K_ADAPT 3        /* fixed-size adaptation */
 #define FADKV_K_RECONSTRUCT 4  /* sparse reconstruction */
 

@@ -218,16 +218,19 @@ def encode_pl(p: Params, atoms: np.ndarray, x: np.ndarray) -> EncodeResult:
                         np.empty((V, 0), np.float64), int(macs.value))
 
 
-def encode_threaded(p: Params, atoms: np.ndarray, x: np.ndarray, threads: int) -> EncodeResult:
-    """The same encode, with the rows of ``x`` split across host threads
-    (ctypes releases the GIL during each C call)."""
+def encode_threaded(p: Params, atoms: np.ndarray, x: np.ndarray, threads: int,
+                    coder: str = "gm") -> EncodeResult:
+    """The same encode (coder "gm": greedy in the pool; "pl": encode_pl),
+    with the rows of ``x`` split across host threads (ctypes releases the
+    GIL during each C call)."""
+    fn = encode_pl if coder == "pl" else encode
     V = x.shape[0]
     threads = max(1, min(threads, V))
     bounds = np.linspace(0, V, threads + 1).astype(int)
     parts = [None] * threads
 
     def run(i):
-        parts[i] = encode(p, atoms, np.ascontiguousarray(x[bounds[i]:bounds[i + 1]]))
+        parts[i] = fn(p, atoms, np.ascontiguousarray(x[bounds[i]:bounds[i + 1]]))
 
     ts = [threading.Thread(target=run, args=(i,)) for i in range(threads)]
     for t in ts:
