@@ -521,15 +521,17 @@ done:
 /*        usage[j] = 1; repl_id[v] = j; repl_coef[v] = ||e||;               */
 /*  5. every other vector: repl_id = -1, repl_coef = 0.                     */
 /* The dictionary keeps exactly N rows.  Flagged vectors beyond |L| are    */
-/* counted in *overflow; *replaced counts the overwritten atoms.           */
+/* counted in *overflow; *replaced counts the overwritten atoms.  A row    */
+/* with a negative usage count is a free slot (see the append-only growth  */
+/* below) and is never taken here.                                        */
 /* Returns 0, or -1 on bad arguments / allocation failure.                  */
 /* ---------------------------------------------------------------------- */
 
-int oracle_adapt(const oracle_params* p, void* atoms, int32_t* usage,
-                 const void* xin, int32_t V, const int32_t* idx,
-                 const double* coef, const double* relres, double delta,
-                 int32_t* repl_id, double* repl_coef,
-                 int64_t* replaced, int64_t* overflow)
+static int adapt_impl(const oracle_params* p, void* atoms, int32_t* usage,
+                      const void* xin, int32_t V, const int32_t* idx,
+                      const double* coef, const double* relres, double delta,
+                      int32_t* repl_id, double* repl_coef,
+                      int64_t* replaced, int64_t* overflow, int append)
 {
     const int N = p->N, d = p->d, s = p->s;
     if (N <= 0 || d <= 0 || s <= 0 || V < 0)
@@ -549,7 +551,7 @@ int oracle_adapt(const oracle_params* p, void* atoms, int32_t* usage,
 
     int nL = 0;
     for (int j = 0; j < N; ++j)
-        if (usage[j] == 0) L[nL++] = j;
+        if (append ? usage[j] < 0 : usage[j] == 0) L[nL++] = j;
 
     int m = 0;
     int64_t flagged = 0;
@@ -581,6 +583,36 @@ int oracle_adapt(const oracle_params* p, void* atoms, int32_t* usage,
     free(L);
     free(e);
     return 0;
+}
+
+int oracle_adapt(const oracle_params* p, void* atoms, int32_t* usage,
+                 const void* xin, int32_t V, const int32_t* idx,
+                 const double* coef, const double* relres, double delta,
+                 int32_t* repl_id, double* repl_coef,
+                 int64_t* replaced, int64_t* overflow)
+{
+    return adapt_impl(p, atoms, usage, xin, V, idx, coef, relres, delta, repl_id, repl_coef,
+                      replaced, overflow, 0);
+}
+
+/* Append-only growth, the strategy the pages contrast FAD-KV with
+   (abstract: naive append-only updates grow the dictionary during
+   generation; Fig. 2 caption: FAD-KV replaces an inactive atom instead of
+   appending a new one).  The dictionary has a fixed capacity of N rows;
+   a row with a negative usage count is a free slot, not an atom.  Steps
+   1-5 of the fixed-size adaptation above, except that L is the list of
+   free slots (usage < 0, ascending) instead of the inactive atoms: a
+   flagged vector's residual atom is appended in the next free slot, no
+   atom is ever reused, and once the capacity is used up further flagged
+   vectors count as overflow. */
+int oracle_adapt_append(const oracle_params* p, void* atoms, int32_t* usage,
+                        const void* xin, int32_t V, const int32_t* idx,
+                        const double* coef, const double* relres, double delta,
+                        int32_t* repl_id, double* repl_coef,
+                        int64_t* replaced, int64_t* overflow)
+{
+    return adapt_impl(p, atoms, usage, xin, V, idx, coef, relres, delta, repl_id, repl_coef,
+                      replaced, overflow, 1);
 }
 
 /* ---------------------------------------------------------------------- */

@@ -91,6 +91,8 @@ def load(path: str):
                                C.c_void_p, C.c_void_p, C.c_void_p, C.c_double,
                                C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
     L.oracle_adapt.restype = C.c_int
+    L.oracle_adapt_append.argtypes = L.oracle_adapt.argtypes
+    L.oracle_adapt_append.restype = C.c_int
     L.oracle_reconstruct.argtypes = [P(_Params), C.c_void_p, C.c_int32, C.c_void_p,
                                      C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
     L.oracle_reconstruct.restype = C.c_int
@@ -253,8 +255,9 @@ class AdaptResult:
 
 
 def adapt(p: Params, atoms: np.ndarray, usage: np.ndarray, x: np.ndarray, idx: np.ndarray,
-          coef: np.ndarray, relres: np.ndarray, delta: float) -> AdaptResult:
-    """Fixed-size adaptation; mutates ``atoms`` and ``usage`` in place."""
+          coef: np.ndarray, relres: np.ndarray, delta: float, append: bool = False) -> AdaptResult:
+    """Fixed-size adaptation (or, with ``append``, append-only growth into the
+    free slots, usage < 0); mutates ``atoms`` and ``usage`` in place."""
     _check_store(atoms, p, "atoms")
     _check_store(x, p, "x")
     if usage.dtype != np.int32 or not usage.flags.c_contiguous:
@@ -268,9 +271,10 @@ def adapt(p: Params, atoms: np.ndarray, usage: np.ndarray, x: np.ndarray, idx: n
     rep = C.c_int64(0)
     ovf = C.c_int64(0)
     pc = p.c()
-    rc = lib().oracle_adapt(C.byref(pc), _ptr(atoms), _ptr(usage), _ptr(x), V, _ptr(idx),
-                            _ptr(coef), _ptr(relres), float(delta), _ptr(rid), _ptr(rcoef),
-                            C.addressof(rep), C.addressof(ovf))
+    fn = lib().oracle_adapt_append if append else lib().oracle_adapt
+    rc = fn(C.byref(pc), _ptr(atoms), _ptr(usage), _ptr(x), V, _ptr(idx),
+            _ptr(coef), _ptr(relres), float(delta), _ptr(rid), _ptr(rcoef),
+            C.addressof(rep), C.addressof(ovf))
     if rc != 0:
         raise RuntimeError(f"oracle_adapt failed: {rc}")
     return AdaptResult(rid, rcoef, int(rep.value), int(ovf.value))

@@ -30,7 +30,9 @@ MUTANTS = [
     ("back substitution transposed", "v -= Lwork[m * k + i] * c[m];", "v -= Lwork[i * k + m] * c[m];"),
     ("relres not relative", "relres[v] = (xn == 0.0) ? 0.0 : en / xn;", "relres[v] = en;"),
     ("adapt threshold not strict", "if (!(relres[v] > delta)) continue;", "if (!(relres[v] >= delta)) continue;"),
-    ("adapt inactive order reversed", "for (int j = 0; j < N; ++j)\n        if (usage[j] == 0) L[nL++] = j;", "for (int j = N - 1; j >= 0; --j)\n        if (usage[j] == 0) L[nL++] = j;"),
+    ("adapt inactive order reversed", "for (int j = 0; j < N; ++j)\n        if (append ? usage[j] < 0 : usage[j] == 0) L[nL++] = j;", "for (int j = N - 1; j >= 0; --j)\n        if (append ? usage[j] < 0 : usage[j] == 0) L[nL++] = j;"),
+    ("append mode reuses inactive atoms", "append ? usage[j] < 0 : usage[j] == 0", "append ? usage[j] <= 0 : usage[j] == 0"),
+    ("fixed size takes free slots", "append ? usage[j] < 0 : usage[j] == 0", "append ? usage[j] < 0 : usage[j] <= 0"),
     ("adapt new atom usage stays 0", "usage[j] = 1;\n        repl_id[v] = j;", "repl_id[v] = j;"),
     ("adapt residual keeps first term only", "for (int k = 0; k < s; ++k) {\n                int32_t a = idx[(int64_t)v * s + k];\n                if (a >= 0)\n                    acc -=", "for (int k = 0; k < 1; ++k) {\n                int32_t a = idx[(int64_t)v * s + k];\n                if (a >= 0)\n                    acc -="),
     ("adapt repl_coef squared norm", "repl_coef[v] = en;", "repl_coef[v] = en * en;"),
@@ -58,6 +60,7 @@ PIN_TESTS = [
     pins.test_zero_and_nonfinite_inputs,
     pins.test_adapt_golden_cases,
     pins.test_adapt_invariants_random,
+    pins.test_append_growth_against_fixed_size,
     pins.test_reconstruct_consistency,
     pins.test_table4_pl_cost_reproduced_by_operation_count,
     pins.test_pl_weighted_orthogonal_closed_form,

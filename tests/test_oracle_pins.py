@@ -465,7 +465,7 @@ def test_adapt_golden_cases(oracle_lib):
         coef = np.array(case["coef"], np.float64)
         rel = np.array([float(v) for v in case["relres"]], np.float64)
         p = O.Params(atoms.shape[0], atoms.shape[1], 2, idx.shape[1], dtype=O.F32)
-        res = O.adapt(p, atoms, usage, x, idx, coef, rel, case["delta"])
+        res = O.adapt(p, atoms, usage, x, idx, coef, rel, case["delta"], append=case.get("mode") == "append")
         assert list(usage) == case["expect_usage"], case["name"]
         assert list(res.repl_id) == case["expect_repl_id"], case["name"]
         assert np.allclose(res.repl_coef, case["expect_repl_coef"], rtol=0, atol=1e-12)
@@ -474,6 +474,43 @@ def test_adapt_golden_cases(oracle_lib):
         for j in range(atoms.shape[0]):
             want = changed.get(j, before[j])
             assert np.array_equal(atoms[j], np.array(want, np.float32)), (case["name"], j)
+
+
+def test_append_growth_against_fixed_size(oracle_lib):
+    """The contrast the pages draw (abstract; Fig. 2 caption; Fig. 3a): over a
+    run of decode steps the append-only dictionary grows by one atom per
+    flagged vector until its capacity is used up, and never rewrites an
+    atom; the fixed-size dictionary never changes size (every row stays an
+    atom) and only rewrites atoms that were inactive."""
+    O = oracle_lib
+    from dataclasses import replace
+    w = replace(S.WORKLOADS["tiny"], off_frac=0.0, sigma=0.3)   # large residuals: many flagged vectors
+    data = S.WorkloadData(w)
+    N0 = 448                                   # atoms at the start; 64 free slots in append mode
+    p = O.Params(w.N, w.d, w.n, w.s, dtype=O.F32)
+    at_f, us_f = data.atoms[0].copy(), data.usage[0].copy()
+    at_a, us_a = data.atoms[0].copy(), data.usage[0].copy()
+    at_a[N0:] = 0
+    us_a[N0:] = -1
+    size = N0
+    for step in range(4):
+        x = data.inputs(step, 48)[0]
+        for at, us, app in ((at_f, us_f, False), (at_a, us_a, True)):
+            before, ub = at.copy(), us.copy()
+            r = O.encode(p, at, x)
+            a = O.adapt(p, at, us, x, r.idx, r.coef, r.relres, 0.5, append=app)
+            flagged = int((r.relres > 0.5).sum())
+            rows = set(np.nonzero((at != before).any(axis=1))[0].tolist())
+            assert rows <= set(a.repl_id[a.repl_id >= 0].tolist())
+            if app:
+                assert a.replaced == min(flagged, w.N - size) and a.overflow == flagged - a.replaced
+                assert sorted(a.repl_id[a.repl_id >= 0]) == list(range(size, size + a.replaced))
+                size += a.replaced
+                assert int((us >= 0).sum()) == size
+            else:
+                assert int((us < 0).sum()) == 0
+                assert all(ub[j] == 0 for j in a.repl_id[a.repl_id >= 0])
+    assert size > N0
 
 
 def test_adapt_invariants_random(oracle_lib):
