@@ -127,6 +127,7 @@ extern "C" fadkv_status fadkv_adapt_noalloc(const fadkv_params* p, void* atoms, 
     a.flagged = (int32_t*)(base + off_flagged);
     a.counters = (long long*)(base + off_counters);
     a.V = V;
+    a.append = 0;
     e = launch_adapt(sh, a, dt, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail("launch", e);
     return FADKV_OK;

@@ -546,8 +546,11 @@ fadkv_status fadkv_encode_pl(fadkv_dict h, const void* x, int32_t V, int32_t* id
     return FADKV_OK;
 }
 
-fadkv_status fadkv_adapt(fadkv_dict h, const void* x, int32_t V, const int32_t* idx, const float* coef,
-                         const float* relres, int32_t* repl_id, float* repl_coef, void* stream)
+namespace {
+
+fadkv_status adapt_call(const char* name, fadkv_dict h, const void* x, int32_t V, const int32_t* idx,
+                        const float* coef, const float* relres, int32_t* repl_id, float* repl_coef, void* stream,
+                        int append)
 {
     if (!h) return FADKV_ERR_INVALID_ARG;
     if (V < 0 || V > h->p.max_batch) return FADKV_ERR_INVALID_ARG;
@@ -556,7 +559,7 @@ fadkv_status fadkv_adapt(fadkv_dict h, const void* x, int32_t V, const int32_t* 
         return FADKV_ERR_INVALID_ARG;
     if (!h->pending || h->pending_V != V) return FADKV_ERR_SEQUENCE;
     if (fault_injected()) {
-        set_error("fadkv_adapt", cudaErrorLaunchFailure);
+        set_error(name, cudaErrorLaunchFailure);
         return FADKV_ERR_CUDA;
     }
     AdaptArgs a;
@@ -572,15 +575,30 @@ fadkv_status fadkv_adapt(fadkv_dict h, const void* x, int32_t V, const int32_t* 
     a.flagged = (int32_t*)(h->ws + h->L.flagged);
     a.counters = counters(h);
     a.V = V;
+    a.append = append;
     cudaStream_t st = (cudaStream_t)stream;
     const cudaError_t e = traced(h, FADKV_K_ADAPT, st, [&] { return launch_adapt(h->sh, a, h->delta, st); });
     if (e != cudaSuccess) {
-        set_error("fadkv_adapt", e);
+        set_error(name, e);
         return FADKV_ERR_CUDA;
     }
     h->pending = false;
     h->pending_V = 0;
     return FADKV_OK;
+}
+
+}  // namespace
+
+fadkv_status fadkv_adapt(fadkv_dict h, const void* x, int32_t V, const int32_t* idx, const float* coef,
+                         const float* relres, int32_t* repl_id, float* repl_coef, void* stream)
+{
+    return adapt_call("fadkv_adapt", h, x, V, idx, coef, relres, repl_id, repl_coef, stream, 0);
+}
+
+fadkv_status fadkv_adapt_append(fadkv_dict h, const void* x, int32_t V, const int32_t* idx, const float* coef,
+                                const float* relres, int32_t* repl_id, float* repl_coef, void* stream)
+{
+    return adapt_call("fadkv_adapt_append", h, x, V, idx, coef, relres, repl_id, repl_coef, stream, 1);
 }
 
 fadkv_status fadkv_reconstruct(fadkv_dict h, int32_t V, const int32_t* idx, const float* coef,

@@ -267,6 +267,7 @@ struct AdaptArgs {
     int32_t* flagged;         // [G][max_batch] scratch
     long long* counters;      // [G][kCntFields]
     int V;
+    int append;               // 0: reuse inactive atoms (usage == 0); 1: fill free slots (usage < 0)
 };
 cudaError_t launch_adapt(const Shape& sh, const AdaptArgs& a, const DeltaTable& delta, cudaStream_t st);
 

@@ -83,16 +83,20 @@ adapt_kernel(Shape sh, AdaptArgs a, DeltaTable delta, int max_batch)
     }
     __syncthreads();
 
-    // 2. flagged vectors in ascending v; 3. inactive atoms in ascending id
-    //    (only needed when some vector is flagged: the N-wide scan is skipped
-    //    in the common step with no replacement)
+    // 2. flagged vectors in ascending v; 3. the rows they may take, in
+    //    ascending id: inactive atoms (usage == 0) for the fixed-size
+    //    adaptation, free slots (usage < 0) for append-only growth (only
+    //    needed when some vector is flagged: the N-wide scan is skipped in
+    //    the common step with no replacement)
     const int nF = block_compact(V, [&](int v) { return relres[v] > dg; }, flagged, ws);
-    const int nL = nF > 0 ? block_compact(N, [&](int j) { return usage[j] == 0; }, inactive, ws) : 0;
+    const bool app = a.append != 0;
+    const int nL = nF > 0 ? block_compact(N, [&](int j) { return app ? usage[j] < 0 : usage[j] == 0; }, inactive, ws)
+                          : 0;
     const int m = min(nL, nF);
 
     // 4. the r-th flagged vector takes the r-th inactive atom (one warp each).
-    //    The residual reads only atoms selected in this batch (usage >= 1),
-    //    never an atom being overwritten (usage == 0 after step 1).
+    //    The residual reads only atoms selected in this batch (usage >= 1
+    //    after step 1), never a row being overwritten (usage <= 0).
     constexpr int PL = D / 32;
     for (int r = warp; r < m; r += kAdaptWarps) {
         const int v = flagged[r], j = inactive[r];

@@ -74,9 +74,11 @@ _SIGS = {
     "fadkv_encode": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p],
                      C.c_int),
     "fadkv_encode_pl": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p],
-                     C.c_int),
+                        C.c_int),
     "fadkv_adapt": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                      C.c_void_p, C.c_void_p], C.c_int),
+    "fadkv_adapt_append": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
+                            C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "fadkv_adapt_noalloc": ([C.POINTER(Params), C.c_void_p, C.c_void_p, C.POINTER(C.c_float), C.c_void_p,
                              C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                              C.c_void_p], C.c_int),
@@ -177,6 +179,13 @@ def adapt(h: int, x, V: int, idx, coef, relres, repl_id, repl_coef, stream=None)
     st = _stream(stream, x, idx)
     _check("fadkv_adapt", lib().fadkv_adapt(h, _addr(x), V, _addr(idx), _addr(coef), _addr(relres),
                                             _addr(repl_id), _addr(repl_coef), st))
+
+
+def adapt_append(h: int, x, V: int, idx, coef, relres, repl_id, repl_coef, stream=None) -> None:
+    """Append-only growth into the free slots (usage < 0)."""
+    st = _stream(stream, x, idx)
+    _check("fadkv_adapt_append", lib().fadkv_adapt_append(h, _addr(x), V, _addr(idx), _addr(coef), _addr(relres),
+                                                          _addr(repl_id), _addr(repl_coef), st))
 
 
 def adapt_noalloc(p: Params, atoms, usage, delta, x, V: int, idx, coef, relres, repl_id, repl_coef,
@@ -306,6 +315,10 @@ class Dictionary:
     def adapt(self, x, codes: Codes, stream=None):
         V = x.shape[1]
         adapt(self.h, x, V, codes.idx, codes.coef, codes.relres, codes.repl_id, codes.repl_coef, stream)
+
+    def adapt_append(self, x, codes: Codes, stream=None):
+        V = x.shape[1]
+        adapt_append(self.h, x, V, codes.idx, codes.coef, codes.relres, codes.repl_id, codes.repl_coef, stream)
 
     def reconstruct(self, codes: Codes, xhat, with_replacement: bool = True, stream=None):
         V = codes.idx.shape[1]

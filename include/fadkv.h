@@ -119,7 +119,10 @@ fadkv_status fadkv_workspace_bytes(const fadkv_params* params, size_t* bytes);
 /* Create a handle over caller-owned device memory.
      atoms      [G][N][d] dictionary (mutated by fadkv_adapt), 16-byte aligned
      usage      [G][N] usage counts (mutated by fadkv_adapt); an atom is
-                inactive while its count is 0
+                inactive while its count is 0; a negative count marks a
+                free slot, a row that holds no atom yet (keep its row zero:
+                screening still reads it, and a zero row scores 0), which
+                only fadkv_adapt_append fills
      delta      HOST array [G] of adaptation thresholds (Table 5: 0.50 for a
                 key dictionary, 0.70 for a value dictionary); copied
      workspace  device buffer of at least fadkv_workspace_bytes bytes,
@@ -173,12 +176,29 @@ fadkv_status fadkv_encode_pl(fadkv_dict dict, const void* x, int32_t V, int32_t*
    the dictionary type), its usage becomes 1, repl_id[v] = its id and
    repl_coef[v] = ||e||.  Other vectors get repl_id = -1, repl_coef = 0.
    Flagged vectors left without an inactive atom keep their s-term code and
-   are counted as overflow.  The dictionary keeps N atoms.
+   are counted as overflow.  The dictionary keeps N atoms; free slots
+   (usage < 0) are never taken.
    Arguments are the same x, V, idx, coef, relres as the encode call.
    Errors: INVALID_ARG, SEQUENCE (no encode pending, or a different V), CUDA. */
 fadkv_status fadkv_adapt(fadkv_dict dict, const void* x, int32_t V, const int32_t* idx,
                          const float* coef, const float* relres, int32_t* repl_id,
                          float* repl_coef, void* stream);
+
+/* Append-only growth: the strategy the pages contrast FAD-KV with (abstract:
+   naive append-only updates grow the dictionary during generation; Fig. 2
+   caption: FAD-KV replaces an inactive atom instead of appending a new one),
+   for side-by-side runs.  The same as fadkv_adapt except for the rows the
+   flagged vectors take: the m-th flagged vector (ascending v, relres >
+   delta[g]) takes the m-th FREE SLOT (usage < 0, ascending id) instead of an
+   inactive atom, so the dictionary grows by one atom per flagged vector
+   into the capacity the caller reserved, and no atom, inactive or not, is
+   ever rewritten.  Flagged vectors beyond the free slots are counted as
+   overflow; "atoms replaced" in fadkv_dict_stats counts appended atoms.
+   The dictionary's size is the number of rows with usage >= 0.  Arguments,
+   sequence contract and errors as for fadkv_adapt. */
+fadkv_status fadkv_adapt_append(fadkv_dict dict, const void* x, int32_t V, const int32_t* idx,
+                                const float* coef, const float* relres, int32_t* repl_id,
+                                float* repl_coef, void* stream);
 
 /* Fixed-size adaptation without a handle and without caller scratch.  The
    pages have no counterpart to this call: it runs the same adaptation as
