@@ -645,3 +645,123 @@ int oracle_reconstruct(const oracle_params* p, const void* atoms, int32_t V,
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Compressed store and attention over it.                                 */
+/*                                                                          */
+/* The codes are what the cache keeps instead of K and V (Table 4: the     */
+/* per-sequence KV memory of the dictionary methods against full KV).  The */
+/* pages do not give a storage format; this library packs each nonzero     */
+/* into one 32-bit word:                                                    */
+/*   bits 31..13  the coefficient rounded to 11 significant bits (round to  */
+/*                nearest, ties to even) in the layout of the top 19 bits   */
+/*                of an IEEE binary32 number: sign, 8-bit biased exponent,  */
+/*                10 fraction bits; magnitudes below 2^-126 become 0;       */
+/*   bits 12..0   the atom id (N <= 8192).                                  */
+/* A vector's code is s + 1 words: its s terms, then the replacement term   */
+/* of the adaptation (word 0 when there is none); a skipped term (id < 0)  */
+/* is word 0.                                                               */
+/* ---------------------------------------------------------------------- */
+
+uint32_t oracle_pack_word(double coef, int32_t id)
+{
+    if (id < 0 || id >= 8192 || coef == 0.0 || !isfinite(coef))
+        return 0u;
+    uint32_t sign = coef < 0.0 ? 1u : 0u;
+    double a = fabs(coef);
+    if (a < ldexp(1.0, -126))
+        return (uint32_t)id;
+    int E;
+    double m = frexp(a, &E);               /* a = m 2^E, m in [0.5, 1) */
+    double q = nearbyint(ldexp(m, 11));    /* 11 significant bits, ties to even */
+    if (q == 2048.0) {                     /* rounded up to the next power of two */
+        q = 1024.0;
+        E += 1;
+    }
+    /* a ~ q 2^(E-11) = (q/1024) 2^(E-1): biased exponent E - 1 + 127 */
+    int be = E - 1 + 127;
+    if (be >= 255)
+        be = 254, q = 2047.0;              /* saturate (not reached by codes) */
+    uint32_t frac = (uint32_t)q - 1024u;
+    return (sign << 31) | ((uint32_t)be << 23) | (frac << 13) | (uint32_t)id;
+}
+
+double oracle_word_coef(uint32_t w)
+{
+    uint32_t be = (w >> 23) & 0xffu;
+    if (be == 0)
+        return 0.0;
+    double v = ldexp(1.0 + (double)((w >> 13) & 0x3ffu) / 1024.0, (int)be - 127);
+    return (w >> 31) ? -v : v;
+}
+
+int32_t oracle_word_id(uint32_t w) { return (int32_t)(w & 0x1fffu); }
+
+/* Decode attention of one layer over the compressed store:
+     dict_k, dict_v  [N][d] key / value dictionaries (storage dtype)
+     cache_k/v       [B][Hkv][Tmax][s+1] packed codes
+     lengths         [B] tokens in the cache per sequence (clamped to Tmax)
+     q               [B][Hq][d] queries (double)
+     out             [B][Hq][d]
+   For sequence b and query head h (KV head h / (Hq/Hkv), grouped-query
+   attention): k_t and v_t are rebuilt from their codes, score_t =
+   scale <q, k_t>, p = softmax over t < lengths[b], out = sum_t p_t v_t
+   (0 for an empty sequence). */
+int oracle_attend(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t s, int32_t N,
+                  int32_t Tmax, int32_t dtype, double scale, const void* dict_k,
+                  const void* dict_v, const uint32_t* cache_k, const uint32_t* cache_v,
+                  const int32_t* lengths, const double* q, double* out)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || s < 0 || N <= 0 || N > 8192 || Tmax < 0)
+        return -1;
+    const int W = s + 1, grp = Hq / Hkv;
+    double* sc = (double*)malloc(sizeof(double) * (Tmax > 0 ? Tmax : 1));
+    double* kv = (double*)malloc(sizeof(double) * d);
+    if (!sc || !kv) {
+        free(sc); free(kv);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        int T = lengths[b] < 0 ? 0 : (lengths[b] > Tmax ? Tmax : lengths[b]);
+        for (int h = 0; h < Hq; ++h) {
+            const int hk = h / grp;
+            const double* qh = q + ((int64_t)b * Hq + h) * d;
+            double* o = out + ((int64_t)b * Hq + h) * d;
+            const uint32_t* ck = cache_k + ((int64_t)b * Hkv + hk) * Tmax * W;
+            const uint32_t* cv = cache_v + ((int64_t)b * Hkv + hk) * Tmax * W;
+            for (int t = 0; t < d; ++t) o[t] = 0.0;
+            if (T == 0) continue;
+            double mx = -INFINITY;
+            for (int t = 0; t < T; ++t) {
+                for (int e = 0; e < d; ++e) kv[e] = 0.0;
+                for (int i = 0; i < W; ++i) {
+                    uint32_t w = ck[(int64_t)t * W + i];
+                    double c = oracle_word_coef(w);
+                    int32_t j = oracle_word_id(w);
+                    if (j >= N) { free(sc); free(kv); return -1; }
+                    for (int e = 0; e < d; ++e) kv[e] += c * load_elem(dict_k, dtype, (int64_t)j * d + e);
+                }
+                sc[t] = scale * dot(qh, kv, d);
+                if (sc[t] > mx) mx = sc[t];
+            }
+            double sum = 0.0;
+            for (int t = 0; t < T; ++t) {
+                sc[t] = exp(sc[t] - mx);
+                sum += sc[t];
+            }
+            for (int t = 0; t < T; ++t) {
+                double pt = sc[t] / sum;
+                for (int i = 0; i < W; ++i) {
+                    uint32_t w = cv[(int64_t)t * W + i];
+                    double c = oracle_word_coef(w);
+                    int32_t j = oracle_word_id(w);
+                    if (j >= N) { free(sc); free(kv); return -1; }
+                    for (int e = 0; e < d; ++e) o[e] += pt * c * load_elem(dict_v, dtype, (int64_t)j * d + e);
+                }
+            }
+        }
+    }
+    free(sc);
+    free(kv);
+    return 0;
+}

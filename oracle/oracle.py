@@ -102,6 +102,16 @@ def load(path: str):
     L.oracle_encode_pl.argtypes = [P(_Params), C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p,
                                    C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
     L.oracle_encode_pl.restype = C.c_int
+    L.oracle_pack_word.argtypes = [C.c_double, C.c_int32]
+    L.oracle_pack_word.restype = C.c_uint32
+    L.oracle_word_coef.argtypes = [C.c_uint32]
+    L.oracle_word_coef.restype = C.c_double
+    L.oracle_word_id.argtypes = [C.c_uint32]
+    L.oracle_word_id.restype = C.c_int32
+    L.oracle_attend.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                C.c_int32, C.c_double, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                C.c_void_p, C.c_void_p, C.c_void_p]
+    L.oracle_attend.restype = C.c_int
     L.oracle_half_to_double.argtypes = [C.c_uint16]
     L.oracle_half_to_double.restype = C.c_double
     L.oracle_double_to_half.argtypes = [C.c_double]
@@ -128,7 +138,8 @@ class Variant:
         import types
         mod = globals()
         for name in ("encode", "adapt", "reconstruct", "half_to_double", "double_to_half",
-                     "encode_threaded", "greedy_on_pool", "encode_pl"):
+                     "encode_threaded", "greedy_on_pool", "encode_pl", "pack_codes", "pack_word", "word_coef", "word_id",
+                     "attend"):
             fn = mod[name]
             setattr(self, name, types.FunctionType(fn.__code__, dict(mod, lib=lambda: self._L),
                                                    fn.__name__, fn.__defaults__, fn.__closure__))
@@ -295,6 +306,61 @@ def reconstruct(p: Params, atoms: np.ndarray, idx: np.ndarray, coef: np.ndarray,
                                   _ptr(repl_id), _ptr(repl_coef), _ptr(out))
     if rc != 0:
         raise RuntimeError(f"oracle_reconstruct failed: {rc}")
+    return out
+
+
+def pack_codes(idx: np.ndarray, coef: np.ndarray, repl_id: np.ndarray | None = None,
+               repl_coef: np.ndarray | None = None) -> np.ndarray:
+    """[..., s] codes (+ optional [...] replacement terms) -> [..., s+1]
+    packed uint32 words (coefficient rounded to 11 significant bits, id in
+    the low 13 bits)."""
+    idx = np.asarray(idx)
+    coef = np.asarray(coef, np.float64)
+    lead = idx.shape[:-1]
+    s = idx.shape[-1]
+    out = np.zeros(lead + (s + 1,), np.uint32)
+    L = lib()
+    for pos in np.ndindex(*lead):
+        for k in range(s):
+            out[pos + (k,)] = L.oracle_pack_word(float(coef[pos + (k,)]), int(idx[pos + (k,)]))
+        if repl_id is not None:
+            out[pos + (s,)] = L.oracle_pack_word(float(repl_coef[pos]), int(repl_id[pos]))
+    return out
+
+
+def pack_word(coef: float, idx: int) -> int:
+    """One packed word (see pack_codes)."""
+    return lib().oracle_pack_word(float(coef), int(idx))
+
+
+def word_coef(w: int) -> float:
+    return lib().oracle_word_coef(int(w))
+
+
+def word_id(w: int) -> int:
+    return lib().oracle_word_id(int(w))
+
+
+def attend(dict_k: np.ndarray, dict_v: np.ndarray, cache_k: np.ndarray, cache_v: np.ndarray,
+           lengths: np.ndarray, q: np.ndarray, scale: float | None = None) -> np.ndarray:
+    """Decode attention of one layer over packed caches [B][Hkv][Tmax][s+1];
+    q [B][Hq][d]; returns [B][Hq][d] float64."""
+    N, d = dict_k.shape
+    B, Hkv, Tmax, W = cache_k.shape
+    Hq = q.shape[1]
+    dtype = F16 if dict_k.dtype == np.float16 else F32
+    dict_k = np.ascontiguousarray(dict_k)
+    dict_v = np.ascontiguousarray(dict_v, dict_k.dtype)
+    cache_k = np.ascontiguousarray(cache_k, np.uint32)
+    cache_v = np.ascontiguousarray(cache_v, np.uint32)
+    lengths = np.ascontiguousarray(lengths, np.int32)
+    q = np.ascontiguousarray(q, np.float64)
+    out = np.empty((B, Hq, d), np.float64)
+    sc = 1.0 / np.sqrt(d) if scale is None else scale
+    rc = lib().oracle_attend(B, Hq, Hkv, d, W - 1, N, Tmax, dtype, float(sc), _ptr(dict_k), _ptr(dict_v),
+                             _ptr(cache_k), _ptr(cache_v), _ptr(lengths), _ptr(q), _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attend failed: {rc}")
     return out
 
 

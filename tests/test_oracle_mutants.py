@@ -39,6 +39,12 @@ MUTANTS = [
     ("reconstruct drops replacement", "acc += repl_coef[v] * load_elem", "acc += 0.0 * load_elem"),
     ("half rounding truncates", "double q = nearbyint(ldexp(a, 10 - E));", "double q = floor(ldexp(a, 10 - E));"),
     ("half subnormal scale", "v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    ("pack truncates", "double q = nearbyint(ldexp(m, 11));", "double q = floor(ldexp(m, 11));"),
+    ("pack exponent off by one", "int be = E - 1 + 127;", "int be = E + 127;"),
+    ("attend scale dropped", "sc[t] = scale * dot(qh, kv, d);", "sc[t] = dot(qh, kv, d);"),
+    ("attend head grouping", "const int hk = h / grp;", "const int hk = h % Hkv;"),
+    ("attend skips the replacement word", "for (int i = 0; i < W; ++i) {\n                    uint32_t w = ck", "for (int i = 0; i + 1 < W; ++i) {\n                    uint32_t w = ck"),
+    ("attend ignores lengths", "int T = lengths[b] < 0 ? 0 : (lengths[b] > Tmax ? Tmax : lengths[b]);", "int T = Tmax;"),
     ("PL takes ranks 1..s", "for (int k = 0; k < s; ++k) S[k] = rk[k].id;", "for (int k = 0; k < s; ++k) S[k] = rk[k + 1].id;"),
     ("PL ids left in rank order", "qsort(S, (size_t)s, sizeof(int32_t), cmp_i32);", ";"),
     ("PL residual drops the last atom", "for (int k = 0; k < s; ++k)\n                acc -= c[k]", "for (int k = 0; k + 1 < s; ++k)\n                acc -= c[k]"),
@@ -68,6 +74,12 @@ PIN_TESTS = [
     pins.test_pl_is_greedy_over_a_pool_of_s,
     pins.test_pl_fit_matches_normal_equations,
     pins.test_pl_zero_and_nonfinite_inputs,
+    pins.test_pack_word_matches_binary16_rounding,
+    pins.test_pack_word_layout,
+    pins.test_attend_single_token_is_its_value,
+    pins.test_attend_two_tokens_closed_form,
+    pins.test_attend_grouped_heads_and_lengths,
+    pins.test_attend_identical_keys_average_values,
 ]
 
 

@@ -450,6 +450,149 @@ def test_pl_zero_and_nonfinite_inputs(oracle_lib):
 
 
 # --------------------------------------------------------------------------
+# compressed store: packed words, and attention over packed codes
+# --------------------------------------------------------------------------
+
+def test_pack_word_matches_binary16_rounding(oracle_lib):
+    """Inside binary16's normal range [2^-14, 65504] a value rounded to 11
+    significant bits (ties to even) is exactly what numpy's binary16
+    conversion gives, so that routine pins the rounding: random values,
+    exact midpoints between neighbouring binary16 numbers, both signs."""
+    O = oracle_lib
+    g = np.random.default_rng(17)
+    vals = np.exp(g.uniform(np.log(2.0 ** -14), np.log(65000.0), 3000))
+    b = np.arange(0x0400, 0x7bff, 37, dtype=np.uint16)
+    mids = (b.view(np.float16).astype(np.float64) + (b + 1).view(np.float16).astype(np.float64)) / 2
+    for v in np.concatenate([vals, mids]):
+        for sgn in (1.0, -1.0):
+            w = O.pack_word(sgn * v, 4321)
+            assert O.word_id(w) == 4321
+            assert O.word_coef(w) == float(np.float16(sgn * v)), (sgn * v)
+
+
+def test_pack_word_layout(oracle_lib):
+    """Bits 31..13 are the top 19 bits of the binary32 encoding of the
+    rounded coefficient; bits 12..0 the id.  Zero coefficients and skipped
+    terms are word 0; magnitudes below 2^-126 keep only the id; outside
+    binary16's range the rounding still keeps 11 significant bits with an
+    error of at most half a unit in the last place."""
+    O = oracle_lib
+    g = np.random.default_rng(18)
+    for c in np.concatenate([g.standard_normal(500) * 10.0 ** g.integers(-30, 30, 500), [1e-20, -3e25]]):
+        j = int(g.integers(0, 8192))
+        w = O.pack_word(float(c), j)
+        r = O.word_coef(w)
+        assert (w & 0x1FFF) == j
+        assert (w >> 13) == (int(np.float32(r).view(np.uint32)) >> 13)
+        m, e = np.frexp(abs(r))
+        assert float(np.ldexp(m, 11)).is_integer()                     # 11 significant bits
+        assert abs(r - c) <= np.ldexp(1.0, int(np.frexp(abs(c))[1]) - 12) * (1 + 1e-12)
+    assert O.pack_word(0.0, 5) == 0 and O.pack_word(1.5, -1) == 0
+    assert O.pack_word(1e-39, 5) == 5
+
+
+def _identity_case(N=64, Tmax=8):
+    D = np.eye(N, dtype=np.float32)
+    return D, D.copy()
+
+
+def test_attend_single_token_is_its_value(oracle_lib):
+    """One cached token: softmax over one score is 1, the output is v_0."""
+    O = oracle_lib
+    N = d = 64
+    g = np.random.default_rng(19)
+    Dk = S.make_dictionary(N, d, np.float32, 5)
+    Dv = S.make_dictionary(N, d, np.float32, 6)
+    ck = O.pack_codes(np.array([[[[3, 9, 40]]]]), np.array([[[[0.5, -1.25, 2.0]]]]))
+    cv = O.pack_codes(np.array([[[[7, 8, 60]]]]), np.array([[[[1.5, 0.75, -0.5]]]]))
+    q = g.standard_normal((1, 1, d))
+    out = O.attend(Dk, Dv, ck, cv, np.array([1]), q)
+    Dv64 = Dv.astype(np.float64)
+    v0 = 1.5 * Dv64[7] + 0.75 * Dv64[8] - 0.5 * Dv64[60]
+    np.testing.assert_allclose(out[0, 0], v0, rtol=1e-14, atol=1e-15)
+
+
+def test_attend_two_tokens_closed_form(oracle_lib):
+    """Identity dictionaries (atom j = e_j): k_0 = 1.5 e_3 (+ a replacement
+    term 0.5 e_3), k_1 = -0.75 e_10, so the scores are (2 q_3, -0.75 q_10) /
+    sqrt(d); v_0 = 2 e_5,
+    v_1 = -0.5 e_6 (+ a replacement term 0.25 e_5 on token 1); the output
+    is p_0 v_0 + p_1 v_1 with p the softmax of the two scores."""
+    O = oracle_lib
+    D, _ = _identity_case()
+    d = 64
+    q = np.zeros((1, 1, d))
+    q[0, 0, 3], q[0, 0, 10] = 2.0, -2.0
+    ck = O.pack_codes(np.array([[[[3], [10]]]]), np.array([[[[1.5], [-0.75]]]]),
+                      np.array([[[3, -1]]]), np.array([[[0.5, 0.0]]]))
+    cv = O.pack_codes(np.array([[[[5], [6]]]]), np.array([[[[2.0], [-0.5]]]]),
+                      np.array([[[-1, 5]]]), np.array([[[0.0, 0.25]]]))
+    out = O.attend(D, D, ck, cv, np.array([2]), q)
+    s0, s1 = (1.5 + 0.5) * 2.0 / 8.0, -0.75 * -2.0 / 8.0
+    p0 = math.exp(s0) / (math.exp(s0) + math.exp(s1))
+    p1 = 1.0 - p0
+    want = np.zeros(d)
+    want[5] = 2.0 * p0 + 0.25 * p1
+    want[6] = -0.5 * p1
+    np.testing.assert_allclose(out[0, 0], want, rtol=1e-14, atol=1e-15)
+
+
+def test_attend_grouped_heads_and_lengths(oracle_lib):
+    """Four query heads over two KV heads: heads 0, 1 read KV head 0 and
+    heads 2, 3 KV head 1.  Every value token of KV head k is c_k e_(20+k),
+    so the output is that vector whatever the weights; tokens at or past a
+    sequence's length hold codes of another atom and must not count; an
+    empty sequence gives 0."""
+    O = oracle_lib
+    D, _ = _identity_case()
+    d, Tmax = 64, 6
+    g = np.random.default_rng(20)
+    B, Hkv, Hq = 3, 2, 4
+    lengths = np.array([6, 2, 0])
+    kid = g.integers(0, 64, (B, Hkv, Tmax, 2))
+    kco = g.standard_normal((B, Hkv, Tmax, 2))
+    vid = np.zeros((B, Hkv, Tmax, 2), np.int64)
+    vco = np.zeros((B, Hkv, Tmax, 2))
+    for b in range(B):
+        for k in range(Hkv):
+            for t in range(Tmax):
+                inside = t < lengths[b]
+                vid[b, k, t] = [20 + k, 40] if inside else [50, 51]
+                vco[b, k, t] = [1.0 + k, 0.0] if inside else [9.0, 9.0]
+    ck = O.pack_codes(kid, kco)
+    cv = O.pack_codes(vid, vco)
+    q = g.standard_normal((B, Hq, d))
+    out = O.attend(D, D, ck, cv, lengths, q)
+    for b in range(B):
+        for h in range(Hq):
+            want = np.zeros(d)
+            if lengths[b] > 0:
+                want[20 + h // 2] = 1.0 + h // 2
+            np.testing.assert_allclose(out[b, h], want, rtol=1e-13, atol=1e-14)
+
+
+def test_attend_identical_keys_average_values(oracle_lib):
+    """All keys equal: every token gets weight 1/T and the output is the
+    mean of the value vectors."""
+    O = oracle_lib
+    N = d = 64
+    T = 5
+    g = np.random.default_rng(21)
+    Dk = S.make_dictionary(N, d, np.float32, 7)
+    Dv = S.make_dictionary(N, d, np.float32, 8)
+    kid = np.broadcast_to(np.array([2, 11]), (1, 1, T, 2))
+    kco = np.broadcast_to(np.array([0.5, -1.0]), (1, 1, T, 2))
+    vid = g.integers(0, N, (1, 1, T, 2))
+    vco = np.round(g.standard_normal((1, 1, T, 2)) * 64) / 64     # exact in 11 bits
+    out = O.attend(Dk, Dv, O.pack_codes(kid, kco), O.pack_codes(vid, vco), np.array([T]),
+                   g.standard_normal((1, 2, d)))
+    Dv64 = Dv.astype(np.float64)
+    mean = sum(vco[0, 0, t, i] * Dv64[vid[0, 0, t, i]] for t in range(T) for i in range(2)) / T
+    for h in range(2):
+        np.testing.assert_allclose(out[0, h], mean, rtol=1e-13, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
 # adapt: hand-derived cases and invariants
 # --------------------------------------------------------------------------
 
