@@ -687,3 +687,89 @@ fadkv_status fadkv_debug_scores(fadkv_dict h, const void* x, int32_t V, float* s
 }
 
 }  // extern "C"
+
+fadkv_status fadkv_store_codes(int32_t G, int32_t B, int32_t H, int32_t s, int32_t N, const int32_t* idx,
+                               const float* coef, const int32_t* repl_id, const float* repl_coef,
+                               const int32_t* pos, uint32_t* cache, int32_t Tmax, void* stream)
+{
+    if (G < 0 || B < 0 || H < 1 || s < 0 || N < 1 || Tmax < 1) return FADKV_ERR_INVALID_ARG;
+    if (N > (1 << FADKV_PACK_ID_BITS) || s > FADKV_MAX_S) return FADKV_ERR_UNSUPPORTED;
+    if ((repl_id == nullptr) != (repl_coef == nullptr)) return FADKV_ERR_INVALID_ARG;
+    const long long work = (long long)G * B * H;
+    if (work > 0 && (!idx || !coef || !pos || !cache)) return FADKV_ERR_INVALID_ARG;
+    if (work > 0 && (!aligned(idx, 4) || !aligned(coef, 4) || !aligned(pos, 4) || !aligned(cache, 4) ||
+                     (repl_id && (!aligned(repl_id, 4) || !aligned(repl_coef, 4)))))
+        return FADKV_ERR_INVALID_ARG;
+    if (fault_injected()) {
+        set_error("fadkv_store_codes", cudaErrorLaunchFailure);
+        return FADKV_ERR_CUDA;
+    }
+    StoreArgs a;
+    a.G = G;
+    a.B = B;
+    a.H = H;
+    a.s = s;
+    a.N = N;
+    a.Tmax = Tmax;
+    a.idx = idx;
+    a.coef = coef;
+    a.repl_id = repl_id;
+    a.repl_coef = repl_coef;
+    a.pos = pos;
+    a.cache = cache;
+    const cudaError_t e = launch_store_codes(a, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        set_error("fadkv_store_codes", e);
+        return FADKV_ERR_CUDA;
+    }
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_attend(const fadkv_attn_params* p, const void* dict_k, const void* dict_v,
+                          const uint32_t* cache_k, const uint32_t* cache_v, const int32_t* lengths,
+                          const float* q, float* out, void* stream)
+{
+    if (!p) return FADKV_ERR_INVALID_ARG;
+    if (p->layers < 0 || p->B < 0 || p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0 || p->s < 0 ||
+        p->N < 1 || p->Tmax < 0 || !(p->scale == p->scale) || p->dict_stride < 0 || p->cache_stride < 0)
+        return FADKV_ERR_INVALID_ARG;
+    if (p->dtype != FADKV_F16 && p->dtype != FADKV_F32) return FADKV_ERR_INVALID_ARG;
+    if (!attend_supported(p->d, p->N, p->s)) return FADKV_ERR_UNSUPPORTED;
+    const long long work = (long long)p->layers * p->B;
+    if (work > 0 && (!dict_k || !dict_v || !cache_k || !cache_v || !lengths || !q || !out))
+        return FADKV_ERR_INVALID_ARG;
+    if (work > 0 && (!aligned(dict_k, 16) || !aligned(dict_v, 16) || p->dict_stride % 8 != 0 ||
+                     !aligned(cache_k, 4) || !aligned(cache_v, 4) || !aligned(lengths, 4) || !aligned(q, 4) ||
+                     !aligned(out, 4)))
+        return FADKV_ERR_INVALID_ARG;
+    if (fault_injected()) {
+        set_error("fadkv_attend", cudaErrorLaunchFailure);
+        return FADKV_ERR_CUDA;
+    }
+    AttendArgs a;
+    a.dict_k = dict_k;
+    a.dict_v = dict_v;
+    a.dict_stride = p->dict_stride;
+    a.cache_k = cache_k;
+    a.cache_v = cache_v;
+    a.cache_stride = p->cache_stride;
+    a.lengths = lengths;
+    a.q = q;
+    a.out = out;
+    a.L = p->layers;
+    a.B = p->B;
+    a.Hq = p->Hq;
+    a.Hkv = p->Hkv;
+    a.d = p->d;
+    a.N = p->N;
+    a.s = p->s;
+    a.Tmax = p->Tmax;
+    a.dtype = p->dtype;
+    a.scale = p->scale;
+    const cudaError_t e = launch_attend(a, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        set_error("fadkv_attend", e);
+        return FADKV_ERR_CUDA;
+    }
+    return FADKV_OK;
+}

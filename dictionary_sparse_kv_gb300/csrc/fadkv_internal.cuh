@@ -253,6 +253,36 @@ struct PlArgs {
 };
 cudaError_t launch_pl_fit(const Shape& sh, const PlArgs& a, cudaStream_t st);
 
+// The compressed store: packed words of a step's codes written into the
+// per-sequence caches [G][B][H][Tmax][s+1] at each sequence's position.
+struct StoreArgs {
+    int G, B, H, s, N, Tmax;
+    const int32_t* idx;       // [G][B*H][s]
+    const float* coef;
+    const int32_t* repl_id;   // [G][B*H] or null
+    const float* repl_coef;
+    const int32_t* pos;       // [B]
+    uint32_t* cache;
+};
+cudaError_t launch_store_codes(const StoreArgs& a, cudaStream_t st);
+
+// Decode attention over packed K/V codes, one CTA per (layer, sequence, KV head).
+struct AttendArgs {
+    const void* dict_k;       // layer l's key dictionary at dict_k + l * dict_stride (elements)
+    const void* dict_v;
+    long long dict_stride;
+    const uint32_t* cache_k;  // [B][Hkv][Tmax][s+1] per layer, layers cache_stride words apart
+    const uint32_t* cache_v;
+    long long cache_stride;
+    const int32_t* lengths;   // [B]
+    const float* q;           // [L][B][Hq][d]
+    float* out;               // [L][B][Hq][d]
+    int L, B, Hq, Hkv, d, N, s, Tmax, dtype;
+    float scale;
+};
+bool attend_supported(int d, int N, int s);
+cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st);
+
 // Fixed-size adaptation, one CTA per dictionary.
 struct AdaptArgs {
     void* atoms;

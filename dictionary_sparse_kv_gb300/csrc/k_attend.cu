@@ -1,0 +1,364 @@
+// The compressed KV store and decode attention that reads it.
+//
+// "FAD-KV: Adaptive Dictionary KV Caching for Efficient Reasoning Decoding",
+// Table 4 (per-sequence KV memory and decode latency of the dictionary
+// methods against full KV) and the abstract (each token's KV state is a
+// sparse combination of atoms).  The pages give neither a storage format
+// nor an attention kernel; this library's choices:
+//
+// Packed words.  One 32-bit word per nonzero: bits 31..13 hold the
+// coefficient rounded to 11 significant bits (round to nearest, ties to
+// even) in the layout of binary32's top 19 bits; bits 12..0 the atom id
+// (N <= 8192).  A token's code is s + 1 words (its s terms and the
+// replacement term, word 0 when absent).
+//
+// Attention.  For a query q and cached tokens with k_t = sum_i c_ti d_(j_ti):
+//   <q, k_t> = sum_i c_ti u_(j_ti),  u = D_K q      (one N x d product per query)
+//   sum_t p_t v_t = D_V^T w,  w_j = sum_t p_t sum_i c'_ti [j'_ti = j]
+// so neither K nor V is rebuilt: the token loop is s + 1 gathers from u and
+// s + 1 scatters into w per token.  One CTA per (layer, sequence, KV head)
+// handles the query heads that share the KV head, `hp` of them per pass:
+//   1. u = scale D_K q for the pass's heads (FP32 pipe, rows read once);
+//   2. tokens in chunks of kChunk: scores into shared memory, the chunk's
+//      maximum; when the running maximum grows, w and the partial sums are
+//      rescaled (online softmax at chunk granularity); then
+//      p = exp(score - max) and the value codes scatter p c' into w;
+//   3. o = D_V^T w / sum p.
+#include "fadkv_internal.cuh"
+
+namespace fadkv {
+namespace {
+
+constexpr int kAttThreads = 256;
+constexpr int kAttWarps = kAttThreads / 32;
+constexpr int kChunk = 2048;                 // tokens per softmax chunk
+constexpr uint32_t kIdMask = (1u << FADKV_PACK_ID_BITS) - 1u;
+
+__device__ __forceinline__ uint32_t pack_word(float c, int id, int N)
+{
+    if (id < 0 || id >= N || !(c != 0.f) || !isfinite(c)) return 0u;
+    uint32_t u = __float_as_uint(c);
+    if ((u & 0x7f800000u) == 0u) return (uint32_t)id;          // below 2^-126: no coefficient
+    u += 0x0fffu + ((u >> 13) & 1u);                          // round to nearest even at bit 13
+    if ((u & 0x7f800000u) == 0x7f800000u) u = (u & 0x80000000u) | 0x7f7fe000u;   // saturate
+    return (u & 0xffffe000u) | (uint32_t)id;
+}
+
+__device__ __forceinline__ float word_coef(uint32_t w) { return __uint_as_float(w & 0xffffe000u); }
+
+__global__ void __launch_bounds__(256)
+store_codes_kernel(StoreArgs a)
+{
+    const int W = a.s + 1;
+    const long long total = (long long)a.G * a.B * a.H * W;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int k = (int)(i % W);
+    const long long gv = i / W;                    // (g, b, h) flattened: v = b H + h
+    const int h = (int)(gv % a.H);
+    const int b = (int)((gv / a.H) % a.B);
+    const int g = (int)(gv / ((long long)a.H * a.B));
+    const int pos = a.pos[b];
+    if (pos < 0 || pos >= a.Tmax) return;
+    uint32_t w = 0u;
+    if (k < a.s) {
+        w = pack_word(a.coef[gv * a.s + k], a.idx[gv * a.s + k], a.N);
+    } else if (a.repl_id) {
+        w = pack_word(a.repl_coef[gv], a.repl_id[gv], a.N);
+    }
+    a.cache[((((size_t)g * a.B + b) * a.H + h) * a.Tmax + pos) * W + k] = w;
+}
+
+// ---------------------------------------------------------------------------
+// attention
+// ---------------------------------------------------------------------------
+
+template <typename T, int D> struct Rows;
+template <int D> struct Rows<__half, D> {
+    // 8 consecutive elements of a row as floats
+    static __device__ __forceinline__ void load8(const __half* p, float (&o)[8])
+    {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+        const __half2* h = reinterpret_cast<const __half2*>(&q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(h[i]);
+            o[2 * i] = f.x;
+            o[2 * i + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ float2 load2(const __half* p)
+    {
+        return __half22float2(*reinterpret_cast<const __half2*>(p));
+    }
+};
+template <int D> struct Rows<float, D> {
+    static __device__ __forceinline__ void load8(const float* p, float (&o)[8])
+    {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+        o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    }
+    static __device__ __forceinline__ float2 load2(const float* p)
+    {
+        return *reinterpret_cast<const float2*>(p);
+    }
+};
+
+__device__ __forceinline__ float block_max(float v, float* red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float m = red[0];
+#pragma unroll
+    for (int w = 1; w < kAttWarps; ++w) m = fmaxf(m, red[w]);
+    return m;
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAttWarps; ++w) s += red[w];
+    return s;
+}
+
+template <typename T, int D, int HP>
+__global__ void __launch_bounds__(kAttThreads)
+attend_kernel(AttendArgs a)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int N = a.N, W = a.s + 1, grp = a.Hq / a.Hkv;
+    const int l = blockIdx.y;
+    const int b = blockIdx.x / a.Hkv, hk = blockIdx.x % a.Hkv;
+    float* u = sm;                                  // [HP][N]
+    float* w = u + (size_t)HP * N;                  // [HP][N]
+    float* sc = w + (size_t)HP * N;                 // [HP][kChunk]
+    float* qs = sc + (size_t)HP * kChunk;           // [HP][D]
+    float* part = qs + HP * D;                      // [kAttThreads / (D/2)][HP][D] partial outputs
+    __shared__ float red[kAttWarps];
+    __shared__ float fac_s[HP];
+
+    const T* Dk = (const T*)a.dict_k + (size_t)l * a.dict_stride;
+    const T* Dv = (const T*)a.dict_v + (size_t)l * a.dict_stride;
+    const size_t cbase = (size_t)l * a.cache_stride + ((size_t)b * a.Hkv + hk) * a.Tmax * W;
+    const uint32_t* ck = a.cache_k + cbase;
+    const uint32_t* cv = a.cache_v + cbase;
+    int T_len = a.lengths[b];
+    T_len = T_len < 0 ? 0 : (T_len > a.Tmax ? a.Tmax : T_len);
+    const int tid = threadIdx.x;
+
+    for (int h0 = 0; h0 < grp; h0 += HP) {
+        const int hn = min(HP, grp - h0);
+        const float* q = a.q + (((size_t)l * a.B + b) * a.Hq + hk * grp + h0) * D;
+        float* out = a.out + (((size_t)l * a.B + b) * a.Hq + hk * grp + h0) * D;
+        for (int i = tid; i < HP * D; i += kAttThreads) qs[i] = (i / D < hn) ? q[i] : 0.f;
+        __syncthreads();
+
+        // 1. u = scale D_K q, one atom row per thread at a time
+        for (int j = tid; j < N; j += kAttThreads) {
+            float acc[HP];
+#pragma unroll
+            for (int h = 0; h < HP; ++h) acc[h] = 0.f;
+            const T* row = Dk + (size_t)j * D;
+#pragma unroll 4
+            for (int e0 = 0; e0 < D; e0 += 8) {
+                float r[8];
+                Rows<T, D>::load8(row + e0, r);
+#pragma unroll
+                for (int h = 0; h < HP; ++h) {
+                    const float4 qa = *reinterpret_cast<const float4*>(qs + h * D + e0);
+                    const float4 qb = *reinterpret_cast<const float4*>(qs + h * D + e0 + 4);
+                    acc[h] = fmaf(r[0], qa.x, acc[h]);
+                    acc[h] = fmaf(r[1], qa.y, acc[h]);
+                    acc[h] = fmaf(r[2], qa.z, acc[h]);
+                    acc[h] = fmaf(r[3], qa.w, acc[h]);
+                    acc[h] = fmaf(r[4], qb.x, acc[h]);
+                    acc[h] = fmaf(r[5], qb.y, acc[h]);
+                    acc[h] = fmaf(r[6], qb.z, acc[h]);
+                    acc[h] = fmaf(r[7], qb.w, acc[h]);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < HP; ++h) {
+                u[(size_t)h * N + j] = acc[h] * a.scale;
+                w[(size_t)h * N + j] = 0.f;
+            }
+        }
+        __syncthreads();
+
+        // 2. tokens, chunk by chunk, with the running maximum and sums
+        float M[HP], psum[HP];
+#pragma unroll
+        for (int h = 0; h < HP; ++h) {
+            M[h] = -INFINITY;
+            psum[h] = 0.f;
+        }
+        for (int c0 = 0; c0 < T_len; c0 += kChunk) {
+            const int cn = min(kChunk, T_len - c0);
+            float mloc[HP];
+#pragma unroll
+            for (int h = 0; h < HP; ++h) mloc[h] = -INFINITY;
+            for (int t = tid; t < cn; t += kAttThreads) {
+                const uint32_t* wk = ck + (size_t)(c0 + t) * W;
+                float s_[HP];
+#pragma unroll
+                for (int h = 0; h < HP; ++h) s_[h] = 0.f;
+                for (int i = 0; i < W; ++i) {
+                    const uint32_t wd = __ldg(wk + i);
+                    const float c = word_coef(wd);
+                    const uint32_t j = min(wd & kIdMask, (uint32_t)(N - 1));
+#pragma unroll
+                    for (int h = 0; h < HP; ++h) s_[h] = fmaf(c, u[(size_t)h * N + j], s_[h]);
+                }
+#pragma unroll
+                for (int h = 0; h < HP; ++h) {
+                    sc[h * kChunk + t] = s_[h];
+                    mloc[h] = fmaxf(mloc[h], s_[h]);
+                }
+            }
+            float Mn[HP];
+#pragma unroll
+            for (int h = 0; h < HP; ++h) Mn[h] = fmaxf(M[h], block_max(mloc[h], red));
+            // rescale w and the partial sums where the maximum grew
+            bool grew = false;
+#pragma unroll
+            for (int h = 0; h < HP; ++h) grew |= Mn[h] > M[h] && M[h] > -INFINITY;
+            if (tid < HP) fac_s[tid] = 1.f;
+            __syncthreads();
+#pragma unroll
+            for (int h = 0; h < HP; ++h) {
+                const float f = (Mn[h] > M[h] && M[h] > -INFINITY) ? __expf(M[h] - Mn[h]) : 1.f;
+                psum[h] *= f;
+                if (tid == 0) fac_s[h] = f;
+                M[h] = Mn[h];
+            }
+            __syncthreads();
+            if (grew) {
+                for (int i = tid; i < HP * N; i += kAttThreads) w[i] *= fac_s[i / N];
+            }
+            __syncthreads();
+            for (int t = tid; t < cn; t += kAttThreads) {
+                const uint32_t* wv = cv + (size_t)(c0 + t) * W;
+                float p[HP];
+#pragma unroll
+                for (int h = 0; h < HP; ++h) {
+                    p[h] = __expf(sc[h * kChunk + t] - M[h]);
+                    psum[h] += p[h];
+                }
+                for (int i = 0; i < W; ++i) {
+                    const uint32_t wd = __ldg(wv + i);
+                    const float c = word_coef(wd);
+                    if (c == 0.f) continue;
+                    const uint32_t j = min(wd & kIdMask, (uint32_t)(N - 1));
+#pragma unroll
+                    for (int h = 0; h < HP; ++h) atomicAdd(&w[(size_t)h * N + j], p[h] * c);
+                }
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int h = 0; h < HP; ++h) {
+            const float S = block_sum(psum[h], red);
+            if (tid == 0) fac_s[h] = S;                 // the sums, read back below
+        }
+
+        // 3. o = D_V^T w / S: thread = (atom group, column pair)
+        constexpr int CP = D / 2;                       // column pairs
+        constexpr int AG = kAttThreads / CP;            // atom groups
+        const int cp = tid % CP, ag = tid / CP;
+        float o[HP][2];
+#pragma unroll
+        for (int h = 0; h < HP; ++h) o[h][0] = o[h][1] = 0.f;
+        for (int j = ag; j < N; j += AG) {
+            const float2 v = Rows<T, D>::load2(Dv + (size_t)j * D + 2 * cp);
+#pragma unroll
+            for (int h = 0; h < HP; ++h) {
+                const float wj = w[(size_t)h * N + j];
+                o[h][0] = fmaf(wj, v.x, o[h][0]);
+                o[h][1] = fmaf(wj, v.y, o[h][1]);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < HP; ++h) {
+            part[((size_t)ag * HP + h) * D + 2 * cp] = o[h][0];
+            part[((size_t)ag * HP + h) * D + 2 * cp + 1] = o[h][1];
+        }
+        __syncthreads();
+        for (int i = tid; i < hn * D; i += kAttThreads) {
+            const int h = i / D;
+            float acc = 0.f;
+            for (int g2 = 0; g2 < AG; ++g2) acc += part[((size_t)g2 * HP + h) * D + (i % D)];
+            const float S = fac_s[h];
+            out[i] = S > 0.f ? acc / S : 0.f;
+        }
+        __syncthreads();
+    }
+}
+
+template <int D, int HP>
+size_t attend_smem(int N)
+{
+    const int AG = kAttThreads / (D / 2);
+    return sizeof(float) * ((size_t)2 * HP * N + (size_t)HP * kChunk + (size_t)HP * D + (size_t)AG * HP * D);
+}
+
+template <typename T, int D, int HP>
+cudaError_t launch_hp(const AttendArgs& a, cudaStream_t st)
+{
+    const size_t smem = attend_smem<D, HP>(a.N);
+    auto k = attend_kernel<T, D, HP>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k<<<dim3(a.B * a.Hkv, a.L), kAttThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+constexpr size_t kAttSmemMax = 200 * 1024;
+
+template <typename T, int D>
+cudaError_t launch_d(const AttendArgs& a, cudaStream_t st)
+{
+    const int grp = a.Hq / a.Hkv;
+    if (grp >= 4 && attend_smem<D, 4>(a.N) <= kAttSmemMax) return launch_hp<T, D, 4>(a, st);
+    if (grp >= 3 && attend_smem<D, 3>(a.N) <= kAttSmemMax) return launch_hp<T, D, 3>(a, st);
+    if (grp >= 2 && attend_smem<D, 2>(a.N) <= kAttSmemMax) return launch_hp<T, D, 2>(a, st);
+    return launch_hp<T, D, 1>(a, st);
+}
+
+}  // namespace
+
+bool attend_supported(int d, int N, int s)
+{
+    if (d != 64 && d != 128) return false;
+    if (N < 1 || N > (1 << FADKV_PACK_ID_BITS) || s < 0 || s > FADKV_MAX_S) return false;
+    return d == 128 ? attend_smem<128, 1>(N) <= kAttSmemMax : attend_smem<64, 1>(N) <= kAttSmemMax;
+}
+
+cudaError_t launch_store_codes(const StoreArgs& a, cudaStream_t st)
+{
+    const long long total = (long long)a.G * a.B * a.H * (a.s + 1);
+    if (total <= 0) return cudaSuccess;
+    store_codes_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st)
+{
+    if (a.L <= 0 || a.B <= 0) return cudaSuccess;
+    if (a.dtype == FADKV_F16) return a.d == 128 ? launch_d<__half, 128>(a, st) : launch_d<__half, 64>(a, st);
+    return a.d == 128 ? launch_d<float, 128>(a, st) : launch_d<float, 64>(a, st);
+}
+
+}  // namespace fadkv

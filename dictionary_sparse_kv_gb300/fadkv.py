@@ -55,6 +55,23 @@ class Params(C.Structure):
     ]
 
 
+class AttnParams(C.Structure):
+    _fields_ = [
+        ("layers", C.c_int32),
+        ("B", C.c_int32),
+        ("Hq", C.c_int32),
+        ("Hkv", C.c_int32),
+        ("d", C.c_int32),
+        ("N", C.c_int32),
+        ("s", C.c_int32),
+        ("Tmax", C.c_int32),
+        ("dtype", C.c_int32),
+        ("scale", C.c_float),
+        ("dict_stride", C.c_int64),
+        ("cache_stride", C.c_int64),
+    ]
+
+
 def params(num_dicts, N, d, n, s, dtype=F16, max_batch=1, lambda_abs=1e-4, lambda_rel=0.20) -> Params:
     """Handle parameters; the ridge defaults are Table 5's 1e-4 + 0.20 diag(G)."""
     return Params(num_dicts, N, d, n, s, lambda_abs, lambda_rel, dtype, max_batch)
@@ -87,6 +104,10 @@ _SIGS = {
     "fadkv_dict_stats": ([C.c_void_p, C.POINTER(C.c_int64), C.c_void_p], C.c_int),
     "fadkv_debug_pool": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "fadkv_debug_scores": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p], C.c_int),
+    "fadkv_store_codes": ([C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                           C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p], C.c_int),
+    "fadkv_attend": ([C.POINTER(AttnParams), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                      C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "fadkv_profile_enable": ([C.c_void_p, C.c_int32], C.c_int),
     "fadkv_profile_select": ([C.c_void_p, C.c_uint32], C.c_int),
     "fadkv_profile_read": ([C.c_void_p, C.POINTER(C.c_int64), C.POINTER(C.c_double), C.c_int32], C.c_int),
@@ -197,6 +218,21 @@ def adapt_noalloc(p: Params, atoms, usage, delta, x, V: int, idx, coef, relres, 
                                    _addr(coef), _addr(relres), _addr(repl_id), _addr(repl_coef), st)
     if rc != 0:
         raise FadkvError("fadkv_adapt_noalloc", rc, last_error())
+
+
+def store_codes(G: int, B: int, H: int, s: int, N: int, idx, coef, repl_id, repl_coef, pos, cache, Tmax: int,
+                stream=None) -> None:
+    """Packed words of one step's codes into caches [G][B][H][Tmax][s+1] at pos[b]."""
+    st = _stream(stream, idx, cache)
+    _check("fadkv_store_codes", lib().fadkv_store_codes(G, B, H, s, N, _addr(idx), _addr(coef), _addr(repl_id),
+                                                        _addr(repl_coef), _addr(pos), _addr(cache), Tmax, st))
+
+
+def attend(p: AttnParams, dict_k, dict_v, cache_k, cache_v, lengths, q, out, stream=None) -> None:
+    """Decode attention over packed K/V codes (see fadkv_attend)."""
+    st = _stream(stream, q, out)
+    _check("fadkv_attend", lib().fadkv_attend(C.byref(p), _addr(dict_k), _addr(dict_v), _addr(cache_k),
+                                              _addr(cache_v), _addr(lengths), _addr(q), _addr(out), st))
 
 
 def reconstruct(h: int, V: int, idx, coef, repl_id, repl_coef, xhat, stream=None) -> None:

@@ -263,6 +263,79 @@ fadkv_status fadkv_debug_pool(fadkv_dict dict, const void* x, int32_t V, int32_t
    (at least min(max_batch, 128)).  Errors: INVALID_ARG, CUDA. */
 fadkv_status fadkv_debug_scores(fadkv_dict dict, const void* x, int32_t V, float* scores, void* stream);
 
+/* ---------------------------------------------------------------------------
+   The compressed KV store and decode attention over it.  Handle-free: both
+   calls work on caller-owned buffers only.
+
+   What the cache keeps instead of K and V is the codes (Table 4: the
+   per-sequence KV memory of the dictionary methods against full KV).  The
+   pages give no storage format; this library packs every nonzero into one
+   32-bit word:
+     bits 31..13  the coefficient rounded to 11 significant bits (round to
+                  nearest, ties to even) in the layout of binary32's top 19
+                  bits (sign, 8-bit exponent, 10 fraction bits); magnitudes
+                  below 2^-126 are stored as 0;
+     bits 12..0   the atom id (so N <= 8192).
+   A token's code is s + 1 words: its s terms, then its replacement term
+   from the adaptation (word 0 when it has none).  A skipped term (id -1, a
+   zero or non-finite coefficient) is word 0: coefficient 0, atom 0.
+   --------------------------------------------------------------------------- */
+#define FADKV_PACK_ID_BITS 13
+
+/* Store one step's codes in the per-sequence caches.
+     G dictionaries, each with V = B * H vectors ordered v = b * H + h
+     (sequence b, KV head h); idx / coef [G][V][s] and repl_id / repl_coef
+     [G][V] (both NULL: no replacement words) as fadkv_encode / fadkv_adapt
+     wrote them; pos [B] device int32: the token position of this step in
+     each sequence's cache; cache [G][B][H][Tmax][s+1] uint32, written at
+     [g][b][h][pos[b]][0..s] only (positions outside [0, Tmax) are skipped).
+   All pointers are device pointers, 4-byte aligned.  Asynchronous on
+   `stream`.  Errors: INVALID_ARG, UNSUPPORTED (N > 8192, s > FADKV_MAX_S),
+   CUDA. */
+fadkv_status fadkv_store_codes(int32_t G, int32_t B, int32_t H, int32_t s, int32_t N, const int32_t* idx,
+                               const float* coef, const int32_t* repl_id, const float* repl_coef,
+                               const int32_t* pos, uint32_t* cache, int32_t Tmax, void* stream);
+
+typedef struct {
+    int32_t layers;     /* L */
+    int32_t B;          /* sequences */
+    int32_t Hq;         /* query heads (a multiple of Hkv) */
+    int32_t Hkv;        /* KV heads; query head h reads KV head h / (Hq / Hkv) */
+    int32_t d;          /* head dimension: 64 or 128 */
+    int32_t N;          /* atoms per dictionary, <= 8192 */
+    int32_t s;          /* terms per code (s + 1 words per token) */
+    int32_t Tmax;       /* cache capacity in tokens */
+    int32_t dtype;      /* fadkv_dtype of the dictionaries */
+    float scale;        /* score scale, 1/sqrt(d) for standard attention */
+    int64_t dict_stride;   /* elements from layer l's key (value) dictionary to layer l+1's; a multiple of 8 */
+    int64_t cache_stride;  /* words from layer l's key (value) cache to layer l+1's */
+} fadkv_attn_params;
+
+/* Decode attention over the compressed store, for every layer, sequence and
+   query head in one launch:
+     out[l][b][h] = sum_t p_t v_t,  p = softmax_t(scale <q[l][b][h], k_t>),
+   over the tokens t < lengths[b] of KV head h / (Hq / Hkv) of sequence b,
+   where k_t and v_t are the sparse combinations their packed codes name:
+   k_t = sum_i c_ti dict_k[j_ti].  Neither K nor V is rebuilt: with
+   u = dict_k q the scores are s + 1 gathers from u per token, and the output
+   is dict_v^T w with w the attention-weighted sum of the value codes.
+     dict_k, dict_v  device, layer l's [N][d] dictionaries at + l*dict_stride
+                     (with one handle's atoms [2L][N][d], keys at even g:
+                     dict_k = atoms, dict_v = atoms + N*d, dict_stride = 2*N*d),
+                     16-byte aligned
+     cache_k, cache_v device, layer l's [B][Hkv][Tmax][s+1] packed codes at
+                     + l*cache_stride (fadkv_store_codes with G = 2L: cache_k
+                     = cache, cache_v = cache + B*Hkv*Tmax*(s+1), cache_stride
+                     = 2*B*Hkv*Tmax*(s+1))
+     lengths         device [B] int32, clamped to [0, Tmax]; an empty
+                     sequence gives 0
+     q, out          device [L][B][Hq][d] float32
+   FP32 arithmetic.  Asynchronous on `stream`.  Errors: INVALID_ARG,
+   UNSUPPORTED, CUDA. */
+fadkv_status fadkv_attend(const fadkv_attn_params* params, const void* dict_k, const void* dict_v,
+                          const uint32_t* cache_k, const uint32_t* cache_v, const int32_t* lengths,
+                          const float* q, float* out, void* stream);
+
 /* Kernel classes reported by fadkv_profile_read. */
 #define FADKV_PROFILE_KERNELS 8
 #define FADKV_K_SCREEN 0       /* screening (tensor cores + candidate filter, or FP32 scores) */
