@@ -19,19 +19,20 @@
 // s + 1 scatters into w per token.  One CTA per (layer, sequence, KV head)
 // handles the query heads that share the KV head, `hp` of them per pass:
 //   1. u = scale D_K q for the pass's heads (FP32 pipe, rows read once);
-//   2. tokens in chunks of kChunk: scores into shared memory, the chunk's
-//      maximum; when the running maximum grows, w and the partial sums are
-//      rescaled (online softmax at chunk granularity); then
-//      p = exp(score - max) and the value codes scatter p c' into w;
+//   2. tokens in chunks (1024 with s + 1 <= 9 words): every thread loads all
+//      words of its tokens at once, keeps their scores in registers, the
+//      block forms the chunk's maximum; when the running maximum grows, w
+//      and the partial sums are rescaled (online softmax at chunk
+//      granularity); then p = exp(score - max) and the value codes scatter
+//      p c' into w;
 //   3. o = D_V^T w / sum p.
 #include "fadkv_internal.cuh"
 
 namespace fadkv {
 namespace {
 
-constexpr int kAttThreads = 256;
+constexpr int kAttThreads = 512;
 constexpr int kAttWarps = kAttThreads / 32;
-constexpr int kChunk = 2048;                 // tokens per softmax chunk
 constexpr uint32_t kIdMask = (1u << FADKV_PACK_ID_BITS) - 1u;
 
 __device__ __forceinline__ uint32_t pack_word(float c, int id, int N)
@@ -106,48 +107,71 @@ template <int D> struct Rows<float, D> {
     }
 };
 
-__device__ __forceinline__ float block_max(float v, float* red)
+// Block-wide maximum / sum of HP values per thread at once (one barrier
+// pair); `red` holds kAttWarps * HP floats.
+template <int HP>
+__device__ __forceinline__ void block_max_n(float (&v)[HP], float* red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float m = red[0];
+    for (int h = 0; h < HP; ++h)
 #pragma unroll
-    for (int w = 1; w < kAttWarps; ++w) m = fmaxf(m, red[w]);
-    return m;
+        for (int o = 16; o > 0; o >>= 1) v[h] = fmaxf(v[h], __shfl_xor_sync(0xffffffffu, v[h], o));
+    __syncthreads();
+    if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < HP; ++h) red[warp * HP + h] = v[h];
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < HP; ++h) {
+        float m = red[h];
+#pragma unroll
+        for (int w = 1; w < kAttWarps; ++w) m = fmaxf(m, red[w * HP + h]);
+        v[h] = m;
+    }
 }
 
-__device__ __forceinline__ float block_sum(float v, float* red)
+template <int HP>
+__device__ __forceinline__ void block_sum_n(float (&v)[HP], float* red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float s = 0.f;
+    for (int h = 0; h < HP; ++h)
 #pragma unroll
-    for (int w = 0; w < kAttWarps; ++w) s += red[w];
-    return s;
+        for (int o = 16; o > 0; o >>= 1) v[h] += __shfl_xor_sync(0xffffffffu, v[h], o);
+    __syncthreads();
+    if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < HP; ++h) red[warp * HP + h] = v[h];
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < HP; ++h) {
+        float m = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAttWarps; ++w) m += red[w * HP + h];
+        v[h] = m;
+    }
 }
 
-template <typename T, int D, int HP>
-__global__ void __launch_bounds__(kAttThreads)
+// Tokens per thread per softmax chunk: a thread holds every word of its
+// tokens in registers before using them (WM words per token at most).
+template <int WM> __host__ __device__ constexpr int tokens_per_thread() { return WM <= 9 ? 2 : 1; }
+
+template <typename T, int D, int HP, int WM>
+__global__ void __launch_bounds__(kAttThreads, 2)
 attend_kernel(AttendArgs a)
 {
+    constexpr int TPT = tokens_per_thread<WM>();
+    constexpr int CH = TPT * kAttThreads;           // tokens per chunk
     extern __shared__ __align__(16) float sm[];
     const int N = a.N, W = a.s + 1, grp = a.Hq / a.Hkv;
     const int l = blockIdx.y;
     const int b = blockIdx.x / a.Hkv, hk = blockIdx.x % a.Hkv;
     float* u = sm;                                  // [HP][N]
     float* w = u + (size_t)HP * N;                  // [HP][N]
-    float* sc = w + (size_t)HP * N;                 // [HP][kChunk]
-    float* qs = sc + (size_t)HP * kChunk;           // [HP][D]
-    float* part = qs + HP * D;                      // [kAttThreads / (D/2)][HP][D] partial outputs
-    __shared__ float red[kAttWarps];
+    float* qs = w + (size_t)HP * N;                 // [HP][D]
+    float* part = qs + HP * D;                      // [atom groups][HP][D] partial outputs
+    __shared__ float red[kAttWarps * HP];
     __shared__ float fac_s[HP];
 
     const T* Dk = (const T*)a.dict_k + (size_t)l * a.dict_stride;
@@ -172,7 +196,7 @@ attend_kernel(AttendArgs a)
 #pragma unroll
             for (int h = 0; h < HP; ++h) acc[h] = 0.f;
             const T* row = Dk + (size_t)j * D;
-#pragma unroll 4
+#pragma unroll 8
             for (int e0 = 0; e0 < D; e0 += 8) {
                 float r[8];
                 Rows<T, D>::load8(row + e0, r);
@@ -198,81 +222,92 @@ attend_kernel(AttendArgs a)
         }
         __syncthreads();
 
-        // 2. tokens, chunk by chunk, with the running maximum and sums
+        // 2. tokens, chunk by chunk, with the running maximum and sums; a
+        //    thread's tokens of a chunk are c0 + tid + k * kAttThreads
         float M[HP], psum[HP];
 #pragma unroll
         for (int h = 0; h < HP; ++h) {
             M[h] = -INFINITY;
             psum[h] = 0.f;
         }
-        for (int c0 = 0; c0 < T_len; c0 += kChunk) {
-            const int cn = min(kChunk, T_len - c0);
-            float mloc[HP];
+        for (int c0 = 0; c0 < T_len; c0 += CH) {
+            uint32_t wd[TPT][WM];
 #pragma unroll
-            for (int h = 0; h < HP; ++h) mloc[h] = -INFINITY;
-            for (int t = tid; t < cn; t += kAttThreads) {
-                const uint32_t* wk = ck + (size_t)(c0 + t) * W;
-                float s_[HP];
+            for (int k = 0; k < TPT; ++k) {
+                const int t = c0 + tid + k * kAttThreads;
+                const uint32_t* src = ck + (size_t)t * W;
 #pragma unroll
-                for (int h = 0; h < HP; ++h) s_[h] = 0.f;
-                for (int i = 0; i < W; ++i) {
-                    const uint32_t wd = __ldg(wk + i);
-                    const float c = word_coef(wd);
-                    const uint32_t j = min(wd & kIdMask, (uint32_t)(N - 1));
-#pragma unroll
-                    for (int h = 0; h < HP; ++h) s_[h] = fmaf(c, u[(size_t)h * N + j], s_[h]);
-                }
-#pragma unroll
-                for (int h = 0; h < HP; ++h) {
-                    sc[h * kChunk + t] = s_[h];
-                    mloc[h] = fmaxf(mloc[h], s_[h]);
-                }
+                for (int i = 0; i < WM; ++i) wd[k][i] = (t < T_len && i < W) ? __ldg(src + i) : 0u;
             }
-            float Mn[HP];
+            float sc[TPT][HP], mx[HP];
 #pragma unroll
-            for (int h = 0; h < HP; ++h) Mn[h] = fmaxf(M[h], block_max(mloc[h], red));
-            // rescale w and the partial sums where the maximum grew
+            for (int h = 0; h < HP; ++h) mx[h] = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < TPT; ++k) {
+#pragma unroll
+                for (int h = 0; h < HP; ++h) sc[k][h] = 0.f;
+#pragma unroll
+                for (int i = 0; i < WM; ++i) {
+                    const float c = word_coef(wd[k][i]);
+                    const uint32_t j = min(wd[k][i] & kIdMask, (uint32_t)(N - 1));
+#pragma unroll
+                    for (int h = 0; h < HP; ++h) sc[k][h] = fmaf(c, u[(size_t)h * N + j], sc[k][h]);
+                }
+                if (c0 + tid + k * kAttThreads < T_len)
+#pragma unroll
+                    for (int h = 0; h < HP; ++h) mx[h] = fmaxf(mx[h], sc[k][h]);
+            }
+            // the value words of the same tokens, loaded while the maximum is formed
+#pragma unroll
+            for (int k = 0; k < TPT; ++k) {
+                const int t = c0 + tid + k * kAttThreads;
+                const uint32_t* src = cv + (size_t)t * W;
+#pragma unroll
+                for (int i = 0; i < WM; ++i) wd[k][i] = (t < T_len && i < W) ? __ldg(src + i) : 0u;
+            }
+            block_max_n<HP>(mx, red);
+            // rescale w and the partial sums where the running maximum grew
             bool grew = false;
 #pragma unroll
-            for (int h = 0; h < HP; ++h) grew |= Mn[h] > M[h] && M[h] > -INFINITY;
-            if (tid < HP) fac_s[tid] = 1.f;
-            __syncthreads();
-#pragma unroll
             for (int h = 0; h < HP; ++h) {
-                const float f = (Mn[h] > M[h] && M[h] > -INFINITY) ? __expf(M[h] - Mn[h]) : 1.f;
+                const float Mn = fmaxf(M[h], mx[h]);
+                const bool g = Mn > M[h] && M[h] > -INFINITY;
+                const float f = g ? __expf(M[h] - Mn) : 1.f;
+                grew |= g;
                 psum[h] *= f;
                 if (tid == 0) fac_s[h] = f;
-                M[h] = Mn[h];
+                M[h] = Mn;
             }
-            __syncthreads();
             if (grew) {
+                __syncthreads();
                 for (int i = tid; i < HP * N; i += kAttThreads) w[i] *= fac_s[i / N];
+                __syncthreads();
             }
-            __syncthreads();
-            for (int t = tid; t < cn; t += kAttThreads) {
-                const uint32_t* wv = cv + (size_t)(c0 + t) * W;
+#pragma unroll
+            for (int k = 0; k < TPT; ++k) {
+                if (c0 + tid + k * kAttThreads >= T_len) continue;
                 float p[HP];
 #pragma unroll
                 for (int h = 0; h < HP; ++h) {
-                    p[h] = __expf(sc[h * kChunk + t] - M[h]);
+                    p[h] = __expf(sc[k][h] - M[h]);
                     psum[h] += p[h];
                 }
-                for (int i = 0; i < W; ++i) {
-                    const uint32_t wd = __ldg(wv + i);
-                    const float c = word_coef(wd);
+#pragma unroll
+                for (int i = 0; i < WM; ++i) {
+                    const float c = word_coef(wd[k][i]);
                     if (c == 0.f) continue;
-                    const uint32_t j = min(wd & kIdMask, (uint32_t)(N - 1));
+                    const uint32_t j = min(wd[k][i] & kIdMask, (uint32_t)(N - 1));
 #pragma unroll
                     for (int h = 0; h < HP; ++h) atomicAdd(&w[(size_t)h * N + j], p[h] * c);
                 }
             }
-            __syncthreads();
         }
+        block_sum_n<HP>(psum, red);
+        if (tid < HP) fac_s[tid] = 0.f;
 #pragma unroll
-        for (int h = 0; h < HP; ++h) {
-            const float S = block_sum(psum[h], red);
-            if (tid == 0) fac_s[h] = S;                 // the sums, read back below
-        }
+        for (int h = 0; h < HP; ++h)
+            if (tid == 0) fac_s[h] = psum[h];           // the sums, read back below
+        __syncthreads();
 
         // 3. o = D_V^T w / S: thread = (atom group, column pair)
         constexpr int CP = D / 2;                       // column pairs
@@ -281,6 +316,7 @@ attend_kernel(AttendArgs a)
         float o[HP][2];
 #pragma unroll
         for (int h = 0; h < HP; ++h) o[h][0] = o[h][1] = 0.f;
+#pragma unroll 8
         for (int j = ag; j < N; j += AG) {
             const float2 v = Rows<T, D>::load2(Dv + (size_t)j * D + 2 * cp);
 #pragma unroll
@@ -311,18 +347,27 @@ template <int D, int HP>
 size_t attend_smem(int N)
 {
     const int AG = kAttThreads / (D / 2);
-    return sizeof(float) * ((size_t)2 * HP * N + (size_t)HP * kChunk + (size_t)HP * D + (size_t)AG * HP * D);
+    return sizeof(float) * ((size_t)2 * HP * N + (size_t)HP * D + (size_t)AG * HP * D);
+}
+
+template <typename T, int D, int HP, int WM>
+cudaError_t launch_hpw(const AttendArgs& a, cudaStream_t st)
+{
+    const size_t smem = attend_smem<D, HP>(a.N);
+    auto k = attend_kernel<T, D, HP, WM>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k<<<dim3(a.B * a.Hkv, a.L), kAttThreads, smem, st>>>(a);
+    return cudaGetLastError();
 }
 
 template <typename T, int D, int HP>
 cudaError_t launch_hp(const AttendArgs& a, cudaStream_t st)
 {
-    const size_t smem = attend_smem<D, HP>(a.N);
-    auto k = attend_kernel<T, D, HP>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k<<<dim3(a.B * a.Hkv, a.L), kAttThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    const int W = a.s + 1;
+    if (W <= 9) return launch_hpw<T, D, HP, 9>(a, st);
+    if (W <= 17) return launch_hpw<T, D, HP, 17>(a, st);
+    return launch_hpw<T, D, HP, 33>(a, st);
 }
 
 constexpr size_t kAttSmemMax = 200 * 1024;
