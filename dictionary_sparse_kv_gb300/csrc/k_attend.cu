@@ -18,7 +18,8 @@
 // so neither K nor V is rebuilt: the token loop is s + 1 gathers from u and
 // s + 1 scatters into w per token.  One CTA per (layer, sequence, KV head)
 // handles the query heads that share the KV head, `hp` of them per pass:
-//   1. u = scale D_K q for the pass's heads (FP32 pipe, rows read once);
+//   1. u = scale D_K q for the pass's heads (FP32 pipe, rows read once,
+//      a half-warp per row);
 //   2. tokens in chunks (1024 with s + 1 <= 9 words): every thread loads all
 //      words of its tokens at once, keeps their scores in registers, the
 //      block forms the chunk's maximum; when the running maximum grows, w
@@ -76,6 +77,19 @@ store_codes_kernel(StoreArgs a)
 
 template <typename T, int D> struct Rows;
 template <int D> struct Rows<__half, D> {
+    // EL (4 or 8) consecutive elements of a row as floats
+    template <int EL>
+    static __device__ __forceinline__ void load(const __half* p, float (&o)[EL])
+    {
+        if constexpr (EL == 8) {
+            load8(p, o);
+        } else {
+            const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&q.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&q.y));
+            o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+        }
+    }
     // 8 consecutive elements of a row as floats
     static __device__ __forceinline__ void load8(const __half* p, float (&o)[8])
     {
@@ -94,6 +108,16 @@ template <int D> struct Rows<__half, D> {
     }
 };
 template <int D> struct Rows<float, D> {
+    template <int EL>
+    static __device__ __forceinline__ void load(const float* p, float (&o)[EL])
+    {
+        if constexpr (EL == 8) {
+            load8(p, o);
+        } else {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+            o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+        }
+    }
     static __device__ __forceinline__ void load8(const float* p, float (&o)[8])
     {
         const float4 a = __ldg(reinterpret_cast<const float4*>(p));
@@ -190,35 +214,44 @@ attend_kernel(AttendArgs a)
         for (int i = tid; i < HP * D; i += kAttThreads) qs[i] = (i / D < hn) ? q[i] : 0.f;
         __syncthreads();
 
-        // 1. u = scale D_K q, one atom row per thread at a time
-        for (int j = tid; j < N; j += kAttThreads) {
-            float acc[HP];
+        // 1. u = scale D_K q: half-warps read whole rows (coalesced), every
+        //    lane takes D/16 consecutive elements against its slice of q held
+        //    in registers, and the half-warp sums by shuffles
+        {
+            constexpr int EL = D / 16;                  // elements per lane
+            const int lane = tid & 31, hl = lane & 15, half = lane >> 4;
+            float qr[HP][EL];
 #pragma unroll
-            for (int h = 0; h < HP; ++h) acc[h] = 0.f;
-            const T* row = Dk + (size_t)j * D;
-#pragma unroll 8
-            for (int e0 = 0; e0 < D; e0 += 8) {
-                float r[8];
-                Rows<T, D>::load8(row + e0, r);
+            for (int h = 0; h < HP; ++h)
+#pragma unroll
+                for (int e = 0; e < EL; ++e) qr[h][e] = qs[h * D + hl * EL + e] * a.scale;
+            for (int j0 = (tid >> 5) * 2; j0 < N; j0 += kAttWarps * 2) {
+                const int j = j0 + half;
+                float r[EL];
+                if (j < N) {
+                    Rows<T, D>::template load<EL>(Dk + (size_t)j * D + hl * EL, r);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) r[e] = 0.f;
+                }
+                float acc[HP];
 #pragma unroll
                 for (int h = 0; h < HP; ++h) {
-                    const float4 qa = *reinterpret_cast<const float4*>(qs + h * D + e0);
-                    const float4 qb = *reinterpret_cast<const float4*>(qs + h * D + e0 + 4);
-                    acc[h] = fmaf(r[0], qa.x, acc[h]);
-                    acc[h] = fmaf(r[1], qa.y, acc[h]);
-                    acc[h] = fmaf(r[2], qa.z, acc[h]);
-                    acc[h] = fmaf(r[3], qa.w, acc[h]);
-                    acc[h] = fmaf(r[4], qb.x, acc[h]);
-                    acc[h] = fmaf(r[5], qb.y, acc[h]);
-                    acc[h] = fmaf(r[6], qb.z, acc[h]);
-                    acc[h] = fmaf(r[7], qb.w, acc[h]);
+                    acc[h] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) acc[h] = fmaf(r[e], qr[h][e], acc[h]);
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], o);
+                }
+                if (hl < HP && j < N) {
+                    float mine = acc[0];
+#pragma unroll
+                    for (int h = 1; h < HP; ++h)
+                        if (hl == h) mine = acc[h];
+                    u[(size_t)hl * N + j] = mine;
                 }
             }
-#pragma unroll
-            for (int h = 0; h < HP; ++h) {
-                u[(size_t)h * N + j] = acc[h] * a.scale;
-                w[(size_t)h * N + j] = 0.f;
-            }
+            for (int i = tid; i < HP * N; i += kAttThreads) w[i] = 0.f;
         }
         __syncthreads();
 

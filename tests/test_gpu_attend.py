@@ -73,6 +73,7 @@ CASES = [
     (np.float16, 4096, 128, 8, 2, 3, 6, 2, 3000, [1, 2500, 0]),      # two softmax chunks, an empty sequence
     (np.float16, 8192, 128, 16, 1, 2, 8, 2, 700, [700, 333]),        # 4 heads per KV head in 2 passes
     (np.float32, 512, 64, 4, 1, 2, 2, 2, 100, [100, 37]),
+    (np.float32, 999, 64, 4, 1, 2, 3, 1, 50, [50, 7]),               # odd N, 3 heads per KV head
 ]
 
 
