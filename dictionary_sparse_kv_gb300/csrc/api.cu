@@ -725,9 +725,9 @@ fadkv_status fadkv_store_codes(int32_t G, int32_t B, int32_t H, int32_t s, int32
     return FADKV_OK;
 }
 
-fadkv_status fadkv_attend(const fadkv_attn_params* p, const void* dict_k, const void* dict_v,
-                          const uint32_t* cache_k, const uint32_t* cache_v, const int32_t* lengths,
-                          const float* q, float* out, void* stream)
+namespace {
+
+fadkv_status attend_check(const fadkv_attn_params* p)
 {
     if (!p) return FADKV_ERR_INVALID_ARG;
     if (p->layers < 0 || p->B < 0 || p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0 || p->s < 0 ||
@@ -735,6 +735,29 @@ fadkv_status fadkv_attend(const fadkv_attn_params* p, const void* dict_k, const 
         return FADKV_ERR_INVALID_ARG;
     if (p->dtype != FADKV_F16 && p->dtype != FADKV_F32) return FADKV_ERR_INVALID_ARG;
     if (!attend_supported(p->d, p->N, p->s)) return FADKV_ERR_UNSUPPORTED;
+    return FADKV_OK;
+}
+
+}  // namespace
+
+fadkv_status fadkv_attend_workspace_bytes(const fadkv_attn_params* p, size_t* bytes)
+{
+    const fadkv_status st = attend_check(p);
+    if (st != FADKV_OK) return st;
+    if (!bytes) return FADKV_ERR_INVALID_ARG;
+    *bytes = attend_workspace_bytes(p->layers, p->B, p->Hq, p->N, p->dtype);
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_attend(const fadkv_attn_params* p, const void* dict_k, const void* dict_v,
+                          const uint32_t* cache_k, const uint32_t* cache_v, const int32_t* lengths,
+                          const float* q, float* out, void* workspace, size_t workspace_bytes, void* stream)
+{
+    const fadkv_status st = attend_check(p);
+    if (st != FADKV_OK) return st;
+    const size_t need = attend_workspace_bytes(p->layers, p->B, p->Hq, p->N, p->dtype);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return FADKV_ERR_WORKSPACE;
+    if (need > 0 && !aligned(workspace, 256)) return FADKV_ERR_INVALID_ARG;
     const long long work = (long long)p->layers * p->B;
     if (work > 0 && (!dict_k || !dict_v || !cache_k || !cache_v || !lengths || !q || !out))
         return FADKV_ERR_INVALID_ARG;
@@ -766,6 +789,11 @@ fadkv_status fadkv_attend(const fadkv_attn_params* p, const void* dict_k, const 
     a.Tmax = p->Tmax;
     a.dtype = p->dtype;
     a.scale = p->scale;
+    a.Npad = attend_npad(p->N);
+    a.U = nullptr;
+    a.Whi = a.Wlo = nullptr;
+    a.wunscale = nullptr;
+    if (need > 0) attend_bind_workspace(a, workspace);
     const cudaError_t e = launch_attend(a, (cudaStream_t)stream);
     if (e != cudaSuccess) {
         set_error("fadkv_attend", e);

@@ -279,8 +279,17 @@ struct AttendArgs {
     float* out;               // [L][B][Hq][d]
     int L, B, Hq, Hkv, d, N, s, Tmax, dtype;
     float scale;
+    // binary16 dictionaries: workspace of the per-layer GEMMs (attend_bind_workspace)
+    int Npad;                 // N rounded up to 16
+    float* U;                 // [L][B*Hq][Npad] scale q D_K^T
+    __half* Whi;              // [L][B*Hq][Npad] w / S, scaled per row, two binary16 terms
+    __half* Wlo;
+    float* wunscale;          // [L][B*Hq] the per-row scale's inverse (0 for an empty sequence)
 };
+inline int attend_npad(int N) { return (N + 15) / 16 * 16; }
 bool attend_supported(int d, int N, int s);
+size_t attend_workspace_bytes(int L, int B, int Hq, int N, int dtype);
+void attend_bind_workspace(AttendArgs& a, void* ws);
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st);
 
 // Fixed-size adaptation, one CTA per dictionary.

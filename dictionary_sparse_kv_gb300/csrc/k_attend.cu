@@ -27,6 +27,13 @@
 //      granularity); then p = exp(score - max) and the value codes scatter
 //      p c' into w;
 //   3. o = D_V^T w / sum p.
+// With binary16 dictionaries steps 1 and 3 run instead as two per-layer
+// tensor-core GEMMs over all sequences and heads (attend_u_kernel before
+// the token pass, attend_o_kernel after it), so each dictionary is read
+// once per layer rather than once per (sequence, KV head); binary32
+// dictionaries keep the fused kernel.
+#include <type_traits>
+
 #include "fadkv_internal.cuh"
 
 namespace fadkv {
@@ -181,7 +188,7 @@ __device__ __forceinline__ void block_sum_n(float (&v)[HP], float* red)
 // tokens in registers before using them (WM words per token at most).
 template <int WM> __host__ __device__ constexpr int tokens_per_thread() { return WM <= 9 ? 2 : 1; }
 
-template <typename T, int D, int HP, int WM>
+template <typename T, int D, int HP, int WM, bool FUSED>
 __global__ void __launch_bounds__(kAttThreads, 2)
 attend_kernel(AttendArgs a)
 {
@@ -214,6 +221,15 @@ attend_kernel(AttendArgs a)
         for (int i = tid; i < HP * D; i += kAttThreads) qs[i] = (i / D < hn) ? q[i] : 0.f;
         __syncthreads();
 
+        if constexpr (!FUSED) {
+            // 1'. u from the per-layer GEMM's output U (scale already applied)
+            const size_t row0 = (size_t)l * a.B * a.Hq + (size_t)b * a.Hq + hk * grp + h0;
+            for (int i = tid; i < HP * N; i += kAttThreads) {
+                const int h = i / N, j = i % N;
+                u[i] = h < hn ? __ldg(a.U + (row0 + h) * a.Npad + j) : 0.f;
+            }
+            for (int i = tid; i < HP * N; i += kAttThreads) w[i] = 0.f;
+        } else
         // 1. u = scale D_K q: half-warps read whole rows (coalesced), every
         //    lane takes D/16 consecutive elements against its slice of q held
         //    in registers, and the half-warp sums by shuffles
@@ -342,6 +358,43 @@ attend_kernel(AttendArgs a)
             if (tid == 0) fac_s[h] = psum[h];           // the sums, read back below
         __syncthreads();
 
+        if constexpr (!FUSED) {
+            // 3'. hand w / S to the second GEMM as two binary16 terms, scaled
+            //     per row by a power of two so the largest lands in [2^14, 2^15)
+            float mw[HP];
+#pragma unroll
+            for (int h = 0; h < HP; ++h) mw[h] = 0.f;
+            for (int i = tid; i < HP * N; i += kAttThreads) {
+                const float v = fabsf(w[i]);
+#pragma unroll
+                for (int h = 0; h < HP; ++h)
+                    if (i / N == h) mw[h] = fmaxf(mw[h], v);
+            }
+            block_max_n<HP>(mw, red);
+            const int Np = a.Npad;
+            const size_t row0 = (size_t)l * a.B * a.Hq + (size_t)b * a.Hq + hk * grp + h0;
+            for (int h = 0; h < hn; ++h) {
+                const float S = fac_s[h];
+                const float m = S > 0.f ? mw[h] / S : 0.f;
+                const int e = m > 0.f ? 14 - ilogbf(m) : 0;
+                const int ec = e > 126 ? 126 : (e < -126 ? -126 : e);
+                const float sc = __int_as_float((127 + ec) << 23);     // 2^ec, exact
+                const float f = S > 0.f ? sc / S : 0.f;
+                __half2* hi = reinterpret_cast<__half2*>(a.Whi + (row0 + h) * Np);
+                __half2* lo = reinterpret_cast<__half2*>(a.Wlo + (row0 + h) * Np);
+                for (int j2 = tid; j2 < Np / 2; j2 += kAttThreads) {
+                    const int j = 2 * j2;
+                    const float v0 = j < N ? w[(size_t)h * N + j] * f : 0.f;
+                    const float v1 = j + 1 < N ? w[(size_t)h * N + j + 1] * f : 0.f;
+                    const __half2 h2 = __floats2half2_rn(v0, v1);
+                    hi[j2] = h2;
+                    lo[j2] = __floats2half2_rn(v0 - __low2float(h2), v1 - __high2float(h2));
+                }
+                if (tid == 0) a.wunscale[row0 + h] = (S > 0.f && m > 0.f) ? 1.f / sc : 0.f;
+            }
+            __syncthreads();
+            continue;
+        }
         // 3. o = D_V^T w / S: thread = (atom group, column pair)
         constexpr int CP = D / 2;                       // column pairs
         constexpr int AG = kAttThreads / CP;            // atom groups
@@ -376,6 +429,189 @@ attend_kernel(AttendArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// binary16 dictionaries: the two dictionary products as per-layer GEMMs on
+// the tensor cores (mma.sync m16n8k16, binary16 operands, FP32 sums), so a
+// layer's dictionaries are read once for all its sequences and heads:
+//   U = scale Q D_K^T   [B Hq][N]   before the token pass,
+//   O = W D_V           [B Hq][d]   after it (W = the token pass's w / S).
+// The FP32 operands (queries, w) enter as two binary16 terms, hi + lo, after
+// a per-row power-of-two scale that puts the row's largest entry in
+// [2^14, 2^15): about 22 significant bits, no overflow.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void hmma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// 2^k for the row maximum m: k = 14 - floor(log2 m), clamped to binary32's
+// normal exponents; 1 for m = 0.
+__device__ __forceinline__ float row_scale(float m)
+{
+    const int e = m > 0.f ? 14 - ilogbf(m) : 0;
+    const int ec = e > 126 ? 126 : (e < -126 ? -126 : e);
+    return __int_as_float((127 + ec) << 23);
+}
+
+// U: one warp per 16 query rows x 64 atoms; CTA = 4 warps (256 atoms).
+template <int D>
+__global__ void __launch_bounds__(128)
+attend_u_kernel(AttendArgs a)
+{
+    constexpr int KT = D / 16;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int M = a.B * a.Hq, N = a.N, l = blockIdx.z;
+    const int row0 = blockIdx.y * 16;
+    const int atom0 = blockIdx.x * 256 + warp * 64;
+    const float* Q = a.q + (size_t)l * M * D;
+    const __half* Dk = (const __half*)a.dict_k + (size_t)l * a.dict_stride;
+
+    // row scales: lanes 2r, 2r+1 scan row r
+    float mx = 0.f;
+    {
+        const int r = lane >> 1, hh = lane & 1;
+        if (row0 + r < M) {
+            const float4* qr = reinterpret_cast<const float4*>(Q + (size_t)(row0 + r) * D + hh * (D / 2));
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) {
+                const float4 v = __ldg(qr + i);
+                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    }
+    const float scr = row_scale(mx);
+    const float scA = __shfl_sync(0xffffffffu, scr, 2 * g8), scB = __shfl_sync(0xffffffffu, scr, 2 * (g8 + 8));
+    const bool okA = row0 + g8 < M, okB = row0 + g8 + 8 < M;
+
+    // A fragments (hi, lo) of the 16 rows for every k step
+    uint32_t ah[KT][4], al[KT][4];
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const bool rowB = r & 1, khi = r >> 1;
+            const bool ok = rowB ? okB : okA;
+            const int row = row0 + g8 + (rowB ? 8 : 0);
+            const int k = kt * 16 + (khi ? 8 : 0) + 2 * t4;
+            float2 v = ok ? __ldg(reinterpret_cast<const float2*>(Q + (size_t)row * D + k)) : make_float2(0.f, 0.f);
+            const float sc = rowB ? scB : scA;
+            v.x *= sc;
+            v.y *= sc;
+            const __half2 h = __floats2half2_rn(v.x, v.y);
+            ah[kt][r] = h2bits(h);
+            al[kt][r] = h2bits(__floats2half2_rn(v.x - __low2float(h), v.y - __high2float(h)));
+        }
+    }
+    float* U = a.U + (size_t)l * M * a.Npad;
+    const float fA = a.scale / scA, fB = a.scale / scB;
+#pragma unroll 2
+    for (int nt = 0; nt < 8; ++nt) {
+        const int n0 = atom0 + nt * 8;
+        if (n0 >= N) break;
+        const int atom = n0 + g8;
+        const __half* brow = Dk + (size_t)(atom < N ? atom : 0) * D + 2 * t4;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+            const uint32_t b0 = atom < N ? __ldg(reinterpret_cast<const uint32_t*>(brow + kt * 16)) : 0u;
+            const uint32_t b1 = atom < N ? __ldg(reinterpret_cast<const uint32_t*>(brow + kt * 16 + 8)) : 0u;
+            hmma16816(c, ah[kt], b0, b1);
+            hmma16816(c, al[kt], b0, b1);
+        }
+        const int col = n0 + 2 * t4;
+        if (okA) {
+            if (col < N) U[(size_t)(row0 + g8) * a.Npad + col] = c[0] * fA;
+            if (col + 1 < N) U[(size_t)(row0 + g8) * a.Npad + col + 1] = c[1] * fA;
+        }
+        if (okB) {
+            if (col < N) U[(size_t)(row0 + g8 + 8) * a.Npad + col] = c[2] * fB;
+            if (col + 1 < N) U[(size_t)(row0 + g8 + 8) * a.Npad + col + 1] = c[3] * fB;
+        }
+    }
+}
+
+// O: 16 rows of W per CTA, the atoms split over 8 warps, each warp all D
+// columns (D/8 n tiles); partial sums reduced in shared memory.
+constexpr int kOWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kOWarps * 32)
+attend_o_kernel(AttendArgs a)
+{
+    constexpr int NTN = D / 8;
+    extern __shared__ float ored[];                    // [kOWarps][16][D + 1] partial sums
+    auto red = reinterpret_cast<float (*)[16][D + 1]>(ored);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int M = a.B * a.Hq, N = a.N, Np = a.Npad, l = blockIdx.y;
+    const int row0 = blockIdx.x * 16;
+    const __half* Dv = (const __half*)a.dict_v + (size_t)l * a.dict_stride;
+    const __half* Whi = a.Whi + (size_t)l * M * Np;
+    const __half* Wlo = a.Wlo + (size_t)l * M * Np;
+    const bool okA = row0 + g8 < M, okB = row0 + g8 + 8 < M;
+    const int ksteps = Np / 16;
+    const int per = (ksteps + kOWarps - 1) / kOWarps;
+    const int k_begin = warp * per, k_end = min(ksteps, k_begin + per);
+
+    float acc[NTN][4];
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    for (int ks = k_begin; ks < k_end; ++ks) {
+        const int k0 = ks * 16;
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const bool rowB = r & 1, khi = r >> 1;
+            const bool ok = rowB ? okB : okA;
+            const size_t off = (size_t)(row0 + g8 + (rowB ? 8 : 0)) * Np + k0 + (khi ? 8 : 0) + 2 * t4;
+            ah[r] = ok ? __ldg(reinterpret_cast<const uint32_t*>(Whi + off)) : 0u;
+            al[r] = ok ? __ldg(reinterpret_cast<const uint32_t*>(Wlo + off)) : 0u;
+        }
+        // B: rows k0 + 2 t4 (+1) and k0 + 8 + 2 t4 (+1) of D_V, column n0 + g8
+        const int ka = k0 + 2 * t4, kb = ka + 8;
+        const bool v0 = ka < N, v1 = ka + 1 < N, v2 = kb < N, v3 = kb + 1 < N;
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+            const int col = nt * 8 + g8;
+            const __half z = __float2half_rn(0.f);
+            const __half e0 = v0 ? Dv[(size_t)ka * D + col] : z;
+            const __half e1 = v1 ? Dv[(size_t)(ka + 1) * D + col] : z;
+            const __half e2 = v2 ? Dv[(size_t)kb * D + col] : z;
+            const __half e3 = v3 ? Dv[(size_t)(kb + 1) * D + col] : z;
+            const uint32_t b0 = h2bits(__halves2half2(e0, e1));
+            const uint32_t b1 = h2bits(__halves2half2(e2, e3));
+            hmma16816(acc[nt], ah, b0, b1);
+            hmma16816(acc[nt], al, b0, b1);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt) {
+        red[warp][g8][nt * 8 + 2 * t4] = acc[nt][0];
+        red[warp][g8][nt * 8 + 2 * t4 + 1] = acc[nt][1];
+        red[warp][g8 + 8][nt * 8 + 2 * t4] = acc[nt][2];
+        red[warp][g8 + 8][nt * 8 + 2 * t4 + 1] = acc[nt][3];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 16 * D; i += kOWarps * 32) {
+        const int r = i / D, c = i % D;
+        if (row0 + r >= M) continue;
+        float v = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kOWarps; ++w2) v += red[w2][r][c];
+        const size_t row = (size_t)l * M + row0 + r;
+        a.out[row * D + c] = v * a.wunscale[row];
+    }
+}
+
 template <int D, int HP>
 size_t attend_smem(int N)
 {
@@ -387,7 +623,7 @@ template <typename T, int D, int HP, int WM>
 cudaError_t launch_hpw(const AttendArgs& a, cudaStream_t st)
 {
     const size_t smem = attend_smem<D, HP>(a.N);
-    auto k = attend_kernel<T, D, HP, WM>;
+    auto k = attend_kernel<T, D, HP, WM, !std::is_same<T, __half>::value>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     k<<<dim3(a.B * a.Hkv, a.L), kAttThreads, smem, st>>>(a);
@@ -432,11 +668,50 @@ cudaError_t launch_store_codes(const StoreArgs& a, cudaStream_t st)
     return cudaGetLastError();
 }
 
+size_t attend_workspace_bytes(int L, int B, int Hq, int N, int dtype)
+{
+    if (dtype != FADKV_F16) return 0;
+    const size_t rows = (size_t)L * B * Hq, Np = (size_t)attend_npad(N);
+    const auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    return up(rows * Np * sizeof(float)) + 2 * up(rows * Np * sizeof(__half)) + up(rows * sizeof(float));
+}
+
+void attend_bind_workspace(AttendArgs& a, void* ws)
+{
+    const size_t rows = (size_t)a.L * a.B * a.Hq, Np = (size_t)a.Npad;
+    const auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    unsigned char* p = (unsigned char*)ws;
+    a.U = (float*)p;
+    p += up(rows * Np * sizeof(float));
+    a.Whi = (__half*)p;
+    p += up(rows * Np * sizeof(__half));
+    a.Wlo = (__half*)p;
+    p += up(rows * Np * sizeof(__half));
+    a.wunscale = (float*)p;
+}
+
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st)
 {
     if (a.L <= 0 || a.B <= 0) return cudaSuccess;
-    if (a.dtype == FADKV_F16) return a.d == 128 ? launch_d<__half, 128>(a, st) : launch_d<__half, 64>(a, st);
-    return a.d == 128 ? launch_d<float, 128>(a, st) : launch_d<float, 64>(a, st);
+    if (a.dtype != FADKV_F16) return a.d == 128 ? launch_d<float, 128>(a, st) : launch_d<float, 64>(a, st);
+    const int M = a.B * a.Hq;
+    const dim3 gu((unsigned)((a.N + 255) / 256), (unsigned)((M + 15) / 16), (unsigned)a.L);
+    if (a.d == 128) attend_u_kernel<128><<<gu, 128, 0, st>>>(a);
+    else attend_u_kernel<64><<<gu, 128, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = a.d == 128 ? launch_d<__half, 128>(a, st) : launch_d<__half, 64>(a, st);
+    if (e != cudaSuccess) return e;
+    const dim3 go((unsigned)((M + 15) / 16), (unsigned)a.L);
+    const size_t osm = sizeof(float) * kOWarps * 16 * (a.d + 1);
+    if (a.d == 128) {
+        e = cudaFuncSetAttribute(attend_o_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)osm);
+        if (e == cudaSuccess) attend_o_kernel<128><<<go, kOWarps * 32, osm, st>>>(a);
+    } else {
+        e = cudaFuncSetAttribute(attend_o_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)osm);
+        if (e == cudaSuccess) attend_o_kernel<64><<<go, kOWarps * 32, osm, st>>>(a);
+    }
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace fadkv

@@ -107,7 +107,8 @@ _SIGS = {
     "fadkv_store_codes": ([C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p], C.c_int),
     "fadkv_attend": ([C.POINTER(AttnParams), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
-                      C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+                      C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "fadkv_attend_workspace_bytes": ([C.POINTER(AttnParams), C.POINTER(C.c_size_t)], C.c_int),
     "fadkv_profile_enable": ([C.c_void_p, C.c_int32], C.c_int),
     "fadkv_profile_select": ([C.c_void_p, C.c_uint32], C.c_int),
     "fadkv_profile_read": ([C.c_void_p, C.POINTER(C.c_int64), C.POINTER(C.c_double), C.c_int32], C.c_int),
@@ -228,11 +229,26 @@ def store_codes(G: int, B: int, H: int, s: int, N: int, idx, coef, repl_id, repl
                                                         _addr(repl_coef), _addr(pos), _addr(cache), Tmax, st))
 
 
-def attend(p: AttnParams, dict_k, dict_v, cache_k, cache_v, lengths, q, out, stream=None) -> None:
-    """Decode attention over packed K/V codes (see fadkv_attend)."""
+def attend_workspace_bytes(p: AttnParams) -> int:
+    out = C.c_size_t(0)
+    _check("fadkv_attend_workspace_bytes", lib().fadkv_attend_workspace_bytes(C.byref(p), C.byref(out)))
+    return out.value
+
+
+def attend(p: AttnParams, dict_k, dict_v, cache_k, cache_v, lengths, q, out, workspace=None,
+           stream=None) -> None:
+    """Decode attention over packed K/V codes (see fadkv_attend).  Without
+    a workspace one is allocated here (a torch tensor on q's device)."""
+    need = attend_workspace_bytes(p)
+    if workspace is None and need > 0:
+        import torch
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    nbytes = 0 if workspace is None else (workspace.numel() * workspace.element_size()
+                                          if hasattr(workspace, "numel") else need)
     st = _stream(stream, q, out)
     _check("fadkv_attend", lib().fadkv_attend(C.byref(p), _addr(dict_k), _addr(dict_v), _addr(cache_k),
-                                              _addr(cache_v), _addr(lengths), _addr(q), _addr(out), st))
+                                              _addr(cache_v), _addr(lengths), _addr(q), _addr(out),
+                                              _addr(workspace), nbytes, st))
 
 
 def reconstruct(h: int, V: int, idx, coef, repl_id, repl_coef, xhat, stream=None) -> None:

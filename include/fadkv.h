@@ -330,11 +330,24 @@ typedef struct {
      lengths         device [B] int32, clamped to [0, Tmax]; an empty
                      sequence gives 0
      q, out          device [L][B][Hq][d] float32
-   FP32 arithmetic.  Asynchronous on `stream`.  Errors: INVALID_ARG,
-   UNSUPPORTED, CUDA. */
+     workspace       device, >= fadkv_attend_workspace_bytes bytes, 256-byte
+                     aligned, caller-owned (contents need no initialisation)
+   With binary16 dictionaries the two dictionary products run as per-layer
+   tensor-core GEMMs over all sequences and heads (q and w enter as two
+   binary16 terms each, about 22 significant bits; FP32 sums); the token
+   pass is FP32.  Binary32 dictionaries: FP32 throughout.  Asynchronous on
+   `stream`.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 fadkv_status fadkv_attend(const fadkv_attn_params* params, const void* dict_k, const void* dict_v,
                           const uint32_t* cache_k, const uint32_t* cache_v, const int32_t* lengths,
-                          const float* q, float* out, void* stream);
+                          const float* q, float* out, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Device workspace fadkv_attend needs for these parameters (host-only;
+   writes *bytes).  Binary16 dictionaries: the per-layer products U = scale
+   Q D_K^T and the token pass's weights W, 8 * layers * B * Hq *
+   round_up(N, 16) bytes and a little more; binary32 dictionaries: 0 (the
+   workspace may then be NULL).  Errors: INVALID_ARG, UNSUPPORTED. */
+fadkv_status fadkv_attend_workspace_bytes(const fadkv_attn_params* params, size_t* bytes);
 
 /* Kernel classes reported by fadkv_profile_read. */
 #define FADKV_PROFILE_KERNELS 8

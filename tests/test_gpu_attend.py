@@ -1,5 +1,7 @@
 """The compressed store (fadkv_store_codes) and decode attention over packed
 codes (fadkv_attend) against the CPU oracle, through the C ABI (needs a GPU).
+Binary16 dictionaries take the three-kernel path (per-layer tensor-core
+GEMMs around the token pass), binary32 the fused kernel.
 
 Packed words: bit-exact.  Attention outputs: per (layer, sequence, query
 head) ||o_gpu - o_oracle|| <= 1e-4 ||o_oracle|| + 1e-5 (FP32 products and
@@ -74,6 +76,7 @@ CASES = [
     (np.float16, 8192, 128, 16, 1, 2, 8, 2, 700, [700, 333]),        # 4 heads per KV head in 2 passes
     (np.float32, 512, 64, 4, 1, 2, 2, 2, 100, [100, 37]),
     (np.float32, 999, 64, 4, 1, 2, 3, 1, 50, [50, 7]),               # odd N, 3 heads per KV head
+    (np.float16, 1000, 64, 4, 2, 3, 4, 2, 40, [40, 3, 0]),           # N not a multiple of 16, d = 64
 ]
 
 
