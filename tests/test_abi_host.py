@@ -147,3 +147,84 @@ def test_fault_injection_leaves_state(L, monkeypatch):
         assert e.value.status == 3
     finally:
         F.dict_destroy(h)
+
+
+def test_pl_and_append_entry_points_without_gpu(L, monkeypatch):
+    """fadkv_encode_pl and fadkv_adapt_append share the sequence contract and
+    the argument checks of fadkv_encode / fadkv_adapt."""
+    p = F.params(1, 512, 64, 32, 4, F.F32, 16)
+    ws = F.workspace_bytes(p)
+    fake = 0x10000
+    h = F.dict_create(p, fake, fake, [0.5], fake, ws)
+    try:
+        with pytest.raises(F.FadkvError) as e:
+            F.adapt_append(h, fake, 4, fake, fake, fake, fake, fake, stream=0)
+        assert e.value.status == 3
+        with pytest.raises(F.FadkvError) as e:
+            F.encode_pl(h, fake, 17, fake, fake, fake, stream=0)
+        assert e.value.status == 1
+        with pytest.raises(F.FadkvError) as e:
+            F.encode_pl(h, fake + 4, 4, fake, fake, fake, stream=0)      # x not 16-byte aligned
+        assert e.value.status == 1
+        monkeypatch.setenv("FADKV_FAULT", "cuda")
+        with pytest.raises(F.FadkvError) as e:
+            F.encode_pl(h, fake, 4, fake, fake, fake, stream=0)
+        assert e.value.status == 4 and "fadkv_encode_pl" in F.last_error()
+        with pytest.raises(F.FadkvError) as e:
+            F.adapt_append(h, fake, 4, fake, fake, fake, fake, fake, stream=0)
+        assert e.value.status == 3
+    finally:
+        F.dict_destroy(h)
+
+
+def test_store_codes_checks_without_gpu(L):
+    fake = 0x10000
+    # no vectors: nothing to launch, OK
+    F.store_codes(0, 4, 8, 8, 4096, fake, fake, fake, fake, fake, fake, 16, stream=0)
+    cases = [
+        ((1, 4, 8, 8, 8193), 2),        # N beyond the 13-bit id
+        ((1, 4, 8, 33, 4096), 2),       # s above the maximum
+        ((1, 4, 0, 8, 4096), 1),        # no heads
+        ((1, -1, 8, 8, 4096), 1),
+    ]
+    for (G, B, H, s, N), status in cases:
+        with pytest.raises(F.FadkvError) as e:
+            F.store_codes(G, B, H, s, N, fake, fake, fake, fake, fake, fake, 16, stream=0)
+        assert e.value.status == status, (G, B, H, s, N)
+    with pytest.raises(F.FadkvError) as e:      # repl_id without repl_coef
+        F.store_codes(1, 4, 8, 8, 4096, fake, fake, fake, None, fake, fake, 16, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(F.FadkvError) as e:      # misaligned cache
+        F.store_codes(1, 4, 8, 8, 4096, fake, fake, fake, fake, fake, fake + 2, 16, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(F.FadkvError) as e:      # Tmax 0
+        F.store_codes(1, 4, 8, 8, 4096, fake, fake, fake, fake, fake, fake, 0, stream=0)
+    assert e.value.status == 1
+
+
+def test_attend_workspace_and_checks_without_gpu(L):
+    def prm(layers=28, B=16, Hq=24, Hkv=8, d=128, N=4096, s=8, Tmax=4096, dtype=F.F16):
+        return F.AttnParams(layers, B, Hq, Hkv, d, N, s, Tmax, dtype, 0.125, 2 * N * d, 2 * B * Hkv * Tmax * (s + 1))
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    p = prm()
+    rows, Np = 28 * 16 * 24, 4096
+    assert F.attend_workspace_bytes(p) == up(rows * Np * 4) + 2 * up(rows * Np * 2) + up(rows * 4)
+    p_odd = prm(N=1000, d=64)
+    assert F.attend_workspace_bytes(p_odd) == up(rows * 1008 * 4) + 2 * up(rows * 1008 * 2) + up(rows * 4)
+    assert F.attend_workspace_bytes(prm(dtype=F.F32)) == 0
+    for bad, status in ((prm(Hq=20), 1), (prm(d=96), 2), (prm(N=9000), 2), (prm(s=40), 2), (prm(B=-1), 1)):
+        with pytest.raises(F.FadkvError) as e:
+            F.attend_workspace_bytes(bad)
+        assert e.value.status == status
+    fake = 0x10000
+    need = F.attend_workspace_bytes(p)
+    rc = L.fadkv_attend(C.byref(p), fake, fake, fake, fake, fake, fake, fake, fake, need - 1, None)
+    assert rc == 5                                        # workspace too small
+    rc = L.fadkv_attend(C.byref(p), fake, fake, fake, fake, fake, fake, fake, fake + 16, need, None)
+    assert rc == 1                                        # workspace not 256-byte aligned
+    rc = L.fadkv_attend(C.byref(p), fake + 8, fake, fake, fake, fake, fake, fake, fake, need, None)
+    assert rc == 1                                        # dictionary not 16-byte aligned
+    assert L.fadkv_attend(C.byref(prm(layers=0)), fake, fake, fake, fake, fake, fake, fake, fake, 0, None) == 0
