@@ -97,15 +97,6 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long t = __shfl_xor_sync(0xffffffffu, v, o);
-        v = t > v ? t : v;
-    }
-    return v;
-}
 
 // Larger |a| first, then the lower atom index (atom < 2^23); the low 10
 // bits carry the pool slot, which never decides the order.

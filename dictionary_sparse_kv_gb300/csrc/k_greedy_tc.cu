@@ -80,18 +80,6 @@ __host__ __device__ inline GtcLayout gtc_layout(int d, int smax, int ns, int C)
     return L;
 }
 
-__device__ __forceinline__ void load8(const __half* p, float (&f)[8])
-{
-    const uint4 q = *reinterpret_cast<const uint4*>(p);
-    const __half2* h = reinterpret_cast<const __half2*>(&q);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 t = __half22float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
-
 __device__ __forceinline__ int tri(int i, int j) { return i * (i + 1) / 2 + j; }
 
 template <int D, int SMAX>

@@ -315,28 +315,29 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
             bool ovf = false;
             // one 32-column group: append the packed keys of the kept scores
             auto stage = [&](const uint32_t (&v)[32], int qq) {
-                if (kDump) {
+                if constexpr (kDump) {
                     if (valid) {
                         float* out = a.dump + ((size_t)g * a.Vc + vloc) * a.N + c * kChunk + qq * 32;
 #pragma unroll
                         for (int t = 0; t < 32; ++t) out[t] = __uint_as_float(v[t]);
                     }
                     return;
-                }
+                } else {
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    const float f = fabsf(__uint_as_float(v[t]));
-                    if (f >= tau) {
-                        myrec[k] = __float_as_uint(fminf(f, top)) + ((uint32_t)((qq & 1) * 32 + t) << 26) + nbase;
-                        ++k;
+                    for (int t = 0; t < 32; ++t) {
+                        const float f = fabsf(__uint_as_float(v[t]));
+                        if (f >= tau) {
+                            myrec[k] = __float_as_uint(fminf(f, top)) + ((uint32_t)((qq & 1) * 32 + t) << 26) + nbase;
+                            ++k;
+                        }
                     }
+                    // a row may run past its record by at most 32 words (into
+                    // the next row's slot, or the warp's guard after row 31):
+                    // flagged below
+                    ovf |= k > kRecWords;
+                    k = min(k, kRecWords);
+                    if (qq == 1) k0 = k - 1;
                 }
-                // a row may run past its record by at most 32 words (into the
-                // next row's slot, or the warp's guard after row 31): flagged
-                // below
-                ovf |= k > kRecWords;
-                k = min(k, kRecWords);
-                if (qq == 1) k0 = k - 1;
             };
             // TMEM loads double-buffered in registers: group g+1 is in flight
             // while group g is filtered
