@@ -18,9 +18,12 @@
 //
 // One warp per vector, everything in registers: lane l holds elements
 // [E l, E l + E) of x and of each of the s atom rows (E = D / 32); the Gram
-// entries and right-hand sides are warp reductions; lane i holds row i of
+// entries and right-hand sides come from one mma.sync tile per 16 columns
+// (binary16, s <= 8) or else from warp reductions; lane i holds row i of
 // the fit matrix, and the Cholesky factorisation and both triangular solves
 // run column by column with shuffles.  FP32 throughout.
+#include <type_traits>
+
 #include "fadkv_internal.cuh"
 
 namespace fadkv {
@@ -159,6 +162,44 @@ pl_fit_kernel(Shape sh, PlArgs a)
     const float la = sh.lambda_abs, lr = sh.lambda_rel;
     float ar[SMAX];
     float bi = 0.f;
+    if constexpr (SMAX == 8 && std::is_same<T, __half>::value) {
+        // binary16, s <= 8: G = D_S D_S^T and b = D_S x from one m16n8k16
+        // tile per 16 columns -- A rows 0..7 the picked atoms, row 8 x (rows
+        // 9..15 zero), B columns the same atoms (exact products, FP32 sums);
+        // lane (g8, t4) ends with G[g8][2t4, 2t4+1] and, for g8 = 0,
+        // b[2t4, 2t4+1]
+        const int g8 = lane >> 2, t4 = lane & 3;
+        int myrow = 0;
+#pragma unroll
+        for (int k = 0; k < SMAX; ++k)
+            if (g8 == k) myrow = sid[k];
+        const bool rowok = g8 < s;
+        const __half* arow = (const __half*)a.atoms + ((size_t)g * N + myrow) * D + 2 * t4;
+        const __half* xrow = (const __half*)a.x + ((size_t)g * a.V + v) * D + 2 * t4;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kt = 0; kt < D / 16; ++kt) {
+            uint32_t f[4];
+            f[0] = rowok ? __ldg(reinterpret_cast<const uint32_t*>(arow + kt * 16)) : 0u;
+            f[1] = g8 == 0 ? __ldg(reinterpret_cast<const uint32_t*>(xrow + kt * 16)) : 0u;
+            f[2] = rowok ? __ldg(reinterpret_cast<const uint32_t*>(arow + kt * 16 + 8)) : 0u;
+            f[3] = g8 == 0 ? __ldg(reinterpret_cast<const uint32_t*>(xrow + kt * 16 + 8)) : 0u;
+            asm volatile(
+                "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                "{%0,%1,%2,%3};\n"
+                : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                : "r"(f[0]), "r"(f[1]), "r"(f[2]), "r"(f[3]), "r"(f[0]), "r"(f[2]));
+        }
+        // lane i gathers row i of G (from lanes 4i + j/2) and b_i (lane i/2)
+#pragma unroll
+        for (int j = 0; j < SMAX; ++j) {
+            const float gij = __shfl_sync(0xffffffffu, (j & 1) ? c[1] : c[0], (4 * lane + (j >> 1)) & 31);
+            ar[j] = (j < s && lane < s) ? (j == lane ? fmaf(gij, lr, gij) + la : gij) : 0.f;
+        }
+        const float be = __shfl_sync(0xffffffffu, c[2], (lane >> 1) & 31);
+        const float bo = __shfl_sync(0xffffffffu, c[3], (lane >> 1) & 31);
+        bi = lane < s ? ((lane & 1) ? bo : be) : 0.f;
+    } else {
 #pragma unroll
     for (int i = 0; i < SMAX; ++i) {
         ar[i] = 0.f;
@@ -184,6 +225,7 @@ pl_fit_kernel(Shape sh, PlArgs a)
                 if (lane == j) ar[i] = p;
             }
         }
+    }
     }
 
     // Cholesky A = L L^T in place: lane i's ar[k] becomes L_ik (k <= i)
