@@ -4,7 +4,7 @@ Compiles every ``csrc/*.cu`` into an object file in parallel (one nvcc per
 translation unit, a single -gencode) and links them into
 ``dictionary_sparse_kv_gb300/_build/libfadkv.so`` with the CUDA runtime linked
 statically, so the library loads without a GPU and its only runtime
-dependency is the driver.
+dependency is the NVIDIA driver (libcuda).
 
     python -m dictionary_sparse_kv_gb300.build [--force] [--verbose]
 """
