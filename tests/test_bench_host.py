@@ -1,0 +1,70 @@
+"""The measurement arithmetic of bench.py, on CPU: algorithmic work per
+launch, the roofline object built from a profile, the traffic table lookup
+and the dominant-kernel choice.  No GPU and no timing involved."""
+import pytest
+
+import bench
+from dictionary_sparse_kv_gb300 import synthetic as S
+
+PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def test_kernel_work_per_launch():
+    w = S.WORKLOADS["decode_3b"]                 # 56 dictionaries, N=4096, d=128, n=256, s=8
+    V = w.V
+    nv = w.G * V
+    bound, work, unit = bench.kernel_work(w, "screen", V)
+    assert (bound, unit) == ("hbm", "GB/s")
+    assert work == 56 * 4096 * 128 * 2 + nv * 128 * 2        # dictionaries once + inputs
+    bound, work, unit = bench.kernel_work(w, "greedy", V)
+    assert (bound, unit) == ("tensor", "TFLOP/s")
+    assert work == 2.0 * 7 * 256 * 128 * nv                  # (s-1) n d multiply-adds per vector
+    bound, work, unit = bench.kernel_work(w, "greedy", V, coder="pl")
+    assert (bound, unit) == ("hbm", "GB/s")
+    assert work == (9 * 128 * 2 + 8.0 * 8 + 4.0) * nv        # s rows + x in, codes out
+    _, topn_gm, _ = bench.kernel_work(w, "topn", V)
+    _, topn_pl, _ = bench.kernel_work(w, "topn", V, coder="pl")
+    assert topn_gm - topn_pl == 4.0 * (256 - 8) * nv         # the pool is s ids for PL
+    with pytest.raises(KeyError):
+        bench.kernel_work(w, "nothing", V)
+
+
+def test_roofline_from_profiles():
+    w = S.WORKLOADS["decode_3b"]
+    # (launches, total ms) per kernel class: the greedy dominates
+    prof = {"screen": (10, 0.31), "topn": (20, 0.31), "greedy": (10, 2.27), "adapt": (10, 0.08)}
+    timed = {"greedy": (20, 4.54)}
+    roof, shares = bench.roofline(w, prof, timed, w.V, PEAKS, "measured", 152, 2070.0)
+    assert roof["kernel"] == "greedy" and roof["bound"] == "tensor" and roof["unit"] == "TFLOP/s"
+    flops = 2.0 * 7 * 256 * 128 * w.G * w.V
+    assert roof["launch_ms"] == pytest.approx(0.227)
+    assert roof["achieved"] == pytest.approx(flops / 0.227e-3 / 1e12, rel=1e-3)
+    assert roof["frac"] == pytest.approx(roof["achieved"] / 1900.0, abs=1e-4)     # rounded to 4 places
+    assert sum(v["share"] for v in shares.values()) == pytest.approx(1.0, abs=1e-3)
+    assert shares["greedy"]["launches"] == 10
+    # without a timed figure for the dominant kernel the profile's own is used
+    roof2, _ = bench.roofline(w, prof, {}, w.V, PEAKS, "measured", 152, 2070.0)
+    assert roof2["launch_ms"] == pytest.approx(0.227)
+    # the PL coder's fit is HBM-bound work
+    roof3, _ = bench.roofline(w, {"greedy": (10, 0.24)}, {}, w.V, PEAKS, "measured", 152, 2070.0, coder="pl")
+    assert roof3["bound"] == "hbm" and roof3["source"] == "k_pl.cu"
+
+
+def test_dominant_kernel_and_traffic_lookup():
+    assert bench.dominant_kernel({}) is None
+    assert bench.dominant_kernel({"a": (1, 0.5), "b": (3, 0.7)}) == "b"
+    w = S.WORKLOADS["decode_3b"]
+    t = bench.traffic_for("greedy", w)
+    # the committed table matches the committed greedy source, or the lookup
+    # says it does not know (never a stale number)
+    assert t is None or t > 56 * 4096 * 128 * 2 * 0.5
+    from dataclasses import replace
+    assert bench.traffic_for("greedy", replace(w, name="no_such_workload")) is None
+
+
+def test_workload_config_names_the_coder():
+    w = S.WORKLOADS["decode_3b"]
+    c = bench.workload_config(w, w.G * w.V)
+    assert c["vectors_per_step"] == 7168 and "decode_3b" in c["workload"] and "greedy" in c["coder"]
+    assert "PL" in bench.workload_config(w, 1, "pl")["coder"]
+    assert bench.job_throughput(1, 20, 7168, 6.0) == pytest.approx(20 * 7168 / 0.006)
