@@ -312,7 +312,8 @@ typedef struct {
 } fadkv_attn_params;
 
 /* Decode attention over the compressed store, for every layer, sequence and
-   query head in one launch:
+   query head in one call (three kernel launches for binary16 dictionaries,
+   one for binary32):
      out[l][b][h] = sum_t p_t v_t,  p = softmax_t(scale <q[l][b][h], k_t>),
    over the tokens t < lengths[b] of KV head h / (Hq / Hkv) of sequence b,
    where k_t and v_t are the sparse combinations their packed codes name:
