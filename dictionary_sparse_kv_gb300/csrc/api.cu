@@ -762,7 +762,7 @@ fadkv_status fadkv_attend(const fadkv_attn_params* p, const void* dict_k, const 
     if (work > 0 && (!dict_k || !dict_v || !cache_k || !cache_v || !lengths || !q || !out))
         return FADKV_ERR_INVALID_ARG;
     if (work > 0 && (!aligned(dict_k, 16) || !aligned(dict_v, 16) || p->dict_stride % 8 != 0 ||
-                     !aligned(cache_k, 4) || !aligned(cache_v, 4) || !aligned(lengths, 4) || !aligned(q, 4) ||
+                     !aligned(cache_k, 4) || !aligned(cache_v, 4) || !aligned(lengths, 4) || !aligned(q, 16) ||
                      !aligned(out, 4)))
         return FADKV_ERR_INVALID_ARG;
     if (fault_injected()) {

@@ -330,7 +330,8 @@ typedef struct {
                      = 2*B*Hkv*Tmax*(s+1))
      lengths         device [B] int32, clamped to [0, Tmax]; an empty
                      sequence gives 0
-     q, out          device [L][B][Hq][d] float32
+     q, out          device [L][B][Hq][d] float32 (q 16-byte aligned: its rows
+                     are read as vectors)
      workspace       device, >= fadkv_attend_workspace_bytes bytes, 256-byte
                      aligned, caller-owned (contents need no initialisation)
    With binary16 dictionaries the two dictionary products run as per-layer

@@ -228,3 +228,5 @@ def test_attend_workspace_and_checks_without_gpu(L):
     rc = L.fadkv_attend(C.byref(p), fake + 8, fake, fake, fake, fake, fake, fake, fake, need, None)
     assert rc == 1                                        # dictionary not 16-byte aligned
     assert L.fadkv_attend(C.byref(prm(layers=0)), fake, fake, fake, fake, fake, fake, fake, fake, 0, None) == 0
+    rc = L.fadkv_attend(C.byref(p), fake, fake, fake, fake, fake, fake + 8, fake, fake, need, None)
+    assert rc == 1                                        # queries not 16-byte aligned
