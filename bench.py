@@ -173,6 +173,21 @@ def kernel_work(w, kernel: str, vectors: int, coder: str = "gm"):
     raise KeyError(kernel)
 
 
+def step_roofline(w, vectors_per_step: int, ms_per_step: float, peaks: dict) -> dict:
+    """HBM fraction of the whole step: its algorithmic bytes -- every
+    dictionary read once, the inputs read, the codes written (s ids and
+    coefficients, relres, replacement id and coefficient per vector) and the
+    usage counts scanned -- over the step time, against the HBM peak."""
+    esz = 2 if w.dtype.__name__ == "float16" else 4
+    V = vectors_per_step // w.G
+    algo = (w.G * w.N * w.d * esz + vectors_per_step * w.d * esz
+            + vectors_per_step * (8 * w.s + 4 + 8) + w.G * w.N * 4)
+    achieved = algo / (ms_per_step / 1e3) / 1e9
+    return {"bound": "hbm", "algorithmic_bytes": algo, "bytes_per_vector": round(algo / vectors_per_step, 1),
+            "vectors_per_dictionary": V, "achieved": round(achieved, 1), "peak": round(peaks["hbm_gbs"], 1),
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+
+
 def kernel_sources():
     import glob
     out = {}
@@ -480,6 +495,7 @@ def run_ours(args):
         "config": workload_config(w, vectors_per_step, args.coder),
         "e2e": {"value": round(e2e, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches, "roofline": roof, "kernels": shares, "clocks": clk, "cpu_baseline": cpu,
+        "step_roofline": step_roofline(w, vectors_per_step, dev_ms / K, peaks),
         "wall_s_timed": round(wall, 4),
         "adapt": {"replaced": sum(s["replaced"] for s in stats), "overflow": sum(s["overflow"] for s in stats)},
     }

@@ -68,3 +68,15 @@ def test_workload_config_names_the_coder():
     assert c["vectors_per_step"] == 7168 and "decode_3b" in c["workload"] and "greedy" in c["coder"]
     assert "PL" in bench.workload_config(w, 1, "pl")["coder"]
     assert bench.job_throughput(1, 20, 7168, 6.0) == pytest.approx(20 * 7168 / 0.006)
+
+
+def test_step_roofline_bytes():
+    """decode_3b: 56 MiB of dictionaries, 1.75 MiB of inputs, 84 B of codes
+    per vector and 0.9 MiB of usage counts per step: about 8.6 KB per vector,
+    the figure the scope table quotes."""
+    w = S.WORKLOADS["decode_3b"]
+    r = bench.step_roofline(w, 7168, 0.300, PEAKS)
+    algo = 56 * 4096 * 128 * 2 + 7168 * 128 * 2 + 7168 * (8 * 8 + 12) + 56 * 4096 * 4
+    assert r["algorithmic_bytes"] == algo
+    assert 8500 < r["bytes_per_vector"] < 8800
+    assert r["frac"] == pytest.approx(algo / 0.3e-3 / 1e9 / 6800.0, abs=1e-4)
