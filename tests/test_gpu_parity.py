@@ -282,13 +282,14 @@ def _run_steps(w, steps, V, resync=True):
         x = data.inputs(t, V)
         atoms0 = D.atoms.cpu().numpy().copy()
         usage0 = D.usage.cpu().numpy().copy()
+        gpool = D.pool(_t(x))[0].cpu().numpy()        # the pools this step's encode uses
         c = gpu_encode(D, x)
         D.adapt(_t(x), c)
         torch.cuda.synchronize()
         idx, coef, rel = (a.cpu().numpy() for a in (c.idx, c.coef, c.relres))
         for g in range(w.G):
             res = O.encode_threaded(p, atoms0[g], x[g], PU.THREADS)
-            rep = PU.compare_encode(res, idx[g], coef[g], rel[g])
+            rep = PU.compare_encode(res, idx[g], coef[g], rel[g], gpool[g], p, atoms0[g], x[g])
             PU.assert_encode_ok(rep)
             exempt += rep.exempt
             checked += rep.checked

@@ -49,6 +49,9 @@ MUTANTS = [
     ("PL ids left in rank order", "qsort(S, (size_t)s, sizeof(int32_t), cmp_i32);", ";"),
     ("PL residual drops the last atom", "for (int k = 0; k < s; ++k)\n                acc -= c[k]", "for (int k = 0; k + 1 < s; ++k)\n                acc -= c[k]"),
     ("PL relres squared norm", "sqrt(en2) / xn", "en2 / xn"),
+    ("given pool read from vector 0", "P[i] = pool_in[(int64_t)v * n + i];", "P[i] = pool_in[i];"),
+    ("given pool shifted by one", "P[i] = pool_in[(int64_t)v * n + i];", "P[i] = pool_in[(int64_t)v * n + i + (i + 1 < n)];"),
+    ("given pool ignored", "        if (pool_in) {\n            for (int i = 0; i < n; ++i) {", "        if (0 && pool_in) {\n            for (int i = 0; i < n; ++i) {"),
 ]
 
 PIN_TESTS = [
@@ -63,6 +66,8 @@ PIN_TESTS = [
     lambda O: pins.test_exact_recovery_incoherent(O, False),
     pins.test_greedy_steps_brute_force,
     pins.test_brute_force_subset_objective,
+    pins.test_greedy_on_pool_restricted_closed_form,
+    pins.test_greedy_on_pool_matches_encode_and_ignores_order,
     pins.test_zero_and_nonfinite_inputs,
     pins.test_adapt_golden_cases,
     pins.test_adapt_invariants_random,

@@ -312,6 +312,70 @@ def test_brute_force_subset_objective(oracle_lib):
 
 
 # --------------------------------------------------------------------------
+# greedy selection on a given pool (steps 3-4 without the screening)
+# --------------------------------------------------------------------------
+
+def test_greedy_on_pool_restricted_closed_form(oracle_lib):
+    """Unit orthonormal atoms, noise-free 6-sparse x on support T, and a
+    given pool P holding only some of T: the picks must come from P alone.
+    With G = I the ridge gives c_j = <d_j, x>/1.2001, so the atoms of T in P
+    come first (by |b|, then id), then pool atoms of zero correlation in id
+    order with c = 0, and relres is known exactly:
+    ||e||^2 = sum_{T in P} (0.2001 b_j / 1.2001)^2 + sum_{T not in P} b_j^2.
+    Every vector has its own pool, whose first entry is its largest in-pool
+    support atom (so a pool read from the wrong row, or shifted, fails)."""
+    O = oracle_lib
+    d = N = 64
+    D = np.eye(N, dtype=np.float32)[::-1].copy()          # atom j = e_{63-j}
+    g = np.random.default_rng(12)
+    n, s, V = 10, 6, 8
+    pools, xs, expect = [], [], []
+    for v in range(V):
+        T = g.choice(N, 6, replace=False)
+        b = g.choice([-1, 1], 6) * (1 + g.permutation(6) / 4.0)   # distinct |b|
+        inP = T[:3]                                        # three support atoms in the pool
+        others = [j for j in g.permutation(N) if j not in T][:n - 3]
+        lead = inP[np.argmax(np.abs(b[:3]))]
+        P = [int(lead)] + [int(j) for j in inP if j != lead] + [int(j) for j in others]
+        pools.append(P)
+        xs.append((b @ D[T].astype(np.float64)).astype(np.float32))
+        order = [int(j) for j in inP[np.lexsort((inP, -np.abs(b[:3])))]]
+        zero = sorted(others)[:s - 3]
+        ce = {int(T[i]): b[i] / 1.2001 for i in range(3)}
+        e2 = sum((0.2001 * b[i] / 1.2001) ** 2 for i in range(3)) + sum(b[i] ** 2 for i in range(3, 6))
+        expect.append((order + zero, ce, math.sqrt(e2) / np.linalg.norm(b)))
+    r = O.greedy_on_pool(O.Params(N, d, n, s, dtype=O.F32), D, np.stack(xs), np.array(pools, np.int32))
+    for v in range(V):
+        ids, ce, rel = expect[v]
+        assert list(r.idx[v]) == ids, v
+        for k, j in enumerate(ids):
+            assert r.coef[v, k] == pytest.approx(ce.get(j, 0.0), rel=1e-14, abs=1e-15)
+        assert r.relres[v] == pytest.approx(rel, rel=1e-13)
+
+
+def test_greedy_on_pool_matches_encode_and_ignores_order(oracle_lib):
+    """Given the oracle's own Top-n pools, greedy_on_pool reproduces
+    encode bit for bit; given the same pools shuffled, it returns the same
+    ids, coefficients and relres (the pool is a set: ties go by atom id,
+    never by position)."""
+    O = oracle_lib
+    w = S.WORKLOADS["tiny"]
+    D = S.make_dictionary(w.N, w.d, np.float32, 0)
+    x = S.make_tiny_inputs(D, 24, w.s, 1)
+    p = O.Params(w.N, w.d, w.n, w.s, dtype=O.F32)
+    full = O.encode(p, D, x)
+    same = O.greedy_on_pool(p, D, x, full.pool)
+    for a, b in ((same.idx, full.idx), (same.coef, full.coef), (same.relres, full.relres),
+                 (same.pick_gap, full.pick_gap)):
+        assert np.array_equal(a, b)
+    g = np.random.default_rng(13)
+    shuffled = np.stack([g.permutation(row) for row in full.pool]).astype(np.int32)
+    sh = O.greedy_on_pool(p, D, x, shuffled)
+    assert np.array_equal(sh.idx, full.idx)
+    assert np.array_equal(sh.coef, full.coef) and np.array_equal(sh.relres, full.relres)
+
+
+# --------------------------------------------------------------------------
 # special inputs
 # --------------------------------------------------------------------------
 
