@@ -51,6 +51,8 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="measure only the headline workload (not " + ", ".join(EXTRA_WORKLOADS) + ")")
     ap.add_argument("--coder", choices=["gm", "pl"], default="gm")
     ap.add_argument("--attend", type=int, default=0, metavar="T",
                     help="time decode attention over packed codes with T cached tokens instead")
@@ -150,8 +152,8 @@ def kernel_work(w, kernel: str, vectors: int, coder: str = "gm"):
     """(bound, algorithmic units per launch, unit) for one launch that covers
     `vectors` vectors of every dictionary (G * vectors vectors in total).
     Per-vector figures: screening streams the dictionary once per launch plus
-    the inputs (HBM); the greedy's contraction is (s - 1) n d multiply-adds
-    per vector over the pool (tensor pipe)."""
+    the inputs (HBM); the greedy gathers the pool's data and (s - 1) Gram
+    rows at the pool's ids (HBM)."""
     G, N, d, n, s = w.G, w.N, w.d, w.n, w.s
     esz = 2 if w.dtype.__name__ == "float16" else 4
     nv = G * vectors
@@ -165,7 +167,15 @@ def kernel_work(w, kernel: str, vectors: int, coder: str = "gm"):
         # the fit: the s rows and x in, ids, coefficients and relres out
         return "hbm", ((s + 1) * d * esz + 8.0 * s + 4.0) * nv, "GB/s"
     if kernel == "greedy":
-        return "tensor", 2.0 * (s - 1) * n * d * nv, "TFLOP/s"
+        # the greedy over the Gram matrix: per vector the pool's ids, scores
+        # and G_jj (12 B each), the (s - 1) Gram rows at the pool's ids
+        # (4 B per entry), x and the s picked rows for the residual, and the
+        # codes out
+        return "hbm", (12.0 * n + 4.0 * (s - 1) * n + (s + 1) * d * esz + 8.0 * s + 4.0) * nv, "GB/s"
+    if kernel == "gram":
+        # the update after an adaptation: the replaced-atom counts (the rows
+        # of replaced atoms are data-dependent and not counted)
+        return "hbm", 4.0 * G, "GB/s"
     if kernel == "adapt":
         return "hbm", 4.0 * (s + 3) * nv + 4.0 * G * N, "GB/s"
     if kernel == "reconstruct":
@@ -197,16 +207,11 @@ def kernel_sources():
     return out
 
 
-def greedy_source() -> str:
-    f = os.environ.get("FADKV_GREEDY", "")
-    return {"tc": "k_greedy_tc.cu", "ffma": "k_greedy.cu", "mma": "k_greedy_mma.cu"}.get(f, "k_greedy_chol.cu")
-
-
 def kernel_files(coder: str = "gm"):
     """Source file of each kernel class on the binary16 path the bench runs."""
     return {"screen": "k_screen_tc.cu", "topn": "k_select.cu",
-            "greedy": "k_pl.cu" if coder == "pl" else greedy_source(),
-            "adapt": "k_adapt_reconstruct.cu", "reconstruct": "k_adapt_reconstruct.cu"}
+            "greedy": "k_pl.cu" if coder == "pl" else "k_gram.cu",
+            "adapt": "k_adapt_reconstruct.cu", "reconstruct": "k_adapt_reconstruct.cu", "gram": "k_gram.cu"}
 
 
 def traffic_for(kernel: str, w, coder: str = "gm"):
@@ -322,8 +327,8 @@ def run_reference(args):
     w = S.WORKLOADS[args.workload]
     data = S.WorkloadData(w)
     threads = os.cpu_count() or 1
-    # warm-up steps, then K timed steps; each step is one full decode step
-    oracle_steps(w, data, max(0, min(args.warmup, 1)), threads, args.coder)
+    # W warm-up steps, then K timed steps; each step is one full decode step
+    oracle_steps(w, data, max(0, args.warmup), threads, args.coder)
     nvec, sec = oracle_steps(w, data, args.steps, threads, args.coder)
     value = nvec / sec
     line = {
@@ -370,6 +375,100 @@ def job_throughput(world: int, steps: int, vectors_per_step: int, ms_max: float)
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
+
+# Workloads measured beside the headline one, in the same run (one GPU).
+EXTRA_WORKLOADS = ("prefill_3b_16k", "decode_8b", "adapt_stress")
+
+
+def screening_fractions(w, prof, steps, peaks):
+    """The screening kernel's own fractions over a profiled pass of `steps`
+    steps: HBM (each launch streams every dictionary once, plus the inputs)
+    and tensor pipe (2 N d flops per vector against the dense bf16 peak,
+    binary16 having the same nominal rate)."""
+    if "screen" not in prof:
+        return None
+    launches, ms = prof["screen"]
+    esz = 2 if w.dtype.__name__ == "float16" else 4
+    vecs = steps * w.G * w.V
+    sec = ms / 1e3
+    byts = launches * w.G * w.N * w.d * esz + vecs * w.d * esz
+    flops = 2.0 * w.N * w.d * vecs
+    return {"launches": launches, "ms_per_launch": round(ms / launches, 5),
+            "hbm": {"achieved_gbs": round(byts / sec / 1e9, 1), "frac": round(byts / sec / 1e9 / peaks["hbm_gbs"], 4)},
+            "tensor": {"achieved_tflops": round(flops / sec / 1e12, 2),
+                       "frac": round(flops / sec / 1e12 / peaks["bf16_tflops"], 4)}}
+
+
+def extra_workload(name, dev, peaks, peak_kind, sm_count, sm_max, coder="gm", K=5, W=3):
+    """The headline's step on another workload, device-timed the same way
+    (CUDA events around each step, L2 flushed between steps, W warm-up
+    steps): ms per step, vectors/s, the dominant kernel's roofline, the
+    screening kernel's own HBM and tensor fractions, and the atoms replaced
+    in the timed steps.  The adaptation stress takes its inputs from the
+    first drift of its sources on (steps 128, 129, ...: the stress case,
+    replacements in every step); the 16K prefill alternates two input
+    batches of 262 144 vectors."""
+    import torch
+    from dictionary_sparse_kv_gb300 import fadkv as F
+    from dictionary_sparse_kv_gb300 import synthetic as S
+    w = S.WORKLOADS[name]
+    data = S.WorkloadData(w)
+    t0 = w.drift_period if w.drift_period > 0 else 0
+    nin = 2 if w.G * w.V > 100_000 else W + 2 * K
+    xs = [torch.from_numpy(data.inputs(t0 + t)).to(dev) for t in range(nin)]
+    D = F.Dictionary(torch.from_numpy(data.atoms).to(dev), torch.from_numpy(data.usage).to(dev),
+                     data.deltas(), w.n, w.s, w.V)
+    codes = D.new_codes(w.V)
+    xhat = torch.empty((w.G, w.V, w.d), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = 0
+    for _ in range(W):
+        D.step(xs[step % nin], codes, xhat, coder=coder)
+        step += 1
+    torch.cuda.synchronize(dev)
+    F.profile_read(D.h, reset=True)
+    F.profile_enable(D.h, True)
+    for t in range(K):
+        flush.fill_(float(t))
+        D.step(xs[step % nin], codes, xhat, coder=coder)
+        step += 1
+    torch.cuda.synchronize(dev)
+    F.profile_enable(D.h, False)
+    prof_all = F.profile_read(D.h, reset=True)
+    dom = dominant_kernel(prof_all)
+    F.profile_select(D.h, [dom] if dom else None)
+    F.profile_enable(D.h, True)
+    rep0 = sum(s["replaced"] for s in D.stats())
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    for t in range(K):
+        flush.fill_(float(t))
+        ev[t][0].record(stream)
+        D.step(xs[step % nin], codes, xhat, coder=coder)
+        ev[t][1].record(stream)
+        step += 1
+    torch.cuda.synchronize(dev)
+    F.profile_enable(D.h, False)
+    F.profile_select(D.h, None)
+    prof = F.profile_read(D.h, reset=True)
+    st = D.stats()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    roof, shares = roofline(w, prof_all, prof, w.V, peaks, peak_kind, sm_count, sm_max, coder)
+    out = {"workload": workload_config(w, w.G * w.V, coder)["workload"], "steps": K, "warmup": W,
+           "ms_per_step": round(ms, 4), "vectors_per_s": round(w.G * w.V / (ms / 1e3), 1),
+           "roofline": roof, "kernels": shares, "screening": screening_fractions(w, prof_all, K, peaks),
+           "replaced_in_timed_steps": sum(s["replaced"] for s in st) - rep0,
+           "status_words": sorted({int(s["status"]) for s in st})}
+    if w.drift_period > 0:
+        out["inputs"] = f"steps {t0}.. (after the first drift of the sources)"
+    if nin == 2:
+        out["inputs"] = "two input batches, alternated"
+    D.close()
+    del D, xs, codes, xhat, flush
+    torch.cuda.empty_cache()
+    return out
+
 
 def run_ours(args):
     import numpy as np
@@ -499,6 +598,15 @@ def run_ours(args):
         "wall_s_timed": round(wall, 4),
         "adapt": {"replaced": sum(s["replaced"] for s in stats), "overflow": sum(s["overflow"] for s in stats)},
     }
+    scr = screening_fractions(w, prof_all, min(K, 10), peaks)
+    if scr:
+        line["screening"] = scr
+    if world == 1 and args.workload == WORKLOAD and not args.no_extra:
+        D.close()
+        del D, codes, xhat, flush, xs_dev, xin
+        torch.cuda.empty_cache()
+        line["workloads"] = {nm: extra_workload(nm, dev, peaks, peak_kind, props.multi_processor_count, sm_max,
+                                                args.coder) for nm in EXTRA_WORKLOADS}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

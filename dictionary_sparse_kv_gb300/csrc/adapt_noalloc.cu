@@ -16,6 +16,7 @@
 // only accumulated, never read back.  Every call on one device uses the same
 // array, so calls that can run at the same time (different streams, or
 // different host threads) race on it: issue them in order on one stream.
+#include <cuda.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -33,22 +34,55 @@ static __device__ __align__(256) unsigned char g_adapt_scratch[kNoallocScratchBy
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-unsigned char* g_scratch_addr[kMaxDevices];   // per device, set by the first call there
+// Per device: the scratch's address and the CUDA context it was looked up in.
+struct ScratchAddr {
+    void* ctx;
+    unsigned char* addr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Device address of this device's copy of the scratch array.  The first call
-// on a device (which must be current) looks it up; later calls reuse it.
+// The calling thread's current CUDA context (the driver's cuCtxGetCurrent,
+// reached through the runtime's entry-point query), or null if unknown.
+void* current_context()
+{
+    using Fn = CUresult (*)(CUcontext*);
+    static Fn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (Fn) nullptr;
+        return (Fn)f;
+    }();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return (void*)c;
+}
+
+// Device address of this device's copy of the scratch array, valid in the
+// context current on the calling thread.  The first call on a device (which
+// must be current) looks it up; later calls in the same context reuse it.
+// A different context on that device (a non-primary context made current,
+// or the primary context re-created after cudaDeviceReset) gets its own
+// lookup, so no call ever writes through an address from a context that
+// may be gone.
 cudaError_t scratch_for_device(int dev, unsigned char** out)
 {
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_addr[dev]) {
+    void* ctx = current_context();
+    ScratchAddr& s = g_scratch[dev];
+    if (!s.addr || !ctx || s.ctx != ctx) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_adapt_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = (unsigned char*)p;
+        // the runtime may have made the device's primary context current
+        // during the lookup: key the cache on the context as it is now
+        s.ctx = current_context();
+        s.addr = (unsigned char*)p;
     }
-    *out = g_scratch_addr[dev];
+    *out = s.addr;
     return cudaSuccess;
 }
 
@@ -125,6 +159,7 @@ extern "C" fadkv_status fadkv_adapt_noalloc(const fadkv_params* p, void* atoms, 
     a.repl_coef = repl_coef;
     a.inactive = (int32_t*)base;
     a.flagged = (int32_t*)(base + off_flagged);
+    a.nrep = nullptr;
     a.counters = (long long*)(base + off_counters);
     a.V = V;
     a.append = 0;

@@ -49,15 +49,18 @@ bool use_tc(const fadkv_params& p)
 
 struct Layout {
     bool tc;     // screening on tensor cores with candidate filtering
+    bool gram;   // greedy over the dictionaries' Gram matrices (binary16, tensor-core screening)
     int chunk;   // vectors per dictionary per encode pass
     int cap;     // candidate capacity per vector
-    size_t counters, scores, cand, cand_count, pool, inactive, flagged, slow, total;
+    size_t counters, scores, cand, cand_count, pool, pool_r, inactive, flagged, slow, nrep, gdiag, gram_off, total;
 };
 
 Layout make_layout(const fadkv_params& p)
 {
     Layout L;
     L.tc = use_tc(p);
+    const Shape sh{p.num_dicts, p.N, p.d, p.n, p.s, p.dtype, p.lambda_abs, p.lambda_rel};
+    L.gram = L.tc && greedy_gram_supported(sh);
     L.cap = cand_cap(p.n);
     const size_t G = (size_t)p.num_dicts;
     const size_t mb = (size_t)(p.max_batch > 0 ? p.max_batch : 1);
@@ -75,9 +78,13 @@ Layout make_layout(const fadkv_params& p)
     L.cand = o;       o = align_up(o + G * chunk * cand_bytes, kAlign);
     L.cand_count = o; o = align_up(o + G * chunk * kCountSlots * sizeof(int), kAlign);
     L.pool = o;       o = align_up(o + (L.tc ? G * chunk * (size_t)p.n * sizeof(int32_t) : 0), kAlign);
+    L.pool_r = o;     o = align_up(o + (L.tc ? G * chunk * (size_t)p.n * sizeof(float) : 0), kAlign);
     L.inactive = o;   o = align_up(o + G * (size_t)p.N * sizeof(int32_t), kAlign);
     L.flagged = o;    o = align_up(o + G * mb * sizeof(int32_t), kAlign);
     L.slow = o;       o = align_up(o + sizeof(uint32_t), kAlign);
+    L.nrep = o;       o = align_up(o + G * sizeof(int32_t), kAlign);
+    L.gdiag = o;      o = align_up(o + (L.gram ? G * (size_t)p.N * sizeof(float) : 0), kAlign);
+    L.gram_off = o;   o = align_up(o + (L.gram ? gram_bytes(sh) : 0), kAlign);
     L.total = o;
     return L;
 }
@@ -160,6 +167,8 @@ struct fadkv_dict_s {
     int32_t pending_V;
     int sms;           // multiprocessors of the device (queried at first use)
     uint32_t seq;      // screening passes issued (the slow-path flag names the pass)
+    bool gram_ready;   // the Gram matrices hold the current atoms
+    unsigned long long wait_ns;   // screening pipeline's wait limit (0: the kernel's default)
     float alpha;       // screening threshold factor
     ScreenTCCache tc_cache;   // tensor maps of the screening kernel
     // tracing
@@ -245,6 +254,7 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
         a.rec = h->ws + h->L.cand;
         a.dump = dump;
         a.counters = counters(h);
+        a.wait_ns = h->wait_ns;
         e = traced(h, FADKV_K_SCREEN, st, [&] { return launch_screen_tc(h->sh, h->atoms, a, h->sms, &h->tc_cache, st); });
         if (e != cudaSuccess || dump) return e;
         SelectArgs sa;
@@ -255,6 +265,7 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
         sa.cap = select_cap(h->p.n);
         sa.rec = h->ws + h->L.cand;
         sa.pool = (int32_t*)(h->ws + h->L.pool);
+        sa.pool_r = (float*)(h->ws + h->L.pool_r);
         if (++h->seq == 0) h->seq = 1;                 // 0 is the workspace's initial value
         sa.slow_seq = (uint32_t*)(h->ws + h->L.slow);
         sa.seq = h->seq;
@@ -272,19 +283,17 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
     });
 }
 
-// Greedy kernel for binary16 dictionaries screened on the tensor cores: by
-// default the correlation-domain kernel (incremental Cholesky factor);
-// FADKV_GREEDY=tc selects one tcgen05 GEMM per pick, FADKV_GREEDY=mma the
-// residual-based mma.sync kernel and FADKV_GREEDY=ffma the FP32-pipe kernel.
-enum class GreedyPath { kChol, kTc, kClassic };
+float* gram_ptr(fadkv_dict h) { return (float*)(h->ws + h->L.gram_off); }
+float* gdiag_ptr(fadkv_dict h) { return (float*)(h->ws + h->L.gdiag); }
 
-GreedyPath greedy_path(fadkv_dict h)
+// The Gram matrices of every dictionary, from the atoms as they stand.
+cudaError_t build_gram(fadkv_dict h, cudaStream_t st)
 {
-    if (!h->L.tc) return GreedyPath::kClassic;
-    const char* f = getenv("FADKV_GREEDY");
-    if (f && strcmp(f, "tc") == 0) return greedy_tc_supported(h->sh) ? GreedyPath::kTc : GreedyPath::kClassic;
-    if (f && (strcmp(f, "mma") == 0 || strcmp(f, "ffma") == 0)) return GreedyPath::kClassic;
-    return greedy_chol_supported(h->sh) ? GreedyPath::kChol : GreedyPath::kClassic;
+    const cudaError_t e = traced(h, FADKV_K_GRAM, st, [&] {
+        return launch_gram_build(h->sh, h->atoms, gram_ptr(h), gdiag_ptr(h), st);
+    });
+    if (e == cudaSuccess) h->gram_ready = true;
+    return e;
 }
 
 GreedyArgs greedy_args(fadkv_dict h, const void* x, int32_t V, int v0, int Vc)
@@ -366,6 +375,8 @@ fadkv_status fadkv_dict_create(const fadkv_params* p, void* atoms, int32_t* usag
     h->pending_V = 0;
     h->sms = 0;
     h->seq = 0;
+    h->gram_ready = false;
+    h->wait_ns = 0;
     h->alpha = screen_alpha(p->n, p->N);
     h->prof_on = false;
     h->prof_mask = 0xffffffffu;
@@ -386,6 +397,22 @@ fadkv_status fadkv_dict_destroy(fadkv_dict h)
     }
     for (auto e : h->prof_free) cudaEventDestroy(e);
     delete h;
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_dict_refresh(fadkv_dict h, void* stream)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    if (fault_injected()) {
+        set_error("fadkv_dict_refresh", cudaErrorLaunchFailure);
+        return FADKV_ERR_CUDA;
+    }
+    if (!h->L.gram) return FADKV_OK;
+    const cudaError_t e = build_gram(h, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        set_error("fadkv_dict_refresh", e);
+        return FADKV_ERR_CUDA;
+    }
     return FADKV_OK;
 }
 
@@ -446,27 +473,33 @@ fadkv_status fadkv_encode(fadkv_dict h, const void* x, int32_t V, int32_t* idx, 
         return FADKV_ERR_CUDA;
     }
     cudaStream_t st = (cudaStream_t)stream;
+    if (V > 0 && h->L.gram && !h->gram_ready) {
+        const cudaError_t e = build_gram(h, st);
+        if (e != cudaSuccess) {
+            set_error("fadkv_encode", e);
+            return FADKV_ERR_CUDA;
+        }
+    }
     const int chunk = h->L.chunk;
     for (int v0 = 0; v0 < V; v0 += chunk) {
         const int Vc = (V - v0 < chunk) ? V - v0 : chunk;
         cudaError_t e = run_screen(h, x, V, v0, Vc, nullptr, st, h->p.n);
-        const GreedyPath gp = greedy_path(h);
-        if (e == cudaSuccess && gp != GreedyPath::kClassic) {
+        if (e == cudaSuccess && h->L.gram) {
             int32_t* pool = (int32_t*)(h->ws + h->L.pool);
+            float* pool_r = (float*)(h->ws + h->L.pool_r);
             GreedyArgs fa = greedy_args(h, x, V, v0, Vc);
-            e = traced(h, FADKV_K_TOPN, st, [&] { return launch_pool_fixup(h->sh, fa, pool, (const uint32_t*)(h->ws + h->L.slow), h->seq, h->sms, st);
+            e = traced(h, FADKV_K_TOPN, st, [&] {
+                return launch_pool_fixup(h->sh, fa, pool, pool_r, (const uint32_t*)(h->ws + h->L.slow), h->seq,
+                                         h->sms, st);
             });
-            if (e == cudaSuccess && gp == GreedyPath::kChol) {
-                GreedyArgs ca = greedy_args(h, x, V, v0, Vc);
-                ca.idx = idx;
-                ca.coef = coef;
-                ca.relres = relres;
-                e = traced(h, FADKV_K_GREEDY, st, [&] { return launch_greedy_chol(h->sh, ca, st); });
-            } else if (e == cudaSuccess) {
-                GreedyTCArgs ga;
-                ga.atoms = h->atoms;
-                ga.x = x;
+            if (e == cudaSuccess) {
+                GramGreedyArgs ga;
+                ga.atoms = (const __half*)h->atoms;
+                ga.x = (const __half*)x;
                 ga.pool = pool;
+                ga.pool_r = pool_r;
+                ga.gram = gram_ptr(h);
+                ga.gdiag = gdiag_ptr(h);
                 ga.idx = idx;
                 ga.coef = coef;
                 ga.relres = relres;
@@ -474,9 +507,12 @@ fadkv_status fadkv_encode(fadkv_dict h, const void* x, int32_t V, int32_t* idx, 
                 ga.V = V;
                 ga.v0 = v0;
                 ga.Vc = Vc;
-                e = traced(h, FADKV_K_GREEDY, st, [&] { return launch_greedy_tc(h->sh, ga, h->sms, st); });
+                e = traced(h, FADKV_K_GREEDY, st, [&] { return launch_greedy_gram(h->sh, ga, st); });
             }
         } else if (e == cudaSuccess) {
+            // FP32-pipe greedy: binary32 dictionaries, atoms not screened on
+            // the tensor cores, or shapes beyond the Gram kernel's (n > 512
+            // or s > 16); it takes the selection's pool where there is one
             GreedyArgs a = greedy_args(h, x, V, v0, Vc);
             a.idx = idx;
             a.coef = coef;
@@ -529,9 +565,11 @@ fadkv_status fadkv_encode_pl(fadkv_dict h, const void* x, int32_t V, int32_t* id
         pa.Vc = Vc;
         if (e == cudaSuccess && h->L.tc) {
             int32_t* pool = (int32_t*)(h->ws + h->L.pool);
+            float* pool_r = (float*)(h->ws + h->L.pool_r);
             GreedyArgs fa = greedy_args(h, x, V, v0, Vc);
             e = traced(h, FADKV_K_TOPN, st, [&] {
-                return launch_pool_fixup(sh, fa, pool, (const uint32_t*)(h->ws + h->L.slow), h->seq, h->sms, st);
+                return launch_pool_fixup(sh, fa, pool, pool_r, (const uint32_t*)(h->ws + h->L.slow), h->seq, h->sms,
+                                         st);
             });
             pa.pool = pool;
         }
@@ -573,11 +611,18 @@ fadkv_status adapt_call(const char* name, fadkv_dict h, const void* x, int32_t V
     a.repl_coef = repl_coef;
     a.inactive = (int32_t*)(h->ws + h->L.inactive);
     a.flagged = (int32_t*)(h->ws + h->L.flagged);
+    a.nrep = (int32_t*)(h->ws + h->L.nrep);
     a.counters = counters(h);
     a.V = V;
     a.append = append;
     cudaStream_t st = (cudaStream_t)stream;
-    const cudaError_t e = traced(h, FADKV_K_ADAPT, st, [&] { return launch_adapt(h->sh, a, h->delta, st); });
+    cudaError_t e = traced(h, FADKV_K_ADAPT, st, [&] { return launch_adapt(h->sh, a, h->delta, st); });
+    // the rows and columns of the atoms just written (none, if the Gram
+    // matrices are not built yet: the build reads the atoms as they stand)
+    if (e == cudaSuccess && h->L.gram && h->gram_ready)
+        e = traced(h, FADKV_K_GRAM, st, [&] {
+            return launch_gram_update(h->sh, h->atoms, a.inactive, a.nrep, h->p.N, gram_ptr(h), gdiag_ptr(h), st);
+        });
     if (e != cudaSuccess) {
         set_error(name, e);
         return FADKV_ERR_CUDA;
@@ -663,6 +708,29 @@ fadkv_status fadkv_debug_pool(fadkv_dict h, const void* x, int32_t V, int32_t* p
             set_error("fadkv_debug_pool", e);
             return FADKV_ERR_CUDA;
         }
+    }
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_debug_wait_limit(fadkv_dict h, uint64_t limit_ns)
+{
+    if (!h) return FADKV_ERR_INVALID_ARG;
+    h->wait_ns = (unsigned long long)limit_ns;
+    return FADKV_OK;
+}
+
+fadkv_status fadkv_debug_wait_probe(fadkv_dict h, uint64_t limit_ns, void* stream)
+{
+    if (!h || limit_ns == 0 || limit_ns > 10ull * 1000 * 1000 * 1000) return FADKV_ERR_INVALID_ARG;
+    if (fault_injected()) {
+        set_error("fadkv_debug_wait_probe", cudaErrorLaunchFailure);
+        return FADKV_ERR_CUDA;
+    }
+    unsigned long long* status = (unsigned long long*)&counters(h)[kCntStatus];
+    const cudaError_t e = launch_wait_probe(status, (unsigned long long)limit_ns, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        set_error("fadkv_debug_wait_probe", e);
+        return FADKV_ERR_CUDA;
     }
     return FADKV_OK;
 }

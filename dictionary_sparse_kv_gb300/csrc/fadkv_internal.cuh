@@ -123,17 +123,20 @@ cudaError_t launch_topn_radix(const Shape& sh, const float* scores, int Vc, unsi
 //   word 0      header: overflow << 31 | eb << 16 | k0 << 8 | count
 //   words 1..   count packed keys, those of atoms c*128 + [0, 64) first (k0
 //               of them), then those of c*128 + [64, 128)
-// A packed key holds |r_j| exactly relative to eb, the exponent field of the
-// vector's threshold tau (every kept |r| >= tau >= 2^(eb-127)):
-//   packed = bits(min(|r|, top)) - (eb << 23) + (col << 26),
+// A packed key holds r_j exactly: |r_j| relative to eb, the exponent field
+// of the vector's threshold tau (every kept |r| >= tau >= 2^(eb-127)), and
+// the sign of r_j:
+//   packed = bits(min(|r|, top)) - (eb << 23) + (sign << 25) + (col << 26),
 //   col = the atom's index within its 64-atom half, top = the float with bits
-//   (eb << 23) + 2^26 - 1 (|r| < 2^(eb-119): eight binades above tau's).  A
-//   key at top may have been clipped, and a record with more than kRecKeys
-//   keys is flagged: the consumer redoes such a vector exactly.
+//   (eb << 23) + 2^25 - 1 (|r| < 2^(eb-123): four binades above tau's, which
+//   holds |r| <= ||x|| for unit atoms whenever alpha > sqrt(d)/8).  A key at
+//   top may have been clipped, and a record with more than kRecKeys keys is
+//   flagged: the consumer redoes such a vector exactly.
 constexpr int kRecWords = 32;
 constexpr int kRecBytes = kRecWords * 4;
 constexpr int kRecKeys = kRecWords - 1;
-constexpr uint32_t kRecValueMask = (1u << 26) - 1u;
+constexpr uint32_t kRecValueMask = (1u << 25) - 1u;
+constexpr int kRecSignShift = 25;
 __host__ __device__ inline uint32_t rec_header(bool over, uint32_t eb, int k0, int count)
 {
     return (over ? 0x80000000u : 0u) | (eb << 16) | ((uint32_t)k0 << 8) | (uint32_t)count;
@@ -145,6 +148,7 @@ struct ScreenTCArgs {
     unsigned char* rec;       // [G][Vc][N/128] records of kRecBytes
     float* dump;              // test hook: if set, write all scores [G][Vc][N] instead
     long long* counters;      // [G][kCntFields] (status word)
+    unsigned long long wait_ns;   // limit of the pipeline's waits (0: the default; a test hook shortens it)
 };
 // Host-side state a handle keeps between launches: the encoded tensor map of
 // the dictionaries (by base address and row count) and whether the kernel's
@@ -161,13 +165,14 @@ cudaError_t launch_screen_tc(const Shape& sh, const void* atoms, const ScreenTCA
                              cudaStream_t st);
 
 // Exact Top-n pool from the screening records, one warp per vector; pool
-// [G][Vc][n] atom ids, pool[0] = -2 where the exact slow path must redo the
-// vector (a record overflowed or was clipped, fewer than n candidates, or
-// more than cap).
+// [G][Vc][n] atom ids and pool_r [G][Vc][n] their scores r_j (signed),
+// pool[0] = -2 where the exact slow path must redo the vector (a record
+// overflowed or was clipped, fewer than n candidates, or more than cap).
 struct SelectArgs {
     int G, Vc, N, n, cap;     // cap: the most candidates taken (else the slow path)
     const unsigned char* rec; // [G][Vc][N/128] screening records
     int32_t* pool;            // [G][Vc][n]
+    float* pool_r;            // [G][Vc][n]
     uint32_t* slow_seq;       // set to `seq` when some vector of the pass needs the slow path
     uint32_t seq;             // number of this screening pass (never 0)
 };
@@ -199,38 +204,41 @@ struct GreedyArgs {
 };
 cudaError_t launch_greedy(const Shape& sh, const GreedyArgs& a, cudaStream_t st);
 size_t greedy_smem_bytes(const Shape& sh);
-// the tensor-core variant for binary16 dictionaries (used by launch_greedy)
-cudaError_t launch_greedy_mma(const Shape& sh, const GreedyArgs& a, cudaStream_t st);
-size_t greedy_mma_smem_bytes(const Shape& sh);
 
-// Greedy selection + ridge refit with the pool correlations on the tensor
-// cores: every pick is one GEMM of the residual tile (128 vectors) against
-// the dictionary, reduced to a masked argmax per vector (binary16
-// dictionaries).  Needs the exact pool of every vector in `pool` (run
-// launch_pool_fixup first).
-struct GreedyTCArgs {
-    const void* atoms;
-    const void* x;            // [G][V][d]
+// Gram matrices of the dictionaries (binary16): gram [G][N][N] fp32 and its
+// diagonal gdiag [G][N].  Build: every entry.  Update: the rows and columns
+// of the nrows[g] atoms listed at rows + g * row_stride (the atoms an
+// adaptation just wrote).
+bool greedy_gram_supported(const Shape& sh);
+size_t gram_bytes(const Shape& sh);
+cudaError_t launch_gram_build(const Shape& sh, const void* atoms, float* gram, float* gdiag, cudaStream_t st);
+cudaError_t launch_gram_update(const Shape& sh, const void* atoms, const int32_t* rows, const int32_t* nrows,
+                               int row_stride, float* gram, float* gdiag, cudaStream_t st);
+
+// Greedy selection + ridge refit over the Gram matrix, in the correlation
+// domain (binary16, n <= 512, s <= 16): the pool's ids and signed scores
+// come from the selection (or the pool fixup), the pick's Gram row from
+// gram; writes idx/coef/relres for vectors [v0, v0+Vc).
+struct GramGreedyArgs {
+    const __half* atoms;      // [G][N][d]
+    const __half* x;          // [G][V][d]
     const int32_t* pool;      // [G][Vc][n]
+    const float* pool_r;      // [G][Vc][n]
+    const float* gram;        // [G][N][N]
+    const float* gdiag;       // [G][N]
     int32_t* idx;             // [G][V][s]
     float* coef;              // [G][V][s]
     float* relres;            // [G][V]
     long long* counters;      // [G][kCntFields]
     int V, v0, Vc;
 };
-bool greedy_tc_supported(const Shape& sh);
-cudaError_t launch_greedy_tc(const Shape& sh, const GreedyTCArgs& a, int sms, cudaStream_t st);
+cudaError_t launch_greedy_gram(const Shape& sh, const GramGreedyArgs& a, cudaStream_t st);
 
-// Greedy + ridge refit in the correlation domain (incremental Cholesky
-// factor, pool resident in registers; binary16, n <= 512, s <= 16).  Needs
-// the exact pool of every vector in a.pool_in (run launch_pool_fixup first).
-bool greedy_chol_supported(const Shape& sh);
-cudaError_t launch_greedy_chol(const Shape& sh, const GreedyArgs& a, cudaStream_t st);
-
-// Exact pool of the vectors the selection kernel left to the slow path
-// (pool[0] == -2): all N scores on the FP32 pipe, exact Top-n.
-cudaError_t launch_pool_fixup(const Shape& sh, const GreedyArgs& a, int32_t* pool, const uint32_t* slow_seq,
-                              uint32_t seq, int sms, cudaStream_t st);
+// Exact pool (ids and signed scores) of the vectors the selection kernel
+// left to the slow path (pool[0] == -2): all N scores on the FP32 pipe,
+// exact Top-n.
+cudaError_t launch_pool_fixup(const Shape& sh, const GreedyArgs& a, int32_t* pool, float* pool_r,
+                              const uint32_t* slow_seq, uint32_t seq, int sms, cudaStream_t st);
 
 // PL encode's fit: the s atoms of the Top-s set in ascending order and one
 // ridge fit over them, one warp per vector.  The set comes from `pool`
@@ -304,11 +312,17 @@ struct AdaptArgs {
     float* repl_coef;
     int32_t* inactive;        // [G][N] scratch
     int32_t* flagged;         // [G][max_batch] scratch
+    int32_t* nrep;            // optional [G]: atoms written by this call (their ids: inactive[g][0..nrep))
     long long* counters;      // [G][kCntFields]
     int V;
     int append;               // 0: reuse inactive atoms (usage == 0); 1: fill free slots (usage < 0)
 };
 cudaError_t launch_adapt(const Shape& sh, const AdaptArgs& a, const DeltaTable& delta, cudaStream_t st);
+
+// Test hook: one thread waits, with a limit of limit_ns, on an mbarrier that
+// nothing arrives on, so the wait runs out and sets FADKV_DEV_TIMEOUT in
+// *status.
+cudaError_t launch_wait_probe(unsigned long long* status, unsigned long long limit_ns, cudaStream_t st);
 
 // xhat = D_S c (+ repl term).
 cudaError_t launch_reconstruct(const Shape& sh, const void* atoms, int V, const int32_t* idx,

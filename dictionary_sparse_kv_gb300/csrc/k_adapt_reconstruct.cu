@@ -125,6 +125,7 @@ adapt_kernel(Shape sh, AdaptArgs a, DeltaTable delta, int max_batch)
         }
     }
     if (tid == 0) {
+        if (a.nrep) a.nrep[g] = m;
         cnt[kCntEncoded] += V;
         cnt[kCntReplaced] += m;
         cnt[kCntFlagged] += nF;

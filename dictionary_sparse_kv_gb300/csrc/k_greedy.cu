@@ -23,8 +23,9 @@
 // The Cholesky factor of A grows by one row per pick (the factor of a
 // leading block is the leading block of the factor), so a refit costs O(k^2).
 //
-// This is the FP32-pipe kernel, used for binary32 dictionaries (and on
-// request for binary16, to cross-check the tensor-core kernel): one CTA
+// This is the FP32-pipe kernel, used for binary32 dictionaries, for binary16
+// dictionaries whose atom count is not a multiple of 128 (screened on the
+// FP32 pipe) and for the pool test hook: one CTA
 // (256 threads) per vector; the pool (exact Top-n from select.cuh) is
 // gathered once into shared memory (rows padded by 16 bytes: eight threads
 // reading eight consecutive rows hit distinct banks); thread t owns pool
@@ -375,23 +376,14 @@ cudaError_t launch_t(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 
 }  // namespace
 
-static bool use_mma(const Shape& sh)
-{
-    if (sh.dtype != FADKV_F16) return false;
-    const char* f = getenv("FADKV_GREEDY");
-    return !(f && strcmp(f, "ffma") == 0);
-}
-
 size_t greedy_smem_bytes(const Shape& sh)
 {
-    if (use_mma(sh)) return greedy_mma_smem_bytes(sh);
     return greedy_layout(sh.n, sh.d, sh.dtype == FADKV_F16 ? 2 : 4, sh.N, cand_cap(sh.n)).total;
 }
 
 cudaError_t launch_greedy(const Shape& sh, const GreedyArgs& a, cudaStream_t st)
 {
     if (a.Vc <= 0) return cudaSuccess;
-    if (use_mma(sh)) return launch_greedy_mma(sh, a, st);
     if (sh.dtype == FADKV_F16) {
         if (sh.d == 128) return launch_t<__half, 128>(sh, a, st);
         return launch_t<__half, 64>(sh, a, st);

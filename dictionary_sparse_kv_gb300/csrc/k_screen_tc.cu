@@ -18,8 +18,8 @@
 // atom j if |S[v][j]| >= tau_v, tau_v = alpha * ||x_v|| / sqrt(d) with alpha
 // set on the host so that an atom uncorrelated with x_v passes with
 // probability ~1.5n/N.  Each kept score becomes a 32-bit packed key (|S|
-// exactly, relative to the exponent of tau_v, and the atom's column; see
-// ScreenTCArgs) appended to the vector's record of the unit in shared
+// exactly, relative to the exponent of tau_v, its sign and the atom's
+// column; see ScreenTCArgs) appended to the vector's record of the unit in shared
 // memory: one predicated 4-byte store per score.  After each unit the warp
 // copies its 32 records out with 16-byte loads and stores, eight lanes on a
 // record: the candidate output lands as whole sectors.  A row with more than kRecKeys kept scores in a unit makes
@@ -30,7 +30,9 @@
 // (warp 4+e reads TMEM lanes 32(e%4).. and handles the units whose
 // accumulator buffer is e/4).  Every wait is bounded by a wall-clock limit;
 // on expiry the CTA sets FADKV_DEV_TIMEOUT in the status word, drains its own
-// copies and MMAs (bounded), frees TMEM and returns.
+// copies and MMAs (the producer waits for every atom chunk it issued, the MMA
+// issuer for its last commit, each with the full limit), frees TMEM and
+// returns.
 #include "tc_common.cuh"
 
 namespace fadkv {
@@ -126,6 +128,7 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
     const int nu = (int)(u1 - u0);
     const int g_first = (int)(u0 / nch / tiles);
     unsigned long long* status = (unsigned long long*)&a.counters[(size_t)g_first * kCntFields + kCntStatus];
+    const unsigned long long wait_ns = a.wait_ns ? a.wait_ns : kWaitNs;   // pipeline waits (drains: kWaitNs)
 
     if (threadIdx.x == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_d)) : "memory");
@@ -169,7 +172,7 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
             uc.init(u0, nch, tiles);
             for (int i = 0; i < nu && ok; ++i, uc.advance(1)) {
                 const int st = i % L::kStages;
-                ok = mbar_wait(empty_bar(st), ((uint32_t)(i / L::kStages) & 1u) ^ 1u, status);
+                ok = mbar_wait(empty_bar(st), ((uint32_t)(i / L::kStages) & 1u) ^ 1u, status, wait_ns);
                 if (!ok) break;
                 mbar_expect_tx(full_bar(st), kTileBytes);
                 const int arow = uc.g * a.N + uc.c * kChunk;
@@ -198,7 +201,7 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
             ++seg;
             const int ab = seg & 1;
             // the buffer's previous tile (segment seg-2) must be done with
-            if (seg >= 2) ok = mbar_wait(aempty_bar(ab), (uint32_t)((seg >> 1) - 1) & 1u, status);
+            if (seg >= 2) ok = mbar_wait(aempty_bar(ab), (uint32_t)((seg >> 1) - 1) & 1u, status, wait_ns);
             if (!ok) break;
             fence_after();
             const int vloc = uc.tile * kTileV + q * 32 + lane;
@@ -234,14 +237,14 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
                     if (seg >= 0) mma_commit(aempty_bar(seg & 1));
                     prev = uc.pair;
                     ++seg;
-                    ok = mbar_wait(afull_bar(seg & 1), (uint32_t)(seg >> 1) & 1u, status);
+                    ok = mbar_wait(afull_bar(seg & 1), (uint32_t)(seg >> 1) & 1u, status, wait_ns);
                     if (!ok) break;
                 }
                 const int buf = i & 1;
-                ok = mbar_wait(tempty_bar(buf), ((uint32_t)(i >> 1) & 1u) ^ 1u, status);
+                ok = mbar_wait(tempty_bar(buf), ((uint32_t)(i >> 1) & 1u) ^ 1u, status, wait_ns);
                 if (!ok) break;
                 const int st = i % L::kStages;
-                ok = mbar_wait(full_bar(st), (uint32_t)(i / L::kStages) & 1u, status);
+                ok = mbar_wait(full_bar(st), (uint32_t)(i / L::kStages) & 1u, status, wait_ns);
                 if (!ok) break;
                 fence_after();
                 const uint32_t dt = tbase + (uint32_t)(buf * kChunk);
@@ -306,7 +309,7 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
                 top = __uint_as_float(base_bits + kRecValueMask);
             }
             const int buf = i & 1;
-            ok = mbar_wait(tfull_bar(buf), (uint32_t)(i >> 1) & 1u, status);
+            ok = mbar_wait(tfull_bar(buf), (uint32_t)(i >> 1) & 1u, status, wait_ns);
             if (!ok) break;
             fence_after();
             const uint32_t tcol = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kChunk);
@@ -327,7 +330,8 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
                     for (int t = 0; t < 32; ++t) {
                         const float f = fabsf(__uint_as_float(v[t]));
                         if (f >= tau) {
-                            myrec[k] = __float_as_uint(fminf(f, top)) + ((uint32_t)((qq & 1) * 32 + t) << 26) + nbase;
+                            myrec[k] = __float_as_uint(fminf(f, top)) + nbase + ((v[t] >> 31) << kRecSignShift) +
+                                       ((uint32_t)((qq & 1) * 32 + t) << 26);
                             ++k;
                         }
                     }
@@ -456,6 +460,24 @@ int screen_tc_grid(const Shape& sh, int Vc, int sms)
     const int tiles = (Vc + kTileV - 1) / kTileV;
     const long long T = (long long)sh.G * tiles * (sh.N / kChunk);
     return (int)(T < sms ? (T > 0 ? T : 1) : sms);
+}
+
+// One thread waits on an mbarrier that expects one arrival and gets none:
+// the bounded wait runs out after limit_ns and flags the status word.  No
+// copy or MMA is issued, so nothing is left in flight when it returns.
+__global__ void wait_probe_kernel(unsigned long long* status, unsigned long long limit_ns)
+{
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(b, 0u, status, limit_ns);
+}
+
+cudaError_t launch_wait_probe(unsigned long long* status, unsigned long long limit_ns, cudaStream_t st)
+{
+    wait_probe_kernel<<<1, 1, 0, st>>>(status, limit_ns);
+    return cudaGetLastError();
 }
 
 bool screen_tc_supported(const Shape& sh)

@@ -6,8 +6,10 @@
 //
 // The candidates of a vector arrive as the screening kernel's records: per
 // 128-atom chunk a header and the kept atoms' packed keys.  A warp decodes
-// them into 64-bit keys (bits(|r_j|) << 32) | (0xffffffff - j) in its slice
-// of shared memory, then:
+// them into 64-bit keys (bits(|r_j|) << 32) | ((0x7fffffff - j) << 1) |
+// sign(r_j) in its slice of shared memory (the larger key is the larger |r|,
+// then the lower atom index; the sign bit never decides, atoms being
+// distinct), then:
 //   1. buckets the keys by |r| on a linear grid of 256 buckets over
 //      [min |r|, max |r|] of the list (monotone in |r|, so every key of a
 //      higher bucket beats every key of a lower one);
@@ -26,6 +28,16 @@ namespace {
 
 constexpr int kWarpsPerCta = 4;
 
+__device__ __forceinline__ unsigned long long sel_key(uint32_t absbits, uint32_t atom, uint32_t sign)
+{
+    return ((unsigned long long)absbits << 32) | (((0x7fffffffu - atom) << 1) | sign);
+}
+__device__ __forceinline__ int key_atom(unsigned long long k) { return (int)(0x7fffffffu - ((uint32_t)k >> 1)); }
+__device__ __forceinline__ float key_r(unsigned long long k)
+{
+    return __uint_as_float((uint32_t)(k >> 32) | ((uint32_t)k << 31));
+}
+
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 select_kernel(SelectArgs a)
 {
@@ -39,12 +51,18 @@ select_kernel(SelectArgs a)
     unsigned long long* keys = kbuf_all + (size_t)wl * a.cap;
     const int n = a.n;
     int32_t* pool = a.pool + gw * n;
+    float* pool_r = a.pool_r + gw * n;
+    auto put = [&](int pos, unsigned long long k) {
+        pool[pos] = key_atom(k);
+        pool_r[pos] = key_r(k);
+    };
 
     // the screening records of this vector, 32 at a time: the headers and
     // every record's 16-byte pieces in one batch of loads (eight lanes on a
     // record, four records per load); record c's keys go to the sum of the
     // counts of the records before it, decoded:
-    //   |r| bits = (packed & (2^26 - 1)) + (eb << 23), atom = 128 c + 64 h + (packed >> 26)
+    //   |r| bits = (packed & (2^25 - 1)) + (eb << 23), sign = bit 25,
+    //   atom = 128 c + 64 h + (packed >> 26)
     // with h = 1 for the keys past the record's first k0
     const int nch = a.N / 128;
     const unsigned char* rec = a.rec + (size_t)gw * nch * kRecBytes;
@@ -91,7 +109,7 @@ select_kernel(SelectArgs a)
                     const uint32_t val = wv[q] & kRecValueMask;
                     clipped |= val == kRecValueMask;
                     const uint32_t atom = jbase + (kk >= k0 ? 64u : 0u) + (wv[q] >> 26);
-                    keys[oj + kk] = ((unsigned long long)(val + ebits) << 32) | (0xffffffffu - atom);
+                    keys[oj + kk] = sel_key(val + ebits, atom, (wv[q] >> kRecSignShift) & 1u);
                 }
             }
         }
@@ -175,7 +193,7 @@ select_kernel(SelectArgs a)
         const unsigned long long k = (i < K) ? keys[i] : 0ull;
         const bool f = (i < K) && bucket(k) > bsel;
         const unsigned bal = __ballot_sync(0xffffffffu, f);
-        if (f) pool[base + __popc(bal & ((1u << lane) - 1u))] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+        if (f) put(base + __popc(bal & ((1u << lane) - 1u)), k);
         base += __popc(bal);
     }
     if (rem == nb) {
@@ -185,7 +203,7 @@ select_kernel(SelectArgs a)
             const unsigned long long k = (i < K) ? keys[i] : 0ull;
             const bool f = (i < K) && bucket(k) == bsel;
             const unsigned bal = __ballot_sync(0xffffffffu, f);
-            if (f) pool[base + __popc(bal & ((1u << lane) - 1u))] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+            if (f) put(base + __popc(bal & ((1u << lane) - 1u)), k);
             base += __popc(bal);
         }
         return;
@@ -211,7 +229,7 @@ select_kernel(SelectArgs a)
         for (int j = 0; j < mb; ++j) rank += (__shfl_sync(0xffffffffu, mk, j) > mk) ? 1u : 0u;
         const bool f = lane < mb && rank < rem;
         const unsigned bal = __ballot_sync(0xffffffffu, f);
-        if (f) pool[base + __popc(bal & ((1u << lane) - 1u))] = (int)(0xffffffffu - (uint32_t)(mk & 0xffffffffull));
+        if (f) put(base + __popc(bal & ((1u << lane) - 1u)), mk);
         return;
     }
     // rare: a crowded bucket -- MSD radix select over the bucket's keys
@@ -268,7 +286,7 @@ select_kernel(SelectArgs a)
         const unsigned long long k = (i < mb) ? bkeys[i] : 0ull;
         const bool f = (i < mb) && (k >> shift) >= lim;
         const unsigned bal = __ballot_sync(0xffffffffu, f);
-        if (f) pool[base + __popc(bal & ((1u << lane) - 1u))] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+        if (f) put(base + __popc(bal & ((1u << lane) - 1u)), k);
         base += __popc(bal);
     }
 }

@@ -11,9 +11,11 @@
 namespace fadkv {
 namespace tc {
 
-// Every wait gives up after this much wall-clock time, flags
-// FADKV_DEV_TIMEOUT in the dictionary's status word and lets the kernel
-// drain and return.
+// Every wait gives up after a wall-clock limit, flags FADKV_DEV_TIMEOUT in
+// the dictionary's status word and lets the kernel drain and return.  The
+// pipeline's waits take the launch's limit (kWaitNs unless a test shortens
+// it); the drain's waits, for copies and MMAs already issued, which complete
+// on their own, always take kWaitNs.
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;   // 200 ms
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
@@ -71,16 +73,18 @@ __device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait; returns false (and flags the status word) on timeout.
+// Bounded wait; returns false (and flags the status word) once limit_ns of
+// wall-clock time have passed without the phase completing.
 template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long* status)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long* status,
+                                          unsigned long long limit_ns = kWaitNs)
 {
     auto probe = [&] { return kCluster ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity); };
     if (probe()) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t i = 0;; ++i) {
         if (probe()) return true;
-        if ((i & 255u) == 255u && globaltimer() - t0 > kWaitNs) {
+        if ((i & 255u) == 255u && globaltimer() - t0 > limit_ns) {
             atomicOr(status, (unsigned long long)FADKV_DEV_TIMEOUT);
             return false;
         }

@@ -88,6 +88,7 @@ _SIGS = {
     "fadkv_dict_create": ([C.POINTER(Params), C.c_void_p, C.c_void_p, C.POINTER(C.c_float), C.c_void_p,
                            C.c_size_t, C.POINTER(C.c_void_p)], C.c_int),
     "fadkv_dict_destroy": ([C.c_void_p], C.c_int),
+    "fadkv_dict_refresh": ([C.c_void_p, C.c_void_p], C.c_int),
     "fadkv_encode": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p],
                      C.c_int),
     "fadkv_encode_pl": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p],
@@ -104,6 +105,8 @@ _SIGS = {
     "fadkv_dict_stats": ([C.c_void_p, C.POINTER(C.c_int64), C.c_void_p], C.c_int),
     "fadkv_debug_pool": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "fadkv_debug_scores": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p], C.c_int),
+    "fadkv_debug_wait_limit": ([C.c_void_p, C.c_uint64], C.c_int),
+    "fadkv_debug_wait_probe": ([C.c_void_p, C.c_uint64, C.c_void_p], C.c_int),
     "fadkv_store_codes": ([C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p], C.c_int),
     "fadkv_attend": ([C.POINTER(AttnParams), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
@@ -115,7 +118,7 @@ _SIGS = {
 }
 
 PROFILE_KERNELS = 8
-KERNEL_NAMES = ("screen", "topn", "greedy", "adapt", "reconstruct", "k5", "k6", "k7")
+KERNEL_NAMES = ("screen", "topn", "greedy", "adapt", "reconstruct", "gram", "k6", "k7")
 
 
 def lib():
@@ -184,6 +187,18 @@ def dict_create(p: Params, atoms, usage, delta, workspace, workspace_bytes_: int
 
 def dict_destroy(h: int) -> None:
     _check("fadkv_dict_destroy", lib().fadkv_dict_destroy(h))
+
+
+def dict_refresh(h: int, stream=None) -> None:
+    """Rebuild the handle's Gram matrices after atoms changed outside its adapt calls."""
+    _check("fadkv_dict_refresh", lib().fadkv_dict_refresh(h, stream if isinstance(stream, int) else
+                                                           (stream.cuda_stream if stream is not None
+                                                            else _default_stream())))
+
+
+def _default_stream():
+    import torch
+    return torch.cuda.current_stream().cuda_stream
 
 
 def encode(h: int, x, V: int, idx, coef, relres, stream=None) -> None:
@@ -277,6 +292,17 @@ def debug_scores(h: int, x, V: int, scores, stream=None) -> None:
     _check("fadkv_debug_scores", lib().fadkv_debug_scores(h, _addr(x), V, _addr(scores), st))
 
 
+def debug_wait_limit(h: int, limit_ns: int) -> None:
+    """Test hook: limit of the screening pipeline's waits (0 = default)."""
+    _check("fadkv_debug_wait_limit", lib().fadkv_debug_wait_limit(h, int(limit_ns)))
+
+
+def debug_wait_probe(h: int, limit_ns: int, stream=None) -> None:
+    """Test hook: a wait that nothing completes, limited to limit_ns."""
+    st = stream if isinstance(stream, int) else (stream.cuda_stream if stream is not None else _default_stream())
+    _check("fadkv_debug_wait_probe", lib().fadkv_debug_wait_probe(h, int(limit_ns), st))
+
+
 def profile_enable(h: int, enable: bool = True) -> None:
     _check("fadkv_profile_enable", lib().fadkv_profile_enable(h, 1 if enable else 0))
 
@@ -355,6 +381,10 @@ class Dictionary:
                      torch.empty((G, V), dtype=torch.float32, device=dev),
                      torch.empty((G, V), dtype=torch.int32, device=dev),
                      torch.empty((G, V), dtype=torch.float32, device=dev))
+
+    def refresh(self, stream=None):
+        """Rebuild the Gram matrices (after changing self.atoms in place)."""
+        dict_refresh(self.h, stream if stream is not None else _stream(None, self.atoms))
 
     def encode(self, x, codes: Codes, stream=None):
         V = x.shape[1]

@@ -135,6 +135,18 @@ fadkv_status fadkv_dict_create(const fadkv_params* params, void* atoms, int32_t*
                                const float* delta, void* workspace, size_t workspace_bytes,
                                fadkv_dict* out);
 
+/* Rebuild the handle's Gram matrices from the atoms as they stand.  For
+   binary16 dictionaries screened on the tensor cores (N a multiple of 128,
+   n <= 512, s <= 16) the greedy coder reads the inner products of the atoms
+   from a Gram matrix per dictionary kept in the workspace (G * N * N * 4
+   bytes of fadkv_workspace_bytes).  It is built by the first fadkv_encode
+   and kept up to date by fadkv_adapt / fadkv_adapt_append, which rewrite its
+   rows and columns of the atoms they write.  A caller that changes atoms in
+   any other way (its own copies, fadkv_adapt_noalloc on the same buffer)
+   calls this before the next fadkv_encode.  Asynchronous on `stream`; a
+   no-op for handles without Gram matrices.  Errors: INVALID_ARG, CUDA. */
+fadkv_status fadkv_dict_refresh(fadkv_dict dict, void* stream);
+
 /* Free the host-side handle.  Device memory stays with the caller.
    The caller must make sure no work of this handle is still running. */
 fadkv_status fadkv_dict_destroy(fadkv_dict dict);
@@ -220,9 +232,13 @@ fadkv_status fadkv_adapt_append(fadkv_dict dict, const void* x, int32_t V, const
    fadkv_last_error(), before any CUDA call.  Nothing in the scratch has to
    start at zero, and the library allocates and frees nothing.
    The first call on a device looks up the scratch's address there
-   (cudaGetSymbolAddress, with that device current); a caller that records
-   its calls under stream capture should make one call on each device before
-   capture begins.  All calls on one device share the one scratch array:
+   (cudaGetSymbolAddress, with that device current) and keeps it for the CUDA
+   context current at the time; a call made in another context of that device
+   (a non-primary context made current, or the primary context re-created
+   after cudaDeviceReset) looks it up again.  A caller that records its calls
+   under stream capture should make one call on each device, in the context
+   it captures in, before capture begins.  All calls on one device share the
+   one scratch array:
    calls that may run concurrently (different streams or host threads) race,
    so issue them in order on one stream.  There is no sequence check and no
    per-dictionary statistics: the caller keeps encode/adapt order itself.
@@ -262,6 +278,22 @@ fadkv_status fadkv_debug_pool(fadkv_dict dict, const void* x, int32_t V, int32_t
    No state changes.  V must not exceed the handle's internal pass size
    (at least min(max_batch, 128)).  Errors: INVALID_ARG, CUDA. */
 fadkv_status fadkv_debug_scores(fadkv_dict dict, const void* x, int32_t V, float* scores, void* stream);
+
+/* Test hook: the wall-clock limit, in nanoseconds, of the waits inside the
+   tensor-core screening pipeline of this handle (0 = the default, 200 ms).
+   A wait that runs out sets FADKV_DEV_TIMEOUT in the status word and the
+   kernel stops early: that pass's candidates are then incomplete (codes stay
+   valid atom ids, but are not the exact encode).  The kernel still waits for
+   every copy and MMA it issued, with the default limit, before it returns.
+   Host-only.  Errors: INVALID_ARG. */
+fadkv_status fadkv_debug_wait_limit(fadkv_dict dict, uint64_t limit_ns);
+
+/* Test hook: launches one thread that waits, with a limit of limit_ns
+   (1 .. 10^10), on a barrier nothing ever arrives on, so the wait runs out
+   and sets FADKV_DEV_TIMEOUT in dictionary 0's status word (read it with
+   fadkv_dict_stats).  Nothing else is touched.  Asynchronous on `stream`.
+   Errors: INVALID_ARG, CUDA. */
+fadkv_status fadkv_debug_wait_probe(fadkv_dict dict, uint64_t limit_ns, void* stream);
 
 /* ---------------------------------------------------------------------------
    The compressed KV store and decode attention over it.  Handle-free: both
@@ -360,6 +392,8 @@ fadkv_status fadkv_attend_workspace_bytes(const fadkv_attn_params* params, size_
                                   fadkv_encode_pl) */
 #define FADKV_K_ADAPT 3        /* fixed-size adaptation */
 #define FADKV_K_RECONSTRUCT 4  /* sparse reconstruction */
+#define FADKV_K_GRAM 5         /* the dictionaries' Gram matrices: the build at the first encode
+                                  (or fadkv_dict_refresh) and the update after each adaptation */
 
 /* Tracing.  The library always counts its kernel launches per class.  With
    profiling enabled it also brackets every launch with a pair of CUDA events

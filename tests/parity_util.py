@@ -76,50 +76,50 @@ def compare_encode(res: O.EncodeResult, idx, coef, relres, gpu_pool=None, p=None
     """res: oracle result for V vectors; idx/coef/relres: GPU arrays [V]...
     With gpu_pool/p/atoms/x given, vectors on a near tie at the Top-n cut are
     checked against the oracle's greedy run on the GPU's pool instead of
-    being skipped."""
+    being skipped.  Vectors off any near tie are compared all at once."""
     ex = exempt_mask(res)
-    bad = []
-    worst_c = 0.0
-    worst_r = 0.0
-    worst_e = 0.0
-    worst_a = 0.0
-    for v in range(len(ex)):
-        if ex[v]:
-            if gpu_pool is None or res.pick_gap[v].min() < PICK_GAP or res.idx[v][0] < 0:
-                continue
-            alt = check_cut_tie(p, atoms, x, res, gpu_pool, v)
-            if alt is None:
-                continue
-            one = O.EncodeResult(alt.idx, alt.coef, alt.relres, alt.pool, np.full(1, np.inf), alt.pick_gap, 0)
-            sub = compare_encode(one, idx[v:v + 1], coef[v:v + 1], relres[v:v + 1])
-            bad += [v] if sub.mismatched_idx else []
-            worst_c = max(worst_c, sub.worst_coef)
-            worst_r = max(worst_r, sub.worst_relres)
-            worst_e = max(worst_e, sub.worst_coef_elem)
-            worst_a = max(worst_a, sub.worst_coef_elem_any)
-            ex[v] = False
-            continue
-        if not np.array_equal(idx[v], res.idx[v]):
-            bad.append(v)
-            continue
-        if res.idx[v][0] < 0:           # non-finite input
-            assert np.isnan(relres[v])
-            continue
-        co = res.coef[v]
-        cn = np.linalg.norm(co)
-        dcv = np.abs(coef[v].astype(np.float64) - co)
-        dc = np.linalg.norm(dcv)
-        worst_c = max(worst_c, dc / cn if cn > 0 else dc)
-        big = np.abs(co) >= COEF_FLOOR * cn
-        if cn > 0 and big.any():
-            worst_e = max(worst_e, float(np.max(dcv[big] / np.abs(co[big]))))
+    idx = np.asarray(idx)
+    coef = np.asarray(coef).astype(np.float64)
+    relres = np.asarray(relres).astype(np.float64)
+    worst_c = worst_r = worst_e = worst_a = 0.0
+    # vectors on no near tie: ids exact, then the tolerances
+    ok = ~ex
+    same = np.all(idx == res.idx, axis=1)
+    bad = [int(v) for v in np.nonzero(ok & ~same)[0]]
+    nonfinite = ok & same & (res.idx[:, 0] < 0)
+    assert np.all(np.isnan(relres[nonfinite])), "a non-finite input must give relres = NaN"
+    chk = ok & same & (res.idx[:, 0] >= 0)
+    if chk.any():
+        co = res.coef[chk]
+        cn = np.linalg.norm(co, axis=1)
+        dcv = np.abs(coef[chk] - co)
+        dc = np.linalg.norm(dcv, axis=1)
+        worst_c = float(np.max(np.where(cn > 0, dc / np.where(cn > 0, cn, 1.0), dc)))
+        big = (np.abs(co) >= COEF_FLOOR * cn[:, None]) & (cn[:, None] > 0)
+        if big.any():
+            worst_e = float(np.max(dcv[big] / np.abs(co[big])))
         nz = co != 0
         if nz.any():
-            worst_a = max(worst_a, float(np.max(dcv[nz] / np.abs(co[nz]))))
-        ro = res.relres[v]
-        dr = abs(float(relres[v]) - ro)
-        worst_r = max(worst_r, dr / ro if ro > 0 else dr)
-    return EncodeReport(len(ex) - int(ex.sum()), int(ex.sum()), bad, worst_c, worst_r, worst_e, worst_a)
+            worst_a = float(np.max(dcv[nz] / np.abs(co[nz])))
+        ro = res.relres[chk]
+        dr = np.abs(relres[chk] - ro)
+        worst_r = float(np.max(np.where(ro > 0, dr / np.where(ro > 0, ro, 1.0), dr)))
+    # vectors on a near tie at the cut: judged on the GPU's pool
+    for v in np.nonzero(ex)[0]:
+        if gpu_pool is None or res.pick_gap[v].min() < PICK_GAP or res.idx[v][0] < 0:
+            continue
+        alt = check_cut_tie(p, atoms, x, res, gpu_pool, v)
+        if alt is None:
+            continue
+        one = O.EncodeResult(alt.idx, alt.coef, alt.relres, alt.pool, np.full(1, np.inf), alt.pick_gap, 0)
+        sub = compare_encode(one, idx[v:v + 1], coef[v:v + 1], relres[v:v + 1])
+        bad += [int(v)] if sub.mismatched_idx else []
+        worst_c = max(worst_c, sub.worst_coef)
+        worst_r = max(worst_r, sub.worst_relres)
+        worst_e = max(worst_e, sub.worst_coef_elem)
+        worst_a = max(worst_a, sub.worst_coef_elem_any)
+        ex[v] = False
+    return EncodeReport(len(ex) - int(ex.sum()), int(ex.sum()), sorted(bad), worst_c, worst_r, worst_e, worst_a)
 
 
 def assert_encode_ok(rep: EncodeReport, max_exempt_frac=MAX_EXEMPT_FRAC):

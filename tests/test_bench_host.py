@@ -17,8 +17,9 @@ def test_kernel_work_per_launch():
     assert (bound, unit) == ("hbm", "GB/s")
     assert work == 56 * 4096 * 128 * 2 + nv * 128 * 2        # dictionaries once + inputs
     bound, work, unit = bench.kernel_work(w, "greedy", V)
-    assert (bound, unit) == ("tensor", "TFLOP/s")
-    assert work == 2.0 * 7 * 256 * 128 * nv                  # (s-1) n d multiply-adds per vector
+    assert (bound, unit) == ("hbm", "GB/s")
+    # pool ids, scores, G_jj; 7 Gram rows at the 256 pool ids; x and 8 rows; codes
+    assert work == (256 * 12 + 7 * 256 * 4 + 9 * 128 * 2 + 8 * 8 + 4) * nv
     bound, work, unit = bench.kernel_work(w, "greedy", V, coder="pl")
     assert (bound, unit) == ("hbm", "GB/s")
     assert work == (9 * 128 * 2 + 8.0 * 8 + 4.0) * nv        # s rows + x in, codes out
@@ -35,11 +36,11 @@ def test_roofline_from_profiles():
     prof = {"screen": (10, 0.31), "topn": (20, 0.31), "greedy": (10, 2.27), "adapt": (10, 0.08)}
     timed = {"greedy": (20, 4.54)}
     roof, shares = bench.roofline(w, prof, timed, w.V, PEAKS, "measured", 152, 2070.0)
-    assert roof["kernel"] == "greedy" and roof["bound"] == "tensor" and roof["unit"] == "TFLOP/s"
-    flops = 2.0 * 7 * 256 * 128 * w.G * w.V
+    assert roof["kernel"] == "greedy" and roof["bound"] == "hbm" and roof["unit"] == "GB/s"
+    byts = (256 * 12 + 7 * 256 * 4 + 9 * 128 * 2 + 8 * 8 + 4) * w.G * w.V
     assert roof["launch_ms"] == pytest.approx(0.227)
-    assert roof["achieved"] == pytest.approx(flops / 0.227e-3 / 1e12, rel=1e-3)
-    assert roof["frac"] == pytest.approx(roof["achieved"] / 1900.0, abs=1e-4)     # rounded to 4 places
+    assert roof["achieved"] == pytest.approx(byts / 0.227e-3 / 1e9, rel=1e-3)
+    assert roof["frac"] == pytest.approx(roof["achieved"] / 6800.0, abs=1e-4)     # rounded to 4 places
     assert sum(v["share"] for v in shares.values()) == pytest.approx(1.0, abs=1e-3)
     assert shares["greedy"]["launches"] == 10
     # without a timed figure for the dominant kernel the profile's own is used
@@ -80,3 +81,18 @@ def test_step_roofline_bytes():
     assert r["algorithmic_bytes"] == algo
     assert 8500 < r["bytes_per_vector"] < 8800
     assert r["frac"] == pytest.approx(algo / 0.3e-3 / 1e9 / 6800.0, abs=1e-4)
+
+
+def test_screening_fractions():
+    """Two launches per step of 2 x 65 536 vectors (the 16K prefill): HBM
+    bytes = each launch's dictionaries + every input once; flops = 2 N d
+    per vector."""
+    w = S.WORKLOADS["prefill_3b_16k"]
+    prof = {"screen": (8, 2.0)}                  # 4 steps, 2 launches each, 0.25 ms per launch
+    r = bench.screening_fractions(w, prof, 4, PEAKS)
+    flops = 2.0 * 4096 * 128 * 4 * 2 * 131072
+    assert r["tensor"]["achieved_tflops"] == pytest.approx(flops / 2e-3 / 1e12, rel=1e-3)
+    assert r["tensor"]["frac"] == pytest.approx(flops / 2e-3 / 1e12 / 1900.0, abs=1e-4)
+    byts = 8 * 2 * 4096 * 128 * 2 + 4 * 2 * 131072 * 128 * 2
+    assert r["hbm"]["achieved_gbs"] == pytest.approx(byts / 2e-3 / 1e9, rel=1e-3)
+    assert bench.screening_fractions(w, {}, 4, PEAKS) is None

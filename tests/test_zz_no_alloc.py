@@ -36,15 +36,48 @@ def test_noalloc_rejects_oversized_scratch(lib):
     assert e.value.status == 1
 
 
+SCRATCH = 4 << 20      # the static scratch's size, as the header states
+
+
+def _round256(v):
+    return (v + 255) // 256 * 256
+
+
+def largest_v(G, N):
+    """The largest V whose scratch (256-rounded inactive list [G][N] and
+    flagged list [G][V], then [G][8] int64 counters) fits in the scratch."""
+    V = (SCRATCH - _round256(4 * G * N) - 64 * G) // (4 * G)
+    while V > 0 and _round256(4 * G * N) + _round256(4 * G * V) + 64 * G > SCRATCH:
+        V -= 1
+    return V
+
+
+def test_noalloc_limit_at_the_decode_shape(lib):
+    """56 dictionaries of 4096 atoms: the largest V that fits is accepted by
+    the size check and one more is refused, before any CUDA call."""
+    G, N = 56, 4096
+    V = largest_v(G, N)
+    assert V == 14612
+    p = F.params(G, N, 128, 256, 8, F.F16, 1)
+    fake = 1 << 20
+    with pytest.raises(F.FadkvError) as e:
+        F.adapt_noalloc(p, fake, fake, [0.5] * G, fake, V + 1, fake, fake, fake, fake, fake, stream=0)
+    assert e.value.status == 5
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["adapt_stress", "tiny"])
-def test_noalloc_matches_adapt_two_steps(lib, name):
+@pytest.mark.parametrize("name,over", [("adapt_stress", {}), ("tiny", {}), ("decode_3b", {"V": 14612})],
+                         ids=["adapt_stress", "tiny", "decode_3b_at_limit"])
+def test_noalloc_matches_adapt_two_steps(lib, name, over):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    w = S.WORKLOADS[name]
+    from dataclasses import replace
+    w = replace(S.WORKLOADS[name], **over)
     data = S.WorkloadData(w)
     V = w.V
+    if name == "decode_3b":
+        assert V == largest_v(w.G, w.N)      # the scratch filled to its limit
 
     def t(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
