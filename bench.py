@@ -54,6 +54,14 @@ def parse(argv=None):
     ap.add_argument("--no-extra", action="store_true",
                     help="measure only the headline workload (not " + ", ".join(EXTRA_WORKLOADS) + ")")
     ap.add_argument("--coder", choices=["gm", "pl"], default="gm")
+    ap.add_argument("--dicts", type=int, default=0,
+                    help="run only the first G dictionaries of the workload (profiling captures)")
+    ap.add_argument("--record-traffic", metavar="CSV", default=None,
+                    help="read an ncu --csv capture of dram__bytes_read.sum / dram__bytes_write.sum and record "
+                         "the bytes per launch of --traffic-kernel in profiles/traffic.json, then exit")
+    ap.add_argument("--traffic-kernel", default="greedy", help="kernel class of --record-traffic")
+    ap.add_argument("--traffic-scale", type=float, default=1.0,
+                    help="multiply the captured bytes per launch by this (a capture on fewer dictionaries)")
     ap.add_argument("--attend", type=int, default=0, metavar="T",
                     help="time decode attention over packed codes with T cached tokens instead")
     return ap.parse_args(argv)
@@ -230,6 +238,60 @@ def traffic_for(kernel: str, w, coder: str = "gm"):
     if ent.get("source_sha256_16") != src:
         return None
     return ent.get("dram_bytes_per_launch")
+
+
+# ncu's kernel names of each kernel class (demangled names contain these)
+KERNEL_SYMBOLS = {"screen": "screen_tc_kernel", "topn": "select_kernel", "greedy": "greedy_gram_kernel",
+                  "adapt": "adapt_kernel", "reconstruct": "reconstruct_kernel", "gram": "gram_kernel"}
+
+
+def traffic_from_ncu_csv(path, symbol):
+    """Mean DRAM bytes (read + write) per launch of the kernels whose name
+    contains `symbol`, from `ncu --metrics dram__bytes_read.sum,
+    dram__bytes_write.sum --csv` output (one row per launch and metric)."""
+    import csv
+    unit_scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+    per_launch = {}
+    with open(path, newline="") as f:
+        rows = [r for r in csv.reader(f)]
+    head = next(i for i, r in enumerate(rows) if "Metric Name" in r and "Kernel Name" in r)
+    cols = rows[head]
+    ki, mi, ui, vi, ii = (cols.index(c) for c in ("Kernel Name", "Metric Name", "Metric Unit", "Metric Value", "ID"))
+    for r in rows[head + 1:]:
+        if len(r) <= vi or symbol not in r[ki]:
+            continue
+        if r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        v = float(r[vi].replace(",", "")) * unit_scale.get(r[ui], 1.0)
+        per_launch[r[ii]] = per_launch.get(r[ii], 0.0) + v
+    if not per_launch:
+        raise ValueError(f"no launch of {symbol} with DRAM metrics in {path}")
+    return sum(per_launch.values()) / len(per_launch), len(per_launch)
+
+
+def record_traffic(args):
+    """Writes the DRAM bytes per launch of one kernel class, with the sha256
+    of its source file as it is now, into profiles/traffic.json."""
+    from dictionary_sparse_kv_gb300 import synthetic as S
+    w = S.WORKLOADS[args.workload]
+    kern = args.traffic_kernel
+    byts, n = traffic_from_ncu_csv(args.record_traffic, KERNEL_SYMBOLS[kern])
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    tab = {}
+    if os.path.exists(path):
+        with open(path) as f:
+            tab = json.load(f)
+    key = w.name + ("+pl" if args.coder == "pl" else "")
+    src = kernel_files(args.coder)[kern]
+    tab.setdefault(key, {})[kern] = {
+        "kernel": KERNEL_SYMBOLS[kern], "dram_bytes_per_launch": int(round(byts * args.traffic_scale)),
+        "launches_captured": n, "scale": args.traffic_scale, "source": src,
+        "source_sha256_16": kernel_sources().get(src), "from": os.path.basename(args.record_traffic)}
+    with open(path, "w") as f:
+        json.dump(tab, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps(tab[key][kern]))
+    return 0
 
 
 def dominant_kernel(prof):
@@ -491,6 +553,8 @@ def run_ours(args):
     F.lib()
 
     w = rank_workload(S.WORKLOADS[args.workload], rank)
+    if args.dicts > 0:
+        w = replace(w, G=min(args.dicts, w.G))
     data = S.WorkloadData(w)
     K, W = args.steps, max(3, args.warmup)
     G, V, d = w.G, w.V, w.d
@@ -601,7 +665,7 @@ def run_ours(args):
     scr = screening_fractions(w, prof_all, min(K, 10), peaks)
     if scr:
         line["screening"] = scr
-    if world == 1 and args.workload == WORKLOAD and not args.no_extra:
+    if world == 1 and args.workload == WORKLOAD and not args.no_extra and args.dicts == 0:
         D.close()
         del D, codes, xhat, flush, xs_dev, xin
         torch.cuda.empty_cache()
@@ -686,6 +750,8 @@ def run_attend(args):
 
 def main(argv=None):
     args = parse(argv)
+    if args.record_traffic:
+        return record_traffic(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.attend > 0:

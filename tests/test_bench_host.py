@@ -96,3 +96,25 @@ def test_screening_fractions():
     byts = 8 * 2 * 4096 * 128 * 2 + 4 * 2 * 131072 * 128 * 2
     assert r["hbm"]["achieved_gbs"] == pytest.approx(byts / 2e-3 / 1e9, rel=1e-3)
     assert bench.screening_fractions(w, {}, 4, PEAKS) is None
+
+
+def test_traffic_from_ncu_csv(tmp_path):
+    """Bytes per launch of one kernel from ncu's --csv rows (one row per
+    launch and metric, units as ncu prints them)."""
+    name = "void fadkv::(anonymous namespace)::greedy_gram_kernel<128, 1, 8, 8, true>(fadkv::Shape, fadkv::GramGreedyArgs)"
+    head = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",'
+            '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"')
+    rows = [("0", name, "dram__bytes_read.sum", "Mbyte", "300.50"),
+            ("0", name, "dram__bytes_write.sum", "Kbyte", "400"),
+            ("1", "select_kernel", "dram__bytes_read.sum", "Mbyte", "29.4"),
+            ("2", name, "dram__bytes_read.sum", "Gbyte", "0.3"),
+            ("2", name, "dram__bytes_write.sum", "byte", "1,000")]
+    lines = ["==PROF== Connected", head] + [
+        f'"{i}","1","python","h","{k}","1","7","(128, 1, 1)","(1792, 1, 1)","0","10.3","m","{m}","{u}","{v}"'
+        for i, k, m, u, v in rows]
+    p = tmp_path / "t.csv"
+    p.write_text("\n".join(lines) + "\n")
+    byts, n = bench.traffic_from_ncu_csv(str(p), "greedy_gram_kernel")
+    assert n == 2 and byts == pytest.approx(((300.5e6 + 400e3) + (0.3e9 + 1000)) / 2)
+    with pytest.raises(ValueError):
+        bench.traffic_from_ncu_csv(str(p), "no_such_kernel")
