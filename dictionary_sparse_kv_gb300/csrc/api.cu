@@ -289,8 +289,10 @@ float* gdiag_ptr(fadkv_dict h) { return (float*)(h->ws + h->L.gdiag); }
 // The Gram matrices of every dictionary, from the atoms as they stand.
 cudaError_t build_gram(fadkv_dict h, cudaStream_t st)
 {
-    const cudaError_t e = traced(h, FADKV_K_GRAM, st, [&] {
-        return launch_gram_build(h->sh, h->atoms, gram_ptr(h), gdiag_ptr(h), st);
+    cudaError_t e = ensure_device_info(h);
+    if (e != cudaSuccess) return e;
+    e = traced(h, FADKV_K_GRAM, st, [&] {
+        return launch_gram_build(h->sh, h->atoms, gram_ptr(h), gdiag_ptr(h), h->sms, st);
     });
     if (e == cudaSuccess) h->gram_ready = true;
     return e;
@@ -617,11 +619,13 @@ fadkv_status adapt_call(const char* name, fadkv_dict h, const void* x, int32_t V
     a.append = append;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = traced(h, FADKV_K_ADAPT, st, [&] { return launch_adapt(h->sh, a, h->delta, st); });
+    if (e == cudaSuccess) h->launches[FADKV_K_ADAPT] += adapt_launches(h->sh, V) - 1;
     // the rows and columns of the atoms just written (none, if the Gram
     // matrices are not built yet: the build reads the atoms as they stand)
     if (e == cudaSuccess && h->L.gram && h->gram_ready)
         e = traced(h, FADKV_K_GRAM, st, [&] {
-            return launch_gram_update(h->sh, h->atoms, a.inactive, a.nrep, h->p.N, gram_ptr(h), gdiag_ptr(h), st);
+            return launch_gram_update(h->sh, h->atoms, a.inactive, a.nrep, h->p.N, gram_ptr(h), gdiag_ptr(h), h->sms,
+                                      st);
         });
     if (e != cudaSuccess) {
         set_error(name, e);

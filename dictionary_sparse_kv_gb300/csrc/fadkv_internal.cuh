@@ -211,9 +211,10 @@ size_t greedy_smem_bytes(const Shape& sh);
 // adaptation just wrote).
 bool greedy_gram_supported(const Shape& sh);
 size_t gram_bytes(const Shape& sh);
-cudaError_t launch_gram_build(const Shape& sh, const void* atoms, float* gram, float* gdiag, cudaStream_t st);
+cudaError_t launch_gram_build(const Shape& sh, const void* atoms, float* gram, float* gdiag, int sms,
+                              cudaStream_t st);
 cudaError_t launch_gram_update(const Shape& sh, const void* atoms, const int32_t* rows, const int32_t* nrows,
-                               int row_stride, float* gram, float* gdiag, cudaStream_t st);
+                               int row_stride, float* gram, float* gdiag, int sms, cudaStream_t st);
 
 // Greedy selection + ridge refit over the Gram matrix, in the correlation
 // domain (binary16, n <= 512, s <= 16): the pool's ids and signed scores
@@ -318,6 +319,9 @@ struct AdaptArgs {
     int append;               // 0: reuse inactive atoms (usage == 0); 1: fill free slots (usage < 0)
 };
 cudaError_t launch_adapt(const Shape& sh, const AdaptArgs& a, const DeltaTable& delta, cudaStream_t st);
+// Kernels launch_adapt launches for V vectors per dictionary (the usage
+// increments run over the whole grid first when the batch is large).
+int adapt_launches(const Shape& sh, int V);
 
 // Test hook: one thread waits, with a limit of limit_ns, on an mbarrier that
 // nothing arrives on, so the wait runs out and sets FADKV_DEV_TIMEOUT in

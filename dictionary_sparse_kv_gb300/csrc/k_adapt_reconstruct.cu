@@ -51,9 +51,30 @@ __device__ int block_compact(int count, Pred pred, int32_t* out, int* ws)
     return base;
 }
 
+// Step 1 of the adaptation for large batches, over the whole grid: usage +=
+// 1 for every selected atom and "no replacement" for every vector, so that
+// the per-dictionary kernel below is left with the ordered compactions.
+__global__ void __launch_bounds__(256)
+usage_kernel(int G, int N, int s, int V, const int32_t* __restrict__ idx, int32_t* usage, int32_t* repl_id,
+             float* repl_coef)
+{
+    pdl_begin();
+    const long long total = (long long)G * V * s;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int j = idx[i];
+        const long long g = i / ((long long)V * s);
+        if (j >= 0 && j < N) atomicAdd(&usage[g * N + j], 1);
+        if (i % s == 0) {
+            repl_id[i / s] = -1;
+            repl_coef[i / s] = 0.f;
+        }
+    }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kAdaptThreads)
-adapt_kernel(Shape sh, AdaptArgs a, DeltaTable delta, int max_batch)
+adapt_kernel(Shape sh, AdaptArgs a, DeltaTable delta, int max_batch, int usage_done)
 {
     pdl_begin();
     __shared__ int ws[kAdaptWarps];
@@ -72,14 +93,17 @@ adapt_kernel(Shape sh, AdaptArgs a, DeltaTable delta, int max_batch)
     long long* cnt = a.counters + (size_t)g * kCntFields;
     const float dg = delta.v[g];
 
-    // 1. usage += 1 for every selected atom; default "no replacement"
-    for (int i = tid; i < V * s; i += kAdaptThreads) {
-        const int j = idx[i];
-        if (j >= 0 && j < N) atomicAdd(&usage[j], 1);
-    }
-    for (int v = tid; v < V; v += kAdaptThreads) {
-        repl_id[v] = -1;
-        repl_coef[v] = 0.f;
+    // 1. usage += 1 for every selected atom; default "no replacement" (done
+    //    by usage_kernel over the whole grid for large batches)
+    if (!usage_done) {
+        for (int i = tid; i < V * s; i += kAdaptThreads) {
+            const int j = idx[i];
+            if (j >= 0 && j < N) atomicAdd(&usage[j], 1);
+        }
+        for (int v = tid; v < V; v += kAdaptThreads) {
+            repl_id[v] = -1;
+            repl_coef[v] = 0.f;
+        }
     }
     __syncthreads();
 
@@ -228,11 +252,25 @@ reconstruct_kernel(const T* __restrict__ atoms, int G, int N, int s, int V, cons
     for (int q = 0; q < PL; ++q) out[q] = acc[q];
 }
 
+// Selected atoms per dictionary above which step 1 runs over the whole grid
+// (one CTA per dictionary would take its atomics one after another).
+constexpr long long kUsageSplit = 16384;
+
 template <typename T, int D>
 cudaError_t adapt_t(const Shape& sh, const AdaptArgs& a, const DeltaTable& delta, int max_batch,
                     cudaStream_t st)
 {
-    return launch_pdl(adapt_kernel<T, D>, dim3(sh.G), dim3(kAdaptThreads), 0, st, sh, a, delta, max_batch);
+    const bool split = (long long)a.V * sh.s > kUsageSplit;
+    if (split) {
+        const long long total = (long long)sh.G * a.V * sh.s;
+        const long long want = (total + 255) / 256;
+        const unsigned blocks = (unsigned)(want < 4096 ? want : 4096);
+        const cudaError_t e = launch_pdl(usage_kernel, dim3(blocks), dim3(256), 0, st, sh.G, sh.N, sh.s, a.V, a.idx,
+                                         a.usage, a.repl_id, a.repl_coef);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(adapt_kernel<T, D>, dim3(sh.G), dim3(kAdaptThreads), 0, st, sh, a, delta, max_batch,
+                      split ? 1 : 0);
 }
 
 template <typename T, int D>
@@ -246,6 +284,8 @@ cudaError_t reconstruct_t(const Shape& sh, const void* atoms, int V, const int32
 }
 
 }  // namespace
+
+int adapt_launches(const Shape& sh, int V) { return (long long)V * sh.s > kUsageSplit ? 2 : 1; }
 
 cudaError_t launch_adapt(const Shape& sh, const AdaptArgs& a, const DeltaTable& delta, cudaStream_t st)
 {

@@ -47,7 +47,6 @@ __device__ __forceinline__ float warp_sum(float v)
 // ---------------------------------------------------------------------------
 constexpr int kGT = 64;                 // rows and columns of a tile
 constexpr int kGThreads = 256;          // 16 x 16 threads, 4 x 4 entries each
-constexpr int kColTilesPerCta = 4;
 
 // Loads atoms ids[0..count) (ids null: first + i) of dictionary A into
 // S[t][i] as fp32 (element-major, so a thread's four rows are one float4).
@@ -73,67 +72,82 @@ __device__ __forceinline__ void load_tile(float (*S)[kGT], const __half* A, cons
     }
 }
 
-// gram[g][r][c] = <d_r, d_c> for the rows r of a list and every column c.
-// Build (rows == null): every atom is a row.  Update: the rows are the
-// nrows[g] ids at rows + g * row_stride, and every entry is also written
-// at [c][r] (both orders give the same bits).
+// gram[g][r][c] = <d_r, d_c> for the rows r of a list and every column c,
+// in 64 x 64 tiles handed out over the grid: tile t of dictionary g is row
+// tile t / ctiles (of its row list) and column tile t % ctiles.  Build
+// (rows == null): every atom is a row.  Update: the rows are the nrows[g]
+// ids at rows + g * row_stride, and every entry is also written at [c][r]
+// (both orders give the same bits); a dictionary with no rows has no tiles,
+// so an update after a step that replaced nothing costs one pass over the
+// counts.
 template <int D>
 __global__ void __launch_bounds__(kGThreads)
-gram_kernel(const __half* __restrict__ atoms, int N, const int32_t* __restrict__ rows,
+gram_kernel(const __half* __restrict__ atoms, int G, int N, const int32_t* __restrict__ rows,
             const int32_t* __restrict__ nrows, int row_stride, float* __restrict__ gram, float* __restrict__ gdiag)
 {
     pdl_begin();
     extern __shared__ __align__(16) float gsm[];
     float (*As)[kGT] = reinterpret_cast<float (*)[kGT]>(gsm);
     float (*Bs)[kGT] = reinterpret_cast<float (*)[kGT]>(gsm + D * kGT);
-    const int g = blockIdx.y;
     const bool update = rows != nullptr;
-    const int nr = update ? nrows[g] : N;
-    if (nr <= 0) return;
-    const int32_t* rl = update ? rows + (size_t)g * row_stride : nullptr;
-    const __half* A = atoms + (size_t)g * N * D;
-    float* Gg = gram + (size_t)g * N * N;
+    const int ctiles = (N + kGT - 1) / kGT;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    for (int ct = 0; ct < kColTilesPerCta; ++ct) {
-        const int c0 = (blockIdx.x * kColTilesPerCta + ct) * kGT;
-        if (c0 >= N) break;
-        const int ccount = min(kGT, N - c0);
+    // the tiles of dictionaries [0, g) come before those of g
+    long long total = 0;
+    for (int g = 0; g < G; ++g) {
+        const int nr = update ? nrows[g] : N;
+        total += (long long)((nr + kGT - 1) / kGT) * ctiles;
+    }
+    // tiles [gbase, gend) belong to dictionary g; t only grows, so g only
+    // advances, and t < total keeps it below G
+    int g = -1;
+    long long gbase = 0, gend = 0;
+    for (long long t = blockIdx.x; t < total; t += gridDim.x) {
+        while (t >= gend) {
+            ++g;
+            gbase = gend;
+            const int ng = update ? nrows[g] : N;
+            gend += (long long)((ng + kGT - 1) / kGT) * ctiles;
+        }
+        const int nr = update ? nrows[g] : N;
+        const long long lt = t - gbase;
+        const int r0 = (int)(lt / ctiles) * kGT, c0 = (int)(lt % ctiles) * kGT;
+        const int rcount = min(kGT, nr - r0), ccount = min(kGT, N - c0);
+        const int32_t* rl = update ? rows + (size_t)g * row_stride : nullptr;
+        const __half* A = atoms + (size_t)g * N * D;
+        float* Gg = gram + (size_t)g * N * N;
         __syncthreads();
         load_tile<D>(Bs, A, nullptr, c0, ccount);
-        for (int r0 = 0; r0 < nr; r0 += kGT) {
-            const int rcount = min(kGT, nr - r0);
-            __syncthreads();
-            load_tile<D>(As, A, rl ? rl + r0 : nullptr, r0, rcount);
-            __syncthreads();
-            float acc[4][4];
+        load_tile<D>(As, A, rl ? rl + r0 : nullptr, r0, rcount);
+        __syncthreads();
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < D; ++k) {
+            const float4 av = *reinterpret_cast<const float4*>(&As[k][ty * 4]);
+            const float4 bv = *reinterpret_cast<const float4*>(&Bs[k][tx * 4]);
+            const float ar[4] = {av.x, av.y, av.z, av.w}, br[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 8
-            for (int t = 0; t < D; ++t) {
-                const float4 av = *reinterpret_cast<const float4*>(&As[t][ty * 4]);
-                const float4 bv = *reinterpret_cast<const float4*>(&Bs[t][tx * 4]);
-                const float ar[4] = {av.x, av.y, av.z, av.w}, br[4] = {bv.x, bv.y, bv.z, bv.w};
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
+        }
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i) {
+            const int ri = ty * 4 + i;
+            if (ri >= rcount) continue;
+            const int r = rl ? rl[r0 + ri] : r0 + ri;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int ri = ty * 4 + i;
-                if (ri >= rcount) continue;
-                const int r = rl ? rl[r0 + ri] : r0 + ri;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int cj = tx * 4 + j;
-                    if (cj >= ccount) continue;
-                    const int c = c0 + cj;
-                    Gg[(size_t)r * N + c] = acc[i][j];
-                    if (update) Gg[(size_t)c * N + r] = acc[i][j];
-                    if (r == c) gdiag[(size_t)g * N + r] = acc[i][j];
-                }
+            for (int j = 0; j < 4; ++j) {
+                const int cj = tx * 4 + j;
+                if (cj >= ccount) continue;
+                const int c = c0 + cj;
+                Gg[(size_t)r * N + c] = acc[i][j];
+                if (update) Gg[(size_t)c * N + r] = acc[i][j];
+                if (r == c) gdiag[(size_t)g * N + r] = acc[i][j];
             }
         }
     }
@@ -428,16 +442,15 @@ cudaError_t launch_d(const Shape& sh, const GramGreedyArgs& a, cudaStream_t st)
 
 template <int D>
 cudaError_t launch_gram_t(const Shape& sh, const void* atoms, const int32_t* rows, const int32_t* nrows,
-                          int row_stride, float* gram, float* gdiag, cudaStream_t st)
+                          int row_stride, float* gram, float* gdiag, int sms, cudaStream_t st)
 {
     const size_t smem = 2 * (size_t)D * kGT * sizeof(float);
     auto k = gram_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int ctiles = (sh.N + kGT - 1) / kGT;
-    dim3 grid((unsigned)((ctiles + kColTilesPerCta - 1) / kColTilesPerCta), (unsigned)sh.G);
-    return launch_pdl(k, grid, dim3(kGThreads), smem, st, (const __half*)atoms, sh.N, rows, nrows, row_stride,
-                      gram, gdiag);
+    // three CTAs per SM fit (64 KB of shared memory each)
+    return launch_pdl(k, dim3((unsigned)(3 * sms)), dim3(kGThreads), smem, st, (const __half*)atoms, sh.G, sh.N, rows,
+                      nrows, row_stride, gram, gdiag);
 }
 
 }  // namespace
@@ -449,17 +462,17 @@ bool greedy_gram_supported(const Shape& sh)
 
 size_t gram_bytes(const Shape& sh) { return (size_t)sh.G * sh.N * sh.N * sizeof(float); }
 
-cudaError_t launch_gram_build(const Shape& sh, const void* atoms, float* gram, float* gdiag, cudaStream_t st)
+cudaError_t launch_gram_build(const Shape& sh, const void* atoms, float* gram, float* gdiag, int sms, cudaStream_t st)
 {
-    return sh.d == 128 ? launch_gram_t<128>(sh, atoms, nullptr, nullptr, 0, gram, gdiag, st)
-                       : launch_gram_t<64>(sh, atoms, nullptr, nullptr, 0, gram, gdiag, st);
+    return sh.d == 128 ? launch_gram_t<128>(sh, atoms, nullptr, nullptr, 0, gram, gdiag, sms, st)
+                       : launch_gram_t<64>(sh, atoms, nullptr, nullptr, 0, gram, gdiag, sms, st);
 }
 
 cudaError_t launch_gram_update(const Shape& sh, const void* atoms, const int32_t* rows, const int32_t* nrows,
-                               int row_stride, float* gram, float* gdiag, cudaStream_t st)
+                               int row_stride, float* gram, float* gdiag, int sms, cudaStream_t st)
 {
-    return sh.d == 128 ? launch_gram_t<128>(sh, atoms, rows, nrows, row_stride, gram, gdiag, st)
-                       : launch_gram_t<64>(sh, atoms, rows, nrows, row_stride, gram, gdiag, st);
+    return sh.d == 128 ? launch_gram_t<128>(sh, atoms, rows, nrows, row_stride, gram, gdiag, sms, st)
+                       : launch_gram_t<64>(sh, atoms, rows, nrows, row_stride, gram, gdiag, sms, st);
 }
 
 cudaError_t launch_greedy_gram(const Shape& sh, const GramGreedyArgs& a, cudaStream_t st)

@@ -109,6 +109,16 @@ def test_prefill_3b_16k_full():
     w = S.WORKLOADS["prefill_3b_16k"]                  # 2 dictionaries x 131072 vectors, in vector chunks
     data = S.WorkloadData(w)
     x = data.inputs(0)
-    _, atoms0, _, out = _run_step(w, x)
+    data, atoms0, usage0, out = _run_step(w, x)
     assert np.all(out["idx"] >= 0)
     assert _check_sample(w, atoms0, x, out, _pairs(w, w.V, 48, 51)) >= 44
+    # the adaptation of both dictionaries (1M usage increments each), replayed
+    # by the oracle on the GPU's codes
+    p = PU.oparams(w)
+    for g in range(w.G):
+        oat, ous = atoms0[g].copy(), usage0[g].copy()
+        r = O.adapt(p, oat, ous, x[g], out["idx"][g], out["coef"][g].astype(np.float64),
+                    out["relres"][g].astype(np.float64), data.deltas()[g])
+        assert np.array_equal(out["usage"][g], ous), g
+        assert np.array_equal(out["repl_id"][g], r.repl_id), g
+        assert out["stats"][g]["replaced"] == r.replaced and out["stats"][g]["overflow"] == r.overflow

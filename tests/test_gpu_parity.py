@@ -196,6 +196,7 @@ def _adapt_case(w, V, step=0):
     ("adapt_stress", dict(off_frac=0.8), 256),        # large residuals: many replacements
     ("decode_3b", dict(G=2, off_frac=1.2), 128),
     ("decode_3b", dict(G=2, inactive=5, off_frac=1.5), 128),   # inactive list runs out
+    ("adapt_stress", dict(off_frac=0.8), 4096),       # a batch whose usage increments run over the grid
 ])
 def test_adapt_matches_oracle(name, over, V):
     w = small(S.WORKLOADS[name], **over)
