@@ -56,6 +56,8 @@ def parse(argv=None):
     ap.add_argument("--coder", choices=["gm", "pl"], default="gm")
     ap.add_argument("--dicts", type=int, default=0,
                     help="run only the first G dictionaries of the workload (profiling captures)")
+    ap.add_argument("--vectors", type=int, default=0,
+                    help="vectors per dictionary per step instead of the workload's (batch-size sweeps)")
     ap.add_argument("--record-traffic", metavar="CSV", default=None,
                     help="read an ncu --csv capture of dram__bytes_read.sum / dram__bytes_write.sum and record "
                          "the bytes per launch of --traffic-kernel in profiles/traffic.json, then exit")
@@ -82,6 +84,28 @@ def workload_config(w, vectors_per_step, coder="gm"):
         "storage": "binary16 atoms and inputs",
         "l2": "flushed between timed steps (256 MiB write outside the step's events)",
     }
+
+
+L2_FETCH_BYTES = 32
+
+
+def set_l2_fetch_granularity(nbytes: int):
+    """Sets the current CUDA context's L2 fetch granularity hint (the
+    driver's CU_LIMIT_MAX_L2_FETCH_GRANULARITY, per context, gone with the
+    process).  The greedy's Gram gathers are scattered 4-byte reads: with
+    32-byte fetches an L2 miss brings one sector instead of two or four.
+    Returns the value the context reports afterwards (None if unknown)."""
+    import ctypes
+    try:
+        cu = ctypes.CDLL("libcuda.so.1")
+    except OSError:
+        return None
+    limit = 0x05                                   # CU_LIMIT_MAX_L2_FETCH_GRANULARITY
+    cu.cuCtxSetLimit(limit, ctypes.c_size_t(nbytes))
+    got = ctypes.c_size_t(0)
+    if cu.cuCtxGetLimit(ctypes.byref(got), limit) != 0:
+        return None
+    return int(got.value)
 
 
 def load_peaks():
@@ -168,9 +192,10 @@ def kernel_work(w, kernel: str, vectors: int, coder: str = "gm"):
     if kernel == "screen":
         return "hbm", float(G * N * d * esz + nv * d * esz), "GB/s"
     if kernel == "topn":
-        # candidate keys in (about 2n per vector, 8 B each) and the pool out
-        # (n ids; s for the PL coder)
-        return "hbm", (8.0 * 2 * n + 4.0 * (s if coder == "pl" else n)) * nv, "GB/s"
+        # the screening records in (per 128 atoms a header and four mask
+        # words, and about 1.3 n kept scores per vector) and the pool out
+        # (ids and scores: n, or s for the PL coder)
+        return "hbm", (4.0 * (5 * (N // 128) + 1.3 * n) + 8.0 * (s if coder == "pl" else n)) * nv, "GB/s"
     if kernel == "greedy" and coder == "pl":
         # the fit: the s rows and x in, ids, coefficients and relres out
         return "hbm", ((s + 1) * d * esz + 8.0 * s + 4.0) * nv, "GB/s"
@@ -546,6 +571,8 @@ def run_ours(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
+    torch.zeros(1, device=dev)                     # the context exists from here
+    l2_fetch = set_l2_fetch_granularity(L2_FETCH_BYTES)
     if rank == 0:
         B.build()
     if world > 1:
@@ -555,6 +582,8 @@ def run_ours(args):
     w = rank_workload(S.WORKLOADS[args.workload], rank)
     if args.dicts > 0:
         w = replace(w, G=min(args.dicts, w.G))
+    if args.vectors > 0:
+        w = replace(w, V=args.vectors)
     data = S.WorkloadData(w)
     K, W = args.steps, max(3, args.warmup)
     G, V, d = w.G, w.V, w.d
@@ -655,7 +684,7 @@ def run_ours(args):
         "metric": METRIC_PL if args.coder == "pl" else METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(dev_ms / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": workload_config(w, vectors_per_step, args.coder),
+        "config": dict(workload_config(w, vectors_per_step, args.coder), l2_fetch_granularity_bytes=l2_fetch),
         "e2e": {"value": round(e2e, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches, "roofline": roof, "kernels": shares, "clocks": clk, "cpu_baseline": cpu,
         "step_roofline": step_roofline(w, vectors_per_step, dev_ms / K, peaks),
@@ -665,7 +694,7 @@ def run_ours(args):
     scr = screening_fractions(w, prof_all, min(K, 10), peaks)
     if scr:
         line["screening"] = scr
-    if world == 1 and args.workload == WORKLOAD and not args.no_extra and args.dicts == 0:
+    if world == 1 and args.workload == WORKLOAD and not args.no_extra and args.dicts == 0 and args.vectors == 0:
         D.close()
         del D, codes, xhat, flush, xs_dev, xin
         torch.cuda.empty_cache()

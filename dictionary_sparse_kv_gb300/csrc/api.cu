@@ -89,14 +89,14 @@ Layout make_layout(const fadkv_params& p)
     return L;
 }
 
-// alpha with P(|Z| >= alpha) = min(1, 1.5n/N) for a standard normal Z, by
+// alpha with P(|Z| >= alpha) = min(1, 1.3n/N) for a standard normal Z, by
 // bisection on erfc: an atom uncorrelated with x has |<d, x>| ~ ||x||/sqrt(d)
-// |Z|, so tau = alpha ||x|| / sqrt(d) keeps about 1.5n candidates per vector
-// (the count sits several standard deviations above n; a list that ends
-// short is redone exactly).
+// |Z|, so tau = alpha ||x|| / sqrt(d) keeps about 1.3n candidates per vector
+// (the count sits four standard deviations above n at the decode shapes; a
+// list that ends short is redone exactly).
 float screen_alpha(int n, int N)
 {
-    double f = 1.5 * n / (double)N;
+    double f = 1.3 * n / (double)N;
     if (f >= 1.0) return 0.f;
     double lo = 0.0, hi = 40.0;
     for (int i = 0; i < 200; ++i) {

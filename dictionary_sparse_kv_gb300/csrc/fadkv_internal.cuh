@@ -120,26 +120,19 @@ cudaError_t launch_topn_radix(const Shape& sh, const float* scores, int Vc, unsi
 //
 // Output: per vector and 128-atom chunk c, one record of kRecBytes at
 // rec + ((g * Vc + v) * (N/128) + c) * kRecBytes, in 32-bit words:
-//   word 0      header: overflow << 31 | eb << 16 | k0 << 8 | count
-//   words 1..   count packed keys, those of atoms c*128 + [0, 64) first (k0
-//               of them), then those of c*128 + [64, 128)
-// A packed key holds r_j exactly: |r_j| relative to eb, the exponent field
-// of the vector's threshold tau (every kept |r| >= tau >= 2^(eb-127)), and
-// the sign of r_j:
-//   packed = bits(min(|r|, top)) - (eb << 23) + (sign << 25) + (col << 26),
-//   col = the atom's index within its 64-atom half, top = the float with bits
-//   (eb << 23) + 2^25 - 1 (|r| < 2^(eb-123): four binades above tau's, which
-//   holds |r| <= ||x|| for unit atoms whenever alpha > sqrt(d)/8).  A key at
-//   top may have been clipped, and a record with more than kRecKeys keys is
-//   flagged: the consumer redoes such a vector exactly.
+//   word 0      header: overflow << 31 | count
+//   words 1..4  masks: bit t of word 1 + k set when atom c*128 + 32k + t
+//               was kept
+//   words 5..   the count kept scores r_j (binary32, exact, with their
+//               sign), in ascending atom order
+// A record with more than kRecVals kept scores is flagged: the consumer
+// redoes such a vector exactly.
 constexpr int kRecWords = 32;
 constexpr int kRecBytes = kRecWords * 4;
-constexpr int kRecKeys = kRecWords - 1;
-constexpr uint32_t kRecValueMask = (1u << 25) - 1u;
-constexpr int kRecSignShift = 25;
-__host__ __device__ inline uint32_t rec_header(bool over, uint32_t eb, int k0, int count)
+constexpr int kRecVals = kRecWords - 5;
+__host__ __device__ inline uint32_t rec_header(bool over, int count)
 {
-    return (over ? 0x80000000u : 0u) | (eb << 16) | ((uint32_t)k0 << 8) | (uint32_t)count;
+    return (over ? 0x80000000u : 0u) | (uint32_t)count;
 }
 struct ScreenTCArgs {
     int G, N, V, v0, Vc;      // V: vectors per dictionary of the whole call
@@ -150,13 +143,16 @@ struct ScreenTCArgs {
     long long* counters;      // [G][kCntFields] (status word)
     unsigned long long wait_ns;   // limit of the pipeline's waits (0: the default; a test hook shortens it)
 };
-// Host-side state a handle keeps between launches: the encoded tensor map of
-// the dictionaries (by base address and row count) and whether the kernel's
-// shared-memory limit was raised.
+// Host-side state a handle keeps between launches: the encoded tensor maps of
+// the dictionaries and of the last inputs (by base address and row count)
+// and whether the kernel's shared-memory limit was raised.
 struct ScreenTCCache {
     alignas(64) unsigned char map_d[128];
+    alignas(64) unsigned char map_x[128];
     const void* d_base = nullptr;
     long long d_rows = -1;
+    const void* x_base = nullptr;
+    long long x_rows = -1;
     bool attr_done[2] = {false, false};
 };
 bool screen_tc_supported(const Shape& sh);

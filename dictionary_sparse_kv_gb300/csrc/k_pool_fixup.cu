@@ -5,9 +5,8 @@
 // the lower atom index (a convention of this library).
 //
 // The selection kernel marks a vector with pool[0] = -2 when its screening
-// records cannot give the pool exactly (a record overflowed, a key may have
-// been clipped at the top of its window, or the list holds fewer than n or
-// more than the selection's capacity).  This kernel recomputes all N scores
+// records cannot give the pool exactly (a record overflowed, or the list
+// holds fewer than n or more than the selection's capacity).  This kernel recomputes all N scores
 // of such a vector on the FP32 pipe, takes the exact Top-n keys and writes
 // the pool ids with their signed scores r_j.  It returns at once when the
 // pass flagged nothing (the selection records the pass number in slow_seq).

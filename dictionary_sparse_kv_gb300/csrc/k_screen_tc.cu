@@ -8,31 +8,36 @@
 // chunk fastest, split evenly over one persistent CTA per SM: CTA b takes the
 // contiguous units [b*T/B, (b+1)*T/B), so every SM streams the same number
 // of atom chunks whatever G and the batch are.  A run of units of one
-// (g, tile) is a segment; its vector tile is the MMA's A operand (two
-// buffers, so the next segment's tile loads under the current one).
+// (g, tile) is a segment; its vector tile is the MMA's A operand.
 //
-// S[v][j] = sum_t X[v][t] D[j][t] per unit: A = the vector tile (M = 128 TMEM
-// lanes), B = the atom chunk (N = 128 columns), both binary16 K-major with the
-// 128-byte swizzle written by TMA; fp32 accumulation in TMEM, two accumulator
-// buffers.  Scores never reach HBM.  The epilogue thread of vector v keeps
-// atom j if |S[v][j]| >= tau_v, tau_v = alpha * ||x_v|| / sqrt(d) with alpha
-// set on the host so that an atom uncorrelated with x_v passes with
-// probability ~1.5n/N.  Each kept score becomes a 32-bit packed key (|S|
-// exactly, relative to the exponent of tau_v, its sign and the atom's
-// column; see ScreenTCArgs) appended to the vector's record of the unit in shared
-// memory: one predicated 4-byte store per score.  After each unit the warp
-// copies its 32 records out with 16-byte loads and stores, eight lanes on a
-// record: the candidate output lands as whole sectors.  A row with more than kRecKeys kept scores in a unit makes
+// S[v][j] = sum_t X[v][t] D[j][t] per unit: A = the vector tile (M = 128
+// rows), B = the atom chunk (N = 128 columns), both binary16 K-major with the
+// 128-byte swizzle, both brought into shared memory by TMA (the vector tile
+// in two buffers, so the next segment's tile loads under the current one;
+// the atom chunks through kStages stages); fp32 accumulation in TMEM, three
+// accumulator buffers.  Scores never reach HBM.  The epilogue thread of
+// vector v keeps atom j if |S[v][j]| >= tau_v, tau_v = alpha * ||x_v|| /
+// sqrt(d), with alpha set on the host so that an atom uncorrelated with x_v
+// passes with probability ~1.3n/N.  A unit's kept scores go to the vector's
+// record (see ScreenTCArgs): four 32-bit masks of the columns kept and the
+// scores themselves, exact binary32, in column order -- per score one
+// compare, and for a kept one a shared-memory store, a pointer bump and a
+// mask bit.  After each unit the warp copies its 32 records out with 16-byte
+// loads and stores, eight lanes on a record: the candidate output lands as
+// whole sectors.  A row with more than kRecVals kept scores in a unit makes
 // the consumer redo the vector.
 //
-// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 issues MMAs (one
-// thread), warp 2 owns the TMEM allocation, warps 4..11 are the epilogue
-// (warp 4+e reads TMEM lanes 32(e%4).. and handles the units whose
-// accumulator buffer is e/4).  Every wait is bounded by a wall-clock limit;
-// on expiry the CTA sets FADKV_DEV_TIMEOUT in the status word, drains its own
-// copies and MMAs (the producer waits for every atom chunk it issued, the MMA
-// issuer for its last commit, each with the full limit), frees TMEM and
-// returns.
+// Warp roles (512 threads): warp 0 issues TMA loads (vector tiles and atom
+// chunks), warp 1 issues MMAs (one thread), warp 2 owns the TMEM allocation,
+// warp 3 asks for the chunks of the next units to be brought into L2,
+// warps 4..15 are the epilogue: three groups of four, group k takes the
+// units i with i mod 3 = k (accumulator buffer k), warp w reads TMEM lanes
+// 32 (w mod 4)...  Each group computes the thresholds of its rows at each
+// new segment from the vectors in global memory (coalesced: sixteen lanes
+// on a row).  Every wait is bounded by a wall-clock limit; on expiry the CTA
+// sets FADKV_DEV_TIMEOUT in the status word, drains its own copies and MMAs
+// (the producer waits for every copy it issued, the MMA issuer for its last
+// commit, each with the full limit), frees TMEM and returns.
 #include "tc_common.cuh"
 
 namespace fadkv {
@@ -41,10 +46,11 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kTileV = 128;        // vectors per tile (MMA M)
 constexpr int kChunk = 128;        // atoms per chunk (MMA N)
-constexpr int kStagesFor(int D) { return D == 64 ? 10 : 5; }  // atom chunk pipeline depth
-constexpr int kTmemCols = 512;     // two accumulator buffers (128 columns each), two vector tiles
-constexpr int kAcol = 2 * kChunk;  // first TMEM column of the vector tiles
-constexpr int kEpiWarps = 8;
+constexpr int kAcc = 3;            // accumulator buffers (and epilogue groups)
+constexpr int kTmemCols = 512;     // kAcc x 128 columns, allocated as a power of two
+constexpr int kEpiWarps = 4 * kAcc;
+constexpr int kStagesFor(int D) { return D == 64 ? 6 : 3; }  // atom chunk pipeline depth
+constexpr int kPrefetch = 10;      // units whose atom chunks are asked into L2 ahead of the loads
 // A row's record in shared memory sits in a slot of kRecWords + 4 words
 // (144 bytes): consecutive rows start 4 banks apart, so the rows' appends,
 // which advance at similar rates, rarely hit the same bank.
@@ -63,14 +69,16 @@ template <int D>
 struct SmemLayout {
     static constexpr int kStages = kStagesFor(D);
     static constexpr int KH = D / 64;                          // 64-element (128-byte) K halves
-    static constexpr int kTileBytes = KH * kChunk * 128;       // one 128-row operand tile
+    static constexpr int kTileBytes = KH * 128 * 128;          // one 128-row operand tile
     static constexpr int b_off = 0;                            // kStages atom chunks
-    static constexpr int s_off = b_off + kStages * kTileBytes; // the epilogue warps' records
+    static constexpr int a_off = b_off + kStages * kTileBytes; // two vector tiles
+    static constexpr int s_off = a_off + 2 * kTileBytes;       // the epilogue warps' records
     static constexpr int bar_off = s_off + kEpiWarps * kWarpStageWords * 4;
-    static constexpr int n_bars = 2 * kStages + 8;
+    static constexpr int n_bars = 2 * kStages + 2 * kAcc + 4;
     static constexpr int taddr_off = bar_off + n_bars * 8;
     static constexpr int total = taddr_off + 16;
     static constexpr int alloc = total + 1024;                 // slack for 1024-byte alignment
+    static_assert(alloc <= 227 * 1024, "shared memory");
 };
 
 // Walks a CTA's units in order without divisions: the unit's chunk c and its
@@ -103,20 +111,22 @@ struct UnitCursor {
 
 template <int D, bool kDump>
 __global__ void __launch_bounds__(kThreads, 1)
-screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
+screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, const __grid_constant__ CUtensorMap map_x,
+                 ScreenTCArgs a)
 {
     using L = SmemLayout<D>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sB = sbase + L::b_off;
+    const uint32_t sA = sbase + L::a_off;
     const uint32_t bar0 = sbase + L::bar_off;
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
     auto empty_bar = [&](int i) { return bar0 + 8u * (L::kStages + i); };
     auto tfull_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + i); };
-    auto tempty_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + 2 + i); };
-    auto afull_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + 4 + i); };
-    auto aempty_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + 6 + i); };
+    auto tempty_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + kAcc + i); };
+    auto afull_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + 2 * kAcc + i); };
+    auto aempty_bar = [&](int i) { return bar0 + 8u * (2 * L::kStages + 2 * kAcc + 2 + i); };
     uint32_t* taddr_slot = (uint32_t*)(smem + L::taddr_off);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -132,23 +142,27 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
 
     if (threadIdx.x == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_d)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
         for (int i = 0; i < L::kStages; ++i) {
             mbar_init(full_bar(i), 1);
             mbar_init(empty_bar(i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kAcc; ++i) {
             mbar_init(tfull_bar(i), 1);
             mbar_init(tempty_bar(i), 128);
-            mbar_init(afull_bar(i), 128);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(afull_bar(i), 1);
             mbar_init(aempty_bar(i), 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        reinterpret_cast<volatile int*>(smem + L::taddr_off + 4)[0] = 0;    // producer's progress
     }
     __syncthreads();
     pdl_begin();                      // the predecessor's writes (x, atoms) are visible from here
     // The TMEM allocation is published to the MMA and epilogue warps (and
     // warp 2) by a named barrier: the producer starts streaming at once.
-    constexpr int kTmemSyncThreads = 32 * (2 + kEpiWarps + 4);
+    constexpr int kTmemSyncThreads = 32 * (2 + kEpiWarps);
     uint32_t tbase = 0;
     if (warp != 0 && warp != 3) {
         if (warp == 2) {
@@ -164,13 +178,28 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
     constexpr uint32_t kTileBytes = (uint32_t)L::kTileBytes;
 
     if (warp == 0) {
-        // ---------------- TMA producer (atom chunks) ----------------
+        // ---------------- TMA producer: vector tiles and atom chunks ----------------
         if (lane == 0) {
-            int issued = 0;
+            int issued = 0, seg = -1, prev = -1;
+            int a_loads[2] = {0, 0};
             bool ok = true;
             UnitCursor uc;
             uc.init(u0, nch, tiles);
             for (int i = 0; i < nu && ok; ++i, uc.advance(1)) {
+                if (uc.pair != prev) {
+                    // a new segment: its vector tile into buffer seg & 1 once
+                    // the MMAs of segment seg - 2 are done with it
+                    prev = uc.pair;
+                    ++seg;
+                    const int ab = seg & 1;
+                    if (seg >= 2) ok = mbar_wait(aempty_bar(ab), (uint32_t)((seg >> 1) - 1) & 1u, status, wait_ns);
+                    if (!ok) break;
+                    mbar_expect_tx(afull_bar(ab), kTileBytes);
+                    const int xrow = uc.g * a.V + a.v0 + uc.tile * kTileV;
+                    for (int h = 0; h < L::KH; ++h)
+                        tma_load_2d(sA + ab * kTileBytes + h * 128 * 128, &map_x, h * 64, xrow, afull_bar(ab));
+                    ++a_loads[ab];
+                }
                 const int st = i % L::kStages;
                 ok = mbar_wait(empty_bar(st), ((uint32_t)(i / L::kStages) & 1u) ^ 1u, status, wait_ns);
                 if (!ok) break;
@@ -179,50 +208,42 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
                 for (int h = 0; h < L::KH; ++h)
                     tma_load_2d(sB + st * kTileBytes + h * kChunk * 128, &map_d, h * 64, arow, full_bar(st));
                 ++issued;
+                *reinterpret_cast<volatile int*>(smem + L::taddr_off + 4) = issued;   // for the prefetcher
             }
             // drain: every issued load must have landed before the CTA exits
             for (int i = max(0, issued - L::kStages); i < issued; ++i)
                 mbar_wait(full_bar(i % L::kStages), (uint32_t)(i / L::kStages) & 1u, status);
+            for (int ab = 0; ab < 2; ++ab)
+                if (a_loads[ab] > 0) mbar_wait(afull_bar(ab), (uint32_t)(a_loads[ab] - 1) & 1u, status);
         }
-    } else if (warp >= 4 + kEpiWarps) {
-        // ---------------- vector tiles into TMEM ----------------
-        // Warp 12+q writes rows 32q.. of each segment's tile (binary16 pairs,
-        // K-major: column k holds elements 2k, 2k+1) into its TMEM buffer,
-        // the MMAs' A operand; rows past the batch are zeros.
-        const int q = warp - 4 - kEpiWarps;
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        int prev = -1, seg = -1;
-        bool ok = true;
-        UnitCursor uc;
-        uc.init(u0, nch, tiles);
-        for (int i = 0; i < nu && ok; ++i, uc.advance(1)) {
-            if (uc.pair == prev) continue;
-            prev = uc.pair;
-            ++seg;
-            const int ab = seg & 1;
-            // the buffer's previous tile (segment seg-2) must be done with
-            if (seg >= 2) ok = mbar_wait(aempty_bar(ab), (uint32_t)((seg >> 1) - 1) & 1u, status, wait_ns);
-            if (!ok) break;
-            fence_after();
-            const int vloc = uc.tile * kTileV + q * 32 + lane;
-            const uint4* xr = reinterpret_cast<const uint4*>((const __half*)a.x +
-                                                             ((size_t)uc.g * a.V + a.v0 + (vloc < a.Vc ? vloc : 0)) * D);
-#pragma unroll
-            for (int h = 0; h < D / 32; ++h) {
-                uint32_t w[16];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint4 t = vloc < a.Vc ? __ldg(xr + h * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
-                    w[4 * k + 0] = t.x;
-                    w[4 * k + 1] = t.y;
-                    w[4 * k + 2] = t.z;
-                    w[4 * k + 3] = t.w;
+    } else if (warp == 3) {
+        // ---------------- L2 prefetch ----------------
+        // Asks for the atom chunks (and each segment's vector tile) of units
+        // up to kPrefetch ahead of the loads the producer has issued, so more
+        // HBM reads are in flight than the stages hold; it never waits on
+        // anything but the producer's progress counter.
+        if (lane == 0) {
+            volatile int* const prog = reinterpret_cast<volatile int*>(smem + L::taddr_off + 4);
+            UnitCursor pc;
+            pc.init(u0, nch, tiles);
+            int pprev = -1;
+            for (int pf = 0; pf < nu; ++pf, pc.advance(1)) {
+                if (pf >= kPrefetch) {
+                    // wait (bounded) until the producer has issued unit pf - kPrefetch
+                    const unsigned long long t0 = globaltimer();
+                    while (*prog < pf - kPrefetch + 1) {
+                        if (globaltimer() - t0 > wait_ns) break;
+                        __nanosleep(64);
+                    }
+                    if (*prog < pf - kPrefetch + 1) break;
                 }
-                tmem_st16(tbase + lane_off + (uint32_t)(kAcol + ab * (D / 2) + h * 16), w);
+                if (pc.pair != pprev) {
+                    pprev = pc.pair;
+                    const int xrow = pc.g * a.V + a.v0 + pc.tile * kTileV;
+                    for (int h = 0; h < L::KH; ++h) tma_prefetch_2d(&map_x, h * 64, xrow);
+                }
+                for (int h = 0; h < L::KH; ++h) tma_prefetch_2d(&map_d, h * 64, pc.g * a.N + pc.c * kChunk);
             }
-            tmem_st_wait();
-            fence_before();
-            mbar_arrive(afull_bar(ab));
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -240,83 +261,104 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
                     ok = mbar_wait(afull_bar(seg & 1), (uint32_t)(seg >> 1) & 1u, status, wait_ns);
                     if (!ok) break;
                 }
-                const int buf = i & 1;
-                ok = mbar_wait(tempty_bar(buf), ((uint32_t)(i >> 1) & 1u) ^ 1u, status, wait_ns);
+                const int buf = i % kAcc;
+                ok = mbar_wait(tempty_bar(buf), ((uint32_t)(i / kAcc) & 1u) ^ 1u, status, wait_ns);
                 if (!ok) break;
                 const int st = i % L::kStages;
                 ok = mbar_wait(full_bar(st), (uint32_t)(i / L::kStages) & 1u, status, wait_ns);
                 if (!ok) break;
                 fence_after();
                 const uint32_t dt = tbase + (uint32_t)(buf * kChunk);
-                const uint32_t at = tbase + (uint32_t)(kAcol + (seg & 1) * (D / 2));
+                const uint32_t aA = sA + (uint32_t)(seg & 1) * kTileBytes;
                 const uint32_t aB = sB + (uint32_t)st * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (uint32_t)((kk >> 2) * kChunk * 128 + (kk & 3) * 32);
-                    mma_ts(dt, at + (uint32_t)(kk * 8), sdesc(aB + koff), kIdesc, kk > 0 ? 1u : 0u);
+                    const uint32_t koff = (uint32_t)((kk >> 2) * 128 * 128 + (kk & 3) * 32);
+                    mma_ss(dt, sdesc(aA + koff), sdesc(aB + koff), kIdesc, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(empty_bar(st));
                 mma_commit(tfull_bar(buf));
                 ++issued;
             }
             // drain: the last accumulator must be complete before TMEM is freed
-            if (issued > 0) mbar_wait(tfull_bar((issued - 1) & 1), (uint32_t)((issued - 1) >> 1) & 1u, status);
+            if (issued > 0)
+                mbar_wait(tfull_bar((issued - 1) % kAcc), (uint32_t)((issued - 1) / kAcc) & 1u, status);
         }
     } else if (warp >= 4) {
         // ---------------- epilogue ----------------
         const int e = warp - 4;
-        const int q = e & 3;                                // TMEM lane group
-        const int hb = e >> 2;                              // accumulator buffer handled
+        const int grp = e >> 2;                             // accumulator buffer handled
+        const int q = warp & 3;                             // TMEM lane group
         const int r = q * 32 + lane;                        // TMEM lane = row of the vector tile
         uint32_t* const recs = reinterpret_cast<uint32_t*>(smem + L::s_off) + e * kWarpStageWords;
-        uint32_t* const myrec = recs + lane * kSlotWords;    // word 0 header, then the keys
+        uint32_t* const myrec = recs + lane * kSlotWords;   // header, four masks, then the scores
+        const uint32_t myrec_s = smem_u32(myrec);
         int cur = -1, g = 0, vloc = 0;
         bool valid = false, ok = true;
-        float tau = __int_as_float(0x7fffffff), top = 0.f;
-        uint32_t eb = 0, nbase = 0;
+        float tau = __int_as_float(0x7fffffff);
         UnitCursor uc;
-        uc.init(u0 + hb, nch, tiles);
-        for (int i = hb; i < nu && ok; i += 2, uc.advance(2)) {
+        uc.init(u0 + grp, nch, tiles);
+        for (int i = grp; i < nu && ok; i += kAcc, uc.advance(kAcc)) {
             const int c = uc.c;
             if (uc.pair != cur) {
                 cur = uc.pair;
                 g = uc.g;
                 vloc = uc.tile * kTileV + r;
                 valid = vloc < a.Vc;
-                // tau from ||x||^2 (rows past the batch: NaN, never passes)
+                // tau from ||x||^2 of this lane's row (rows past the batch:
+                // NaN, never passes).  The warp's 32 rows are read whole,
+                // sixteen lanes (eight for d = 64) on a row.
                 tau = __int_as_float(0x7fffffff);
-                if (valid && !kDump) {
-                    const uint4* xr =
-                        reinterpret_cast<const uint4*>((const __half*)a.x + ((size_t)g * a.V + a.v0 + vloc) * D);
-                    float sq = 0.f;
+                if constexpr (!kDump) {
+                    constexpr int LPR = D / 8;                  // lanes per row, 16 bytes each
+                    constexpr int RPI = 32 / LPR;               // rows per load
+                    const int wrow0 = uc.tile * kTileV + q * 32;
+                    const __half* xw = (const __half*)a.x + ((size_t)g * a.V + a.v0) * D;
+                    float mine = 0.f;
+                    constexpr int NIT = 32 / RPI;
+                    uint4 xw4[NIT];                             // every load in flight at once
 #pragma unroll
-                    for (int k = 0; k < D / 8; ++k) {
-                        const uint4 w = __ldg(xr + k);
-                        const __half2* hv = reinterpret_cast<const __half2*>(&w);
+                    for (int it = 0; it < NIT; ++it) {
+                        const int rr = it * RPI + lane / LPR;   // row within the warp's 32
+                        xw4[it] = (wrow0 + rr < a.Vc)
+                                      ? __ldg(reinterpret_cast<const uint4*>(xw + (size_t)(wrow0 + rr) * D) + (lane % LPR))
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                    }
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const float2 f = __half22float2(hv[t]);
-                            sq = fmaf(f.x, f.x, sq);
-                            sq = fmaf(f.y, f.y, sq);
+                    for (int it = 0; it < NIT; ++it) {
+                        float s = 0.f;
+                        {
+                            const __half2* hv = reinterpret_cast<const __half2*>(&xw4[it]);
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const float2 f = __half22float2(hv[t]);
+                                s = fmaf(f.x, f.x, s);
+                                s = fmaf(f.y, f.y, s);
+                            }
+                        }
+#pragma unroll
+                        for (int o = LPR / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                        // row it*RPI + k sits in lanes k*LPR .. ; lane `lane` owns row `lane`
+#pragma unroll
+                        for (int k = 0; k < RPI; ++k) {
+                            const float v = __shfl_sync(0xffffffffu, s, k * LPR);
+                            if (lane == it * RPI + k) mine = v;
                         }
                     }
-                    tau = a.alpha * sqrtf(sq * (1.0f / (float)D));
+                    if (valid) tau = a.alpha * sqrtf(mine * (1.0f / (float)D));
                 }
-                // the key window: tau's exponent field, the largest value kept exactly
-                const uint32_t base_bits = __float_as_uint(tau) & 0x7f800000u;
-                eb = base_bits >> 23;
-                nbase = 0u - base_bits;
-                top = __uint_as_float(base_bits + kRecValueMask);
             }
-            const int buf = i & 1;
-            ok = mbar_wait(tfull_bar(buf), (uint32_t)(i >> 1) & 1u, status, wait_ns);
+            const int buf = i % kAcc;
+            ok = mbar_wait(tfull_bar(buf), (uint32_t)(i / kAcc) & 1u, status, wait_ns);
             if (!ok) break;
             fence_after();
             const uint32_t tcol = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kChunk);
-            int k = 1;                                      // next word of this row's record
-            int k0 = 0;                                     // keys of atoms c*128 + [0, 64)
+            // shared-memory address of this row's next score slot
+            uint32_t wp = myrec_s + 5u * 4u;
+            const uint32_t wend = myrec_s + (uint32_t)kRecWords * 4u;
             bool ovf = false;
-            // one 32-column group: append the packed keys of the kept scores
+            uint32_t mask[4];
+            // one 32-column group: the kept scores and their mask bits
             auto stage = [&](const uint32_t (&v)[32], int qq) {
                 if constexpr (kDump) {
                     if (valid) {
@@ -324,23 +366,24 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
 #pragma unroll
                         for (int t = 0; t < 32; ++t) out[t] = __uint_as_float(v[t]);
                     }
+                    mask[qq] = 0u;
                     return;
                 } else {
+                    uint32_t m = 0u;
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
-                        const float f = fabsf(__uint_as_float(v[t]));
-                        if (f >= tau) {
-                            myrec[k] = __float_as_uint(fminf(f, top)) + nbase + ((v[t] >> 31) << kRecSignShift) +
-                                       ((uint32_t)((qq & 1) * 32 + t) << 26);
-                            ++k;
+                        if (fabsf(__uint_as_float(v[t])) >= tau) {
+                            asm volatile("st.shared.b32 [%0], %1;" ::"r"(wp), "r"(v[t]) : "memory");
+                            wp += 4u;
+                            m |= 1u << t;
                         }
                     }
+                    mask[qq] = m;
                     // a row may run past its record by at most 32 words (into
                     // the next row's slot, or the warp's guard after row 31):
                     // flagged below
-                    ovf |= k > kRecWords;
-                    k = min(k, kRecWords);
-                    if (qq == 1) k0 = k - 1;
+                    ovf |= wp > wend;
+                    wp = wp > wend ? wend : wp;
                 }
             };
             // TMEM loads double-buffered in registers: group g+1 is in flight
@@ -368,13 +411,17 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, ScreenTCArgs a)
             // flagged
             const int prev_ovf = __shfl_up_sync(0xffffffffu, ovf ? 1 : 0, 1);   // every lane takes part
             const bool over = ovf || (lane > 0 && prev_ovf != 0);
-            const int cnt = k - 1;
-            myrec[0] = rec_header(over, eb, k0, cnt);
+            const int cnt = (int)((wp - myrec_s) >> 2) - 5;
+            myrec[0] = rec_header(over, cnt);
+            myrec[1] = mask[0];
+            myrec[2] = mask[1];
+            myrec[3] = mask[2];
+            myrec[4] = mask[3];
             __syncwarp();
             // copy the 32 records out: eight lanes on a record (16 bytes each),
             // four records at a time, only the pieces holding words
             const int part = lane & 7, rsub = lane >> 3;
-            const int pieces = valid ? (cnt + 4) / 4 : 0;
+            const int pieces = valid ? (cnt + 5 + 3) / 4 : 0;
             unsigned char* const out = a.rec + ((size_t)g * a.Vc + (size_t)(vloc - lane)) * nch * kRecBytes +
                                        (size_t)c * kRecBytes;
 #pragma unroll
@@ -415,6 +462,17 @@ cudaError_t launch_t(const Shape& sh, const void* atoms, const ScreenTCArgs& a, 
         cache->d_base = atoms;
         cache->d_rows = drows;
     }
+    // the inputs [G][V][d]: one map over all G * V rows (a tile past a
+    // dictionary's batch reads the next rows, whose scores are never kept;
+    // past the last row TMA fills zeros)
+    CUtensorMap* mx = reinterpret_cast<CUtensorMap*>(cache->map_x);
+    const long long xrows = (long long)sh.G * a.V;
+    if (cache->x_base != a.x || cache->x_rows != xrows) {
+        cache->x_base = nullptr;
+        if (!make_tma_map_f16(mx, a.x, xrows, D, 128)) return cudaErrorInvalidValue;
+        cache->x_base = a.x;
+        cache->x_rows = xrows;
+    }
     auto k = screen_tc_kernel<D, kDump>;
     const int smem = SmemLayout<D>::alloc;
     if (!cache->attr_done[kDump ? 1 : 0]) {
@@ -422,7 +480,7 @@ cudaError_t launch_t(const Shape& sh, const void* atoms, const ScreenTCArgs& a, 
         if (e != cudaSuccess) return e;
         cache->attr_done[kDump ? 1 : 0] = true;
     }
-    return launch_pdl(k, dim3(screen_tc_grid(sh, a.Vc, sms)), dim3(kThreads), smem, st, *md, a);
+    return launch_pdl(k, dim3(screen_tc_grid(sh, a.Vc, sms)), dim3(kThreads), smem, st, *md, *mx, a);
 }
 
 }  // namespace

@@ -5,7 +5,8 @@
 // ties go to the lower atom index (a convention of this library).
 //
 // The candidates of a vector arrive as the screening kernel's records: per
-// 128-atom chunk a header and the kept atoms' packed keys.  A warp decodes
+// 128-atom chunk a header, the mask of the atoms kept and their scores.  A
+// warp decodes
 // them into 64-bit keys (bits(|r_j|) << 32) | ((0x7fffffff - j) << 1) |
 // sign(r_j) in its slice of shared memory (the larger key is the larger |r|,
 // then the lower atom index; the sign bit never decides, atoms being
@@ -44,6 +45,10 @@ select_kernel(SelectArgs a)
     pdl_begin();
     extern __shared__ unsigned long long kbuf_all[];   // [kWarpsPerCta][cap]
     __shared__ uint32_t hist_all[kWarpsPerCta][256];
+    // 32 records of a warp, one 36-word row each (16-byte aligned rows; a
+    // record's reads by its lane hit banks four apart from the next lane's)
+    constexpr int kStageRow = 36;
+    __shared__ __align__(16) uint32_t stage_all[kWarpsPerCta][32 * kStageRow];
     const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
     const long long gw = (long long)blockIdx.x * kWarpsPerCta + wl;   // (g, vc) flattened
     if (gw >= (long long)a.G * a.Vc) return;
@@ -57,23 +62,22 @@ select_kernel(SelectArgs a)
         pool_r[pos] = key_r(k);
     };
 
-    // the screening records of this vector, 32 at a time: the headers and
-    // every record's 16-byte pieces in one batch of loads (eight lanes on a
-    // record, four records per load); record c's keys go to the sum of the
-    // counts of the records before it, decoded:
-    //   |r| bits = (packed & (2^25 - 1)) + (eb << 23), sign = bit 25,
-    //   atom = 128 c + 64 h + (packed >> 26)
-    // with h = 1 for the keys past the record's first k0
+    // the screening records of this vector, 32 at a time: every record's
+    // 16-byte pieces in one batch of loads (eight lanes on a record, four
+    // records per load) into the warp's staging rows; then lane l decodes
+    // record l: its scores go to the sum of the counts of the records before
+    // it, the v-th score with the atom of the (v+1)-th set bit of the
+    // record's 128-bit mask (128 c + the bit's position)
     const int nch = a.N / 128;
     const unsigned char* rec = a.rec + (size_t)gw * nch * kRecBytes;
+    uint32_t* const stage = stage_all[wl];
     const int part = lane & 7, rsub = lane >> 3;
     constexpr int kIt = 8;                  // loads per lane: 32 records x 8 pieces over 32 lanes
     static_assert(kRecBytes / 16 == 8, "eight lanes cover a record");
-    bool bad = false, clipped = false;
+    bool bad = false;
     int gbase = 0;
     for (int cg = 0; cg < nch; cg += 32) {
         const int cc = cg + lane;
-        const uint32_t h = cc < nch ? __ldg(reinterpret_cast<const uint32_t*>(rec + (size_t)cc * kRecBytes)) : 0u;
         uint4 w[kIt];
 #pragma unroll
         for (int it = 0; it < kIt; ++it) {
@@ -81,6 +85,12 @@ select_kernel(SelectArgs a)
             w[it] = j < nch ? __ldg(reinterpret_cast<const uint4*>(rec + (size_t)j * kRecBytes) + part)
                             : make_uint4(0u, 0u, 0u, 0u);
         }
+#pragma unroll
+        for (int it = 0; it < kIt; ++it)
+            reinterpret_cast<uint4*>(stage + (it * 4 + rsub) * kStageRow)[part] = w[it];
+        __syncwarp();
+        const uint32_t* const mine = stage + lane * kStageRow;
+        const uint32_t h = cc < nch ? mine[0] : 0u;
         bad |= (h >> 31) != 0u;
         const int cnt = (int)(h & 0xffu);
         int incl = cnt;
@@ -90,30 +100,24 @@ select_kernel(SelectArgs a)
             if (lane >= o) incl += t;
         }
         const int off = gbase + incl - cnt;
+        if (cc < nch) {
+            int vi = 0;
 #pragma unroll
-        for (int it = 0; it < kIt; ++it) {
-            const int j = it * 4 + rsub;
-            const uint32_t hj = __shfl_sync(0xffffffffu, h, j);
-            const int oj = __shfl_sync(0xffffffffu, off, j);
-            const int cj = (int)(hj & 0xffu), k0 = (int)((hj >> 8) & 0xffu);
-            const uint32_t ebits = ((hj >> 16) & 0xffu) << 23;
-            const uint32_t jbase = (uint32_t)(cg + j) * 128u;
-            const uint32_t wv[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                // word 4*part+q of record j is key 4*part+q-1 (word 0 is the
-                // header); keys past the buffer are dropped, the vector then
-                // takes the slow path below
-                const int kk = 4 * part + q - 1;
-                if (kk >= 0 && kk < cj && oj + kk < a.cap) {
-                    const uint32_t val = wv[q] & kRecValueMask;
-                    clipped |= val == kRecValueMask;
-                    const uint32_t atom = jbase + (kk >= k0 ? 64u : 0u) + (wv[q] >> 26);
-                    keys[oj + kk] = sel_key(val + ebits, atom, (wv[q] >> kRecSignShift) & 1u);
+            for (int qq = 0; qq < 4; ++qq) {
+                uint32_t m = mine[1 + qq];
+                while (m != 0u && vi < cnt) {
+                    const uint32_t t = (uint32_t)(__ffs(m) - 1);
+                    m &= m - 1u;
+                    if (off + vi < a.cap) {
+                        const uint32_t val = mine[5 + vi];
+                        keys[off + vi] = sel_key(val & 0x7fffffffu, (uint32_t)cc * 128u + 32u * qq + t, val >> 31);
+                    }
+                    ++vi;
                 }
             }
         }
         gbase = __shfl_sync(0xffffffffu, off + cnt, 31);
+        __syncwarp();
     }
     const int K = gbase;
     auto slow = [&]() {
@@ -122,9 +126,8 @@ select_kernel(SelectArgs a)
             *a.slow_seq = a.seq;                       // every writer stores the same value
         }
     };
-    // an overflowed record, a key that may have been clipped at the top of its
-    // window, too few or too many keys: the slow path
-    if (__any_sync(0xffffffffu, bad || clipped) || K < n || K > a.cap) {
+    // an overflowed record, too few or too many keys: the slow path
+    if (__any_sync(0xffffffffu, bad) || K < n || K > a.cap) {
         slow();
         return;
     }

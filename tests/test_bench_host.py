@@ -25,7 +25,7 @@ def test_kernel_work_per_launch():
     assert work == (9 * 128 * 2 + 8.0 * 8 + 4.0) * nv        # s rows + x in, codes out
     _, topn_gm, _ = bench.kernel_work(w, "topn", V)
     _, topn_pl, _ = bench.kernel_work(w, "topn", V, coder="pl")
-    assert topn_gm - topn_pl == 4.0 * (256 - 8) * nv         # the pool is s ids for PL
+    assert topn_gm - topn_pl == pytest.approx(8.0 * (256 - 8) * nv)   # the pool is s ids and scores for PL
     with pytest.raises(KeyError):
         bench.kernel_work(w, "nothing", V)
 

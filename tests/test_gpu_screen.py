@@ -148,13 +148,13 @@ def test_more_candidates_than_the_selection_holds():
     PU.assert_encode_ok(PU.compare_encode(res, idx, coef, rel, pool, p, A, x[0]))
 
 
-def test_score_beyond_the_key_window():
+def test_scores_far_above_the_threshold_are_kept_exactly():
     """A dictionary with one atom 300 times longer than the others: the
-    vector along it scores far more than four binades above its threshold,
-    so its packed key is clipped and the selection hands the vector to the
-    exact slow path; an ordinary vector beside it (orthogonal to the long
-    atom, which would otherwise lift its score out of the window too) is
-    not.  Pools and codes match the oracle."""
+    vector along it scores hundreds of times its threshold, and the vector
+    beside it (a sparse mixture) scores well above it on the long atom too.
+    The screening records hold every kept score as an exact binary32 value,
+    so neither vector needs the slow path, and pools and codes match the
+    oracle."""
     d, N, n, s = 128, 4096, 256, 8
     g = np.random.default_rng(14)
     A = g.standard_normal((N, d))
@@ -163,17 +163,16 @@ def test_score_beyond_the_key_window():
     A = A.astype(np.float16)
     x = np.empty((1, 2, d), np.float16)
     x[0, 0] = (A[777].astype(np.float64) / 300.0 + 0.05 * g.standard_normal(d) / np.sqrt(d)).astype(np.float16)
-    x1 = S.make_sparse_inputs(A[:700], 1, s, 8)[0].astype(np.float64)
-    u = A[777].astype(np.float64) / np.linalg.norm(A[777].astype(np.float64))
-    x[0, 1] = (x1 - (x1 @ u) * u).astype(np.float16)
+    x[0, 1] = S.make_sparse_inputs(A[:700], 1, s, 8)[0]
     D = _dict(A[None], np.ones((1, N), np.int32), [0.5], n, s, 2)
     pool = D.pool(_t(x))[0].cpu().numpy()[0]
     c = D.new_codes(2)
     D.encode(_t(x), c)
     torch.cuda.synchronize()
-    assert D.stats()[0]["topn_slow_path"] == 2             # vector 0 in pool() and in encode()
+    assert D.stats()[0]["topn_slow_path"] == 0
     p = O.Params(N, d, n, s)
     res = O.encode(p, A, x[0])
+    assert 777 in res.pool[0] and 777 in res.pool[1]
     ok = ~PU.exempt_mask(res)
     for v in range(2):
         if ok[v]:
