@@ -690,6 +690,7 @@ def run_ours(args):
         "step_roofline": step_roofline(w, vectors_per_step, dev_ms / K, peaks),
         "wall_s_timed": round(wall, 4),
         "adapt": {"replaced": sum(s["replaced"] for s in stats), "overflow": sum(s["overflow"] for s in stats)},
+        "topn_slow_path_vectors": sum(s["topn_slow_path"] for s in stats),
     }
     scr = screening_fractions(w, prof_all, min(K, 10), peaks)
     if scr:

@@ -263,6 +263,11 @@ cudaError_t run_screen(fadkv_dict h, const void* x, int32_t V, int v0, int Vc, f
         sa.N = h->p.N;
         sa.n = n_sel;
         sa.cap = select_cap(h->p.n);
+        sa.d = h->p.d;
+        sa.V = V;
+        sa.v0 = v0;
+        sa.x = (const __half*)x;
+        sa.atoms = (const __half*)h->atoms;
         sa.rec = h->ws + h->L.cand;
         sa.pool = (int32_t*)(h->ws + h->L.pool);
         sa.pool_r = (float*)(h->ws + h->L.pool_r);

@@ -161,11 +161,16 @@ cudaError_t launch_screen_tc(const Shape& sh, const void* atoms, const ScreenTCA
                              cudaStream_t st);
 
 // Exact Top-n pool from the screening records, one warp per vector; pool
-// [G][Vc][n] atom ids and pool_r [G][Vc][n] their scores r_j (signed),
-// pool[0] = -2 where the exact slow path must redo the vector (a record
-// overflowed or was clipped, fewer than n candidates, or more than cap).
+// [G][Vc][n] atom ids and pool_r [G][Vc][n] their scores r_j (signed).  A
+// record that overflowed still lists every kept atom in its masks: the warp
+// recomputes those scores on the FP32 pipe.  pool[0] = -2 where the exact
+// slow path must redo the vector (fewer than n candidates, or more than
+// cap).
 struct SelectArgs {
     int G, Vc, N, n, cap;     // cap: the most candidates taken (else the slow path)
+    int d, V, v0;             // head dimension; the call's vectors per dictionary and this pass's first
+    const __half* x;          // [G][V][d] (for records whose scores must be recomputed)
+    const __half* atoms;      // [G][N][d]
     const unsigned char* rec; // [G][Vc][N/128] screening records
     int32_t* pool;            // [G][Vc][n]
     float* pool_r;            // [G][Vc][n]

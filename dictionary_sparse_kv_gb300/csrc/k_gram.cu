@@ -157,16 +157,17 @@ gram_kernel(const __half* __restrict__ atoms, int G, int N, const int32_t* __res
 // Greedy selection + ridge refit over the Gram matrix
 // ---------------------------------------------------------------------------
 // WPV warps per vector; each lane keeps SP pool slots (slot i = sp * 32 WPV
-// + 32 w + lane of warp w): the atom id, the running correlation <d_j, e>,
-// |l_j|^2, G_jj and l_j itself (SMAX - 1 entries: the last pick needs no
-// update).  A CTA of four warps serves 4 / WPV vectors, in the order of
+// + 32 w + lane of warp w): the atom id, the running correlation <d_j, e>
+// and l_j itself (SMAX - 1 entries: the last pick needs no update); G_jj of
+// the slots sits in shared memory and |l_j|^2 is summed by the lane that
+// publishes a pick, in the order of l_j's entries.  A CTA of four warps serves 4 / WPV vectors, in the order of
 // (dictionary, vector), so consecutive CTAs read the same dictionary's Gram
 // matrix.  FIXED: s == SMAX, known at compile time, so the pick loop unrolls
 // and every index into a slot's l is a constant.
 constexpr int kGreedyWarps = 4;
 
 template <int D, int WPV, int SP, int SMAX, bool FIXED>
-__global__ void __launch_bounds__(kGreedyWarps * 32)
+__global__ void __launch_bounds__(kGreedyWarps * 32, 4)
 greedy_gram_kernel(Shape sh, GramGreedyArgs a)
 {
     pdl_begin();
@@ -177,6 +178,7 @@ greedy_gram_kernel(Shape sh, GramGreedyArgs a)
     constexpr int EPL = D / 32;
     static_assert(SMAX % 4 == 0, "published rows are read as float4");
     __shared__ __align__(16) float publ[VPC][2][WPV][PL];
+    __shared__ float gjj_s[VPC][GS * SP];           // G_jj of every pool slot (read by the pick's lane)
     __shared__ unsigned long long kred[VPC][2][WPV];
     __shared__ float lrow[VPC][SMAX][SMAX];
     __shared__ float zrec[VPC][SMAX], irec[VPC][SMAX];
@@ -239,7 +241,7 @@ greedy_gram_kernel(Shape sh, GramGreedyArgs a)
     // ---- the pool: ids, scores r_j, G_jj ----
     const size_t pb = ((size_t)g * a.Vc + vc) * n;
     int id[SP];
-    float corr[SP], ll[SP], gjj[SP], l[SP][LW];
+    float corr[SP], l[SP][LW];
     uint32_t live = 0u;
 #pragma unroll
     for (int sp = 0; sp < SP; ++sp) {
@@ -250,8 +252,7 @@ greedy_gram_kernel(Shape sh, GramGreedyArgs a)
     }
 #pragma unroll
     for (int sp = 0; sp < SP; ++sp) {
-        gjj[sp] = id[sp] >= 0 ? __ldg(a.gdiag + (size_t)g * N + id[sp]) : 0.f;
-        ll[sp] = 0.f;
+        gjj_s[grp][sp * GS + w * 32 + lane] = id[sp] >= 0 ? __ldg(a.gdiag + (size_t)g * N + id[sp]) : 0.f;
 #pragma unroll
         for (int i = 0; i < LW; ++i) l[sp][i] = 0.f;
     }
@@ -278,12 +279,11 @@ greedy_gram_kernel(Shape sh, GramGreedyArgs a)
         const uint32_t amin = __reduce_min_sync(0xffffffffu, (bk == m) ? bid : 0xffffffffu);
         float* pw = publ[grp][par][w];
         if (m != 0u && bk == m && bid == amin) {
-            auto pick = [&](const float (&arr)[SP]) {
-                float r = arr[0];
+            // the winning slot's l (and |l|^2, summed in the order its
+            // entries were made), correlation, G_jj and atom
+            float llw = 0.f, cw = corr[0];
 #pragma unroll
-                for (int sp = 1; sp < SP; ++sp) r = (bsp == sp) ? arr[sp] : r;
-                return r;
-            };
+            for (int sp = 1; sp < SP; ++sp) cw = (bsp == sp) ? corr[sp] : cw;
 #pragma unroll
             for (int i = 0; i < LW; ++i) {
                 if (i < k) {
@@ -291,11 +291,12 @@ greedy_gram_kernel(Shape sh, GramGreedyArgs a)
 #pragma unroll
                     for (int sp = 1; sp < SP; ++sp) r = (bsp == sp) ? l[sp][i] : r;
                     pw[i] = r;
+                    llw = fmaf(r, r, llw);
                 }
             }
-            pw[SMAX] = pick(corr);
-            pw[SMAX + 1] = pick(ll);
-            pw[SMAX + 2] = pick(gjj);
+            pw[SMAX] = cw;
+            pw[SMAX + 1] = llw;
+            pw[SMAX + 2] = gjj_s[grp][bsp * GS + w * 32 + lane];
             pw[SMAX + 3] = __int_as_float((int)bid);
         }
         if (WPV > 1 && lane == 0)
@@ -360,7 +361,6 @@ greedy_gram_kernel(Shape sh, GramGreedyArgs a)
 #pragma unroll
             for (int i = 0; i < LW; ++i)
                 if (i == k) l[sp][i] = t;
-            ll[sp] = fmaf(t, t, ll[sp]);
             corr[sp] = fmaf(-zk, t, corr[sp]);
         }
     }
@@ -448,9 +448,11 @@ cudaError_t launch_gram_t(const Shape& sh, const void* atoms, const int32_t* row
     auto k = gram_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    // three CTAs per SM fit (64 KB of shared memory each)
-    return launch_pdl(k, dim3((unsigned)(3 * sms)), dim3(kGThreads), smem, st, (const __half*)atoms, sh.G, sh.N, rows,
-                      nrows, row_stride, gram, gdiag);
+    // the build: three CTAs per SM (64 KB of shared memory each); an update
+    // (usually a few tiles, often none): one per SM
+    const unsigned grid = (unsigned)(rows ? sms : 3 * sms);
+    return launch_pdl(k, dim3(grid), dim3(kGThreads), smem, st, (const __half*)atoms, sh.G, sh.N, rows, nrows,
+                      row_stride, gram, gdiag);
 }
 
 }  // namespace

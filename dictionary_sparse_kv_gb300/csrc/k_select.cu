@@ -74,7 +74,6 @@ select_kernel(SelectArgs a)
     const int part = lane & 7, rsub = lane >> 3;
     constexpr int kIt = 8;                  // loads per lane: 32 records x 8 pieces over 32 lanes
     static_assert(kRecBytes / 16 == 8, "eight lanes cover a record");
-    bool bad = false;
     int gbase = 0;
     for (int cg = 0; cg < nch; cg += 32) {
         const int cc = cg + lane;
@@ -90,9 +89,12 @@ select_kernel(SelectArgs a)
             reinterpret_cast<uint4*>(stage + (it * 4 + rsub) * kStageRow)[part] = w[it];
         __syncwarp();
         const uint32_t* const mine = stage + lane * kStageRow;
-        const uint32_t h = cc < nch ? mine[0] : 0u;
-        bad |= (h >> 31) != 0u;
-        const int cnt = (int)(h & 0xffu);
+        const bool live = cc < nch;
+        const uint32_t h = live ? mine[0] : 0u;
+        const uint32_t mk[4] = {live ? mine[1] : 0u, live ? mine[2] : 0u, live ? mine[3] : 0u, live ? mine[4] : 0u};
+        // every kept atom is in the masks, also past the record's room
+        const int cnt = __popc(mk[0]) + __popc(mk[1]) + __popc(mk[2]) + __popc(mk[3]);
+        const bool over = (h >> 31) != 0u;
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -100,11 +102,11 @@ select_kernel(SelectArgs a)
             if (lane >= o) incl += t;
         }
         const int off = gbase + incl - cnt;
-        if (cc < nch) {
+        if (live && !over) {
             int vi = 0;
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
-                uint32_t m = mine[1 + qq];
+                uint32_t m = mk[qq];
                 while (m != 0u && vi < cnt) {
                     const uint32_t t = (uint32_t)(__ffs(m) - 1);
                     m &= m - 1u;
@@ -114,6 +116,54 @@ select_kernel(SelectArgs a)
                     }
                     ++vi;
                 }
+            }
+        }
+        // a record that overflowed (or that a neighbour's overflow wrote
+        // into) has its masks but not all its scores: the warp recomputes
+        // the scores of its kept atoms on the FP32 pipe, lane l the l-th
+        // kept atom of each 32-atom group
+        unsigned ob = __ballot_sync(0xffffffffu, live && over);
+        while (ob != 0u) {
+            const int j = __ffs(ob) - 1;
+            ob &= ob - 1u;
+            const int offj = __shfl_sync(0xffffffffu, off, j);
+            const int cj = cg + j;
+            const int g = (int)(gw / a.Vc), vc = (int)(gw - (long long)g * a.Vc);
+            const __half* xr = a.x + ((size_t)g * a.V + a.v0 + vc) * a.d;
+            int base = 0;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const uint32_t mq = __shfl_sync(0xffffffffu, mk[qq], j);
+                const int pq = __popc(mq);
+                if (lane < pq) {
+                    uint32_t mm = mq;
+                    for (int r = 0; r < lane; ++r) mm &= mm - 1u;
+                    const uint32_t atom = (uint32_t)cj * 128u + 32u * qq + (uint32_t)(__ffs(mm) - 1);
+                    const __half* ar = a.atoms + ((size_t)g * a.N + atom) * a.d;
+                    // every 16-byte piece of both rows in flight at once (d <= 128)
+                    uint4 xa[16], aa[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const bool in = c < a.d / 8;
+                        xa[c] = in ? __ldg(reinterpret_cast<const uint4*>(xr) + c) : make_uint4(0u, 0u, 0u, 0u);
+                        aa[c] = in ? __ldg(reinterpret_cast<const uint4*>(ar) + c) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    float acc = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const __half2* xh = reinterpret_cast<const __half2*>(&xa[c]);
+                        const __half2* ah = reinterpret_cast<const __half2*>(&aa[c]);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float2 xf = __half22float2(xh[u]), af = __half22float2(ah[u]);
+                            acc = fmaf(xf.x, af.x, acc);
+                            acc = fmaf(xf.y, af.y, acc);
+                        }
+                    }
+                    const uint32_t bits = __float_as_uint(acc);
+                    if (offj + base + lane < a.cap) keys[offj + base + lane] = sel_key(bits & 0x7fffffffu, atom, bits >> 31);
+                }
+                base += pq;
             }
         }
         gbase = __shfl_sync(0xffffffffu, off + cnt, 31);
@@ -126,8 +176,8 @@ select_kernel(SelectArgs a)
             *a.slow_seq = a.seq;                       // every writer stores the same value
         }
     };
-    // an overflowed record, too few or too many keys: the slow path
-    if (__any_sync(0xffffffffu, bad) || K < n || K > a.cap) {
+    // too few or too many keys: the slow path
+    if (K < n || K > a.cap) {
         slow();
         return;
     }

@@ -116,6 +116,42 @@ def test_slow_path_short_and_overflowing_lists():
         assert abs(rel[v] - res.relres[v]) <= PU.RELRES_TOL * res.relres[v] + 1e-7
 
 
+def test_overflowing_record_scores_recomputed():
+    """Forty atoms of the first 128-atom chunk are near-copies of x's
+    direction, so x keeps more scores in that chunk than a record holds
+    (27): the record keeps its masks, and the selection recomputes the kept
+    atoms' scores on the FP32 pipe instead of redoing the whole vector.  The
+    next vector of the tile (whose record the overflow ran into) takes the
+    same path.  Neither vector needs the slow path, and pools and codes
+    match the oracle."""
+    d, N, n, s = 128, 4096, 256, 8
+    g = np.random.default_rng(21)
+    A = g.standard_normal((N, d))
+    u = g.standard_normal(d)
+    u /= np.linalg.norm(u)
+    A[:40] = u + 0.5 * g.standard_normal((40, d)) / np.sqrt(d)
+    A = (A / np.linalg.norm(A, axis=1, keepdims=True)).astype(np.float16)
+    x = np.empty((1, 3, d), np.float16)
+    x[0, 0] = (3.0 * u + 0.3 * g.standard_normal(d) / np.sqrt(d)).astype(np.float16)
+    x[0, 1] = S.make_sparse_inputs(A[100:], 1, s, 5)[0]
+    x[0, 2] = S.make_sparse_inputs(A[100:], 1, s, 6)[0]
+    D = _dict(A[None], np.ones((1, N), np.int32), [0.5], n, s, 3)
+    pool = D.pool(_t(x))[0].cpu().numpy()[0]
+    c = D.new_codes(3)
+    D.encode(_t(x), c)
+    torch.cuda.synchronize()
+    assert D.stats()[0]["topn_slow_path"] == 0
+    p = O.Params(N, d, n, s)
+    res = O.encode(p, A, x[0])
+    assert len(set(range(40)) & set(res.pool[0].tolist())) == 40      # the chunk's 40 atoms are all kept
+    ok = ~PU.exempt_mask(res)
+    for v in range(3):
+        if ok[v]:
+            assert np.array_equal(np.sort(pool[v]), np.sort(res.pool[v])), v
+    idx, coef, rel = (t.cpu().numpy()[0] for t in (c.idx, c.coef, c.relres))
+    PU.assert_encode_ok(PU.compare_encode(res, idx, coef, rel, pool, p, A, x[0]))
+
+
 def test_more_candidates_than_the_selection_holds():
     """A vector with far more candidates than the selection kernel's 2n-key
     buffer, none of its 128-atom records overflowing (512 near-copies of x's
