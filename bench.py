@@ -639,21 +639,28 @@ def run_ours(args):
 
     # ---- end to end: pinned host inputs in, codes out, every step ----
     xin = torch.empty_like(xs_dev[0])
-    outs = [torch.empty(c.shape, dtype=c.dtype).pin_memory() for c in
-            (codes.idx, codes.coef, codes.relres, codes.repl_id, codes.repl_coef)]
+    # the codes live in one buffer: one copy brings every array back
+    outs = [torch.empty(codes.buf.shape, dtype=codes.buf.dtype).pin_memory()]
     h2d = xs_host[0].numel() * xs_host[0].element_size()
     d2h = sum(o.numel() * o.element_size() for o in outs)
     ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+
+    def e2e_step(t):
+        xin.copy_(xs_host[t], non_blocking=True)
+        D.step(xin, codes, xhat, coder=args.coder)
+        for o, c in zip(outs, (codes.buf,)):
+            o.copy_(c, non_blocking=True)
+
+    # untimed warm-up of the same loop (first touch of the pinned buffers)
+    for t in range(W):
+        e2e_step(t)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     for t in range(K):
         flush.fill_(float(t))
         ev2[t][0].record(stream)
-        xin.copy_(xs_host[W + t], non_blocking=True)
-        D.step(xin, codes, xhat, coder=args.coder)
-        for o, c in zip(outs, (codes.idx, codes.coef, codes.relres, codes.repl_id, codes.repl_coef)):
-            o.copy_(c, non_blocking=True)
+        e2e_step(W + t)
         ev2[t][1].record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev2), dev)

@@ -11,13 +11,15 @@
 // sign(r_j) in its slice of shared memory (the larger key is the larger |r|,
 // then the lower atom index; the sign bit never decides, atoms being
 // distinct), then:
-//   1. buckets the keys by |r| on a linear grid of 256 buckets over
-//      [min |r|, max |r|] of the list (monotone in |r|, so every key of a
-//      higher bucket beats every key of a lower one);
+//   1. buckets the keys by |r| on a grid of 256 buckets over the binary32
+//      bit patterns between the smallest and largest |r| of the list (the
+//      range is tracked while decoding; the grid is monotone in |r|, so every
+//      key of a higher bucket beats every key of a lower one);
 //   2. finds the bucket B holding the n-th largest key from the histogram;
-//   3. takes all keys above B, and the best `rem` keys of B by full 64-bit
-//      key (|r|, then the lower index) -- by rank within the warp when B holds
-//      at most 32 keys, else by an MSD radix select restricted to B.
+//   3. in one pass takes all keys above B and compacts B's keys, then the
+//      best `rem` keys of B by full 64-bit key (|r|, then the lower index) --
+//      by rank within the warp when B holds at most 32 keys, else by an MSD
+//      radix select restricted to B.
 // Only warp-level synchronisation, so many warps share an SM and hide each
 // other's latency.  A vector whose list overflowed or holds fewer than n
 // keys gets pool[0] = -2 and is left to the exact slow path of the greedy
@@ -39,7 +41,9 @@ __device__ __forceinline__ float key_r(unsigned long long k)
     return __uint_as_float((uint32_t)(k >> 32) | ((uint32_t)k << 31));
 }
 
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+// KPL: keys per lane held in registers after the decode (cap <= 32 KPL)
+template <int KPL>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, 5)
 select_kernel(SelectArgs a)
 {
     pdl_begin();
@@ -75,6 +79,7 @@ select_kernel(SelectArgs a)
     constexpr int kIt = 8;                  // loads per lane: 32 records x 8 pieces over 32 lanes
     static_assert(kRecBytes / 16 == 8, "eight lanes cover a record");
     int gbase = 0;
+    uint32_t lo = 0xffffffffu, hi = 0u;      // range of |r| bits over the keys this lane writes
     for (int cg = 0; cg < nch; cg += 32) {
         const int cc = cg + lane;
         uint4 w[kIt];
@@ -112,7 +117,10 @@ select_kernel(SelectArgs a)
                     m &= m - 1u;
                     if (off + vi < a.cap) {
                         const uint32_t val = mine[5 + vi];
-                        keys[off + vi] = sel_key(val & 0x7fffffffu, (uint32_t)cc * 128u + 32u * qq + t, val >> 31);
+                        const uint32_t ab = val & 0x7fffffffu;
+                        keys[off + vi] = sel_key(ab, (uint32_t)cc * 128u + 32u * qq + t, val >> 31);
+                        lo = min(lo, ab);
+                        hi = max(hi, ab);
                     }
                     ++vi;
                 }
@@ -161,7 +169,11 @@ select_kernel(SelectArgs a)
                         }
                     }
                     const uint32_t bits = __float_as_uint(acc);
-                    if (offj + base + lane < a.cap) keys[offj + base + lane] = sel_key(bits & 0x7fffffffu, atom, bits >> 31);
+                    if (offj + base + lane < a.cap) {
+                        keys[offj + base + lane] = sel_key(bits & 0x7fffffffu, atom, bits >> 31);
+                        lo = min(lo, bits & 0x7fffffffu);
+                        hi = max(hi, bits & 0x7fffffffu);
+                    }
                 }
                 base += pq;
             }
@@ -183,30 +195,36 @@ select_kernel(SelectArgs a)
     }
     __syncwarp();
 
-    // 1. range of |r| and the bucket grid
-    uint32_t lo = 0xffffffffu, hi = 0u;
-    for (int i = lane; i < K; i += 32) {
-        const uint32_t m = (uint32_t)(keys[i] >> 32);
-        lo = min(lo, m);
-        hi = max(hi, m);
-    }
+    // 1. the bucket grid: 256 buckets over the bit patterns of |r| between
+    //    the smallest and largest kept (non-negative binary32 values order
+    //    like their bits, so the buckets are monotone in |r|; the grid is
+    //    near logarithmic, which spreads the many scores just above the
+    //    screening threshold over many buckets)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
         hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     }
-    const float flo = __uint_as_float(lo), fhi = __uint_as_float(hi);
-    const float scale = (fhi > flo) ? 255.99f / (fhi - flo) : 0.f;
+    const uint32_t span = hi - lo;
+    const int bsh = span > 255u ? (32 - __clz(span)) - 8 : 0;   // (span >> bsh) <= 255
     auto bucket = [&](unsigned long long k) -> uint32_t {
-        const float m = __uint_as_float((uint32_t)(k >> 32));
-        return min(255u, (uint32_t)((m - flo) * scale));
+        return min(255u, ((uint32_t)(k >> 32) - lo) >> bsh);
     };
+
+    // the keys into registers, key i in lane i % 32 at slot i / 32: the
+    // passes below read no shared memory
+    const int nk = (K + 31) >> 5;
+    unsigned long long kr[KPL];
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) kr[j] = (j * 32 + lane < K) ? keys[j * 32 + lane] : 0ull;
 
     // 2. histogram and the boundary bucket (lane l scans buckets 255-8l .. 248-8l)
 #pragma unroll
     for (int b = 0; b < 8; ++b) hist[lane * 8 + b] = 0;
     __syncwarp();
-    for (int i = lane; i < K; i += 32) atomicAdd(&hist[bucket(keys[i])], 1u);
+#pragma unroll
+    for (int j = 0; j < KPL; ++j)
+        if (j * 32 + lane < K) atomicAdd(&hist[bucket(kr[j])], 1u);
     __syncwarp();
     const int top = 255 - 8 * lane;
     uint32_t local = 0;
@@ -239,42 +257,28 @@ select_kernel(SelectArgs a)
     rem = __shfl_sync(0xffffffffu, rem, sl);
     nb = __shfl_sync(0xffffffffu, nb, sl);
 
-    // 3a. keys above the boundary bucket
-    int base = 0;
-    for (int i0 = 0; i0 < K; i0 += 32) {
-        const int i = i0 + lane;
-        const unsigned long long k = (i < K) ? keys[i] : 0ull;
-        const bool f = (i < K) && bucket(k) > bsel;
-        const unsigned bal = __ballot_sync(0xffffffffu, f);
-        if (f) put(base + __popc(bal & ((1u << lane) - 1u)), k);
-        base += __popc(bal);
-    }
-    if (rem == nb) {
-        // the whole boundary bucket
-        for (int i0 = 0; i0 < K; i0 += 32) {
-            const int i = i0 + lane;
-            const unsigned long long k = (i < K) ? keys[i] : 0ull;
-            const bool f = (i < K) && bucket(k) == bsel;
-            const unsigned bal = __ballot_sync(0xffffffffu, f);
-            if (f) put(base + __popc(bal & ((1u << lane) - 1u)), k);
-            base += __popc(bal);
-        }
-        return;
-    }
-    // 3b. the boundary bucket's keys, compacted in place to the front of the
-    //     buffer (a write never passes the read position); one per lane when
-    //     the bucket holds at most 32
+    // 3. one pass: keys above the boundary bucket go to the pool (with the
+    //    bucket's own when all of it is taken); otherwise the bucket's keys
+    //    are compacted to the front of the shared buffer
+    const bool whole_b = rem == nb;
     unsigned long long* bkeys = keys;
-    int mb = 0;
-    for (int i0 = 0; i0 < K; i0 += 32) {
-        const int i = i0 + lane;
-        const unsigned long long k = (i < K) ? keys[i] : 0ull;
-        const bool f = (i < K) && bucket(k) == bsel;
-        const unsigned bal = __ballot_sync(0xffffffffu, f);
-        if (f) bkeys[mb + __popc(bal & ((1u << lane) - 1u))] = k;
-        mb += __popc(bal);
-        __syncwarp();
+    int base = 0, mb = 0;
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) {
+        if (j >= nk) break;
+        const int i = j * 32 + lane;
+        const unsigned long long k = kr[j];
+        const uint32_t b = (i < K) ? bucket(k) : 0u;
+        const bool fp = (i < K) && (b > bsel || (whole_b && b == bsel));
+        const bool fc = (i < K) && !whole_b && b == bsel;
+        const unsigned balp = __ballot_sync(0xffffffffu, fp);
+        const unsigned balc = __ballot_sync(0xffffffffu, fc);
+        if (fp) put(base + __popc(balp & ((1u << lane) - 1u)), k);
+        if (fc) bkeys[mb + __popc(balc & ((1u << lane) - 1u))] = k;
+        base += __popc(balp);
+        mb += __popc(balc);
     }
+    if (whole_b) return;
     __syncwarp();
     if (mb <= 32) {
         const unsigned long long mk = (lane < mb) ? bkeys[lane] : 0ull;
@@ -352,11 +356,13 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st)
 {
     const long long warps = (long long)a.G * a.Vc;
     if (warps <= 0) return cudaSuccess;
+    if (a.cap > 32 * 32) return cudaErrorInvalidValue;
     const size_t smem = select_smem_bytes(a.cap);
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto k = a.cap <= 32 * 16 ? select_kernel<16> : select_kernel<32>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
-    return launch_pdl(select_kernel, dim3(blocks), dim3(kWarpsPerCta * 32), smem, st, a);
+    return launch_pdl(k, dim3(blocks), dim3(kWarpsPerCta * 32), smem, st, a);
 }
 
 }  // namespace fadkv

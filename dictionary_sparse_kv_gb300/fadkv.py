@@ -338,6 +338,7 @@ class Codes:
     relres: "object"    # float32 [G][V]
     repl_id: "object"   # int32 [G][V]
     repl_coef: "object"  # float32 [G][V]
+    buf: "object" = None  # int32 words holding all five back to back (one copy moves every code)
 
 
 class Dictionary:
@@ -376,11 +377,17 @@ class Dictionary:
         import torch
         dev = self.atoms.device
         G, s = self.G, self.s
-        return Codes(torch.empty((G, V, s), dtype=torch.int32, device=dev),
-                     torch.empty((G, V, s), dtype=torch.float32, device=dev),
-                     torch.empty((G, V), dtype=torch.float32, device=dev),
-                     torch.empty((G, V), dtype=torch.int32, device=dev),
-                     torch.empty((G, V), dtype=torch.float32, device=dev))
+        # the five arrays as slices of one buffer, each starting on a
+        # 256-byte boundary
+        sizes = [G * V * s, G * V * s, G * V, G * V, G * V]
+        offs, o = [], 0
+        for n_ in sizes:
+            offs.append(o)
+            o += (n_ + 63) // 64 * 64
+        buf = torch.empty(max(o, 1), dtype=torch.int32, device=dev)
+        part = lambda i, shape: buf[offs[i]:offs[i] + sizes[i]].view(shape)
+        return Codes(part(0, (G, V, s)), part(1, (G, V, s)).view(torch.float32), part(2, (G, V)).view(torch.float32),
+                     part(3, (G, V)), part(4, (G, V)).view(torch.float32), buf)
 
     def refresh(self, stream=None):
         """Rebuild the Gram matrices (after changing self.atoms in place)."""
