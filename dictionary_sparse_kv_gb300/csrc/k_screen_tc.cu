@@ -294,7 +294,7 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, const __grid_constan
         uint32_t* const myrec = recs + lane * kSlotWords;   // header, four masks, then the scores
         const uint32_t myrec_s = smem_u32(myrec);
         int cur = -1, g = 0, vloc = 0;
-        bool valid = false, ok = true;
+        bool valid = false, wlive = false, ok = true;
         float tau = __int_as_float(0x7fffffff);
         UnitCursor uc;
         uc.init(u0 + grp, nch, tiles);
@@ -305,6 +305,7 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, const __grid_constan
                 g = uc.g;
                 vloc = uc.tile * kTileV + r;
                 valid = vloc < a.Vc;
+                wlive = __any_sync(0xffffffffu, valid);     // a small or ragged batch leaves whole warps idle
                 // tau from ||x||^2 of this lane's row (rows past the batch:
                 // NaN, never passes).  The warp's 32 rows are read whole,
                 // sixteen lanes (eight for d = 64) on a row.
@@ -352,6 +353,14 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, const __grid_constan
             ok = mbar_wait(tfull_bar(buf), (uint32_t)(i / kAcc) & 1u, status, wait_ns);
             if (!ok) break;
             fence_after();
+            if (!wlive) {
+                // none of this warp's 32 rows is in the batch: nothing to read
+                // or write; the buffer is released as soon as it is full, so
+                // the warp never runs ahead of the group
+                fence_before();
+                mbar_arrive(tempty_bar(buf));
+                continue;
+            }
             const uint32_t tcol = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kChunk);
             // shared-memory address of this row's next score slot
             uint32_t wp = myrec_s + 5u * 4u;

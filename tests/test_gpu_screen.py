@@ -288,3 +288,42 @@ def test_select_exact_ties(case):
     assert D.stats()[0]["topn_slow_path"] == 0      # decided by the selection kernel
     res = O.encode(O.Params(N, d, n, s), A, x[0])
     assert sorted(pool) == sorted(res.pool[0])
+
+
+
+@pytest.mark.parametrize("N,d,G,V", [(4096, 128, 3, 1), (4096, 128, 2, 7), (8192, 128, 2, 16), (1024, 64, 2, 12)])
+def test_small_batch_scores_against_float64(N, d, G, V):
+    """A few vectors per dictionary fill a small part of the 128-row tile
+    (the rest of the epilogue's warps skip their units): raw scores within
+    the fp32 accumulation bound."""
+    atoms = np.stack([S.make_dictionary(N, d, np.float16, 9, g) for g in range(G)])
+    x = np.stack([S.make_sparse_inputs(atoms[g], V, 8, 8, 100 + g) for g in range(G)])
+    D = _dict(atoms, np.ones((G, N), np.int32), [0.5] * G, 64, 8, V)
+    sc = D.scores(_t(x)).cpu().numpy().astype(np.float64)
+    for g in range(G):
+        A = atoms[g].astype(np.float64)
+        X = x[g].astype(np.float64)
+        exact = X @ A.T
+        bound = d * 2.0 ** -24 * (np.abs(X) @ np.abs(A).T) + 1e-30
+        err = np.abs(sc[g] - exact)
+        assert np.all(err <= bound), float(np.max(err / bound))
+
+
+@pytest.mark.parametrize("V", [1, 8, 16, 33, 100])
+def test_small_batch_encode_matches_oracle(V):
+    """Encodes of small and ragged batches (1, 8, 16, 33 and 100 vectors: one,
+    two or four of the epilogue's lane groups hold rows) match the oracle:
+    pools off near ties, coefficients and residuals within the parity bar."""
+    from dataclasses import replace
+    w = replace(S.WORKLOADS["decode_3b"], G=3, V=V)
+    data = S.WorkloadData(w)
+    D = _dict(data.atoms, data.usage, data.deltas(), w.n, w.s, V)
+    x = data.inputs(0, V)
+    c = D.new_codes(V)
+    D.encode(_t(x), c)
+    assert sum(st["topn_slow_path"] for st in D.stats()) == 0
+    idx, coef, rel = c.idx.cpu().numpy(), c.coef.cpu().numpy(), c.relres.cpu().numpy()
+    p = O.Params(w.N, w.d, w.n, w.s)
+    for g in range(w.G):
+        res = O.encode_threaded(p, data.atoms[g], x[g], PU.THREADS)
+        PU.assert_encode_ok(PU.compare_encode(res, idx[g], coef[g], rel[g]))
