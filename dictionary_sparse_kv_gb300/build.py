@@ -72,6 +72,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
         return obj
 
     srcs = _sources()
+    # objects of sources that no longer exist
+    keep = {os.path.basename(x)[:-3] + ".o" for x in srcs}
+    for f in os.listdir(OUT):
+        if f.endswith(".o") and f not in keep:
+            os.remove(os.path.join(OUT, f))
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
     tmp = LIB + f".{os.getpid()}.tmp"

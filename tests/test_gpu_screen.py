@@ -219,32 +219,19 @@ def test_scores_far_above_the_threshold_are_kept_exactly():
 
 @pytest.mark.parametrize("name,G,V", [("decode_3b", 3, 200), ("decode_8b", 2, 64)])
 def test_greedy_kernels_agree(monkeypatch, name, G, V):
-    """The greedy kernels all match the oracle: the correlation-domain kernel
-    with an incremental Cholesky factor (default), one tcgen05 GEMM per pick
-    over the whole dictionary with a pool-masked argmax (cluster size chosen
-    by the launcher, and forced to 1 and 3), the residual-based mma.sync
-    kernel (2 or 4 m16 tiles per warp) and the FP32-pipe kernel."""
+    """Both greedy kernels match the oracle on coefficients and residuals as
+    well as ids: the batch-OMP kernel over the Gram matrices (behind the
+    tensor-core screening, the default) and the FP32-pipe kernel (behind the
+    FP32 screening, FADKV_SCREEN=ffma)."""
     from dataclasses import replace
     w = replace(S.WORKLOADS[name], G=G)
     data = S.WorkloadData(w)
     x = data.inputs(0, V)
     outs = {}
-    paths = ("chol", "tc", "tc_c1", "tc_c3", "mma", "mma4", "ffma")
+    paths = ("gram", "ffma")
     for path in paths:
-        if path == "tc":
-            monkeypatch.setenv("FADKV_GREEDY", "tc")
-        if path == "tc_c1":
-            monkeypatch.setenv("FADKV_GREEDY_CLUSTER", "1")
-        if path == "tc_c3":
-            monkeypatch.setenv("FADKV_GREEDY_CLUSTER", "3")
-        if path == "mma":
-            monkeypatch.delenv("FADKV_GREEDY_CLUSTER")
-            monkeypatch.setenv("FADKV_GREEDY", "mma")
-        if path == "mma4":
-            monkeypatch.setenv("FADKV_GREEDY_TILES", "4")
         if path == "ffma":
-            monkeypatch.delenv("FADKV_GREEDY_TILES")
-            monkeypatch.setenv("FADKV_GREEDY", "ffma")
+            monkeypatch.setenv("FADKV_SCREEN", "ffma")
         D = _dict(data.atoms, data.usage, data.deltas(), w.n, w.s, V)
         c = D.new_codes(V)
         D.encode(_t(x), c)
