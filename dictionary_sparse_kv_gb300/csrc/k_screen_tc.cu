@@ -29,10 +29,10 @@
 //
 // Warp roles (512 threads): warp 0 issues TMA loads (vector tiles and atom
 // chunks), warp 1 issues MMAs (one thread), warp 2 owns the TMEM allocation,
-// warp 3 asks for the chunks of the next units to be brought into L2,
-// warps 4..15 are the epilogue: three groups of four, group k takes the
-// units i with i mod 3 = k (accumulator buffer k), warp w reads TMEM lanes
-// 32 (w mod 4)...  Each group computes the thresholds of its rows at each
+// warp 3 has no role (asking for chunks ahead into L2 was measured: it only
+// slowed the stream), warps 4..15 are the epilogue: three groups of four,
+// group k takes the units i with i mod 3 = k (accumulator buffer k), warp w
+// reads TMEM lanes 32 (w mod 4)...  Each group computes the thresholds of its rows at each
 // new segment from the vectors in global memory (coalesced: sixteen lanes
 // on a row).  Every wait is bounded by a wall-clock limit; on expiry the CTA
 // sets FADKV_DEV_TIMEOUT in the status word, drains its own copies and MMAs
@@ -50,7 +50,6 @@ constexpr int kAcc = 3;            // accumulator buffers (and epilogue groups)
 constexpr int kTmemCols = 512;     // kAcc x 128 columns, allocated as a power of two
 constexpr int kEpiWarps = 4 * kAcc;
 constexpr int kStagesFor(int D) { return D == 64 ? 6 : 3; }  // atom chunk pipeline depth
-constexpr int kPrefetch = 10;      // units whose atom chunks are asked into L2 ahead of the loads
 // A row's record in shared memory sits in a slot of kRecWords + 4 words
 // (144 bytes): consecutive rows start 4 banks apart, so the rows' appends,
 // which advance at similar rates, rarely hit the same bank.
@@ -156,7 +155,6 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, const __grid_constan
             mbar_init(aempty_bar(i), 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        reinterpret_cast<volatile int*>(smem + L::taddr_off + 4)[0] = 0;    // producer's progress
     }
     __syncthreads();
     pdl_begin();                      // the predecessor's writes (x, atoms) are visible from here
@@ -208,42 +206,12 @@ screen_tc_kernel(const __grid_constant__ CUtensorMap map_d, const __grid_constan
                 for (int h = 0; h < L::KH; ++h)
                     tma_load_2d(sB + st * kTileBytes + h * kChunk * 128, &map_d, h * 64, arow, full_bar(st));
                 ++issued;
-                *reinterpret_cast<volatile int*>(smem + L::taddr_off + 4) = issued;   // for the prefetcher
             }
             // drain: every issued load must have landed before the CTA exits
             for (int i = max(0, issued - L::kStages); i < issued; ++i)
                 mbar_wait(full_bar(i % L::kStages), (uint32_t)(i / L::kStages) & 1u, status);
             for (int ab = 0; ab < 2; ++ab)
                 if (a_loads[ab] > 0) mbar_wait(afull_bar(ab), (uint32_t)(a_loads[ab] - 1) & 1u, status);
-        }
-    } else if (warp == 3) {
-        // ---------------- L2 prefetch ----------------
-        // Asks for the atom chunks (and each segment's vector tile) of units
-        // up to kPrefetch ahead of the loads the producer has issued, so more
-        // HBM reads are in flight than the stages hold; it never waits on
-        // anything but the producer's progress counter.
-        if (lane == 0) {
-            volatile int* const prog = reinterpret_cast<volatile int*>(smem + L::taddr_off + 4);
-            UnitCursor pc;
-            pc.init(u0, nch, tiles);
-            int pprev = -1;
-            for (int pf = 0; pf < nu; ++pf, pc.advance(1)) {
-                if (pf >= kPrefetch) {
-                    // wait (bounded) until the producer has issued unit pf - kPrefetch
-                    const unsigned long long t0 = globaltimer();
-                    while (*prog < pf - kPrefetch + 1) {
-                        if (globaltimer() - t0 > wait_ns) break;
-                        __nanosleep(64);
-                    }
-                    if (*prog < pf - kPrefetch + 1) break;
-                }
-                if (pc.pair != pprev) {
-                    pprev = pc.pair;
-                    const int xrow = pc.g * a.V + a.v0 + pc.tile * kTileV;
-                    for (int h = 0; h < L::KH; ++h) tma_prefetch_2d(&map_x, h * 64, xrow);
-                }
-                for (int h = 0; h < L::KH; ++h) tma_prefetch_2d(&map_d, h * 64, pc.g * a.N + pc.c * kChunk);
-            }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------

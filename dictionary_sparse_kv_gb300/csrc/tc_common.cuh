@@ -99,16 +99,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Asks the TMA unit to bring a box of the tensor into L2 (no shared memory,
-// nothing to wait for): issued some units ahead, it keeps more HBM reads in
-// flight than the shared-memory stages hold.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
-                 : "memory");
-}
-
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart; the start address advances 32 bytes per K = 16 step.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr)
