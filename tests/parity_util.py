@@ -30,7 +30,7 @@ COEF_TOL = 1e-3
 RELRES_TOL = 1e-3
 XHAT_TOL = 1e-5
 COEF_FLOOR = 1e-2       # element-wise check for |c_i| >= COEF_FLOOR * ||c||
-MAX_EXEMPT_FRAC = 0.05  # vectors on an unjudged near tie, at most (or 2)
+MAX_EXEMPT_FRAC = 0.05  # vectors on a near tie left unchecked, at most (or 2)
 THREADS = max(1, min(16, os.cpu_count() or 1))
 
 
@@ -104,7 +104,7 @@ def compare_encode(res: O.EncodeResult, idx, coef, relres, gpu_pool=None, p=None
         ro = res.relres[chk]
         dr = np.abs(relres[chk] - ro)
         worst_r = float(np.max(np.where(ro > 0, dr / np.where(ro > 0, ro, 1.0), dr)))
-    # vectors on a near tie at the cut: judged on the GPU's pool
+    # vectors on a near tie at the cut: checked on the GPU's pool
     for v in np.nonzero(ex)[0]:
         if gpu_pool is None or res.pick_gap[v].min() < PICK_GAP or res.idx[v][0] < 0:
             continue

@@ -12,7 +12,7 @@ near tie cannot make the two drift apart):
   of the generating sources redrawn every 128 steps; and 64 steps of it with
   a threshold low enough that atoms are replaced in every early step.
 
-At every step: selected ids bit-exact (near ties judged on the GPU's pool),
+At every step: selected ids bit-exact (near ties checked on the GPU's pool),
 coefficients and relres within 1e-3, the usage counts and replacement ids
 equal to the oracle's adaptation of the GPU's codes, replaced atoms within
 one storage ulp plus the fp32 bound, the dictionary size fixed at N and the
