@@ -92,12 +92,17 @@ gram_kernel(const __half* __restrict__ atoms, int G, int N, const int32_t* __res
     const bool update = rows != nullptr;
     const int ctiles = (N + kGT - 1) / kGT;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    // the tiles of dictionaries [0, g) come before those of g
+    // the tiles of dictionaries [0, g) come before those of g; the total
+    // over every dictionary by each warp (lanes over dictionaries): an
+    // update after a step without replacements leaves at once
     long long total = 0;
-    for (int g = 0; g < G; ++g) {
+    for (int g = (int)(threadIdx.x & 31); g < G; g += 32) {
         const int nr = update ? nrows[g] : N;
         total += (long long)((nr + kGT - 1) / kGT) * ctiles;
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    if (total == 0) return;
     // tiles [gbase, gend) belong to dictionary g; t only grows, so g only
     // advances, and t < total keeps it below G
     int g = -1;
