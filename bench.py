@@ -677,6 +677,8 @@ def run_ours(args):
     outs2 = [torch.empty(codes.buf.shape, dtype=codes.buf.dtype).pin_memory() for _ in range(2)]
 
     def pipelined(t0, n):
+        if n <= 0:
+            return None
         in_ev = [torch.cuda.Event() for _ in range(n)]
         done = [torch.cuda.Event() for _ in range(n)]
         fl = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
