@@ -320,3 +320,16 @@ def test_multistep_adaptation_stress():
     ex, ch, reps, D = _run_steps(w, 6, 64)
     assert reps > 0
     assert D.atoms.shape == (2, w.N, w.d)
+
+
+@pytest.mark.parametrize("s,n,V", [(4, 128, 150), (8, 64, 33)], ids=["s4_n128_V150", "s8_n64_V33"])
+def test_multistep_binary16_d64(s, n, V):
+    """Binary16 dictionaries of d = 64 through the whole tensor-core path
+    (screening with 64-wide tiles, the selection, the Gram greedy with fewer
+    picks than its compile-time maximum, adapt and the Gram update): three
+    steps, each against the oracle on the GPU's state."""
+    from dataclasses import replace
+    w = replace(S.WORKLOADS["decode_3b"], G=2, d=64, N=2048, n=n, s=s, off_frac=0.3)
+    ex, ch, reps, D = _run_steps(w, 3, V)
+    assert ch > 0
+    assert D.atoms.shape == (2, w.N, w.d)

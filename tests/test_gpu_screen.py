@@ -296,13 +296,15 @@ def test_small_batch_scores_against_float64(N, d, G, V):
         assert np.all(err <= bound), float(np.max(err / bound))
 
 
-@pytest.mark.parametrize("V", [1, 8, 16, 33, 100])
-def test_small_batch_encode_matches_oracle(V):
+@pytest.mark.parametrize("name,V", [("decode_3b", 1), ("decode_3b", 8), ("decode_3b", 16), ("decode_3b", 33),
+                                    ("decode_3b", 100), ("decode_8b", 33)])
+def test_small_batch_encode_matches_oracle(name, V):
     """Encodes of small and ragged batches (1, 8, 16, 33 and 100 vectors: one,
-    two or four of the epilogue's lane groups hold rows) match the oracle:
-    pools off near ties, coefficients and residuals within the parity bar."""
+    two or four of the epilogue's lane groups hold rows; and the 8B shape's
+    n = 512, s = 16) match the oracle: pools off near ties, coefficients and
+    residuals within the parity bar."""
     from dataclasses import replace
-    w = replace(S.WORKLOADS["decode_3b"], G=3, V=V)
+    w = replace(S.WORKLOADS[name], G=2 if name == "decode_8b" else 3, V=V)
     data = S.WorkloadData(w)
     D = _dict(data.atoms, data.usage, data.deltas(), w.n, w.s, V)
     x = data.inputs(0, V)
