@@ -197,6 +197,7 @@ def _adapt_case(w, V, step=0):
     ("decode_3b", dict(G=2, off_frac=1.2), 128),
     ("decode_3b", dict(G=2, inactive=5, off_frac=1.5), 128),   # inactive list runs out
     ("adapt_stress", dict(off_frac=0.8), 4096),       # a batch whose usage increments run over the grid
+    ("decode_8b", dict(G=2, deltas=(0.25, 0.25)), 64),   # N = 8192: replacements and their Gram rows
 ])
 def test_adapt_matches_oracle(name, over, V):
     w = small(S.WORKLOADS[name], **over)
@@ -333,3 +334,14 @@ def test_multistep_binary16_d64(s, n, V):
     ex, ch, reps, D = _run_steps(w, 3, V)
     assert ch > 0
     assert D.atoms.shape == (2, w.N, w.d)
+
+
+def test_multistep_8b_shape_with_replacements():
+    """The 8B shape (N = 8192, n = 512, s = 16) over three steps with a low
+    threshold: atoms are replaced every step, so every later encode reads
+    Gram rows and columns the update rewrote; each step against the oracle
+    on the GPU's state."""
+    from dataclasses import replace
+    w = replace(S.WORKLOADS["decode_8b"], G=2, deltas=(0.25, 0.25))
+    ex, ch, reps, D = _run_steps(w, 3, 48)
+    assert reps > 0 and ch > 0
