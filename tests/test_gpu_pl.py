@@ -80,6 +80,8 @@ CASES = [
     ("decode_3b", dict(G=2, N=1984), 50),           # binary16, N not a multiple of 128: FP32 screening
     ("decode_3b", dict(G=1, s=1), 64),
     ("decode_3b", dict(G=1, s=32, n=64), 64),       # the largest s
+    ("decode_3b", dict(G=2), 1),                    # one vector a dictionary: one live epilogue warp
+    ("decode_3b", dict(G=2, d=64, N=2048, n=128, s=4), 40),   # binary16, d = 64 tiles
 ]
 
 
