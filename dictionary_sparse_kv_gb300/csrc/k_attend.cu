@@ -430,9 +430,10 @@ attend_kernel(AttendArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// binary16 dictionaries: the two dictionary products as per-layer GEMMs on
-// the tensor cores (mma.sync m16n8k16, binary16 operands, FP32 sums), so a
-// layer's dictionaries are read once for all its sequences and heads:
+// binary16 dictionaries: the two dictionary products as per-layer GEMMs
+// (mma.sync m16n8k16 from shared-memory tiles, binary16 operands, FP32
+// sums), so a layer's dictionaries are read once per tile of query rows, not
+// once per (sequence, KV head):
 //   U = scale Q D_K^T   [B Hq][N]   before the token pass,
 //   O = W D_V           [B Hq][d]   after it (W = the token pass's w / S).
 // The FP32 operands (queries, w) enter as two binary16 terms, hi + lo, after
@@ -460,156 +461,260 @@ __device__ __forceinline__ float row_scale(float m)
     return __int_as_float((127 + ec) << 23);
 }
 
-// U: one warp per 16 query rows x 64 atoms; CTA = 4 warps (256 atoms).
+// Shared-memory fragments: four 8x8 binary16 matrices (row addresses given by
+// lanes 8j..8j+7 for matrix j); .trans delivers them transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ uint32_t saddr(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+// 16 bytes global -> shared, asynchronous; zero-filled when `valid` is false
+// (no byte is read then).
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// U: a CTA takes 64 query rows x 128 atoms of one layer.  The rows enter
+// shared memory as two binary16 terms after their power-of-two scale, the
+// atoms as stored (rows padded by 16 bytes, so the eight rows an ldmatrix
+// reads sit in different banks); 8 warps, 2 (rows) x 4 (atoms), 32 x 32
+// outputs each, every fragment from shared memory.
+constexpr int kUBM = 64, kUBN = 128, kUThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(128)
+struct USmem {
+    static constexpr int LD = D + 8;
+    __half qh[kUBM][LD], ql[kUBM][LD], dk[kUBN][LD];
+    float rs[kUBM];
+};
+
+template <int D>
+__global__ void __launch_bounds__(kUThreads)
 attend_u_kernel(AttendArgs a)
 {
-    constexpr int KT = D / 16;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g8 = lane >> 2, t4 = lane & 3;
+    extern __shared__ __align__(16) unsigned char u_raw[];
+    USmem<D>& sm = *reinterpret_cast<USmem<D>*>(u_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int M = a.B * a.Hq, N = a.N, l = blockIdx.z;
-    const int row0 = blockIdx.y * 16;
-    const int atom0 = blockIdx.x * 256 + warp * 64;
+    const int row0 = blockIdx.y * kUBM, atom0 = blockIdx.x * kUBN;
     const float* Q = a.q + (size_t)l * M * D;
     const __half* Dk = (const __half*)a.dict_k + (size_t)l * a.dict_stride;
 
-    // row scales: lanes 2r, 2r+1 scan row r
-    float mx = 0.f;
+    // the atom tile (zeros past N) is on its way while the rows are scaled
+    for (int i = tid; i < kUBN * (D / 8); i += kUThreads) {
+        const int r = i / (D / 8), c = (i % (D / 8)) * 8;
+        const bool ok = atom0 + r < N;
+        cp16(saddr(&sm.dk[r][c]), Dk + (size_t)(ok ? atom0 + r : 0) * D + c, ok);
+    }
+    cp_commit();
+    // per-row scale: four lanes on a row
     {
-        const int r = lane >> 1, hh = lane & 1;
+        const int r = tid >> 2, part = tid & 3;
+        float mx = 0.f;
         if (row0 + r < M) {
-            const float4* qr = reinterpret_cast<const float4*>(Q + (size_t)(row0 + r) * D + hh * (D / 2));
+            const float4* qr = reinterpret_cast<const float4*>(Q + (size_t)(row0 + r) * D + part * (D / 4));
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
+            for (int i = 0; i < D / 16; ++i) {
                 const float4 v = __ldg(qr + i);
                 mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
             }
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        if (part == 0) sm.rs[r] = row_scale(mx);
     }
-    const float scr = row_scale(mx);
-    const float scA = __shfl_sync(0xffffffffu, scr, 2 * g8), scB = __shfl_sync(0xffffffffu, scr, 2 * (g8 + 8));
-    const bool okA = row0 + g8 < M, okB = row0 + g8 + 8 < M;
+    __syncthreads();
+    for (int i = tid; i < kUBM * (D / 2); i += kUThreads) {
+        const int r = i / (D / 2), c = (i % (D / 2)) * 2;
+        float2 v = make_float2(0.f, 0.f);
+        if (row0 + r < M) v = __ldg(reinterpret_cast<const float2*>(Q + (size_t)(row0 + r) * D + c));
+        const float sc = sm.rs[r];
+        v.x *= sc;
+        v.y *= sc;
+        const __half2 h = __floats2half2_rn(v.x, v.y);
+        *reinterpret_cast<__half2*>(&sm.qh[r][c]) = h;
+        *reinterpret_cast<__half2*>(&sm.ql[r][c]) = __floats2half2_rn(v.x - __low2float(h), v.y - __high2float(h));
+    }
+    cp_wait<0>();
+    __syncthreads();
 
-    // A fragments (hi, lo) of the 16 rows for every k step
-    uint32_t ah[KT][4], al[KT][4];
+    const int wm = warp >> 2, wn = warp & 3;
+    float acc[2][4][4];
 #pragma unroll
-    for (int kt = 0; kt < KT; ++kt) {
+    for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const bool rowB = r & 1, khi = r >> 1;
-            const bool ok = rowB ? okB : okA;
-            const int row = row0 + g8 + (rowB ? 8 : 0);
-            const int k = kt * 16 + (khi ? 8 : 0) + 2 * t4;
-            float2 v = ok ? __ldg(reinterpret_cast<const float2*>(Q + (size_t)row * D + k)) : make_float2(0.f, 0.f);
-            const float sc = rowB ? scB : scA;
-            v.x *= sc;
-            v.y *= sc;
-            const __half2 h = __floats2half2_rn(v.x, v.y);
-            ah[kt][r] = h2bits(h);
-            al[kt][r] = h2bits(__floats2half2_rn(v.x - __low2float(h), v.y - __high2float(h)));
+        for (int ni = 0; ni < 4; ++ni) acc[mi][ni][0] = acc[mi][ni][1] = acc[mi][ni][2] = acc[mi][ni][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D; kk += 16) {
+        uint32_t ah[2][4], al[2][4], b[4][2];
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+            const int r = wm * 32 + mi * 16 + (lane & 15), c = kk + (lane >> 4) * 8;
+            ldsm_x4(ah[mi], saddr(&sm.qh[r][c]));
+            ldsm_x4(al[mi], saddr(&sm.ql[r][c]));
         }
+#pragma unroll
+        for (int ni = 0; ni < 4; ni += 2) {
+            const int n = wn * 32 + ni * 8 + (lane & 7) + ((lane >> 4) << 3), c = kk + ((lane >> 3) & 1) * 8;
+            uint32_t t[4];
+            ldsm_x4(t, saddr(&sm.dk[n][c]));
+            b[ni][0] = t[0];
+            b[ni][1] = t[1];
+            b[ni + 1][0] = t[2];
+            b[ni + 1][1] = t[3];
+        }
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                hmma16816(acc[mi][ni], ah[mi], b[ni][0], b[ni][1]);
+                hmma16816(acc[mi][ni], al[mi], b[ni][0], b[ni][1]);
+            }
     }
     float* U = a.U + (size_t)l * M * a.Npad;
-    const float fA = a.scale / scA, fB = a.scale / scB;
-#pragma unroll 2
-    for (int nt = 0; nt < 8; ++nt) {
-        const int n0 = atom0 + nt * 8;
-        if (n0 >= N) break;
-        const int atom = n0 + g8;
-        const __half* brow = Dk + (size_t)(atom < N ? atom : 0) * D + 2 * t4;
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+    const int g8 = lane >> 2, t4 = lane & 3;
 #pragma unroll
-        for (int kt = 0; kt < KT; ++kt) {
-            const uint32_t b0 = atom < N ? __ldg(reinterpret_cast<const uint32_t*>(brow + kt * 16)) : 0u;
-            const uint32_t b1 = atom < N ? __ldg(reinterpret_cast<const uint32_t*>(brow + kt * 16 + 8)) : 0u;
-            hmma16816(c, ah[kt], b0, b1);
-            hmma16816(c, al[kt], b0, b1);
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int rl = wm * 32 + mi * 16 + g8 + hr * 8, row = row0 + rl;
+            if (row >= M) continue;
+            const float f = a.scale / sm.rs[rl];
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) {
+                const int col = atom0 + wn * 32 + ni * 8 + 2 * t4;
+                const float v0 = acc[mi][ni][2 * hr] * f, v1 = acc[mi][ni][2 * hr + 1] * f;
+                float* dst = U + (size_t)row * a.Npad + col;
+                if (col + 1 < N)
+                    *reinterpret_cast<float2*>(dst) = make_float2(v0, v1);
+                else if (col < N)
+                    *dst = v0;
+            }
         }
-        const int col = n0 + 2 * t4;
-        if (okA) {
-            if (col < N) U[(size_t)(row0 + g8) * a.Npad + col] = c[0] * fA;
-            if (col + 1 < N) U[(size_t)(row0 + g8) * a.Npad + col + 1] = c[1] * fA;
-        }
-        if (okB) {
-            if (col < N) U[(size_t)(row0 + g8 + 8) * a.Npad + col] = c[2] * fB;
-            if (col + 1 < N) U[(size_t)(row0 + g8 + 8) * a.Npad + col + 1] = c[3] * fB;
-        }
-    }
 }
 
-// O: 16 rows of W per CTA, the atoms split over 8 warps, each warp all D
-// columns (D/8 n tiles); partial sums reduced in shared memory.
-constexpr int kOWarps = 8;
+// O: a CTA takes 32 rows of W and all D columns of one layer and runs over
+// the atoms in chunks of 64, two chunks in flight (cp.async): W's two
+// binary16 terms and D_V's rows in shared memory, D_V's fragments by
+// transposing ldmatrix; 4 warps, each the 32 rows x D/4 columns.
+constexpr int kOBM = 32, kOBK = 64, kOThreads = 128;
 
 template <int D>
-__global__ void __launch_bounds__(kOWarps * 32)
+struct OSmem {
+    static constexpr int LDW = kOBK + 8, LDV = D + 8;
+    __half wh[2][kOBM][LDW], wl[2][kOBM][LDW], dv[2][kOBK][LDV];
+};
+
+template <int D>
+__global__ void __launch_bounds__(kOThreads)
 attend_o_kernel(AttendArgs a)
 {
-    constexpr int NTN = D / 8;
-    extern __shared__ float ored[];                    // [kOWarps][16][D + 1] partial sums
-    auto red = reinterpret_cast<float (*)[16][D + 1]>(ored);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g8 = lane >> 2, t4 = lane & 3;
+    constexpr int NT = D / 32;                          // n8 tiles per warp
+    extern __shared__ __align__(16) unsigned char o_raw[];
+    OSmem<D>& sm = *reinterpret_cast<OSmem<D>*>(o_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int M = a.B * a.Hq, N = a.N, Np = a.Npad, l = blockIdx.y;
-    const int row0 = blockIdx.x * 16;
+    const int row0 = blockIdx.x * kOBM;
     const __half* Dv = (const __half*)a.dict_v + (size_t)l * a.dict_stride;
     const __half* Whi = a.Whi + (size_t)l * M * Np;
     const __half* Wlo = a.Wlo + (size_t)l * M * Np;
-    const bool okA = row0 + g8 < M, okB = row0 + g8 + 8 < M;
-    const int ksteps = Np / 16;
-    const int per = (ksteps + kOWarps - 1) / kOWarps;
-    const int k_begin = warp * per, k_end = min(ksteps, k_begin + per);
+    const int nchunks = (Np + kOBK - 1) / kOBK;
 
-    float acc[NTN][4];
-#pragma unroll
-    for (int nt = 0; nt < NTN; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    for (int ks = k_begin; ks < k_end; ++ks) {
-        const int k0 = ks * 16;
-        uint32_t ah[4], al[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const bool rowB = r & 1, khi = r >> 1;
-            const bool ok = rowB ? okB : okA;
-            const size_t off = (size_t)(row0 + g8 + (rowB ? 8 : 0)) * Np + k0 + (khi ? 8 : 0) + 2 * t4;
-            ah[r] = ok ? __ldg(reinterpret_cast<const uint32_t*>(Whi + off)) : 0u;
-            al[r] = ok ? __ldg(reinterpret_cast<const uint32_t*>(Wlo + off)) : 0u;
+    auto load = [&](int ch, int buf) {
+        const int k0 = ch * kOBK;
+        for (int i = tid; i < kOBM * (kOBK / 8); i += kOThreads) {
+            const int r = i / (kOBK / 8), c = (i % (kOBK / 8)) * 8;
+            const bool ok = row0 + r < M && k0 + c < Np;
+            const size_t off = ok ? (size_t)(row0 + r) * Np + k0 + c : 0;
+            cp16(saddr(&sm.wh[buf][r][c]), Whi + off, ok);
+            cp16(saddr(&sm.wl[buf][r][c]), Wlo + off, ok);
         }
-        // B: rows k0 + 2 t4 (+1) and k0 + 8 + 2 t4 (+1) of D_V, column n0 + g8
-        const int ka = k0 + 2 * t4, kb = ka + 8;
-        const bool v0 = ka < N, v1 = ka + 1 < N, v2 = kb < N, v3 = kb + 1 < N;
-#pragma unroll
-        for (int nt = 0; nt < NTN; ++nt) {
-            const int col = nt * 8 + g8;
-            const __half z = __float2half_rn(0.f);
-            const __half e0 = v0 ? Dv[(size_t)ka * D + col] : z;
-            const __half e1 = v1 ? Dv[(size_t)(ka + 1) * D + col] : z;
-            const __half e2 = v2 ? Dv[(size_t)kb * D + col] : z;
-            const __half e3 = v3 ? Dv[(size_t)(kb + 1) * D + col] : z;
-            const uint32_t b0 = h2bits(__halves2half2(e0, e1));
-            const uint32_t b1 = h2bits(__halves2half2(e2, e3));
-            hmma16816(acc[nt], ah, b0, b1);
-            hmma16816(acc[nt], al, b0, b1);
+        for (int i = tid; i < kOBK * (D / 8); i += kOThreads) {
+            const int r = i / (D / 8), c = (i % (D / 8)) * 8;
+            const bool ok = k0 + r < N;
+            cp16(saddr(&sm.dv[buf][r][c]), Dv + (size_t)(ok ? k0 + r : 0) * D + c, ok);
         }
-    }
+        cp_commit();
+    };
+
+    float acc[2][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NTN; ++nt) {
-        red[warp][g8][nt * 8 + 2 * t4] = acc[nt][0];
-        red[warp][g8][nt * 8 + 2 * t4 + 1] = acc[nt][1];
-        red[warp][g8 + 8][nt * 8 + 2 * t4] = acc[nt][2];
-        red[warp][g8 + 8][nt * 8 + 2 * t4 + 1] = acc[nt][3];
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < 16 * D; i += kOWarps * 32) {
-        const int r = i / D, c = i % D;
-        if (row0 + r >= M) continue;
-        float v = 0.f;
+    for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-        for (int w2 = 0; w2 < kOWarps; ++w2) v += red[w2][r][c];
-        const size_t row = (size_t)l * M + row0 + r;
-        a.out[row * D + c] = v * a.wunscale[row];
+        for (int ni = 0; ni < NT; ++ni) acc[mi][ni][0] = acc[mi][ni][1] = acc[mi][ni][2] = acc[mi][ni][3] = 0.f;
+    load(0, 0);
+    for (int ch = 0; ch < nchunks; ++ch) {
+        const int buf = ch & 1;
+        if (ch + 1 < nchunks) {
+            load(ch + 1, buf ^ 1);
+            cp_wait<1>();
+        } else {
+            cp_wait<0>();
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < kOBK; kk += 16) {
+            uint32_t ah[2][4], al[2][4], b[NT][2];
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi) {
+                const int r = mi * 16 + (lane & 15), c = kk + (lane >> 4) * 8;
+                ldsm_x4(ah[mi], saddr(&sm.wh[buf][r][c]));
+                ldsm_x4(al[mi], saddr(&sm.wl[buf][r][c]));
+            }
+#pragma unroll
+            for (int ni = 0; ni < NT; ni += 2) {
+                // matrices: (atoms kk..+7, cols n0..+7), (kk+8.., n0..), (kk.., n0+8..), (kk+8.., n0+8..)
+                const int k = kk + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int n = warp * (D / 4) + ni * 8 + (lane >> 4) * 8;
+                uint32_t t[4];
+                ldsm_x4_trans(t, saddr(&sm.dv[buf][k][n]));
+                b[ni][0] = t[0];
+                b[ni][1] = t[1];
+                b[ni + 1][0] = t[2];
+                b[ni + 1][1] = t[3];
+            }
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                for (int ni = 0; ni < NT; ++ni) {
+                    hmma16816(acc[mi][ni], ah[mi], b[ni][0], b[ni][1]);
+                    hmma16816(acc[mi][ni], al[mi], b[ni][0], b[ni][1]);
+                }
+        }
+        __syncthreads();                                // the buffer is loaded again two chunks on
     }
+    const int g8 = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int row = row0 + mi * 16 + g8 + hr * 8;
+            if (row >= M) continue;
+            const size_t orow = (size_t)l * M + row;
+            const float f = a.wunscale[orow];
+#pragma unroll
+            for (int ni = 0; ni < NT; ++ni) {
+                const int col = warp * (D / 4) + ni * 8 + 2 * t4;
+                *reinterpret_cast<float2*>(a.out + orow * D + col) =
+                    make_float2(acc[mi][ni][2 * hr] * f, acc[mi][ni][2 * hr + 1] * f);
+            }
+        }
 }
 
 template <int D, int HP>
@@ -649,6 +754,29 @@ cudaError_t launch_d(const AttendArgs& a, cudaStream_t st)
     if (grp >= 3 && attend_smem<D, 3>(a.N) <= kAttSmemMax) return launch_hp<T, D, 3>(a, st);
     if (grp >= 2 && attend_smem<D, 2>(a.N) <= kAttSmemMax) return launch_hp<T, D, 2>(a, st);
     return launch_hp<T, D, 1>(a, st);
+}
+
+template <int D>
+cudaError_t launch_u(const AttendArgs& a, cudaStream_t st)
+{
+    const int M = a.B * a.Hq;
+    const size_t smem = sizeof(USmem<D>);
+    cudaError_t e = cudaFuncSetAttribute(attend_u_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((a.N + kUBN - 1) / kUBN), (unsigned)((M + kUBM - 1) / kUBM), (unsigned)a.L);
+    attend_u_kernel<D><<<grid, kUThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_o(const AttendArgs& a, cudaStream_t st)
+{
+    const int M = a.B * a.Hq;
+    const size_t smem = sizeof(OSmem<D>);
+    cudaError_t e = cudaFuncSetAttribute(attend_o_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attend_o_kernel<D><<<dim3((unsigned)((M + kOBM - 1) / kOBM), (unsigned)a.L), kOThreads, smem, st>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -694,24 +822,11 @@ cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st)
 {
     if (a.L <= 0 || a.B <= 0) return cudaSuccess;
     if (a.dtype != FADKV_F16) return a.d == 128 ? launch_d<float, 128>(a, st) : launch_d<float, 64>(a, st);
-    const int M = a.B * a.Hq;
-    const dim3 gu((unsigned)((a.N + 255) / 256), (unsigned)((M + 15) / 16), (unsigned)a.L);
-    if (a.d == 128) attend_u_kernel<128><<<gu, 128, 0, st>>>(a);
-    else attend_u_kernel<64><<<gu, 128, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = a.d == 128 ? launch_u<128>(a, st) : launch_u<64>(a, st);
     if (e != cudaSuccess) return e;
     e = a.d == 128 ? launch_d<__half, 128>(a, st) : launch_d<__half, 64>(a, st);
     if (e != cudaSuccess) return e;
-    const dim3 go((unsigned)((M + 15) / 16), (unsigned)a.L);
-    const size_t osm = sizeof(float) * kOWarps * 16 * (a.d + 1);
-    if (a.d == 128) {
-        e = cudaFuncSetAttribute(attend_o_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)osm);
-        if (e == cudaSuccess) attend_o_kernel<128><<<go, kOWarps * 32, osm, st>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(attend_o_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)osm);
-        if (e == cudaSuccess) attend_o_kernel<64><<<go, kOWarps * 32, osm, st>>>(a);
-    }
-    return e != cudaSuccess ? e : cudaGetLastError();
+    return a.d == 128 ? launch_o<128>(a, st) : launch_o<64>(a, st);
 }
 
 }  // namespace fadkv
